@@ -1,0 +1,188 @@
+"""Python binding of the symmetric-slot GEMV + one-shot all-reduce C ABI.
+
+The functions below carry the names of ``include/symm_gemv.h`` and only
+marshal arguments into ``libsymm_gemv.so``; every step of the computation runs
+in that library's CUDA kernels.  Non-zero return codes raise ``SymmError``
+(its ``code`` is the SYMM_E* value, its message the library's last error).
+
+Pointers are device addresses as Python ints (for example
+``tensor.data_ptr()``); streams are CUDA stream handles as ints, objects with a
+``cuda_stream`` attribute (``torch.cuda.Stream``), or None for the legacy
+default stream.
+
+There is no fallback: if the library has not been built, importing works but
+the first call raises.  Build it with ``__graft_entry__.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH
+
+SYMM_OK = 0
+SYMM_EINVAL = -1
+SYMM_ENOMEM = -2
+SYMM_ECUDA = -3
+SYMM_ERANGE = -4
+SYMM_EPROTO = -5
+SYMM_ECORRUPT = -6
+
+SYMM_MAX_RANKS = 64
+SYMM_MAX_BATCH = 16
+
+SYMM_OPT_GEMV_PATH = 1
+SYMM_OPT_TILE_ORDER = 2
+
+GEMV_PATH_AUTO, GEMV_PATH_FFMA = 0, 1
+
+EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
+            "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
+            "symm_info", "symm_gemv_rows_per_tile", "symm_free", "symm_last_error")
+
+_lib = None
+
+
+class SymmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class SymmInfo(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int), ("device", ctypes.c_int), ("stride", ctypes.c_size_t),
+                ("slot_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t),
+                ("signal_pad_bytes", ctypes.c_size_t), ("max_tiles", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libsymm_gemv.so``; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library has not been built "
+                               "(run __graft_entry__.build()); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.symm_layout.argtypes = [i, sz, sz, sz, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.symm_alloc.argtypes = [i, sz, sz, sz, vp, sz, ctypes.POINTER(vp)]
+        L.symm_rendezvous.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(sz)]
+        L.one_shot_all_reduce.argtypes = [vp, vp, vp, i, sz, vp]
+        L.gemv_all_reduce.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.symm_status.argtypes = [vp, vp, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.symm_check_guards.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.symm_set_option.argtypes = [vp, i, i]
+        L.symm_info.argtypes = [vp, ctypes.POINTER(SymmInfo)]
+        L.symm_gemv_rows_per_tile.argtypes = [vp, i]
+        L.symm_free.argtypes = [vp]
+        L.symm_last_error.argtypes = []
+        L.symm_last_error.restype = ctypes.c_char_p
+        for name in EXPORTED[:-1]:
+            getattr(L, name).restype = i
+        _lib = L
+    return _lib
+
+
+def symm_last_error() -> str:
+    return lib().symm_last_error().decode(errors="replace")
+
+
+def _check(rc: int) -> int:
+    if rc != SYMM_OK:
+        raise SymmError(rc, symm_last_error())
+    return rc
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        return ctypes.c_void_p(0)
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(int(stream.cuda_stream))
+    return ctypes.c_void_p(int(stream))
+
+
+def _vp(p) -> ctypes.c_void_p:
+    return ctypes.c_void_p(int(p) if p is not None else 0)
+
+
+def symm_layout(R: int, slot_bytes: int, scratch_bytes: int, signal_pad_bytes: int):
+    """-> (stride, total_bytes)"""
+    stride, total = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().symm_layout(R, slot_bytes, scratch_bytes, signal_pad_bytes,
+                             ctypes.byref(stride), ctypes.byref(total)))
+    return stride.value, total.value
+
+
+def symm_alloc(R: int, slot_bytes: int, scratch_bytes: int, signal_pad_bytes: int,
+               backing: int | None = None, backing_bytes: int = 0) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().symm_alloc(R, slot_bytes, scratch_bytes, signal_pad_bytes, _vp(backing),
+                            backing_bytes, ctypes.byref(h)))
+    return h
+
+
+def symm_rendezvous(h):
+    """-> (slot_ptrs[R], signal_pad_ptrs[R], stride)"""
+    info = symm_info(h)
+    R = info["R"]
+    slots = (ctypes.c_void_p * R)()
+    pads = (ctypes.c_void_p * R)()
+    stride = ctypes.c_size_t()
+    _check(lib().symm_rendezvous(h, slots, pads, ctypes.byref(stride)))
+    return [int(p or 0) for p in slots], [int(p or 0) for p in pads], stride.value
+
+
+def one_shot_all_reduce(h, inp: int, out: int, R: int, n: int, stream=None) -> None:
+    _check(lib().one_shot_all_reduce(h, _vp(inp), _vp(out), R, n, _stream(stream)))
+
+
+def gemv_all_reduce(h, W_r: int, x_r: int, y: int, R: int, N: int, K: int, B: int, stream=None) -> None:
+    _check(lib().gemv_all_reduce(h, _vp(W_r), _vp(x_r), _vp(y), R, N, K, B, _stream(stream)))
+
+
+def symm_status(h, stream=None):
+    """-> (code, rank, tile); code is SYMM_OK or SYMM_EPROTO."""
+    code, rank, tile = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().symm_status(h, _stream(stream), ctypes.byref(code), ctypes.byref(rank),
+                             ctypes.byref(tile)))
+    return code.value, rank.value, tile.value
+
+
+def symm_check_guards(h):
+    """-> (rc, bad_rank, bad_band); rc is SYMM_OK or SYMM_ECORRUPT."""
+    rank, band = ctypes.c_int(), ctypes.c_int()
+    rc = lib().symm_check_guards(h, ctypes.byref(rank), ctypes.byref(band))
+    if rc not in (SYMM_OK, SYMM_ECORRUPT):
+        _check(rc)
+    return rc, rank.value, band.value
+
+
+def symm_set_option(h, option: int, value: int) -> None:
+    _check(lib().symm_set_option(h, option, value))
+
+
+def symm_info(h) -> dict:
+    info = SymmInfo()
+    _check(lib().symm_info(h, ctypes.byref(info)))
+    return {k: getattr(info, k) for k, _ in SymmInfo._fields_}
+
+
+def symm_gemv_rows_per_tile(h, B: int) -> int:
+    return lib().symm_gemv_rows_per_tile(h, B)
+
+
+def symm_free(h) -> None:
+    _check(lib().symm_free(h))
+
+
+class DeviceView:
+    """A raw device range exposed through ``__cuda_array_interface__`` so that
+    ``torch.as_tensor(view, device='cuda')`` aliases slot memory."""
+
+    def __init__(self, ptr: int, shape, typestr: str = "|u1"):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}

@@ -1,0 +1,126 @@
+// One-shot all-reduce over R symmetric slots.
+//
+// out_s[i] = bf16_rne( in_0[i] + in_1[i] + ... + in_{R-1}[i] ) (fp32, rank
+// order) for every slot s.  This is the one-shot algorithm of the "PyTorch
+// Symmetric Memory" talk (outer loop over data blocks, inner loop over ranks,
+// local or remote loads alike, reduce locally) with the accumulation the
+// symmetric-memory docs give for bf16 ("higher-precision reduction": fp32).
+// Because the R ranks are slots of one GPU, one thread computes the sum once
+// and stores it into all R output slots instead of R GPUs each computing it.
+//
+// The start/end signal-pad barriers of the symmetric-memory kernel exist to
+// order a rank's reads after its peers' writes and to protect buffer reuse
+// across ranks.  On one GPU with one stream per handle, stream order gives
+// both: the inputs were produced by earlier work on the stream, and the next
+// launch starts after this one ends.
+//
+// Each thread owns one 16-byte vector (8 elements) at a time and reads it in
+// every slot before writing it anywhere, so in == out is safe.  The loads of
+// the R slots are issued back to back (R x 16 B in flight per thread).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "protocol.cuh"
+
+namespace symm {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v) {
+    acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x);
+    acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
+    acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z);
+    acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half)
+    return *reinterpret_cast<const uint32_t *>(&p);
+}
+
+// RT > 0: rank count known at compile time; RT == 0: runtime a.R.
+template <int RT>
+__global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceArgs a) {
+    const int R = RT > 0 ? RT : a.R;
+    const size_t nvec = a.n / 8;
+    const size_t step = (size_t)gridDim.x * kThreads;
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < nvec; i += step) {
+        const uint8_t *src = a.in + i * 16;
+        float acc[8];
+        if (RT > 0) {
+            uint4 v[RT > 0 ? RT : 1];
+#pragma unroll
+            for (int q = 0; q < (RT > 0 ? RT : 1); ++q) v[q] = ld_v4(src + (long long)q * a.stride);
+            acc[0] = bf16lo(v[0].x); acc[1] = bf16hi(v[0].x);
+            acc[2] = bf16lo(v[0].y); acc[3] = bf16hi(v[0].y);
+            acc[4] = bf16lo(v[0].z); acc[5] = bf16hi(v[0].z);
+            acc[6] = bf16lo(v[0].w); acc[7] = bf16hi(v[0].w);
+#pragma unroll
+            for (int q = 1; q < (RT > 0 ? RT : 1); ++q) add8(acc, v[q]);
+        } else {
+            const uint4 v0 = ld_v4(src);
+            acc[0] = bf16lo(v0.x); acc[1] = bf16hi(v0.x);
+            acc[2] = bf16lo(v0.y); acc[3] = bf16hi(v0.y);
+            acc[4] = bf16lo(v0.z); acc[5] = bf16hi(v0.z);
+            acc[6] = bf16lo(v0.w); acc[7] = bf16hi(v0.w);
+            int q = 1;
+            for (; q + 4 <= R; q += 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = ld_v4(src + (long long)(q + j) * a.stride);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) add8(acc, v[j]);
+            }
+            for (; q < R; ++q) add8(acc, ld_v4(src + (long long)q * a.stride));
+        }
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        uint8_t *dst = a.out + i * 16;
+#pragma unroll 8
+        for (int s = 0; s < R; ++s) st_v4(dst + (long long)s * a.stride, o);
+    }
+    // Ragged tail (n % 8 elements): scalar, handled by the first threads of CTA 0.
+    const size_t tail0 = nvec * 8;
+    if (blockIdx.x == 0 && tail0 + threadIdx.x < a.n) {
+        const size_t e = tail0 + threadIdx.x;
+        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(a.in) + e;
+        float acc = __bfloat162float(*src);
+        for (int q = 1; q < R; ++q)
+            acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                reinterpret_cast<const uint8_t *>(src) + (long long)q * a.stride));
+        const __nv_bfloat16 v = __float2bfloat16_rn(acc);
+        for (int s = 0; s < R; ++s)
+            *reinterpret_cast<__nv_bfloat16 *>(a.out + e * 2 + (long long)s * a.stride) = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s) {
+    const size_t nvec = a.n / 8;
+    int sms = 152;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // Enough CTAs for one vector per thread, capped at 8 resident CTAs per SM
+    // (grid-stride beyond that); at least one CTA for the ragged tail.
+    size_t blocks = (nvec + kThreads - 1) / kThreads;
+    const size_t cap = (size_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    switch (a.R) {
+        case 1: one_shot_ar_kernel<1><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+        case 2: one_shot_ar_kernel<2><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+        case 4: one_shot_ar_kernel<4><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+        case 8: one_shot_ar_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+        default: one_shot_ar_kernel<0><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace symm

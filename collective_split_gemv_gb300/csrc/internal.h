@@ -1,0 +1,56 @@
+// Internal interface between the host runtime (symm_runtime.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace symm {
+
+// Signal-pad layout of every slot (byte offsets from the pad start):
+//   [0, 128)                status words {code, rank, tile, epoch} (slot 0 only)
+//   [128, 128 + 4*T)        flags[T]     tile t of rank r published (epoch)
+//   [cnt_off, cnt_off+4*T)  counters[T]  arrivals at tile t (slot 0 only)
+constexpr size_t kPadStatusBytes = 128;
+constexpr int kStatusCode = 0, kStatusRank = 1, kStatusTile = 2, kStatusEpoch = 3;
+constexpr int kProtoStaleFlag = 1;    // device codes; host maps them to SYMM_EPROTO
+constexpr int kProtoBadTicket = 2;
+
+// Arguments of one fused GEMV + all-reduce launch.  Every pointer is the
+// slot-0 instance; rank r's instance is ptr + r * stride bytes.
+struct GemvArgs {
+    const uint8_t *W;        // bf16 [N][Kr]
+    const uint8_t *x;        // bf16 [B][Kr]
+    uint8_t *y;              // bf16 [B][N]
+    uint8_t *scratch;        // fp32 [B][N] partial of the slot's rank
+    uint32_t *flags;         // [max_tiles]
+    uint32_t *counters;      // [max_tiles], slot 0
+    uint32_t *status;        // [4], slot 0
+    long long stride;        // bytes between slots
+    int R, N, Kr, B;
+    int rows_per_tile;
+    int num_tiles;
+    int kc_cap;              // 16-byte chunks of x staged in shared memory per pass
+    uint32_t epoch;          // this launch's epoch (>= 1)
+    int reverse_order;       // 1: CTAs take work in reverse (arrival-order tests)
+};
+
+struct AllReduceArgs {
+    const uint8_t *in;       // bf16 [n], slot 0
+    uint8_t *out;            // bf16 [n], slot 0
+    long long stride;
+    int R;
+    size_t n;
+};
+
+// Kernel launchers; return the launch's cudaError_t.
+cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s);
+
+// FFMA (CUDA-core) fused kernel: any B in 1..16.
+int ffma_rows_per_tile(int B);
+size_t ffma_smem_bytes(int B, int kc_cap);
+int ffma_kc_cap(int B, int Kr);
+cudaError_t launch_gemv_ffma(const GemvArgs &a, cudaStream_t s);
+
+}  // namespace symm

@@ -1,0 +1,142 @@
+// Device-side pieces shared by the fused GEMV kernels: streaming loads,
+// bf16 unpacking, and the publish / last-arriver reduction protocol.
+//
+// Protocol (one row tile t, R contributing CTAs, one per rank):
+//  1. every thread stores its share of the rank's fp32 partial into the
+//     rank's scratch slot, then fences (gpu scope);
+//  2. after a CTA barrier, thread 0 release-stores flag_r[t] = epoch and takes
+//     an arrival ticket with an acq_rel atomic add on counter[t];
+//  3. tickets are monotone across launches: launch `epoch` owns tickets
+//     (epoch-1)*R .. epoch*R-1; the holder of the last one is the reducer.  A
+//     ticket outside that range latches a protocol error instead;
+//  4. the reducer acquires the R flags (each must equal epoch), sums the R
+//     partials in rank order 0..R-1 in fp32, rounds to bf16 (RNE) and stores
+//     the value into every rank's output slot.
+// No CTA ever waits for another: a tile whose contributors have not all
+// arrived is finished by whichever contributor arrives last.
+//
+// This is the publish-as-soon-as-done / reduce-locally scheme of the fused
+// GEMV + AllReduce ("Overlapping Collective Communication with Dependent
+// Computation ...", Abstract) and the one-shot all-reduce ("PyTorch Symmetric
+// Memory" talk, one-shot segment), with the start/end signal-pad barriers of
+// the symmetric-memory kernels replaced by per-tile release flags.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace symm {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ float ld_relaxed_gpu_f32(const float *p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Two bf16 values packed in one 32-bit word (element 2i in the low half):
+// a bf16 is the top half of an fp32 word, so widening is a shift / mask.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void latch_status(uint32_t *status, int code, int rank, int tile,
+                                             uint32_t epoch) {
+    if (atomicCAS(status + kStatusCode, 0u, (uint32_t)code) == 0u) {
+        status[kStatusRank] = (uint32_t)rank;
+        status[kStatusTile] = (uint32_t)tile;
+        status[kStatusEpoch] = epoch;
+    }
+}
+
+// Steps 2-4 of the protocol.  Called by ALL threads of the CTA after each
+// thread has stored its part of rank r's partial for tile t.
+__device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int r) {
+    __shared__ int s_last;
+    __shared__ int s_bad;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
+                                                      (long long)r * a.stride) + t;
+        st_release_gpu(flag, a.epoch);
+        uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
+        uint32_t first = (a.epoch - 1u) * (uint32_t)a.R;
+        uint32_t pos = ticket - first;
+        if (pos >= (uint32_t)a.R) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
+        s_last = (pos == (uint32_t)a.R - 1u);
+        s_bad = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x < (unsigned)a.R) {
+        const uint32_t *f = reinterpret_cast<const uint32_t *>(
+                                reinterpret_cast<const uint8_t *>(a.flags) +
+                                (long long)threadIdx.x * a.stride) + t;
+        if (ld_acquire_gpu(f) != a.epoch) {
+            latch_status(a.status, kProtoStaleFlag, (int)threadIdx.x, t, a.epoch);
+            s_bad = 1;
+        }
+    }
+    __syncthreads();
+    if (s_bad) return;
+
+    const int n0 = t * a.rows_per_tile;
+    const int rows = min(a.rows_per_tile, a.N - n0);
+    const int count = rows * a.B;
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+        const int b = i / rows;
+        const int n = n0 + (i - b * rows);
+        const size_t off = ((size_t)b * a.N + n) * sizeof(float);
+        float acc = ld_relaxed_gpu_f32(reinterpret_cast<const float *>(a.scratch + off));
+        for (int q = 1; q < a.R; ++q)
+            acc += ld_relaxed_gpu_f32(
+                reinterpret_cast<const float *>(a.scratch + (long long)q * a.stride + off));
+        const __nv_bfloat16 v = __float2bfloat16_rn(acc);
+        const size_t yoff = ((size_t)b * a.N + n) * sizeof(__nv_bfloat16);
+        for (int s = 0; s < a.R; ++s)
+            *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)s * a.stride + yoff) = v;
+    }
+}
+
+}  // namespace symm

@@ -1,0 +1,414 @@
+// Host runtime of the symmetric-slot library: the C ABI of include/symm_gemv.h.
+//
+// Slot layout (every slot identical; stride rounded up to 2 MiB):
+//
+//   [user region  slot_bytes][guard 4 KiB][scratch][guard][signal pad][guard]
+//
+// The user region holds the caller's tensors at symmetric offsets (W_r, x_r,
+// y, all-reduce in/out), like the per-peer buffers of a symmetric-memory
+// handle ("PyTorch Symmetric Memory" docs, "Write your own kernel":
+// buffer_ptrs / signal_pad_ptrs).  The scratch region receives the fused
+// kernel's fp32 partials, one slot per rank (the peer-visible buffer the
+// fused GEMV + AllReduce writes its partials into).  The signal pad holds the
+// per-tile flags, the tile arrival counters and the status words.  Guard bands
+// are filled with 0xA5 and checked by symm_check_guards.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/symm_gemv.h"
+#include "internal.h"
+
+using namespace symm;
+
+struct symm_handle {
+    int R = 0;
+    int device = 0;
+    size_t slot_bytes = 0, scratch_bytes = 0, pad_bytes = 0;
+    size_t stride = 0, total = 0;
+    size_t guard0 = 0, scratch_off = 0, guard1 = 0, pad_off = 0, guard2 = 0;
+    size_t flags_off = 0, counters_off = 0;   // within the pad
+    int max_tiles = 0;
+    uint8_t *base = nullptr;
+    bool owned = false;
+    uint32_t epoch = 0;                       // epoch of the last GEMV launch
+    int opt_gemv_path = 0;
+    int opt_tile_order = 0;
+};
+
+namespace {
+
+constexpr size_t kGuard = 4096;
+constexpr size_t kAlign = 256;
+constexpr size_t kStrideAlign = 2u << 20;
+constexpr unsigned char kGuardByte = 0xA5;
+
+thread_local char g_err[512];
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(SYMM_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool mul_overflows(size_t a, size_t b) { return a != 0 && b > SIZE_MAX / a; }
+
+// Fills a handle's offsets from the sizes; returns false on overflow.
+bool compute_layout(symm_handle &h) {
+    if (h.slot_bytes > SIZE_MAX / 4 || h.scratch_bytes > SIZE_MAX / 4 || h.pad_bytes > SIZE_MAX / 4)
+        return false;
+    h.guard0 = round_up(h.slot_bytes, kAlign);
+    h.scratch_off = h.guard0 + kGuard;
+    h.guard1 = h.scratch_off + round_up(h.scratch_bytes, kAlign);
+    h.pad_off = h.guard1 + kGuard;
+    h.guard2 = h.pad_off + round_up(h.pad_bytes, kAlign);
+    h.stride = round_up(h.guard2 + kGuard, kStrideAlign);
+    if (mul_overflows(h.stride, (size_t)h.R)) return false;
+    h.total = h.stride * (size_t)h.R;
+    // Pad: status, then flags[T] and counters[T], each 128-byte aligned.
+    size_t room = round_up(h.pad_bytes, kAlign) - kPadStatusBytes;
+    size_t T = room / 8;
+    T = T / 32 * 32;
+    while (T > 0 && kPadStatusBytes + round_up(4 * T, 128) * 2 > round_up(h.pad_bytes, kAlign)) T -= 32;
+    h.max_tiles = (int)std::min<size_t>(T, 1u << 30);
+    h.flags_off = kPadStatusBytes;
+    h.counters_off = kPadStatusBytes + round_up(4 * (size_t)h.max_tiles, 128);
+    return true;
+}
+
+uint8_t *slot(const symm_handle *h, int r) { return h->base + (size_t)r * h->stride; }
+uint32_t *pad_word(const symm_handle *h, int r, size_t off) {
+    return reinterpret_cast<uint32_t *>(slot(h, r) + h->pad_off + off);
+}
+
+int check_device(const symm_handle *h) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device)
+        return fail(SYMM_EINVAL, "current device %d differs from the handle's device %d", dev, h->device);
+    return SYMM_OK;
+}
+
+// [p, p + bytes) inside slot 0's user region?
+bool in_user_region(const symm_handle *h, const void *p, size_t bytes) {
+    const uint8_t *q = static_cast<const uint8_t *>(p);
+    if (q < h->base) return false;
+    size_t off = (size_t)(q - h->base);
+    return off <= h->slot_bytes && bytes <= h->slot_bytes - off;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uint8_t *x = static_cast<const uint8_t *>(a), *y = static_cast<const uint8_t *>(b);
+    if (na == 0 || nb == 0) return false;
+    return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Zero flags and counters of every slot (stream-ordered) and restart epochs.
+int reset_protocol(symm_handle *h, cudaStream_t s) {
+    for (int r = 0; r < h->R; ++r) {
+        cudaError_t e = cudaMemsetAsync(slot(h, r) + h->pad_off + h->flags_off, 0,
+                                        h->pad_bytes - h->flags_off, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(signal pad)");
+    }
+    h->epoch = 0;
+    return SYMM_OK;
+}
+
+int gemv_path(const symm_handle *h, int B) {
+    (void)B;
+    return h->opt_gemv_path == 0 ? 1 : h->opt_gemv_path;
+}
+
+int rows_per_tile_for(const symm_handle *h, int B) {
+    if (B < 1 || B > SYMM_MAX_BATCH) return 0;
+    switch (gemv_path(h, B)) {
+        case 1: return ffma_rows_per_tile(B);
+        default: return 0;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *symm_last_error(void) { return g_err; }
+
+int symm_layout(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+                size_t *stride_out, size_t *total_bytes_out) {
+    if (R < 1 || R > SYMM_MAX_RANKS) return fail(SYMM_EINVAL, "R=%d outside 1..%d", R, SYMM_MAX_RANKS);
+    if (slot_bytes == 0) return fail(SYMM_EINVAL, "slot_bytes must be > 0");
+    if (signal_pad_bytes < 4096) return fail(SYMM_EINVAL, "signal_pad_bytes must be >= 4096");
+    symm_handle h;
+    h.R = R;
+    h.slot_bytes = slot_bytes;
+    h.scratch_bytes = scratch_bytes;
+    h.pad_bytes = signal_pad_bytes;
+    if (!compute_layout(h)) return fail(SYMM_EINVAL, "sizes overflow");
+    if (stride_out) *stride_out = h.stride;
+    if (total_bytes_out) *total_bytes_out = h.total;
+    g_err[0] = 0;
+    return SYMM_OK;
+}
+
+int symm_alloc(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+               void *backing, size_t backing_bytes, symm_handle_t **out) {
+    if (!out) return fail(SYMM_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = symm_layout(R, slot_bytes, scratch_bytes, signal_pad_bytes, nullptr, nullptr);
+    if (rc != SYMM_OK) return rc;
+    symm_handle *h = new (std::nothrow) symm_handle;
+    if (!h) return fail(SYMM_ENOMEM, "host allocation of the handle failed");
+    h->R = R;
+    h->slot_bytes = slot_bytes;
+    h->scratch_bytes = scratch_bytes;
+    h->pad_bytes = signal_pad_bytes;
+    compute_layout(*h);
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    if (backing) {
+        if ((reinterpret_cast<uintptr_t>(backing) % kAlign) != 0) {
+            delete h;
+            return fail(SYMM_EINVAL, "backing pointer is not %zu-byte aligned", kAlign);
+        }
+        if (backing_bytes < h->total) {
+            delete h;
+            return fail(SYMM_ENOMEM, "backing holds %zu bytes, layout needs %zu", backing_bytes, h->total);
+        }
+        h->base = static_cast<uint8_t *>(backing);
+        h->owned = false;
+    } else {
+        e = cudaMalloc(reinterpret_cast<void **>(&h->base), h->total);
+        if (e != cudaSuccess) {
+            delete h;
+            cudaGetLastError();
+            return fail(SYMM_ENOMEM, "cudaMalloc(%zu) failed: %s", h->total, cudaGetErrorString(e));
+        }
+        h->owned = true;
+    }
+    for (int r = 0; r < R && e == cudaSuccess; ++r) {
+        uint8_t *s = slot(h, r);
+        e = cudaMemset(s + h->guard0, kGuardByte, kGuard);
+        if (e == cudaSuccess) e = cudaMemset(s + h->scratch_off, 0, h->guard1 - h->scratch_off);
+        if (e == cudaSuccess) e = cudaMemset(s + h->guard1, kGuardByte, kGuard);
+        if (e == cudaSuccess) e = cudaMemset(s + h->pad_off, 0, h->guard2 - h->pad_off);
+        if (e == cudaSuccess) e = cudaMemset(s + h->guard2, kGuardByte, kGuard);
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (h->owned) cudaFree(h->base);
+        delete h;
+        return cuda_fail(e, "initialising slots");
+    }
+    *out = h;
+    g_err[0] = 0;
+    return SYMM_OK;
+}
+
+int symm_rendezvous(symm_handle_t *h, void **slot_ptrs, void **signal_pad_ptrs, size_t *stride_out) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    for (int r = 0; r < h->R; ++r) {
+        if (slot_ptrs) slot_ptrs[r] = slot(h, r);
+        if (signal_pad_ptrs) signal_pad_ptrs[r] = slot(h, r) + h->pad_off;
+    }
+    if (stride_out) *stride_out = h->stride;
+    return SYMM_OK;
+}
+
+int symm_info(symm_handle_t *h, symm_info_t *info) {
+    if (!h || !info) return fail(SYMM_EINVAL, "NULL argument");
+    info->R = h->R;
+    info->device = h->device;
+    info->stride = h->stride;
+    info->slot_bytes = h->slot_bytes;
+    info->scratch_bytes = h->scratch_bytes;
+    info->signal_pad_bytes = h->pad_bytes;
+    info->max_tiles = h->max_tiles;
+    return SYMM_OK;
+}
+
+int symm_set_option(symm_handle_t *h, int option, int value) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    switch (option) {
+        case SYMM_OPT_GEMV_PATH:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma)", value);
+            h->opt_gemv_path = value;
+            return SYMM_OK;
+        case SYMM_OPT_TILE_ORDER:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "tile order %d unknown", value);
+            h->opt_tile_order = value;
+            return SYMM_OK;
+        default:
+            return fail(SYMM_EINVAL, "unknown option %d", option);
+    }
+}
+
+int symm_gemv_rows_per_tile(symm_handle_t *h, int B) { return h ? rows_per_tile_for(h, B) : 0; }
+
+int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    if (n == 0) return SYMM_OK;
+    if (n > SIZE_MAX / 2) return fail(SYMM_EINVAL, "n too large");
+    const size_t bytes = n * 2;
+    if (!in_user_region(h, in, bytes)) return fail(SYMM_EINVAL, "in + n elements is not inside slot 0's user region");
+    if (!in_user_region(h, out, bytes)) return fail(SYMM_EINVAL, "out + n elements is not inside slot 0's user region");
+    if (!aligned16(in) || !aligned16(out)) return fail(SYMM_EINVAL, "in/out must be 16-byte aligned");
+    if (in != out && overlaps(in, bytes, out, bytes)) return fail(SYMM_EINVAL, "in and out partially overlap");
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+    AllReduceArgs a;
+    a.in = static_cast<const uint8_t *>(in);
+    a.out = static_cast<uint8_t *>(out);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.n = n;
+    cudaError_t e = launch_one_shot_all_reduce(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "one_shot_all_reduce launch");
+    return SYMM_OK;
+}
+
+int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,
+                    symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    if (N < 0 || K < 0) return fail(SYMM_EINVAL, "N=%d K=%d must be >= 0", N, K);
+    if (B < 0 || B > SYMM_MAX_BATCH) return fail(SYMM_EINVAL, "B=%d outside 0..%d", B, SYMM_MAX_BATCH);
+    if (K % R) return fail(SYMM_EINVAL, "K=%d is not a multiple of R=%d", K, R);
+    const int Kr = K / R;
+    if (Kr % 8) return fail(SYMM_EINVAL, "K/R=%d is not a multiple of 8", Kr);
+    if (N == 0 || B == 0) return SYMM_OK;
+    const size_t wbytes = (size_t)N * (size_t)Kr * 2;
+    const size_t xbytes = (size_t)B * (size_t)Kr * 2;
+    const size_t ybytes = (size_t)B * (size_t)N * 2;
+    if (!in_user_region(h, W_r, wbytes)) return fail(SYMM_EINVAL, "W_r (N x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, x_r, xbytes)) return fail(SYMM_EINVAL, "x_r (B x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, y, ybytes)) return fail(SYMM_EINVAL, "y (B x N bf16) is not inside slot 0's user region");
+    if (!aligned16(W_r) || !aligned16(x_r) || !aligned16(y)) return fail(SYMM_EINVAL, "W_r, x_r and y must be 16-byte aligned");
+    if (overlaps(y, ybytes, W_r, wbytes) || overlaps(y, ybytes, x_r, xbytes))
+        return fail(SYMM_EINVAL, "y overlaps W_r or x_r");
+    if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
+        return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
+                    (size_t)B * (size_t)N * 4, h->scratch_bytes);
+    const int rows = rows_per_tile_for(h, B);
+    if (rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
+    const int tiles = (N + rows - 1) / rows;
+    if (tiles > h->max_tiles)
+        return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", tiles, h->max_tiles);
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Tickets of launch e are (e-1)*R .. e*R-1 (mod 2^32); restart before e*R wraps.
+    if (((uint64_t)h->epoch + 1) * (uint64_t)h->R > 0xFFFFFFFFull || h->epoch == 0) {
+        rc = reset_protocol(h, s);
+        if (rc != SYMM_OK) return rc;
+    }
+    h->epoch += 1;
+
+    GemvArgs a;
+    a.W = static_cast<const uint8_t *>(W_r);
+    a.x = static_cast<const uint8_t *>(x_r);
+    a.y = static_cast<uint8_t *>(y);
+    a.scratch = h->base + h->scratch_off;
+    a.flags = pad_word(h, 0, h->flags_off);
+    a.counters = pad_word(h, 0, h->counters_off);
+    a.status = pad_word(h, 0, 0);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.N = N;
+    a.Kr = Kr;
+    a.B = B;
+    a.rows_per_tile = rows;
+    a.num_tiles = tiles;
+    a.epoch = h->epoch;
+    a.reverse_order = h->opt_tile_order;
+    cudaError_t e = cudaSuccess;
+    switch (gemv_path(h, B)) {
+        case 1:
+            a.kc_cap = ffma_kc_cap(B, Kr);
+            e = launch_gemv_ffma(a, s);
+            break;
+        default:
+            return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "gemv_all_reduce launch");
+    return SYMM_OK;
+}
+
+int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t st[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(st, pad_word(h, 0, 0), sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (code) *code = st[kStatusCode] ? SYMM_EPROTO : SYMM_OK;
+    if (rank) *rank = st[kStatusCode] ? (int)st[kStatusRank] : -1;
+    if (tile) *tile = st[kStatusCode] ? (int)st[kStatusTile] : -1;
+    if (st[kStatusCode]) {
+        snprintf(g_err, sizeof g_err, "protocol error %u at rank %u tile %u epoch %u", st[kStatusCode],
+                 st[kStatusRank], st[kStatusTile], st[kStatusEpoch]);
+        e = cudaMemsetAsync(pad_word(h, 0, 0), 0, kPadStatusBytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+        int rc = reset_protocol(h, s);
+        if (rc != SYMM_OK) return rc;
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    }
+    return SYMM_OK;
+}
+
+int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (bad_rank) *bad_rank = -1;
+    if (bad_band) *bad_band = -1;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    static thread_local unsigned char buf[kGuard];
+    const size_t offs[3] = {h->guard0, h->guard1, h->guard2};
+    for (int r = 0; r < h->R; ++r)
+        for (int band = 0; band < 3; ++band) {
+            e = cudaMemcpy(buf, slot(h, r) + offs[band], kGuard, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return cuda_fail(e, "reading a guard band");
+            for (size_t i = 0; i < kGuard; ++i)
+                if (buf[i] != kGuardByte) {
+                    if (bad_rank) *bad_rank = r;
+                    if (bad_band) *bad_band = band;
+                    return fail(SYMM_ECORRUPT, "guard band %d of rank %d overwritten at byte %zu", band, r, i);
+                }
+        }
+    return SYMM_OK;
+}
+
+int symm_free(symm_handle_t *h) {
+    if (!h) return SYMM_OK;
+    int rc = SYMM_OK;
+    if (h->owned && h->base) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaFree(h->base);
+        if (e != cudaSuccess) rc = cuda_fail(e, "cudaFree");
+    }
+    delete h;
+    return rc;
+}
+
+}  // extern "C"

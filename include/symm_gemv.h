@@ -1,0 +1,226 @@
+/*
+ * symm_gemv.h -- C ABI of the GB300 symmetric-slot GEMV + one-shot all-reduce.
+ *
+ * The library computes the row-parallel (tensor-parallel) linear layer
+ *
+ *     y = sum_{r=0}^{R-1} W_r x_r
+ *
+ * in one fused CUDA kernel: each rank's partial product is published as soon
+ * as its row tile is done and the last contributor of a tile sums all ranks'
+ * partials in fixed rank order and stores the bf16 result into every rank's
+ * output slot.  The R ranks are R "symmetric slots" of one HBM allocation on
+ * one GPU: the same offset in every slot names the same tensor of each rank,
+ * the way a symmetric-memory handle's per-peer buffer pointers do.
+ *
+ * Sources for the semantics (page titles and sections):
+ *  - "PyTorch Symmetric Memory" documentation: symmetric allocation
+ *    (`empty`), `rendezvous` and the handle's buffer / signal-pad pointers
+ *    ("Hello World", "Write your own kernel", API reference); the signal pad
+ *    whose size scales with launched blocks and world size
+ *    (`set_signal_pad_size`); op reference `one_shot_all_reduce` (sum only);
+ *    the warning that all symmetric-memory collectives of a group must run on
+ *    one CUDA stream; the "higher-precision reduction" note (bf16 in, fp32
+ *    accumulate, bf16 out).
+ *  - "PyTorch Symmetric Memory: A New Programming Paradigm for Distributed
+ *    AI" (talk): the one-shot all-reduce -- every rank loads the block of every
+ *    rank and reduces locally.
+ *  - "Overlapping Collective Communication with Dependent Computation in
+ *    Distributed Machine Learning using GPU-Initiated Intra-Kernel
+ *    Networking" (summary of "Optimizing Distributed ML Communication with
+ *    Fused Computation-Collective Operations"), Abstract: the fused GEMV +
+ *    AllReduce operator, partials pushed as soon as each share is computed,
+ *    zero-copy writes into peer memory, communication-aware workgroup
+ *    scheduling.
+ *  - "Bay.Area.AI: Tensor and 2D Parallelism" (talk): column-wise then
+ *    row-wise sharding, which ends in exactly one all-reduce.
+ *
+ * Conventions for every call:
+ *  - Returns SYMM_OK (0) or a negative SYMM_E* code; never aborts.  On error
+ *    symm_last_error() describes the failure (thread-local string).
+ *  - "Symmetric pointer": a device address inside SLOT 0's user region.  Rank
+ *    r's instance is that address + r * stride (stride from symm_rendezvous).
+ *  - Tensors are bf16, row-major, 16-byte aligned.
+ *  - Calls that take a stream only enqueue work and return; device-side
+ *    protocol errors are latched in the handle's status word (symm_status).
+ *  - All calls on one handle must be issued on ONE stream (or streams the
+ *    caller serialises): the per-tile counters and flags of the signal pad
+ *    are shared by every launch on the handle.  Overlapping launches on the
+ *    same handle are detected (SYMM_EPROTO in symm_status) rather than hung:
+ *    no kernel in this library waits on another CTA.
+ *  - Device memory ownership: the library owns what symm_alloc allocates
+ *    (backing == NULL) and frees it in symm_free; borrowed backing memory
+ *    stays the caller's and must outlive the handle.
+ */
+#ifndef SYMM_GEMV_H
+#define SYMM_GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle: R slots carved from one device allocation. */
+typedef struct symm_handle symm_handle_t;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *symm_stream_t;
+
+enum {
+    SYMM_OK = 0,
+    SYMM_EINVAL = -1,   /* bad argument: count, size, alignment, pointer outside slot 0 */
+    SYMM_ENOMEM = -2,   /* device allocation failed or backing too small */
+    SYMM_ECUDA = -3,    /* a CUDA runtime call failed (message names it) */
+    SYMM_ERANGE = -4,   /* the problem exceeds the handle's scratch or signal-pad capacity */
+    SYMM_EPROTO = -5,   /* device protocol error: stale or missing tile flag, bad ticket */
+    SYMM_ECORRUPT = -6  /* a guard band around a region was overwritten */
+};
+
+/* Largest rank count and batch width the kernels accept. */
+#define SYMM_MAX_RANKS 64
+#define SYMM_MAX_BATCH 16
+
+/*
+ * symm_layout -- the slot stride and total bytes symm_alloc needs for these
+ * sizes, so a caller can provide (borrow) the backing memory itself.
+ *   R                 ranks, 1..SYMM_MAX_RANKS
+ *   slot_bytes        user region per slot (W_r, x_r, y, all-reduce in/out)
+ *   scratch_bytes     fp32 partial-product region per slot (>= 4*B*N for a
+ *                     gemv_all_reduce of batch B and N rows; 0 if unused)
+ *   signal_pad_bytes  per-slot signal pad; holds one flag and one counter per
+ *                     row tile (PyTorch Symmetric Memory docs,
+ *                     set_signal_pad_size: size proportional to launched
+ *                     blocks and world size); >= 4096
+ * Writes *stride_out and *total_bytes_out.  Host only; no device work.
+ */
+int symm_layout(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+                size_t *stride_out, size_t *total_bytes_out);
+
+/*
+ * symm_alloc -- carve R symmetric slots out of one device allocation
+ * (PyTorch Symmetric Memory docs, API reference `empty`: host-synchronous,
+ * meant for initialisation, allocate once and reuse).
+ *   backing, backing_bytes  NULL/0: the library cudaMalloc's the memory on the
+ *       current device and owns it.  Otherwise a device pointer the caller
+ *       owns (256-byte aligned, >= total bytes from symm_layout); the library
+ *       borrows it until symm_free.
+ *   out  receives the handle.
+ * Zeroes every slot's scratch region and signal pad and fills the guard bands,
+ * then synchronises the device.  Errors: SYMM_EINVAL (R outside 1..64,
+ * slot_bytes == 0, pad < 4096, misaligned or undersized backing),
+ * SYMM_ENOMEM, SYMM_ECUDA.
+ */
+int symm_alloc(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+               void *backing, size_t backing_bytes, symm_handle_t **out);
+
+/*
+ * symm_rendezvous -- the per-rank pointer tables of the handle (PyTorch
+ * Symmetric Memory docs, `rendezvous` and the handle's `buffer_ptrs` /
+ * `signal_pad_ptrs`).  Host only, not stream-ordered, not capturable; later
+ * calls return the same values.  No multicast pointer exists.
+ *   slot_ptrs        [R] out: device address of each rank's user region
+ *                    (NULL to skip)
+ *   signal_pad_ptrs  [R] out: device address of each rank's signal pad
+ *                    (NULL to skip)
+ *   stride_out       out: bytes between consecutive slots (NULL to skip)
+ * The pointers are borrowed; valid until symm_free.
+ */
+int symm_rendezvous(symm_handle_t *h, void **slot_ptrs, void **signal_pad_ptrs,
+                    size_t *stride_out);
+
+/*
+ * one_shot_all_reduce -- out_s[i] = bf16_rne( sum_{r=0}^{R-1} in_r[i] ) for
+ * every rank s, the sum taken in fp32 in rank order 0..R-1 (PyTorch Symmetric
+ * Memory docs, op reference `one_shot_all_reduce`, reduce op "sum"; the
+ * symmetric-memory talk's one-shot algorithm: each rank reads every rank's
+ * block and reduces locally; "higher-precision reduction": fp32 accumulate).
+ *   in, out  symmetric bf16 pointers (slot 0), 16-byte aligned; n elements
+ *            must fit in the user region.  in == out (in place) is allowed:
+ *            each element is read in all slots before it is written.  Partial
+ *            overlap of in and out is rejected.
+ *   R        must equal the handle's rank count.
+ *   n        elements per rank; 0 is a no-op.
+ * Every slot's out receives identical bits.  Errors: SYMM_EINVAL, SYMM_ECUDA.
+ */
+int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n,
+                        symm_stream_t stream);
+
+/*
+ * gemv_all_reduce -- the fused row-parallel GEMV + one-shot all-reduce
+ * ("Overlapping Collective Communication with Dependent Computation ...",
+ * Abstract, the GEMV + AllReduce fused operator; "Bay.Area.AI: Tensor and 2D
+ * Parallelism", row-wise sharded linear ending in one all-reduce):
+ *
+ *     y_s[b][n] = bf16_rne( sum_{r=0}^{R-1} sum_{k<K/R} W_r[n][k] x_r[b][k] )
+ *
+ * for every rank s, fp32 accumulation, ranks summed in order 0..R-1.
+ *   W_r  symmetric bf16 pointer; rank r's N x (K/R) row-major column block.
+ *   x_r  symmetric bf16 pointer; rank r's B x (K/R) row-major activations.
+ *   y    symmetric bf16 pointer; B x N row-major output, written in every slot.
+ *   R    must equal the handle's rank count.
+ *   N    output rows (>= 0).   K  TOTAL reduction length: K % R == 0 and
+ *        (K/R) % 8 == 0 (rows are read in 16-byte vectors).  K == 0 writes +0.
+ *   B    batch columns, 0..SYMM_MAX_BATCH.  N == 0 or B == 0 is a no-op.
+ * Requirements: W_r, x_r, y 16-byte aligned inside slot 0's user region; y
+ * must not overlap W_r or x_r; 4*B*N <= scratch bytes per slot; the number of
+ * row tiles fits the signal pad (else SYMM_ERANGE).
+ * Results are deterministic (fixed intra-tile and rank order) and bitwise
+ * identical across the R output slots.  Errors: SYMM_EINVAL, SYMM_ERANGE,
+ * SYMM_ECUDA; device-side protocol errors via symm_status.
+ */
+int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N,
+                    int K, int B, symm_stream_t stream);
+
+/*
+ * symm_status -- synchronise `stream`, read the device status word, clear it.
+ *   code  out: SYMM_OK, or SYMM_EPROTO when a launch found a stale or missing
+ *         tile flag or an out-of-range arrival ticket (e.g. two launches on
+ *         the handle overlapped on different streams).
+ *   rank, tile  out: where it was detected (-1 if none).
+ * After an error the signal pad's flags and counters are reset so the handle
+ * is usable again.  Returns SYMM_OK if the status could be read (whatever
+ * `code` says), SYMM_ECUDA otherwise.
+ */
+int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile);
+
+/*
+ * symm_check_guards -- verify the guard bands around every slot's user
+ * region, scratch region and signal pad (synchronises the device).
+ * Returns SYMM_OK, or SYMM_ECORRUPT with *bad_rank / *bad_band set
+ * (band 0: after the user region, 1: after scratch, 2: after the pad).
+ */
+int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band);
+
+/* Per-handle options (defaults 0). */
+enum {
+    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto, 1 FFMA kernel, 2 tensor-core kernel */
+    SYMM_OPT_TILE_ORDER = 2   /* 0 tile-major CTA order, 1 reversed (tests arrival order) */
+};
+int symm_set_option(symm_handle_t *h, int option, int value);
+
+/* Capacities of the handle: ranks, user/scratch/pad bytes per slot, and the
+ * number of row tiles the signal pad can hold. */
+typedef struct {
+    int R;
+    int device;
+    size_t stride, slot_bytes, scratch_bytes, signal_pad_bytes;
+    int max_tiles;
+} symm_info_t;
+int symm_info(symm_handle_t *h, symm_info_t *info);
+
+/* Row-tile height the chosen GEMV kernel uses for batch B (0 if B invalid);
+ * the tile count ceil(N / rows) must fit max_tiles. */
+int symm_gemv_rows_per_tile(symm_handle_t *h, int B);
+
+/* Release the handle; frees owned memory (synchronises the device first). */
+int symm_free(symm_handle_t *h);
+
+/* Last error message of the calling thread ("" if none). */
+const char *symm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SYMM_GEMV_H */

@@ -93,6 +93,20 @@ uint16_t oracle_bf16_round(double v) {
     return (uint16_t)(sign | (uint16_t)word);
 }
 
+/* Decoded value of every bf16 word, filled once from oracle_bf16_value; the
+ * sums below look values up here instead of re-decoding each element. */
+static double g_bf16_table[65536];
+static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
+
+static void fill_table(void) {
+    for (uint32_t h = 0; h < 65536u; ++h) g_bf16_table[h] = oracle_bf16_value((uint16_t)h);
+}
+
+static const double *bf16_table(void) {
+    pthread_once(&g_table_once, fill_table);
+    return g_bf16_table;
+}
+
 /* ------------------------------------------------------ GEMV + all-reduce */
 
 typedef struct {
@@ -109,9 +123,10 @@ typedef struct {
 static double rank_partial(const gemv_job *g, int r, int b, int n) {
     const uint16_t *w = g->W + ((size_t)r * g->N + n) * g->Kr;
     const uint16_t *xv = g->x + ((size_t)r * g->B + b) * g->Kr;
+    const double *val = bf16_table();
     double p = 0.0;
     for (int k = 0; k < g->Kr; ++k)
-        p += oracle_bf16_value(w[k]) * oracle_bf16_value(xv[k]);
+        p += val[w[k]] * val[xv[k]];
     return p;
 }
 
@@ -219,9 +234,10 @@ typedef struct {
 
 static void *ar_worker(void *arg) {
     ar_job *a = (ar_job *)arg;
+    const double *val = bf16_table();
     for (size_t i = a->lo; i < a->hi; ++i) {
         double s = 0.0;
-        for (int j = 0; j < a->R; ++j) s += oracle_bf16_value(a->in[(size_t)a->order[j] * a->n + i]);
+        for (int j = 0; j < a->R; ++j) s += val[a->in[(size_t)a->order[j] * a->n + i]];
         a->ref[i] = s;
         if (a->out) {
             uint16_t h = oracle_bf16_round(s);

@@ -1,0 +1,89 @@
+"""The C-ABI library loads and exports every declared entry point; host-only
+validation works without a GPU (no compute calls here)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import collective_split_gemv_gb300 as csg
+from collective_split_gemv_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "symm_gemv.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    names = re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{]*\)\s*;", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return csg.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("symm_alloc", "symm_rendezvous", "one_shot_all_reduce", "gemv_all_reduce",
+                     "symm_status", "symm_free", "symm_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in csg.EXPORTED, f"{name} has no Python binding"
+
+
+def test_layout_arithmetic(lib):
+    stride, total = csg.symm_layout(8, 1000, 4096, 4096)
+    assert stride % (2 << 20) == 0 and stride >= 1000 + 4096 + 4096 + 3 * 4096
+    assert total == 8 * stride
+    stride2, _ = csg.symm_layout(1, 5 << 20, 0, 65536)
+    assert stride2 == 6 << 20
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 1024, 0, 4096), csg.SYMM_EINVAL),
+    ((65, 1024, 0, 4096), csg.SYMM_EINVAL),
+    ((2, 0, 0, 4096), csg.SYMM_EINVAL),
+    ((2, 1024, 0, 100), csg.SYMM_EINVAL),
+])
+def test_layout_rejects(lib, args, code):
+    with pytest.raises(csg.SymmError) as e:
+        csg.symm_layout(*args)
+    assert e.value.code == code
+    assert csg.symm_last_error()
+
+
+def test_null_handle_is_rejected(lib):
+    for call in (lambda: csg.gemv_all_reduce(None, 0, 0, 0, 2, 8, 16, 1),
+                 lambda: csg.one_shot_all_reduce(None, 0, 0, 2, 8),
+                 lambda: csg.symm_status(None),
+                 lambda: csg.symm_set_option(None, 1, 0)):
+        with pytest.raises(csg.SymmError) as e:
+            call()
+        assert e.value.code == csg.SYMM_EINVAL
+    csg.symm_free(None)   # freeing NULL is a no-op
+
+
+def test_alloc_without_gpu_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(csg.SymmError) as e:
+        csg.symm_alloc(2, 1024, 1024, 4096)
+    assert e.value.code in (csg.SYMM_ECUDA, csg.SYMM_ENOMEM)
+
+
+def test_library_is_sm103a_only():
+    assert any("compute_103a,code=sm_103a" in f for f in _build.NVCC_FLAGS)
+    assert not any("sm_90" in f or "sm_100" in f for f in _build.NVCC_FLAGS)

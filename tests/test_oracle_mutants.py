@@ -19,8 +19,7 @@ MUTANTS = [
     ("drop_last_k", "for (int k = 0; k < g->Kr; ++k)", "for (int k = 0; k < g->Kr - 1; ++k)"),
     ("w_row_uses_b", "g->W + ((size_t)r * g->N + n) * g->Kr", "g->W + ((size_t)r * g->N + b) * g->Kr"),
     ("x_always_rank0", "g->x + ((size_t)r * g->B + b) * g->Kr", "g->x + ((size_t)0 * g->B + b) * g->Kr"),
-    ("negated_product", "p += oracle_bf16_value(w[k]) * oracle_bf16_value(xv[k]);",
-     "p -= oracle_bf16_value(w[k]) * oracle_bf16_value(xv[k]);"),
+    ("negated_product", "p += val[w[k]] * val[xv[k]];", "p -= val[w[k]] * val[xv[k]];"),
     ("ties_away", "(rem == half && (keep & 1))", "(rem == half)"),
     ("truncate", "if (rem > half || (rem == half && (keep & 1))) keep += 1;", "(void)half;"),
     ("decode_exponent_off", "ldexp((double)(128 + m), e - 134)", "ldexp((double)(128 + m), e - 133)"),

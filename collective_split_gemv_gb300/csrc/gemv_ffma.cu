@@ -163,7 +163,7 @@ template <int B>
 cudaError_t launch_b(const GemvArgs &a, cudaStream_t s) {
     const size_t smem = ffma_smem_bytes(B, a.kc_cap);
     auto kern = gemv_ar_ffma_kernel<B>;
-    if (smem > 48 * 1024) {
+    if (smem > 46 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
@@ -192,10 +192,11 @@ int ffma_rows_per_tile(int B) {
 size_t ffma_smem_bytes(int B, int kc_cap) { return (size_t)B * 2 * (size_t)kc_cap * sizeof(float4); }
 
 // Chunks of x staged per pass: all of K/R when B * K/R * 4 bytes fit in
-// 48 KB, otherwise passes of that size.
+// 46 KB (the default 48 KB limit also covers the kernel's static shared
+// memory), otherwise passes of that size.
 int ffma_kc_cap(int B, int Kr) {
     const int nchunk = Kr / 8;
-    const int cap = (48 * 1024) / (B * 2 * (int)sizeof(float4));
+    const int cap = (46 * 1024) / (B * 2 * (int)sizeof(float4));
     return nchunk < 1 ? 1 : (nchunk < cap ? nchunk : cap);
 }
 

@@ -262,7 +262,12 @@ def test_corrupted_counter_is_reported_and_recovered():
         assert code == csg.SYMM_EPROTO and tile == 0, (code, rank, tile)
         y = ws.read_y()
         rows = csg.symm_gemv_rows_per_tile(ws.h, B)
-        assert np.all(y[:, :, :rows] == 0xFFFF)               # tile 0 was not stored
+        # Tile 0's first arriver holds the "last" ticket.  It stores nothing
+        # if some peer's flag is still stale; if every peer had already
+        # published (flags are set before tickets are taken) its sum is the
+        # correct one.  Either way nothing else changes.
+        t0 = y[:, :, :rows]
+        assert np.all(t0 == 0xFFFF) or np.array_equal(t0, y1[:, :, :rows])
         assert np.array_equal(y[:, :, rows:], y1[:, :, rows:])  # other tiles unaffected
         ws.run(s)                                 # the handle recovered
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK

@@ -34,7 +34,7 @@ SYMM_MAX_BATCH = 16
 SYMM_OPT_GEMV_PATH = 1
 SYMM_OPT_TILE_ORDER = 2
 
-GEMV_PATH_AUTO, GEMV_PATH_FFMA = 0, 1
+GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC = 0, 1, 2
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",

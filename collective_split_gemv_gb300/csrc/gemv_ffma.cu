@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a
         for (int b = 0; b < B; ++b)
             if (rowok[g] && lane == ((g * B + b) & 31)) P[(size_t)b * a.N + row0 + g] = acc[g][b];
 
-    publish_and_reduce(a, t, r);
+    publish_and_reduce(a, t, r, 0);
 }
 
 template <int B>

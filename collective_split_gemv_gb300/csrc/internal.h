@@ -17,18 +17,27 @@ constexpr int kStatusCode = 0, kStatusRank = 1, kStatusTile = 2, kStatusEpoch = 
 constexpr int kProtoStaleFlag = 1;    // device codes; host maps them to SYMM_EPROTO
 constexpr int kProtoBadTicket = 2;
 
+constexpr int kProtoTimeout = 3;      // a bounded wait inside a kernel gave up
+
 // Arguments of one fused GEMV + all-reduce launch.  Every pointer is the
 // slot-0 instance; rank r's instance is ptr + r * stride bytes.
+//
+// A tile's contributors are the (rank r, K-split s) pairs, r < R, s < splits:
+// contributor (r, s) sums k in its split of rank r's K/R columns, writes the
+// fp32 partial to scratch + r * stride + s * partial_stride ([B][N]) and
+// publishes flags_r[t * splits + s].
 struct GemvArgs {
     const uint8_t *W;        // bf16 [N][Kr]
     const uint8_t *x;        // bf16 [B][Kr]
     uint8_t *y;              // bf16 [B][N]
-    uint8_t *scratch;        // fp32 [B][N] partial of the slot's rank
+    uint8_t *scratch;        // fp32 [splits][B][N] partials of the slot's rank
     uint32_t *flags;         // [max_tiles]
     uint32_t *counters;      // [max_tiles], slot 0
     uint32_t *status;        // [4], slot 0
     long long stride;        // bytes between slots
+    long long partial_stride;  // bytes between the splits' partial arrays (4 * B * N)
     int R, N, Kr, B;
+    int splits;              // K-splits per rank (1 for the FFMA kernel)
     int rows_per_tile;
     int num_tiles;
     int kc_cap;              // 16-byte chunks of x staged in shared memory per pass
@@ -52,5 +61,14 @@ int ffma_rows_per_tile(int B);
 size_t ffma_smem_bytes(int B, int kc_cap);
 int ffma_kc_cap(int B, int Kr);
 cudaError_t launch_gemv_ffma(const GemvArgs &a, cudaStream_t s);
+
+// Tensor-core (tcgen05 + TMA) fused kernel: 128-row tiles, batch padded to 16.
+constexpr int kTcRows = 128;
+constexpr int kTcBlockK = 64;
+// Encodes the TMA descriptors for this launch (cached by the caller) and
+// launches.  `maps` points at two CUtensorMap objects (W, x), 64-byte aligned.
+int tc_encode_maps(const GemvArgs &a, void *maps);
+cudaError_t launch_gemv_tc(const GemvArgs &a, const void *maps, cudaStream_t s);
+size_t tc_smem_bytes();
 
 }  // namespace symm

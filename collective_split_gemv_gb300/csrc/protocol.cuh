@@ -1,17 +1,21 @@
 // Device-side pieces shared by the fused GEMV kernels: streaming loads,
 // bf16 unpacking, and the publish / last-arriver reduction protocol.
 //
-// Protocol (one row tile t, R contributing CTAs, one per rank):
-//  1. every thread stores its share of the rank's fp32 partial into the
-//     rank's scratch slot, then fences (gpu scope);
-//  2. after a CTA barrier, thread 0 release-stores flag_r[t] = epoch and takes
-//     an arrival ticket with an acq_rel atomic add on counter[t];
-//  3. tickets are monotone across launches: launch `epoch` owns tickets
-//     (epoch-1)*R .. epoch*R-1; the holder of the last one is the reducer.  A
-//     ticket outside that range latches a protocol error instead;
-//  4. the reducer acquires the R flags (each must equal epoch), sums the R
-//     partials in rank order 0..R-1 in fp32, rounds to bf16 (RNE) and stores
-//     the value into every rank's output slot.
+// Protocol (one row tile t, C = R * splits contributing CTAs: one per rank
+// and K-split):
+//  1. every thread stores its share of the contributor's fp32 partial into
+//     the rank's scratch slot, then fences (gpu scope);
+//  2. after a CTA barrier, thread 0 release-stores the contributor's flag
+//     (epoch) and takes an arrival ticket with an acq_rel atomic add on
+//     counter[t];
+//  3. tickets are monotone across launches of one geometry (the host resets
+//     the pad when the tile count or C changes): launch `epoch` owns tickets
+//     (epoch-1)*C .. epoch*C-1 and the holder of the last one is the
+//     reducer.  A ticket outside that range latches a protocol error;
+//  4. the reducer acquires the C flags (each must equal epoch), sums the C
+//     partials in fixed order (rank 0..R-1, split 0..splits-1) in fp32,
+//     rounds to bf16 (RNE) and stores the value into every rank's output
+//     slot.
 // No CTA ever waits for another: a tile whose contributors have not all
 // arrived is finished by whichever contributor arrives last.
 //
@@ -89,38 +93,42 @@ __device__ __forceinline__ void latch_status(uint32_t *status, int code, int ran
 }
 
 // Steps 2-4 of the protocol.  Called by ALL threads of the CTA after each
-// thread has stored its part of rank r's partial for tile t.
-__device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int r) {
+// thread has stored its part of contributor (r, s)'s partial for tile t.
+__device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int r, int s) {
     __shared__ int s_last;
     __shared__ int s_bad;
+    const int S = a.splits;
+    const uint32_t C = (uint32_t)a.R * (uint32_t)S;   // contributors per tile
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
-                                                      (long long)r * a.stride) + t;
+                                                      (long long)r * a.stride) + (size_t)t * S + s;
         st_release_gpu(flag, a.epoch);
-        uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
-        uint32_t first = (a.epoch - 1u) * (uint32_t)a.R;
-        uint32_t pos = ticket - first;
-        if (pos >= (uint32_t)a.R) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
-        s_last = (pos == (uint32_t)a.R - 1u);
+        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
+        const uint32_t pos = ticket - (a.epoch - 1u) * C;
+        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
+        s_last = (pos == C - 1u);
         s_bad = 0;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (threadIdx.x < (unsigned)a.R) {
+    for (uint32_t i = threadIdx.x; i < C; i += blockDim.x) {
+        const int q = (int)(i / (uint32_t)S);
+        const int qs = (int)(i % (uint32_t)S);
         const uint32_t *f = reinterpret_cast<const uint32_t *>(
-                                reinterpret_cast<const uint8_t *>(a.flags) +
-                                (long long)threadIdx.x * a.stride) + t;
+                                reinterpret_cast<const uint8_t *>(a.flags) + (long long)q * a.stride) +
+                            (size_t)t * S + qs;
         if (ld_acquire_gpu(f) != a.epoch) {
-            latch_status(a.status, kProtoStaleFlag, (int)threadIdx.x, t, a.epoch);
+            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
             s_bad = 1;
         }
     }
     __syncthreads();
     if (s_bad) return;
 
+    // Sum in fixed order: rank 0..R-1, and within a rank split 0..S-1.
     const int n0 = t * a.rows_per_tile;
     const int rows = min(a.rows_per_tile, a.N - n0);
     const int count = rows * a.B;
@@ -129,13 +137,16 @@ __device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int
         const int n = n0 + (i - b * rows);
         const size_t off = ((size_t)b * a.N + n) * sizeof(float);
         float acc = ld_relaxed_gpu_f32(reinterpret_cast<const float *>(a.scratch + off));
-        for (int q = 1; q < a.R; ++q)
-            acc += ld_relaxed_gpu_f32(
-                reinterpret_cast<const float *>(a.scratch + (long long)q * a.stride + off));
+        for (int j = 1; j < (int)C; ++j) {
+            const int q = j / S;
+            const int qs = j - q * S;
+            acc += ld_relaxed_gpu_f32(reinterpret_cast<const float *>(
+                a.scratch + (long long)q * a.stride + (long long)qs * a.partial_stride + off));
+        }
         const __nv_bfloat16 v = __float2bfloat16_rn(acc);
         const size_t yoff = ((size_t)b * a.N + n) * sizeof(__nv_bfloat16);
-        for (int s = 0; s < a.R; ++s)
-            *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)s * a.stride + yoff) = v;
+        for (int q = 0; q < a.R; ++q)
+            *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = v;
     }
 }
 

@@ -36,8 +36,19 @@ struct symm_handle {
     uint8_t *base = nullptr;
     bool owned = false;
     uint32_t epoch = 0;                       // epoch of the last GEMV launch
+    // Geometry of the launches since the last pad reset: tickets of launch e
+    // are (e-1)*C .. e*C-1 only while every launch uses the same tiles and C.
+    int geom_tiles = -1, geom_contrib = -1;
     int opt_gemv_path = 0;
     int opt_tile_order = 0;
+    // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
+    struct MapEntry {
+        const void *W = nullptr, *x = nullptr;
+        int N = 0, Kr = 0, B = 0;
+        alignas(64) unsigned char maps[2][128];
+    };
+    MapEntry map_cache[8];
+    int map_next = 0;
 };
 
 namespace {
@@ -126,20 +137,68 @@ int reset_protocol(symm_handle *h, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(signal pad)");
     }
     h->epoch = 0;
+    h->geom_tiles = -1;
+    h->geom_contrib = -1;
     return SYMM_OK;
 }
 
-int gemv_path(const symm_handle *h, int B) {
-    (void)B;
-    return h->opt_gemv_path == 0 ? 1 : h->opt_gemv_path;
+// Batch width from which the automatic choice is the tensor-core kernel.
+constexpr int kTcMinBatch = 5;
+
+int gemv_path(const symm_handle *h, int B, int Kr) {
+    if (h->opt_gemv_path != 0) return h->opt_gemv_path;
+    return (B >= kTcMinBatch && Kr > 0) ? 2 : 1;
 }
 
-int rows_per_tile_for(const symm_handle *h, int B) {
+int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
     if (B < 1 || B > SYMM_MAX_BATCH) return 0;
-    switch (gemv_path(h, B)) {
+    switch (gemv_path(h, B, Kr)) {
         case 1: return ffma_rows_per_tile(B);
+        case 2: return kTcRows;
         default: return 0;
     }
+}
+
+int num_sms(int device) {
+    static int cached_dev = -1, cached = 0;
+    if (device != cached_dev) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
+        cached = v;
+        cached_dev = device;
+    }
+    return cached;
+}
+
+// K-splits per rank for the tensor-core kernel: enough CTAs for two per SM
+// when the row tiles alone are too few, limited by K blocks, scratch and pad.
+int tc_splits(const symm_handle *h, int tiles, int N, int Kr, int B) {
+    const int kb_total = (Kr + kTcBlockK - 1) / kTcBlockK;
+    const long long base = (long long)tiles * h->R;
+    const int sms = num_sms(h->device);
+    int S = 1;
+    if (base < sms) S = (int)std::min<long long>((2LL * sms + base - 1) / base, 16);
+    S = std::max(1, std::min(S, kb_total));
+    while (S > 1 && ((size_t)S * B * N * 4 > h->scratch_bytes || (long long)tiles * S > h->max_tiles)) --S;
+    // no empty split: with kb_per = ceil(kb_total / S), use exactly ceil(kb_total / kb_per) splits
+    const int kb_per = (kb_total + S - 1) / S;
+    return std::max(1, (kb_total + kb_per - 1) / kb_per);
+}
+
+const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
+    for (auto &e : h->map_cache)
+        if (e.W == a.W && e.x == a.x && e.N == a.N && e.Kr == a.Kr && e.B == a.B) return e.maps;
+    auto &e = h->map_cache[h->map_next];
+    h->map_next = (h->map_next + 1) % 8;
+    e.W = nullptr;
+    *err = tc_encode_maps(a, e.maps);
+    if (*err != 0) return nullptr;
+    e.W = a.W;
+    e.x = a.x;
+    e.N = a.N;
+    e.Kr = a.Kr;
+    e.B = a.B;
+    return e.maps;
 }
 
 }  // namespace
@@ -248,7 +307,8 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     switch (option) {
         case SYMM_OPT_GEMV_PATH:
-            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma)", value);
+            if (value < 0 || value > 2)
+                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma, 2 tensor core)", value);
             h->opt_gemv_path = value;
             return SYMM_OK;
         case SYMM_OPT_TILE_ORDER:
@@ -260,7 +320,7 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
     }
 }
 
-int symm_gemv_rows_per_tile(symm_handle_t *h, int B) { return h ? rows_per_tile_for(h, B) : 0; }
+int symm_gemv_rows_per_tile(symm_handle_t *h, int B) { return h ? rows_per_tile_for(h, B, 8) : 0; }
 
 int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
@@ -307,19 +367,26 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
         return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
                     (size_t)B * (size_t)N * 4, h->scratch_bytes);
-    const int rows = rows_per_tile_for(h, B);
+    const int path = gemv_path(h, B, Kr);
+    const int rows = rows_per_tile_for(h, B, Kr);
     if (rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     const int tiles = (N + rows - 1) / rows;
     if (tiles > h->max_tiles)
         return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", tiles, h->max_tiles);
+    const int splits = path == 2 ? tc_splits(h, tiles, N, Kr, B) : 1;
     int rc = check_device(h);
     if (rc != SYMM_OK) return rc;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Tickets of launch e are (e-1)*R .. e*R-1 (mod 2^32); restart before e*R wraps.
-    if (((uint64_t)h->epoch + 1) * (uint64_t)h->R > 0xFFFFFFFFull || h->epoch == 0) {
+    // Tickets of launch e are (e-1)*C .. e*C-1 (C = R * splits contributors per
+    // tile): restart the pad when the geometry changes or before e*C wraps.
+    const int contrib = h->R * splits;
+    if (((uint64_t)h->epoch + 1) * (uint64_t)contrib > 0xFFFFFFFFull || h->epoch == 0 ||
+        tiles != h->geom_tiles || contrib != h->geom_contrib) {
         rc = reset_protocol(h, s);
         if (rc != SYMM_OK) return rc;
+        h->geom_tiles = tiles;
+        h->geom_contrib = contrib;
     }
     h->epoch += 1;
 
@@ -340,12 +407,26 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     a.num_tiles = tiles;
     a.epoch = h->epoch;
     a.reverse_order = h->opt_tile_order;
+    a.splits = splits;
+    a.partial_stride = (long long)B * N * 4;
+    a.kc_cap = 0;
     cudaError_t e = cudaSuccess;
-    switch (gemv_path(h, B)) {
+    switch (path) {
         case 1:
             a.kc_cap = ffma_kc_cap(B, Kr);
             e = launch_gemv_ffma(a, s);
             break;
+        case 2: {
+            if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
+            int err = 0;
+            const void *maps = tc_maps_for(h, a, &err);
+            if (!maps) {
+                h->epoch -= 1;
+                return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
+            }
+            e = launch_gemv_tc(a, maps, s);
+            break;
+        }
         default:
             return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     }

@@ -15,11 +15,11 @@ import synth
 from collective_split_gemv_gb300 import DeviceView
 from collective_split_gemv_gb300.workspace import GemvWorkspace
 from gpu_common import check_gemv, require_gpu, run_gemv
-from helpers import f64_to_words_via_f32, words_to_f64
+from helpers import f64_to_words_via_f32, tolerance_ratio, ulp_distance, words_to_f64
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA]
+PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -74,8 +74,7 @@ def test_every_batch_width(path, B):
     W, x = _normal_case(4, 77, 4 * 264, B, seed=100 + B)
     (y,), status = run_gemv(W, x, path=path)
     assert status[0] == csg.SYMM_OK
-    ratio, eq, ulp = check_gemv(W, x, y)
-    assert ulp <= 1
+    check_gemv(W, x, y)
 
 
 def test_x_staged_in_several_passes():
@@ -158,13 +157,18 @@ def test_full_size_workload(name):
     for s in range(1, R):
         assert np.array_equal(outs[0][s], outs[0][0])
     assert np.array_equal(outs[0], outs[1])
-    from helpers import tolerance_ratio, ulp_distance
     ratio = tolerance_ratio(words_to_f64(outs[0][0]), y_ref)
     eq = float(np.mean(outs[0][0] == y_or[0]))
-    ulp = int(ulp_distance(outs[0][0], y_or[0]).max())
-    print(f"{name}: tolerance ratio {ratio:.3f}, bit-equal {eq:.5f}, max ulp {ulp}")
+    # Away from zero the fp32 sum is within half a bf16 step of the fp64 one,
+    # so the rounded results differ by at most one step; near zero the fp32
+    # rounding error of a long sum can exceed a (tiny) bf16 step there.
+    big = np.abs(y_ref) >= 0.1 * np.sqrt(np.mean(y_ref ** 2))
+    ulp_all = int(ulp_distance(outs[0][0], y_or[0]).max())
+    ulp_big = int(ulp_distance(outs[0][0][big], y_or[0][big]).max())
+    print(f"{name}: tolerance ratio {ratio:.3f}, bit-equal {eq:.5f}, max ulp {ulp_all} "
+          f"({ulp_big} where |y| >= 0.1 rms)")
     assert ratio <= 1.0
-    assert eq >= 0.99 and ulp <= 1
+    assert eq >= 0.99 and ulp_big <= 1
     (y_rev,), _ = run_gemv(W, x, order=1)
     assert np.array_equal(y_rev, outs[0])
 
@@ -272,6 +276,30 @@ def test_corrupted_counter_is_reported_and_recovered():
         ws.run(s)                                 # the handle recovered
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
         check_gemv(W, x, ws.read_y())
+    finally:
+        ws.close()
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_shape_changes_on_one_handle(path):
+    """One handle, calls of different N and B (hence different tile counts and
+    K-splits) in a row: the signal pad's tickets stay consistent."""
+    R, N, K, B = 4, 700, 4 * 256, 8
+    W, x = _normal_case(R, N, K, B, seed=23)
+    ws = GemvWorkspace(R, N, K, B)
+    try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
+        ws.load_W(W)
+        ws.load_x(x)
+        s = torch.cuda.current_stream()
+        for n_rows, b in ((700, 8), (100, 8), (700, 3), (5, 16 if B >= 16 else 8), (700, 8)):
+            ws.fill_y(0xFF)
+            csg.gemv_all_reduce(ws.h, ws.W_ptr(), ws.x_ptr(), ws.y_ptr(), R, n_rows, K, b, s)
+            assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK, (n_rows, b)
+            y = ws.read_y().reshape(R, -1)[:, : b * n_rows].reshape(R, b, n_rows)
+            # the sub-problem: first n_rows rows of W, x rows 0..b-1 laid out
+            # with row stride K/R (x is [B][K/R], so rows 0..b-1 are a prefix)
+            check_gemv(np.ascontiguousarray(W[:, :n_rows]), np.ascontiguousarray(x[:, :b]), y)
     finally:
         ws.close()
 

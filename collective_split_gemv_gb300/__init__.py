@@ -38,7 +38,8 @@ GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC = 0, 1, 2
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
-            "symm_info", "symm_gemv_rows_per_tile", "symm_free", "symm_last_error")
+            "symm_info", "symm_gemv_rows_per_tile", "gemv_all_reduce_noalloc", "symm_free",
+            "symm_last_error")
 
 _lib = None
 
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.symm_set_option.argtypes = [vp, i, i]
         L.symm_info.argtypes = [vp, ctypes.POINTER(SymmInfo)]
         L.symm_gemv_rows_per_tile.argtypes = [vp, i]
+        L.gemv_all_reduce_noalloc.argtypes = [vp, vp, vp, sz, i, i, i, i, vp]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
         L.symm_last_error.restype = ctypes.c_char_p
@@ -173,6 +175,14 @@ def symm_info(h) -> dict:
 
 def symm_gemv_rows_per_tile(h, B: int) -> int:
     return lib().symm_gemv_rows_per_tile(h, B)
+
+
+def gemv_all_reduce_noalloc(W_r: int, x_r: int, y: int, stride: int, R: int, N: int, K: int, B: int,
+                            stream=None) -> None:
+    """The fused call for callers that cannot allocate device memory: works on
+    caller-owned tensors (rank r at ptr + r * stride) with the library's fixed
+    16 MiB working array instead of a handle."""
+    _check(lib().gemv_all_reduce_noalloc(_vp(W_r), _vp(x_r), _vp(y), stride, R, N, K, B, _stream(stream)))
 
 
 def symm_free(h) -> None:

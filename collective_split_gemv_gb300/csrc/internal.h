@@ -45,6 +45,10 @@ struct GemvArgs {
     int reverse_order;       // 1: CTAs take work in reverse (arrival-order tests)
 };
 
+// Sets the calling thread's last-error message (see symm_last_error) and
+// returns `code`.
+int report_error(int code, const char *msg);
+
 struct AllReduceArgs {
     const uint8_t *in;       // bf16 [n], slot 0
     uint8_t *out;            // bf16 [n], slot 0

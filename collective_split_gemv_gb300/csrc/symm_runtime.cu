@@ -203,6 +203,11 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 
 }  // namespace
 
+namespace symm {
+// Lets other translation units of the library report through symm_last_error.
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace symm
+
 extern "C" {
 
 const char *symm_last_error(void) { return g_err; }

@@ -213,6 +213,43 @@ int symm_info(symm_handle_t *h, symm_info_t *info);
  * the tile count ceil(N / rows) must fit max_tiles. */
 int symm_gemv_rows_per_tile(symm_handle_t *h, int B);
 
+/*
+ * gemv_all_reduce_noalloc -- the fused GEMV + one-shot all-reduce for callers
+ * that cannot allocate device memory: code whose device memory is owned by
+ * another allocator (a framework's caching allocator, a serving process with
+ * a fixed memory budget), or that runs on a hot path where cudaMalloc's
+ * implicit synchronisation is not allowed.  Such a caller cannot create a
+ * handle, because symm_alloc allocates.
+ *
+ * The source pages have no counterpart of this call; it is an addition of
+ * this library.
+ *
+ * Same result as gemv_all_reduce (y_s = bf16_rne(sum_r W_r x_r), fp32
+ * accumulation, ranks summed in order 0..R-1, every rank's y written), on
+ * tensors the caller owns: rank r's W_r, x_r and y are at W_r + r * stride,
+ * x_r + r * stride and y + r * stride (bytes).  Layouts as for
+ * gemv_all_reduce; pointers and stride 16-byte aligned; no instance of y may
+ * overlap an instance of W_r or x_r.  R in 1..64, B in 0..16, K % R == 0,
+ * (K/R) % 8 == 0; N == 0 or B == 0 is a no-op.
+ *
+ * Working memory: a fixed 16 MiB device array inside this library (present
+ * on every GPU that loads the library until the process exits).  It holds the
+ * fp32 partials of all ranks (4 * R * B * N bytes, rounded up to 256) plus one
+ * 4-byte counter per row tile; larger problems return SYMM_ERANGE.  No
+ * cudaMalloc, cudaFree or allocating library call is made.
+ *
+ * Every call on a device shares that array and it keeps the last call's
+ * contents (the counters are cleared by a stream-ordered memset at the start
+ * of each call).  Calls that overlap on the GPU race on the array: issue them
+ * on one stream.  The first call on each device, with that device current,
+ * looks up the array's address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.
+ *
+ * Returns SYMM_OK after enqueueing, SYMM_EINVAL, SYMM_ERANGE or SYMM_ECUDA.
+ */
+int gemv_all_reduce_noalloc(const void *W_r, const void *x_r, void *y, size_t stride, int R, int N, int K,
+                            int B, symm_stream_t stream);
+
 /* Release the handle; frees owned memory (synchronises the device first). */
 int symm_free(symm_handle_t *h);
 

@@ -195,6 +195,8 @@ def run_ours(args, rank, world, local_rank):
     w_total = W.nbytes
     copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(w_total, 1))))
     ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
+    paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC}
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path])
     for c in range(copies):
         ws.load_W(W, copy=c)
     ws.load_x(x)
@@ -297,7 +299,8 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = measured_hbm_peak()
     achieved = nbytes / (mean_launch_ms * 1e-3) / 1e9
-    kernel = "gemv_ar_ffma_kernel"
+    kernel = {"ffma": "gemv_ar_ffma_kernel", "tc": "gemv_ar_tc_kernel"}.get(
+        args.gemv_path, "gemv_ar_tc_kernel" if B >= 5 else "gemv_ar_ffma_kernel")
     line = {
         "metric": METRIC,
         "value": round(world * nbytes / (step_ms * 1e-3) / 1e9, 2),
@@ -437,6 +440,8 @@ def main():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="mlp_down_decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc"), default="auto",
+                   help="force the CUDA-core or the tensor-core kernel (measurement only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     args = p.parse_args()
     if args.warmup < 3:

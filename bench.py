@@ -162,6 +162,15 @@ def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
     return None
 
 
+def kernel_name(plan):
+    if plan["path"] == 1:
+        return "gemv_ar_ffma_kernel"
+    if plan["path"] == 2:
+        return "gemv_ar_tc_kernel"
+    engine = "tcgen05" if plan["engine"] == 0 else "ffma"
+    return f"gemv_ar_sk_kernel<{engine},slabs={plan['slabs']}>"
+
+
 def kernel_source_sha():
     import hashlib
 
@@ -195,8 +204,12 @@ def run_ours(args, rank, world, local_rank):
     w_total = W.nbytes
     copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(w_total, 1))))
     ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
-    paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC}
+    paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
+             "sk": csg.GEMV_PATH_SK}
     csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path])
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, args.sk_slabs)
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, args.sk_engine)
+    plan = csg.symm_gemv_plan(ws.h, N, K, B)
     for c in range(copies):
         ws.load_W(W, copy=c)
     ws.load_x(x)
@@ -299,8 +312,7 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = measured_hbm_peak()
     achieved = nbytes / (mean_launch_ms * 1e-3) / 1e9
-    kernel = {"ffma": "gemv_ar_ffma_kernel", "tc": "gemv_ar_tc_kernel"}.get(
-        args.gemv_path, "gemv_ar_tc_kernel" if B >= 5 else "gemv_ar_ffma_kernel")
+    kernel = kernel_name(plan)
     line = {
         "metric": METRIC,
         "value": round(world * nbytes / (step_ms * 1e-3) / 1e9, 2),
@@ -324,6 +336,7 @@ def run_ours(args, rank, world, local_rank):
                    f"inputs larger than L2: {copies} rotating copies of W ({working_set / 1e9:.2f} GB)"),
             "parallelism": "R ranks as symmetric slots on one GPU" + (f"; {world} independent replicas"
                                                                      if world > 1 else ""),
+            "plan": plan,
         },
         "roofline": {
             "bound": "hbm",
@@ -440,8 +453,12 @@ def main():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="mlp_down_decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc"), default="auto",
-                   help="force the CUDA-core or the tensor-core kernel (measurement only)")
+    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk"), default="auto",
+                   help="force one kernel (measurement only)")
+    p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 4),
+                   help="stream-K slabs per pipeline stage (0 = library default)")
+    p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
+                   help="stream-K engine: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     args = p.parse_args()
     if args.warmup < 3:

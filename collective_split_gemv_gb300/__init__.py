@@ -33,12 +33,14 @@ SYMM_MAX_BATCH = 16
 
 SYMM_OPT_GEMV_PATH = 1
 SYMM_OPT_TILE_ORDER = 2
+SYMM_OPT_SK_SLABS = 3
+SYMM_OPT_SK_ENGINE = 4
 
-GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC = 0, 1, 2
+GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK = 0, 1, 2, 3
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
-            "symm_info", "symm_gemv_rows_per_tile", "gemv_all_reduce_noalloc", "symm_free",
+            "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "symm_free",
             "symm_last_error")
 
 _lib = None
@@ -54,6 +56,11 @@ class SymmInfo(ctypes.Structure):
     _fields_ = [("R", ctypes.c_int), ("device", ctypes.c_int), ("stride", ctypes.c_size_t),
                 ("slot_bytes", ctypes.c_size_t), ("scratch_bytes", ctypes.c_size_t),
                 ("signal_pad_bytes", ctypes.c_size_t), ("max_tiles", ctypes.c_int)]
+
+
+class GemvPlan(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int) for k in ("path", "engine", "slabs", "rows_per_tile", "tiles", "splits",
+                                            "grid", "parts_max", "kblocks")]
 
 
 def library_path() -> str:
@@ -78,7 +85,7 @@ def lib() -> ctypes.CDLL:
         L.symm_check_guards.argtypes = [vp, ctypes.POINTER(i), ctypes.POINTER(i)]
         L.symm_set_option.argtypes = [vp, i, i]
         L.symm_info.argtypes = [vp, ctypes.POINTER(SymmInfo)]
-        L.symm_gemv_rows_per_tile.argtypes = [vp, i]
+        L.symm_gemv_plan.argtypes = [vp, i, i, i, ctypes.POINTER(GemvPlan)]
         L.gemv_all_reduce_noalloc.argtypes = [vp, vp, vp, sz, i, i, i, i, vp]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
@@ -173,8 +180,12 @@ def symm_info(h) -> dict:
     return {k: getattr(info, k) for k, _ in SymmInfo._fields_}
 
 
-def symm_gemv_rows_per_tile(h, B: int) -> int:
-    return lib().symm_gemv_rows_per_tile(h, B)
+def symm_gemv_plan(h, N: int, K: int, B: int) -> dict:
+    """Kernel and launch geometry gemv_all_reduce would use (no launch)."""
+    plan = GemvPlan()
+    _check(lib().symm_gemv_plan(h, N, K, B, ctypes.byref(plan)))
+    return {k: getattr(plan, k) for k, _ in GemvPlan._fields_}
+
 
 
 def gemv_all_reduce_noalloc(W_r: int, x_r: int, y: int, stride: int, R: int, N: int, K: int, B: int,

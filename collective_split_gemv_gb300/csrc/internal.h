@@ -18,6 +18,7 @@ constexpr int kProtoStaleFlag = 1;    // device codes; host maps them to SYMM_EP
 constexpr int kProtoBadTicket = 2;
 
 constexpr int kProtoTimeout = 3;      // a bounded wait inside a kernel gave up
+constexpr int kMaxRanks = 64;
 
 // Arguments of one fused GEMV + all-reduce launch.  Every pointer is the
 // slot-0 instance; rank r's instance is ptr + r * stride bytes.
@@ -74,5 +75,20 @@ constexpr int kTcBlockK = 64;
 int tc_encode_maps(const GemvArgs &a, void *maps);
 cudaError_t launch_gemv_tc(const GemvArgs &a, const void *maps, cudaStream_t s);
 size_t tc_smem_bytes();
+
+// Persistent stream-K kernel (TMA ring; tcgen05 or FFMA engine).  The U = T*R
+// units of KB K-blocks each form one sequence of total = U*KB blocks, cut into
+// G equal contiguous ranges (one per CTA).  Pmax bounds the parts a unit is
+// cut into; partial p of unit (t, r) lives at scratch_r + p * partial_stride
+// and its flag at flags_r[t * Pmax + p].
+struct SkGeom {
+    long long total;
+    int KB;
+    int G;
+    int Pmax;
+};
+int sk_block_k(int slabs);
+cudaError_t launch_gemv_sk(const GemvArgs &a, const SkGeom &geo, const void *maps, int engine, int slabs,
+                           cudaStream_t s);
 
 }  // namespace symm

@@ -37,10 +37,13 @@ struct symm_handle {
     bool owned = false;
     uint32_t epoch = 0;                       // epoch of the last GEMV launch
     // Geometry of the launches since the last pad reset: tickets of launch e
-    // are (e-1)*C .. e*C-1 only while every launch uses the same tiles and C.
-    int geom_tiles = -1, geom_contrib = -1;
+    // are (e-1)*C_t .. e*C_t-1 only while every launch has the same tiles and
+    // contributors per tile.
+    uint64_t geom_key = 0;
     int opt_gemv_path = 0;
     int opt_tile_order = 0;
+    int opt_sk_slabs = 0;
+    int opt_sk_engine = -1;
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -137,26 +140,8 @@ int reset_protocol(symm_handle *h, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(signal pad)");
     }
     h->epoch = 0;
-    h->geom_tiles = -1;
-    h->geom_contrib = -1;
+    h->geom_key = 0;
     return SYMM_OK;
-}
-
-// Batch width from which the automatic choice is the tensor-core kernel.
-constexpr int kTcMinBatch = 5;
-
-int gemv_path(const symm_handle *h, int B, int Kr) {
-    if (h->opt_gemv_path != 0) return h->opt_gemv_path;
-    return (B >= kTcMinBatch && Kr > 0) ? 2 : 1;
-}
-
-int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
-    if (B < 1 || B > SYMM_MAX_BATCH) return 0;
-    switch (gemv_path(h, B, Kr)) {
-        case 1: return ffma_rows_per_tile(B);
-        case 2: return kTcRows;
-        default: return 0;
-    }
 }
 
 int num_sms(int device) {
@@ -169,6 +154,70 @@ int num_sms(int device) {
     }
     return cached;
 }
+
+// Kernels: 1 CUDA-core, one CTA per (tile, rank), 128-bit loads;
+// 2 tensor-core, one CTA per (tile, rank, K-split); 3 persistent stream-K
+// (TMA ring, tcgen05 engine or, for B <= kSkFfmaMaxBatch, FFMA engine).
+// The automatic choice is 3 whenever K > 0.
+constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3;
+constexpr int kSkFfmaMaxBatch = 2;
+
+int gemv_path(const symm_handle *h, int B, int Kr) {
+    (void)B;
+    if (h->opt_gemv_path != 0) return h->opt_gemv_path;
+    return Kr > 0 ? kPathSk : kPathFfma;
+}
+
+int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
+    if (B < 1 || B > SYMM_MAX_BATCH) return 0;
+    switch (gemv_path(h, B, Kr)) {
+        case kPathFfma: return ffma_rows_per_tile(B);
+        case kPathTc: return kTcRows;
+        case kPathSk: return kTcRows;
+        default: return 0;
+    }
+}
+
+int sk_engine(const symm_handle *h, int B) {
+    if (h->opt_sk_engine >= 0) return (h->opt_sk_engine == 1 && B > kSkFfmaMaxBatch) ? 0 : h->opt_sk_engine;
+    return B <= kSkFfmaMaxBatch ? 1 : 0;
+}
+
+int sk_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }
+
+// CTA whose range holds block g (same arithmetic as the kernel).
+int sk_cta_of_block(long long g, long long total, int G) {
+    return (int)(((g + 1) * (long long)G + total - 1) / total) - 1;
+}
+
+// Stream-K geometry: G <= SM count CTAs over total = tiles * R * KB blocks,
+// shrunk until the parts per unit fit the scratch region and the signal pad.
+bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slabs, SkGeom *geo) {
+    const long long KB = (Kr + sk_block_k(slabs) - 1) / sk_block_k(slabs);
+    const long long units = (long long)tiles * h->R;
+    const long long total = units * KB;
+    if (total <= 0 || KB > (1LL << 30)) return false;
+    long long G = std::min<long long>(total, num_sms(h->device));
+    const size_t part_bytes = (size_t)B * N * 4;
+    while (G >= 1) {
+        int pmax = 1;
+        for (long long u = 0; u < units; ++u) {
+            const int P = sk_cta_of_block((u + 1) * KB - 1, total, (int)G) - sk_cta_of_block(u * KB, total, (int)G) + 1;
+            pmax = std::max(pmax, P);
+        }
+        if ((size_t)pmax * part_bytes <= h->scratch_bytes && (long long)tiles * pmax <= h->max_tiles) {
+            geo->total = total;
+            geo->KB = (int)KB;
+            geo->G = (int)G;
+            geo->Pmax = pmax;
+            return true;
+        }
+        if (G == 1) break;
+        G = std::max<long long>(1, G * 3 / 4);
+    }
+    return false;
+}
+
 
 // K-splits per rank for the tensor-core kernel: enough CTAs for two per SM
 // when the row tiles alone are too few, limited by K blocks, scratch and pad.
@@ -199,6 +248,35 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
     e.Kr = a.Kr;
     e.B = a.B;
     return e.maps;
+}
+
+// The kernel and launch geometry gemv_all_reduce would use.
+struct Plan {
+    int path = 0, engine = 0, slabs = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
+    SkGeom geo = {0, 0, 0, 1};
+};
+
+int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
+    if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
+        return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
+                    (size_t)B * (size_t)N * 4, h->scratch_bytes);
+    pl->path = gemv_path(h, B, Kr);
+    pl->rows = rows_per_tile_for(h, B, Kr);
+    if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
+    pl->tiles = (N + pl->rows - 1) / pl->rows;
+    if (pl->tiles > h->max_tiles)
+        return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", pl->tiles, h->max_tiles);
+    pl->splits = pl->path == kPathTc ? tc_splits(h, pl->tiles, N, Kr, B) : 1;
+    pl->grid = pl->tiles * h->R * pl->splits;
+    if (pl->path == kPathSk) {
+        if (Kr == 0) return fail(SYMM_EINVAL, "the stream-K kernel needs K > 0");
+        pl->engine = sk_engine(h, B);
+        pl->slabs = sk_slabs(h);
+        if (!sk_geometry(h, pl->tiles, N, Kr, B, pl->slabs, &pl->geo))
+            return fail(SYMM_ERANGE, "stream-K partials do not fit the scratch region or the signal pad");
+        pl->grid = pl->geo.G;
+    }
+    return SYMM_OK;
 }
 
 }  // namespace
@@ -312,20 +390,46 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     switch (option) {
         case SYMM_OPT_GEMV_PATH:
-            if (value < 0 || value > 2)
-                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma, 2 tensor core)", value);
+            if (value < 0 || value > 3)
+                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma, 2 tensor core, 3 stream-K)", value);
             h->opt_gemv_path = value;
             return SYMM_OK;
         case SYMM_OPT_TILE_ORDER:
             if (value < 0 || value > 1) return fail(SYMM_EINVAL, "tile order %d unknown", value);
             h->opt_tile_order = value;
             return SYMM_OK;
+        case SYMM_OPT_SK_SLABS:
+            if (value != 0 && value != 1 && value != 2 && value != 4)
+                return fail(SYMM_EINVAL, "stream-K slabs %d not in {0 auto, 1, 2, 4}", value);
+            h->opt_sk_slabs = value;
+            return SYMM_OK;
+        case SYMM_OPT_SK_ENGINE:
+            if (value < -1 || value > 1) return fail(SYMM_EINVAL, "stream-K engine %d not in {-1 auto, 0, 1}", value);
+            h->opt_sk_engine = value;
+            return SYMM_OK;
         default:
             return fail(SYMM_EINVAL, "unknown option %d", option);
     }
 }
 
-int symm_gemv_rows_per_tile(symm_handle_t *h, int B) { return h ? rows_per_tile_for(h, B, 8) : 0; }
+int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out) {
+    if (!h || !out) return fail(SYMM_EINVAL, "NULL argument");
+    if (N < 1 || K < 0 || B < 1 || B > SYMM_MAX_BATCH || K % h->R || (K / h->R) % 8)
+        return fail(SYMM_EINVAL, "no plan for N=%d K=%d B=%d on %d ranks", N, K, B, h->R);
+    Plan pl;
+    int rc = make_plan(h, N, K / h->R, B, &pl);
+    if (rc != SYMM_OK) return rc;
+    out->path = pl.path;
+    out->engine = pl.engine;
+    out->slabs = pl.slabs;
+    out->rows_per_tile = pl.rows;
+    out->tiles = pl.tiles;
+    out->splits = pl.splits;
+    out->grid = pl.grid;
+    out->parts_max = pl.geo.Pmax;
+    out->kblocks = pl.geo.KB;
+    return SYMM_OK;
+}
 
 int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
@@ -369,29 +473,30 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     if (!aligned16(W_r) || !aligned16(x_r) || !aligned16(y)) return fail(SYMM_EINVAL, "W_r, x_r and y must be 16-byte aligned");
     if (overlaps(y, ybytes, W_r, wbytes) || overlaps(y, ybytes, x_r, xbytes))
         return fail(SYMM_EINVAL, "y overlaps W_r or x_r");
-    if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
-        return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
-                    (size_t)B * (size_t)N * 4, h->scratch_bytes);
-    const int path = gemv_path(h, B, Kr);
-    const int rows = rows_per_tile_for(h, B, Kr);
-    if (rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
-    const int tiles = (N + rows - 1) / rows;
-    if (tiles > h->max_tiles)
-        return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", tiles, h->max_tiles);
-    const int splits = path == 2 ? tc_splits(h, tiles, N, Kr, B) : 1;
-    int rc = check_device(h);
+    Plan pl;
+    int rc = make_plan(h, N, Kr, B, &pl);
+    if (rc != SYMM_OK) return rc;
+    const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
+              slabs = pl.slabs;
+    const SkGeom geo = pl.geo;
+    rc = check_device(h);
     if (rc != SYMM_OK) return rc;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Tickets of launch e are (e-1)*C .. e*C-1 (C = R * splits contributors per
-    // tile): restart the pad when the geometry changes or before e*C wraps.
-    const int contrib = h->R * splits;
-    if (((uint64_t)h->epoch + 1) * (uint64_t)contrib > 0xFFFFFFFFull || h->epoch == 0 ||
-        tiles != h->geom_tiles || contrib != h->geom_contrib) {
+    // Tickets of launch e are (e-1)*C_t .. e*C_t-1 (C_t contributors of tile t,
+    // at most R * max(splits, Pmax)): restart the pad when the geometry
+    // changes or before the tickets would wrap.
+    const int cmax = h->R * std::max(splits, geo.Pmax);
+    uint64_t key = 1469598103934665603ull;
+    for (long long v : {(long long)path, (long long)tiles, (long long)splits, (long long)geo.KB, (long long)geo.G,
+                        (long long)geo.Pmax, (long long)engine, (long long)slabs}) {
+        key ^= (uint64_t)v;
+        key *= 1099511628211ull;
+    }
+    if (((uint64_t)h->epoch + 1) * (uint64_t)cmax > 0xFFFFFFFFull || h->epoch == 0 || key != h->geom_key) {
         rc = reset_protocol(h, s);
         if (rc != SYMM_OK) return rc;
-        h->geom_tiles = tiles;
-        h->geom_contrib = contrib;
+        h->geom_key = key;
     }
     h->epoch += 1;
 
@@ -417,11 +522,12 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     a.kc_cap = 0;
     cudaError_t e = cudaSuccess;
     switch (path) {
-        case 1:
+        case kPathFfma:
             a.kc_cap = ffma_kc_cap(B, Kr);
             e = launch_gemv_ffma(a, s);
             break;
-        case 2: {
+        case kPathTc:
+        case kPathSk: {
             if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
             int err = 0;
             const void *maps = tc_maps_for(h, a, &err);
@@ -429,7 +535,12 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
                 h->epoch -= 1;
                 return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
             }
-            e = launch_gemv_tc(a, maps, s);
+            if (path == kPathTc) {
+                e = launch_gemv_tc(a, maps, s);
+            } else {
+                a.partial_stride = (long long)B * N * 4;
+                e = launch_gemv_sk(a, geo, maps, engine, slabs, s);
+            }
             break;
         }
         default:

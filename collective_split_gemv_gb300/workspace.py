@@ -48,7 +48,8 @@ class GemvWorkspace:
         self.y_off = off
         off += _up(max(self.y_bytes, 1))
         self.slot_bytes = off
-        self.scratch_bytes = _up(max(4 * B * N, 1))
+        # room for up to 8 partial arrays per rank (stream-K parts, K-splits)
+        self.scratch_bytes = _up(max(8 * 4 * B * N, 1))
         self.pad_bytes = pad_bytes_for(N)
         with torch.cuda.device(self.device):
             self.h = symm_alloc(R, self.slot_bytes, self.scratch_bytes, self.pad_bytes)

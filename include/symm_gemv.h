@@ -192,10 +192,15 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
  */
 int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band);
 
-/* Per-handle options (defaults 0). */
+/* Per-handle options.  The kernel choice is automatic by default; the
+ * others exist for tests and measurements. */
 enum {
-    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto, 1 FFMA kernel, 2 tensor-core kernel */
-    SYMM_OPT_TILE_ORDER = 2   /* 0 tile-major CTA order, 1 reversed (tests arrival order) */
+    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto (3 when K > 0, else 1); 1 CUDA-core kernel, one CTA per
+                                 (row tile, rank); 2 tensor-core kernel, one CTA per (tile, rank,
+                                 K-split); 3 persistent stream-K kernel (TMA ring, one CTA per SM) */
+    SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
+    SYMM_OPT_SK_SLABS = 3,    /* stream-K: 64-column slabs per pipeline stage, 0 auto (2), 1, 2 or 4 */
+    SYMM_OPT_SK_ENGINE = 4    /* stream-K: -1 auto (FFMA for B <= 2, else tcgen05), 0 tcgen05, 1 FFMA */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 
@@ -209,9 +214,21 @@ typedef struct {
 } symm_info_t;
 int symm_info(symm_handle_t *h, symm_info_t *info);
 
-/* Row-tile height the chosen GEMV kernel uses for batch B (0 if B invalid);
- * the tile count ceil(N / rows) must fit max_tiles. */
-int symm_gemv_rows_per_tile(symm_handle_t *h, int B);
+/* The kernel and launch geometry gemv_all_reduce would use for (N, K, B) on
+ * this handle, without launching anything (SYMM_EINVAL / SYMM_ERANGE exactly
+ * as the call would return them).
+ *   path           1 CUDA-core, 2 tensor-core per tile, 3 persistent stream-K
+ *   engine         stream-K compute engine: 0 tcgen05, 1 FFMA
+ *   slabs          stream-K 64-column slabs per pipeline stage
+ *   rows_per_tile  output rows per tile; tiles = ceil(N / rows_per_tile)
+ *   splits         K-splits per rank (path 2)
+ *   grid           CTAs launched
+ *   parts_max      stream-K: most partials one (tile, rank) is cut into
+ *   kblocks        stream-K: K blocks per (tile, rank) */
+typedef struct {
+    int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks;
+} symm_gemv_plan_t;
+int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out);
 
 /*
  * gemv_all_reduce_noalloc -- the fused GEMV + one-shot all-reduce for callers

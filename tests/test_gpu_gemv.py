@@ -19,7 +19,7 @@ from helpers import f64_to_words_via_f32, tolerance_ratio, ulp_distance, words_t
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC]
+PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC, csg.GEMV_PATH_SK]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -222,7 +222,7 @@ def test_capacity_errors():
     try:
         base = csg.symm_rendezvous(h)[0][0]
         tiles = csg.symm_info(h)["max_tiles"]
-        rows = csg.symm_gemv_rows_per_tile(h, 1)
+        rows = csg.symm_gemv_plan(h, 16, 0, 1)["rows_per_tile"]   # K = 0: CUDA-core kernel
         N = (tiles + 1) * rows
         with pytest.raises(csg.SymmError) as e:
             csg.gemv_all_reduce(h, base, base + 65536, base + 131072, 2, N, 0, 1)
@@ -265,7 +265,7 @@ def test_corrupted_counter_is_reported_and_recovered():
         code, rank, tile = csg.symm_status(ws.h, s)
         assert code == csg.SYMM_EPROTO and tile == 0, (code, rank, tile)
         y = ws.read_y()
-        rows = csg.symm_gemv_rows_per_tile(ws.h, B)
+        rows = csg.symm_gemv_plan(ws.h, N, K, B)["rows_per_tile"]
         # Tile 0's first arriver holds the "last" ticket.  It stores nothing
         # if some peer's flag is still stale; if every peer had already
         # published (flags are set before tickets are taken) its sum is the
@@ -304,18 +304,67 @@ def test_shape_changes_on_one_handle(path):
         ws.close()
 
 
-def test_many_launches_keep_tickets_consistent():
-    R, N, K, B = 8, 256, 8 * 64, 2
+@pytest.mark.parametrize("path", [csg.GEMV_PATH_FFMA, csg.GEMV_PATH_SK])
+def test_many_launches_keep_tickets_consistent(path):
+    R, N, K, B = 8, 1000, 8 * 512, 2
     W, x = _normal_case(R, N, K, B, seed=17)
     ws = GemvWorkspace(R, N, K, B)
     try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
         ws.load_W(W)
         ws.load_x(x)
         s = torch.cuda.current_stream()
         for _ in range(50):
             ws.run(s)
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
-        assert int(_counter_view(ws, 3).item()) == 50 * R
+        if path == csg.GEMV_PATH_FFMA:
+            assert int(_counter_view(ws, 3).item()) == 50 * R   # one contributor per rank
+        else:
+            assert int(_counter_view(ws, 3).item()) % 50 == 0   # C_3 contributors per launch
         check_gemv(W, x, ws.read_y())
     finally:
         ws.close()
+
+
+# ------------------------------------------------------ stream-K variants
+
+SK_VARIANTS = [(engine, slabs) for engine in (0, 1) for slabs in (1, 2, 4)]
+SK_SHAPES = [(8, 8192, 8 * 3584, 1), (8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1),
+             (3, 513, 3 * 4096, 2), (8, 8192, 8 * 512, 1)]
+
+
+@pytest.mark.parametrize("engine,slabs", SK_VARIANTS, ids=[f"eng{e}-slabs{s}" for e, s in SK_VARIANTS])
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=[f"R{a}N{b}K{c}B{d}" for a, b, c, d in SK_SHAPES])
+def test_stream_k_engines_and_slabs(engine, slabs, shape):
+    """Both stream-K engines at every pipeline depth: integer inputs bit-exact,
+    normal inputs within tolerance, replicas identical, reversed CTA order
+    identical."""
+    R, N, K, B = shape
+    for kind in ("int", "normal"):
+        if kind == "int":
+            W, x = _int_case(R, N, K // R, B, seed=N + slabs)
+        else:
+            W, x = _normal_case(R, N, K, B, seed=N + 7 * slabs)
+        ws = GemvWorkspace(R, N, K, B)
+        try:
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_SK)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, slabs)
+            plan = csg.symm_gemv_plan(ws.h, N, K, B)
+            assert plan["path"] == csg.GEMV_PATH_SK and plan["engine"] == engine and plan["slabs"] == slabs
+            ws.load_W(W)
+            ws.load_x(x)
+            s = torch.cuda.current_stream()
+            ws.fill_y(0xFF)
+            ws.run(s)
+            assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+            y0 = ws.read_y()
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_TILE_ORDER, 1)
+            ws.fill_y(0xFF)
+            ws.run(s)
+            assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+            assert np.array_equal(ws.read_y(), y0), "reversed CTA order changed bits"
+            assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
+        finally:
+            ws.close()
+        check_gemv(W, x, y0, exact=(kind == "int"))

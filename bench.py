@@ -168,7 +168,8 @@ def kernel_name(plan):
     if plan["path"] == 2:
         return "gemv_ar_tc_kernel"
     engine = "tcgen05" if plan["engine"] == 0 else "ffma"
-    return f"gemv_ar_sk_kernel<{engine},slabs={plan['slabs']}>"
+    name = "gemv_ar_sk_kernel" if plan["path"] == 3 else "gemv_ar_dyn_kernel"
+    return f"{name}<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
 
 
 def kernel_source_sha():
@@ -205,10 +206,13 @@ def run_ours(args, rank, world, local_rank):
     copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(w_total, 1))))
     ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
     paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
-             "sk": csg.GEMV_PATH_SK}
+             "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
     csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path])
     csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, args.sk_slabs)
     csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, args.sk_engine)
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps)
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_GRID, args.sk_grid)
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits)
     plan = csg.symm_gemv_plan(ws.h, N, K, B)
     for c in range(copies):
         ws.load_W(W, copy=c)
@@ -453,10 +457,16 @@ def main():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="mlp_down_decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk"), default="auto",
+    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk", "dyn"), default="auto",
                    help="force one kernel (measurement only)")
     p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 4),
                    help="stream-K slabs per pipeline stage (0 = library default)")
+    p.add_argument("--sk-cps", type=int, default=0, choices=(0, 1, 2, 3),
+                   help="stream-K resident CTAs per SM (0 = library default)")
+    p.add_argument("--sk-grid", type=int, default=0,
+                   help="stream-K grid: 0 library default, -1 one CTA per (tile, rank), or a count")
+    p.add_argument("--dyn-splits", type=int, default=0,
+                   help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
                    help="stream-K engine: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--cpu-seconds", type=float, default=10.0)

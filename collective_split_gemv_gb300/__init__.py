@@ -35,8 +35,11 @@ SYMM_OPT_GEMV_PATH = 1
 SYMM_OPT_TILE_ORDER = 2
 SYMM_OPT_SK_SLABS = 3
 SYMM_OPT_SK_ENGINE = 4
+SYMM_OPT_SK_CTAS_PER_SM = 5
+SYMM_OPT_SK_GRID = 6
+SYMM_OPT_DYN_SPLITS = 7
 
-GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK = 0, 1, 2, 3
+GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK, GEMV_PATH_DYN = 0, 1, 2, 3, 4
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
@@ -60,7 +63,7 @@ class SymmInfo(ctypes.Structure):
 
 class GemvPlan(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int) for k in ("path", "engine", "slabs", "rows_per_tile", "tiles", "splits",
-                                            "grid", "parts_max", "kblocks")]
+                                            "grid", "parts_max", "kblocks", "ctas_per_sm")]
 
 
 def library_path() -> str:

@@ -1,0 +1,566 @@
+// Persistent, dynamically scheduled fused GEMV + one-shot all-reduce: one or
+// more CTAs per SM draw whole (row tile, rank) units from an atomic work
+// counter and stream them through a TMA ring into the tcgen05 tensor cores
+// (wider batches) or into CUDA-core FFMA (B <= 2).
+//
+// Why this shape: W is read exactly once, so the kernel is bound by HBM, and
+// what costs time besides bytes is (a) a CTA's start-up and wind-down, which
+// do not stream, and (b) SMs that finish their share early.  Persistent CTAs
+// pay (a) once per launch instead of once per unit, and drawing units from a
+// shared counter removes (b) -- a static partition cannot adapt to SMs whose
+// bandwidth differs.  A unit's epilogue (partial store, publish, and the
+// tile reduction when it is the last contributor) overlaps the streaming of
+// the CTA's next unit: the accumulator is double-buffered in TMEM.
+//
+// Units: a unit is one K split of one (row tile, rank) pair, numbered
+// tile-major, u = (t * R + r) * S + s, so that a tile's contributors are
+// drawn close together.  S > 1 only serves to make units small enough that
+// drawing them balances the SMs.
+//
+// Work counter: slot 0's signal pad holds one u32 that only grows.  CTA c
+// starts with unit c (G <= U) and then draws: launch `epoch` owns tickets
+// (epoch-1)*U .. epoch*U-1, ticket k naming unit G + k; U - G tickets name
+// units and each of the G CTAs draws exactly one ticket past the end, which
+// tells it to stop.  The host resets the pad when the geometry changes.
+//
+// Roles (192 threads):
+//   warp 0, lane 0  draws units, issues the TMA loads of each unit's K blocks
+//                   (W 128 rows x 64*kSlabs, x 16 rows x 64*kSlabs, 128-byte
+//                   swizzle) and tags every stage with (unit, block);
+//   warp 1          tcgen05 engine: TMEM owner; lane 0 issues the MMAs of each
+//                   stage and, at a unit's last block, hands the accumulator
+//                   and the unit id to the epilogue;
+//   warps 2-5       tcgen05 engine: tcgen05.ld of the accumulator, then the
+//                   partial store and the publish / last-arriver protocol of
+//                   the tile (R * S contributors);
+//                   FFMA engine: one row per thread straight from the stage;
+//                   each unit's row sums go through a two-entry shared-memory
+//                   mailbox to warp 1, which stores, publishes and reduces
+//                   while these warps stream on.
+// Unit ids travel with the stages (producer -> MMA / FFMA consumers) and
+// through a two-entry mailbox (MMA -> epilogue) guarded by its own mbarrier.
+// A stage tagged -1 ends the stream.
+//
+// Follows the fused GEMV + AllReduce of "Overlapping Collective Communication
+// with Dependent Computation ... GPU-Initiated Intra-Kernel Networking"
+// (Abstract): partials are published as soon as a unit is computed, the
+// reduction of a tile overlaps the streaming of other units, and the
+// workgroup scheduling is communication-aware (units are drawn tile-major, so
+// a tile's R contributors run close together and its partials stay in L2).
+//
+// Safety: all mbarrier waits are bounded (%globaltimer); decisions that
+// steer the group's named barrier are made uniform with bar.red.and; a CTA
+// that gave up latches a status code, waits (bounded) for its copies and MMAs
+// in flight, frees TMEM and exits without publishing.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "protocol.cuh"
+#include "sm100.cuh"
+
+namespace symm {
+
+namespace {
+
+constexpr int kM = 128;
+constexpr int kNmma = 16;
+constexpr int kSlabA = kM * 64 * 2;
+constexpr int kSlabX = kNmma * 64 * 2;
+constexpr int kThreads = 192;
+constexpr int kGroupThreads = 128;
+constexpr int kGroupBarrier = 1;
+constexpr uint32_t kTmemCols = 32;
+constexpr uint32_t kIdesc = mma_idesc_bf16_f32(kM, kNmma);
+
+template <int kSlabs, int kCps>
+struct Ring {
+    static constexpr int kStageBytes = kSlabs * (kSlabA + kSlabX);
+    static constexpr int kStages = ((216 * 1024) / kCps) / kStageBytes;
+    static constexpr int kSmem = kStages * kStageBytes + 1024;
+};
+
+__device__ __forceinline__ bool group_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\n"
+        "setp.ne.u32 q, %1, 0;\n"
+        "bar.red.and.pred p, %2, %3, q;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(kGroupBarrier), "r"(kGroupThreads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Steps 2-4 of the protocol for contributor (r, s) of tile t (C = R * S
+// contributors: every rank's K range in S splits), run by the 128 threads of
+// warps 2-5 (gt = 0..127).  The caller has stored its partial.
+__device__ __forceinline__ void publish_reduce_unit(const GemvArgs &a, int S, int t, int r, int s, int gt,
+                                                    int *s_last, int *s_bad) {
+    const uint32_t C = (uint32_t)a.R * (uint32_t)S;
+    __threadfence();
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (gt == 0) {
+        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
+                                                      (long long)r * a.stride) + (size_t)t * S + s;
+        st_release_gpu(flag, a.epoch);
+        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
+        const uint32_t pos = ticket - (a.epoch - 1u) * C;
+        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
+        *s_last = (pos == C - 1u);
+        *s_bad = 0;
+    }
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (!*s_last) return;
+    __threadfence();
+    for (int i = gt; i < (int)C; i += kGroupThreads) {
+        const int q = i / S;
+        const int qs = i - q * S;
+        const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
+                                                               (long long)q * a.stride) + (size_t)t * S + qs;
+        if (ld_acquire_gpu(f) != a.epoch) {
+            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
+            *s_bad = 1;
+        }
+    }
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (*s_bad) return;
+    // Contributors in order: rank 0..R-1, split 0..S-1.
+    reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
+                [&](int j) {
+                    const int q = j / S;
+                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                },
+                gt, kGroupThreads);
+}
+
+// The same protocol run by one warp (the FFMA engine's epilogue warp).
+__device__ __forceinline__ void publish_reduce_warp(const GemvArgs &a, int S, int t, int r, int s, int lane) {
+    const uint32_t C = (uint32_t)a.R * (uint32_t)S;
+    __threadfence();
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
+                                                      (long long)r * a.stride) + (size_t)t * S + s;
+        st_release_gpu(flag, a.epoch);
+        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
+        const uint32_t pos = ticket - (a.epoch - 1u) * C;
+        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
+        last = pos == C - 1u;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    bool bad = false;
+    for (int i = lane; i < (int)C; i += 32) {
+        const int q = i / S;
+        const int qs = i - q * S;
+        const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
+                                                               (long long)q * a.stride) + (size_t)t * S + qs;
+        if (ld_acquire_gpu(f) != a.epoch) {
+            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
+            bad = true;
+        }
+    }
+    if (__any_sync(0xffffffffu, bad)) return;
+    reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
+                [&](int j) {
+                    const int q = j / S;
+                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                },
+                lane, 32);
+}
+
+__device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
+    acc = fmaf(bf16lo(w.x), bf16lo(x.x), acc);
+    acc = fmaf(bf16hi(w.x), bf16hi(x.x), acc);
+    acc = fmaf(bf16lo(w.y), bf16lo(x.y), acc);
+    acc = fmaf(bf16hi(w.y), bf16hi(x.y), acc);
+    acc = fmaf(bf16lo(w.z), bf16lo(x.z), acc);
+    acc = fmaf(bf16hi(w.z), bf16hi(x.z), acc);
+    acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
+    acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
+    return acc;
+}
+
+template <int kEngine, int kSlabs, int kB, int kCps>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const GemvArgs a, const DynGeom geo) {
+    using RingT = Ring<kSlabs, kCps>;
+    static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
+    constexpr int kStages = RingT::kStages;
+    constexpr int kStageBytes = RingT::kStageBytes;
+    constexpr int kBK = 64 * kSlabs;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t unit_full[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ int stage_unit[kStages];
+    __shared__ int stage_flags[kStages];   // bit 0: first block of the unit, bit 1: last
+    __shared__ int acc_unit[2];
+    __shared__ float part_buf[2][kM * 2];   // FFMA engine: [buffer][b * 128 + row] partials, B <= 2
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    __shared__ int s_last, s_bad;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int U = geo.units;            // (tile, rank, split) triples, tile-major
+    const int S = geo.splits;
+    const int KBs = geo.KBs;            // K blocks per split (the last split may have fewer)
+    const int KB = geo.KB;
+    const uint32_t base_ticket = (a.epoch - 1u) * (uint32_t)U;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kEngine == 0 ? 1 : 4);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&acc_full[j], 1);
+            // tcgen05 engine: drained by the 4 epilogue warps, unit id from the
+            // MMA thread.  FFMA engine: drained by the epilogue warp (warp 1),
+            // partials handed over by the 4 compute warps.
+            mbar_init(&acc_empty[j], kEngine == 0 ? 4 : 1);
+            mbar_init(&unit_full[j], kEngine == 0 ? 1 : 4);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_sh = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (kEngine == 0 && warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = kEngine == 0 ? tmem_base_sh : 0u;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+            int issued = 0;
+            // The first unit is the CTA's own index (G <= U); later ones are
+            // drawn: ticket k names unit G + k.
+            uint32_t tk = blockIdx.x;
+            bool ok = true;
+            while (ok) {
+                const int st0 = issued % kStages;
+                const uint32_t ph0 = (uint32_t)(issued / kStages) & 1u;
+                if (tk >= (uint32_t)U) {
+                    // End of the stream: an empty stage tagged -1.
+                    if (!mbar_wait(&empty_bar[st0], ph0 ^ 1u, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    stage_unit[st0] = -1;
+                    stage_flags[st0] = 0;
+                    mbar_arrive(&full_bar[st0]);
+                    ++issued;
+                    break;
+                }
+                const int u = a.reverse_order ? U - 1 - (int)tk : (int)tk;
+                const int tr = u / S;
+                const int sp = u - tr * S;
+                const int t = tr / a.R;
+                const int r = tr - t * a.R;
+                const int kb0 = sp * KBs;
+                const int kb1 = min(kb0 + KBs, KB);
+                // Draw the next unit now; its value is needed only after this one.
+                const uint32_t next = atom_add_relaxed_gpu(geo.work, 1u) - base_ticket + (uint32_t)geo.G;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const int st = issued % kStages;
+                    const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
+                    if (!mbar_wait(&empty_bar[st], ph ^ 1u, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    stage_unit[st] = u;
+                    stage_flags[st] = (kb == kb0 ? 1 : 0) | (kb == kb1 - 1 ? 2 : 0);
+                    mbar_arrive_expect_tx(&full_bar[st], (uint32_t)kStageBytes);
+                    uint8_t *dst = smem + (size_t)st * kStageBytes;
+#pragma unroll
+                    for (int s = 0; s < kSlabs; ++s)
+                        tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[st], kb * kBK + s * 64, t * kM, r);
+#pragma unroll
+                    for (int s = 0; s < kSlabs; ++s)
+                        tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0,
+                                    r);
+                    ++issued;
+                }
+                tk = next;
+            }
+            if (!ok) {
+                latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                abort_sh = 1;
+                volatile int never = 0;
+                for (int j = max(0, issued - kStages); j < issued; ++j)
+                    mbar_wait(&full_bar[j % kStages], (uint32_t)(j / kStages) & 1u, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if constexpr (kEngine == 0) {
+            if (lane == 0) {
+                int i = 0, seg = 0;
+                bool ok = true;
+                while (true) {
+                    const int st = i % kStages;
+                    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                    if (!mbar_wait(&full_bar[st], ph, &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    const int u = stage_unit[st];
+                    const int fl = stage_flags[st];
+                    const int j = seg & 1;
+                    const uint32_t use = (uint32_t)(seg >> 1);
+                    if (u < 0 || (fl & 1)) {
+                        // Buffer j must have been drained (its previous unit read out).
+                        if (!mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (u < 0) {
+                        acc_unit[j] = -1;
+                        mbar_arrive(&unit_full[j]);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(j * kNmma);
+                    const uint32_t a_addr = smem_u32(smem + (size_t)st * kStageBytes);
+                    const uint32_t x_addr = a_addr + kSlabs * kSlabA;
+#pragma unroll
+                    for (int s = 0; s < kSlabs; ++s)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma(d, smem_desc_sw128(a_addr + s * kSlabA + kk * 32),
+                                   smem_desc_sw128(x_addr + s * kSlabX + kk * 32), kIdesc,
+                                   ((fl & 1) && s == 0 && kk == 0) ? 0u : 1u);
+                    tc_commit(&empty_bar[st]);
+                    ++i;
+                    if (fl & 2) {
+                        acc_unit[j] = u;
+                        mbar_arrive(&unit_full[j]);
+                        tc_commit(&acc_full[j]);
+                        ++seg;
+                    }
+                }
+                if (!ok) {
+                    latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                    abort_sh = 1;
+                }
+                tc_commit(&drain_bar);
+                volatile int never = 0;
+                mbar_wait(&drain_bar, 0, &never);
+            }
+        } else {
+            // ------------------------------ FFMA engine: epilogue warp
+            // Takes each unit's partial from the compute warps, stores it,
+            // publishes it and, as the tile's last contributor, reduces the
+            // tile -- while the compute warps already stream the next unit.
+            int seg = 0;
+            bool ok = true;
+            while (true) {
+                const int j = seg & 1;
+                const uint32_t use = (uint32_t)(seg >> 1);
+                ok = __all_sync(0xffffffffu, mbar_wait_sleepy(&unit_full[j], use & 1u, &abort_sh)) != 0;
+                if (!ok) break;
+                const int u = acc_unit[j];
+                if (u < 0) break;
+                const int tr = u / S;
+                const int sp = u - tr * S;
+                const int t = tr / a.R;
+                const int r = tr - t * a.R;
+                float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
+                                                     (long long)sp * a.partial_stride);
+                for (int idx = lane; idx < kM * kB; idx += 32) {
+                    const int b = idx / kM;
+                    const int n = t * kM + (idx - b * kM);
+                    if (n < a.N) P[(size_t)b * a.N + n] = part_buf[j][idx];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[j]);
+                publish_reduce_warp(a, S, t, r, sp, lane);
+                ++seg;
+            }
+            if (!ok) {
+                latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                abort_sh = 1;
+            }
+        }
+    } else {
+        // ------------------------------- epilogue / FFMA consumers (warps 2-5)
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        const int gt = threadIdx.x - 64;
+        bool ok = true;
+        if constexpr (kEngine == 0) {
+            int seg = 0;
+            while (true) {
+                const int j = seg & 1;
+                const uint32_t use = (uint32_t)(seg >> 1);
+                ok = group_all(mbar_wait_sleepy(&unit_full[j], use & 1u, &abort_sh));
+                if (!ok) break;
+                const int u = acc_unit[j];
+                if (u < 0) break;
+                ok = group_all(mbar_wait_sleepy(&acc_full[j], use & 1u, &abort_sh));
+                if (!ok) break;
+                tc_fence_after();
+                float v[16];
+                tmem_ld_16(tmem + (uint32_t)(j * kNmma) + ((uint32_t)(q4 * 32) << 16), v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[j]);
+                const int tr = u / S;
+                const int sp = u - tr * S;
+                const int t = tr / a.R;
+                const int r = tr - t * a.R;
+                const int n = t * kM + row;
+                if (n < a.N) {
+                    float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
+                                                         (long long)sp * a.partial_stride);
+#pragma unroll
+                    for (int b = 0; b < kNmma; ++b)
+                        if (b < a.B) P[(size_t)b * a.N + n] = v[b];
+                }
+                publish_reduce_unit(a, S, t, r, sp, gt, &s_last, &s_bad);
+                ++seg;
+            }
+        } else {
+            int i = 0, seg = 0;
+            float acc0[kB], acc1[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) acc0[b] = acc1[b] = 0.f;
+            while (true) {
+                const int st = i % kStages;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                ok = group_all(mbar_wait(&full_bar[st], ph, &abort_sh));
+                if (!ok) break;
+                const int u = stage_unit[st];
+                const int fl = stage_flags[st];
+                if (u < 0) {
+                    // End of the stream: tell the epilogue warp.
+                    const int j = seg & 1;
+                    const uint32_t use = (uint32_t)(seg >> 1);
+                    ok = group_all(mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh));
+                    if (!ok) break;
+                    if (gt == 0) acc_unit[j] = -1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&unit_full[j]);
+                    break;
+                }
+                if (fl & 1) {
+#pragma unroll
+                    for (int b = 0; b < kB; ++b) acc0[b] = acc1[b] = 0.f;
+                }
+                const uint8_t *A = smem + (size_t)st * kStageBytes;
+                const uint8_t *X = A + kSlabs * kSlabA;
+#pragma unroll
+                for (int s = 0; s < kSlabs; ++s)
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj += 2) {
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(A + s * kSlabA + row * 128 +
+                                                                          ((jj ^ (row & 7)) << 4));
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(A + s * kSlabA + row * 128 +
+                                                                          (((jj + 1) ^ (row & 7)) << 4));
+#pragma unroll
+                        for (int b = 0; b < kB; ++b) {
+                            const uint4 x0 = *reinterpret_cast<const uint4 *>(X + s * kSlabX + b * 128 +
+                                                                              ((jj ^ (b & 7)) << 4));
+                            const uint4 x1 = *reinterpret_cast<const uint4 *>(X + s * kSlabX + b * 128 +
+                                                                              (((jj + 1) ^ (b & 7)) << 4));
+                            acc0[b] = dot8_bf16(w0, x0, acc0[b]);
+                            acc1[b] = dot8_bf16(w1, x1, acc1[b]);
+                        }
+                    }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[st]);
+                ++i;
+                if (fl & 2) {
+                    // Hand the unit's partial to the epilogue warp (buffer j is
+                    // free once the unit two before it has been taken).
+                    const int j = seg & 1;
+                    const uint32_t use = (uint32_t)(seg >> 1);
+                    ok = group_all(mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh));
+                    if (!ok) break;
+#pragma unroll
+                    for (int b = 0; b < kB; ++b) part_buf[j][b * kM + row] = acc0[b] + acc1[b];
+                    if (gt == 0) acc_unit[j] = u;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&unit_full[j]);
+                    ++seg;
+                }
+            }
+        }
+        if (!ok) {
+            latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+            abort_sh = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (kEngine == 0 && warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int kEngine, int kSlabs, int kB, int kCps>
+cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, cudaStream_t s) {
+    auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps>;
+    constexpr int smem = Ring<kSlabs, kCps>::kSmem;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);
+    return cudaGetLastError();
+}
+
+template <int kEngine, int kB>
+cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, int slabs, int cps,
+                          cudaStream_t s) {
+    switch (cps * 10 + slabs) {
+        case 11: return launch_cfg<kEngine, 1, kB, 1>(a, geo, m, s);
+        case 12: return launch_cfg<kEngine, 2, kB, 1>(a, geo, m, s);
+        case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, s);
+        case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, s);
+        case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, s);
+        case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,
+                            cudaStream_t s) {
+    const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
+    if (engine == 0) return launch_engine<0, 0>(a, geo, m, slabs, cps, s);
+    if (a.B == 1) return launch_engine<1, 1>(a, geo, m, slabs, cps, s);
+    if (a.B == 2) return launch_engine<1, 2>(a, geo, m, slabs, cps, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace symm

@@ -64,10 +64,11 @@ constexpr int kGroupBarrier = 1;
 constexpr uint32_t kTmemCols = 32;
 constexpr uint32_t kIdesc = mma_idesc_bf16_f32(kM, kNmma);
 
-template <int kSlabs>
+// Ring of one CTA when kCps CTAs share an SM's 228 KB of shared memory.
+template <int kSlabs, int kCps>
 struct Ring {
     static constexpr int kStageBytes = kSlabs * (kSlabA + kSlabX);
-    static constexpr int kStages = (216 * 1024) / kStageBytes;
+    static constexpr int kStages = ((216 * 1024) / kCps) / kStageBytes;
     static constexpr int kSmem = kStages * kStageBytes + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
 };
@@ -134,25 +135,45 @@ __device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeo
     }
     named_barrier(kGroupBarrier, kGroupThreads);
     if (*s_bad) return;
+    // Partials of the tile in fixed order (rank, then part): plain L2 loads
+    // after the acquire above.  Each thread owns up to kPer outputs and loads
+    // all of them for one contributor before adding, so one L2 round trip
+    // serves kPer outputs; contributions are added strictly in order.
     const int n0 = t * kM;
     const int rows = min(kM, a.N - n0);
     const int count = rows * a.B;
-    for (int i = gt; i < count; i += kGroupThreads) {
-        const int b = i / rows;
-        const int n = n0 + (i - b * rows);
-        const size_t off = ((size_t)b * a.N + n) * sizeof(float);
-        float acc = 0.f;
+    constexpr int kPer = 16;
+    for (int i0 = gt; i0 < count; i0 += kGroupThreads * kPer) {
+        size_t off[kPer];
+        float acc[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = min(i0 + k * kGroupThreads, count - 1);
+            const int b = i / rows;
+            const int n = n0 + (i - b * rows);
+            off[k] = ((size_t)b * a.N + n) * sizeof(float);
+        }
         bool first = true;
         for (int q = 0; q < a.R; ++q)
             for (int qp = 0; qp < s_parts[q]; ++qp) {
-                const float v = ld_relaxed_gpu_f32(reinterpret_cast<const float *>(
-                    a.scratch + (long long)q * a.stride + (long long)qp * a.partial_stride + off));
-                acc = first ? v : acc + v;
+                const uint8_t *base = a.scratch + (long long)q * a.stride + (long long)qp * a.partial_stride;
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const float v = __ldcg(reinterpret_cast<const float *>(base + off[k]));
+                    acc[k] = first ? v : acc[k] + v;
+                }
                 first = false;
             }
-        const __nv_bfloat16 h = __float2bfloat16_rn(acc);
-        const size_t yoff = ((size_t)b * a.N + n) * sizeof(__nv_bfloat16);
-        for (int q = 0; q < a.R; ++q) *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = i0 + k * kGroupThreads;
+            if (i < count) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(acc[k]);
+                const size_t yoff = off[k] / 2;
+                for (int q = 0; q < a.R; ++q)
+                    *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+            }
+        }
     }
 }
 
@@ -170,11 +191,12 @@ __device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float
 }
 
 // kEngine 0: tcgen05 MMA (any B <= 16); kEngine 1: CUDA-core FFMA with kB batch columns.
-template <int kEngine, int kSlabs, int kB>
+template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, const SkGeom geo) {
-    using RingT = Ring<kSlabs>;
+    using RingT = Ring<kSlabs, kCps>;
+    static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;
     constexpr int kStageBytes = RingT::kStageBytes;
     constexpr int kBK = 64 * kSlabs;
@@ -224,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
             int issued = 0;
+            // (unit, K-block) of block g, advanced without divisions.
+            const long long u0 = beg / KB;
+            int kb = (int)(beg - u0 * KB);
+            int t = (int)(u0 / a.R);
+            int r = (int)(u0 - (long long)t * a.R);
             for (long long g = beg; g < end; ++g) {
-                const long long u = g / KB;
-                const int kb = (int)(g - u * KB);
-                const int t = (int)(u / a.R);
-                const int r = (int)(u - (long long)t * a.R);
                 const int st = issued % kStages;
                 const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
                 if (!mbar_wait(&empty_bar[st], ph ^ 1u, &abort_sh)) {
@@ -245,6 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < kSlabs; ++s)
                     tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0, r);
                 ++issued;
+                if (++kb == geo.KB) {
+                    kb = 0;
+                    if (++r == a.R) {
+                        r = 0;
+                        ++t;
+                    }
+                }
             }
             if (abort_sh) {
                 volatile int never = 0;
@@ -320,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kEngine == 0) {
                 const int j = seg & 1;
                 const uint32_t use = (uint32_t)(seg >> 1);
-                ok = mbar_wait(&acc_full[j], use & 1u, &abort_sh);
+                ok = mbar_wait_sleepy(&acc_full[j], use & 1u, &abort_sh);
                 ok = group_all(ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -391,10 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int kEngine, int kSlabs, int kB>
+template <int kEngine, int kSlabs, int kB, int kCps>
 cudaError_t launch_cfg(const GemvArgs &a, const SkGeom &geo, const CUtensorMap *m, cudaStream_t s) {
-    auto kern = gemv_ar_sk_kernel<kEngine, kSlabs, kB>;
-    constexpr int smem = Ring<kSlabs>::kSmem;
+    auto kern = gemv_ar_sk_kernel<kEngine, kSlabs, kB, kCps>;
+    constexpr int smem = Ring<kSlabs, kCps>::kSmem;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -409,26 +439,34 @@ cudaError_t launch_cfg(const GemvArgs &a, const SkGeom &geo, const CUtensorMap *
 
 int sk_block_k(int slabs) { return 64 * slabs; }
 
-cudaError_t launch_gemv_sk(const GemvArgs &a, const SkGeom &geo, const void *maps, int engine, int slabs,
-                           cudaStream_t s) {
-    const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
-    if (engine == 0) {
-        switch (slabs) {
-            case 1: return launch_cfg<0, 1, 0>(a, geo, m, s);
-            case 2: return launch_cfg<0, 2, 0>(a, geo, m, s);
-            case 4: return launch_cfg<0, 4, 0>(a, geo, m, s);
-            default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (slabs * 100 + a.B) {
-        case 101: return launch_cfg<1, 1, 1>(a, geo, m, s);
-        case 102: return launch_cfg<1, 1, 2>(a, geo, m, s);
-        case 201: return launch_cfg<1, 2, 1>(a, geo, m, s);
-        case 202: return launch_cfg<1, 2, 2>(a, geo, m, s);
-        case 401: return launch_cfg<1, 4, 1>(a, geo, m, s);
-        case 402: return launch_cfg<1, 4, 2>(a, geo, m, s);
+// Pipeline shapes that are instantiated: (slabs, CTAs per SM) with a ring of
+// at least two stages.
+bool sk_config_supported(int slabs, int cps) {
+    return (cps == 1 && (slabs == 1 || slabs == 2 || slabs == 4)) ||
+           (cps == 2 && (slabs == 1 || slabs == 2)) || (cps == 3 && slabs == 1);
+}
+
+template <int kEngine, int kB>
+cudaError_t launch_engine(const GemvArgs &a, const SkGeom &geo, const CUtensorMap *m, int slabs, int cps,
+                          cudaStream_t s) {
+    switch (cps * 10 + slabs) {
+        case 11: return launch_cfg<kEngine, 1, kB, 1>(a, geo, m, s);
+        case 12: return launch_cfg<kEngine, 2, kB, 1>(a, geo, m, s);
+        case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, s);
+        case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, s);
+        case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, s);
+        case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_gemv_sk(const GemvArgs &a, const SkGeom &geo, const void *maps, int engine, int slabs, int cps,
+                           cudaStream_t s) {
+    const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
+    if (engine == 0) return launch_engine<0, 0>(a, geo, m, slabs, cps, s);
+    if (a.B == 1) return launch_engine<1, 1>(a, geo, m, slabs, cps, s);
+    if (a.B == 2) return launch_engine<1, 2>(a, geo, m, slabs, cps, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace symm

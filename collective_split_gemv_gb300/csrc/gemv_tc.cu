@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[16];
         bool ok = true;
         if (nkb > 0) {
-            ok = mbar_wait(&accum_bar, 0, &abort_sh);
+            ok = mbar_wait_sleepy(&accum_bar, 0, &abort_sh);
             if (!ok) {
                 latch_status(a.status, kProtoTimeout, r, t, a.epoch);
                 abort_sh = 1;

@@ -87,8 +87,23 @@ struct SkGeom {
     int G;
     int Pmax;
 };
+// Persistent dynamically scheduled kernel: G CTAs draw the U = T*R units (KB
+// K-blocks each) from the work counter `work` (slot 0's pad).
+struct DynGeom {
+    int units;      // T * R * splits
+    int splits;     // K splits per (tile, rank)
+    int KB;         // K blocks per (tile, rank)
+    int KBs;        // K blocks per split
+    int G;
+    uint32_t *work;
+};
+constexpr size_t kPadWorkOffset = 64;   // byte offset of the work counter in slot 0's pad
+cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,
+                            int ctas_per_sm, cudaStream_t s);
+
 int sk_block_k(int slabs);
+bool sk_config_supported(int slabs, int ctas_per_sm);
 cudaError_t launch_gemv_sk(const GemvArgs &a, const SkGeom &geo, const void *maps, int engine, int slabs,
-                           cudaStream_t s);
+                           int ctas_per_sm, cudaStream_t s);
 
 }  // namespace symm

@@ -92,6 +92,58 @@ __device__ __forceinline__ void latch_status(uint32_t *status, int code, int ran
     }
 }
 
+// The reduction of one tile by its last contributor: for each output (b, n)
+// of rows [n0, n0 + rows), sum the C contributors' fp32 partials in
+// contributor order j = 0..C-1 (contributor j's [B][N] array at
+// contributor_base(j)), round to bf16 (RNE) and store into every rank's y.
+// The flags have been acquired and fenced, so plain L2 loads (.cg) see the
+// partials.  Each thread takes kPer outputs and loads kBatch contributors of
+// all of them before adding anything, so one L2 round trip serves
+// kPer * kBatch values; the additions stay in contributor order.
+template <class BaseFn>
+__device__ __forceinline__ void reduce_tile(const GemvArgs &a, int n0, int rows, int C, BaseFn contributor_base,
+                                            int tid, int nthreads) {
+    constexpr int kPer = 4;
+    constexpr int kBatch = 8;
+    const int count = rows * a.B;
+    for (int i0 = tid; i0 < count; i0 += nthreads * kPer) {
+        size_t off[kPer];
+        float acc[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = min(i0 + k * nthreads, count - 1);
+            const int b = i / rows;
+            const int n = n0 + (i - b * rows);
+            off[k] = ((size_t)b * a.N + n) * sizeof(float);
+            acc[k] = 0.f;
+        }
+        for (int j0 = 0; j0 < C; j0 += kBatch) {
+            float v[kBatch][kPer];
+#pragma unroll
+            for (int c = 0; c < kBatch; ++c) {
+                const uint8_t *base = contributor_base(min(j0 + c, C - 1));
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) v[c][k] = __ldcg(reinterpret_cast<const float *>(base + off[k]));
+            }
+#pragma unroll
+            for (int c = 0; c < kBatch; ++c)
+                if (j0 + c < C) {
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) acc[k] = (j0 + c == 0) ? v[c][k] : acc[k] + v[c][k];
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            if (i0 + k * nthreads < count) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(acc[k]);
+                const size_t yoff = off[k] / 2;   // the same (b, n) in bf16
+                for (int q = 0; q < a.R; ++q)
+                    *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+            }
+        }
+    }
+}
+
 // Steps 2-4 of the protocol.  Called by ALL threads of the CTA after each
 // thread has stored its part of contributor (r, s)'s partial for tile t.
 __device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int r, int s) {
@@ -131,23 +183,12 @@ __device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int
     // Sum in fixed order: rank 0..R-1, and within a rank split 0..S-1.
     const int n0 = t * a.rows_per_tile;
     const int rows = min(a.rows_per_tile, a.N - n0);
-    const int count = rows * a.B;
-    for (int i = threadIdx.x; i < count; i += blockDim.x) {
-        const int b = i / rows;
-        const int n = n0 + (i - b * rows);
-        const size_t off = ((size_t)b * a.N + n) * sizeof(float);
-        float acc = ld_relaxed_gpu_f32(reinterpret_cast<const float *>(a.scratch + off));
-        for (int j = 1; j < (int)C; ++j) {
-            const int q = j / S;
-            const int qs = j - q * S;
-            acc += ld_relaxed_gpu_f32(reinterpret_cast<const float *>(
-                a.scratch + (long long)q * a.stride + (long long)qs * a.partial_stride + off));
-        }
-        const __nv_bfloat16 v = __float2bfloat16_rn(acc);
-        const size_t yoff = ((size_t)b * a.N + n) * sizeof(__nv_bfloat16);
-        for (int q = 0; q < a.R; ++q)
-            *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = v;
-    }
+    reduce_tile(a, n0, rows, (int)C,
+                [&](int j) {
+                    const int q = j / S;
+                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                },
+                (int)threadIdx.x, (int)blockDim.x);
 }
 
 }  // namespace symm

@@ -44,6 +44,9 @@ struct symm_handle {
     int opt_tile_order = 0;
     int opt_sk_slabs = 0;
     int opt_sk_engine = -1;
+    int opt_sk_cps = 0;
+    int opt_sk_grid = 0;
+    int opt_dyn_splits = 0;
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -132,8 +135,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Zero flags and counters of every slot (stream-ordered) and restart epochs.
+// Zero flags, counters and the work counter (stream-ordered); restart epochs.
 int reset_protocol(symm_handle *h, cudaStream_t s) {
+    cudaError_t e0 = cudaMemsetAsync(slot(h, 0) + h->pad_off + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "cudaMemsetAsync(work counter)");
     for (int r = 0; r < h->R; ++r) {
         cudaError_t e = cudaMemsetAsync(slot(h, r) + h->pad_off + h->flags_off, 0,
                                         h->pad_bytes - h->flags_off, s);
@@ -156,16 +161,20 @@ int num_sms(int device) {
 }
 
 // Kernels: 1 CUDA-core, one CTA per (tile, rank), 128-bit loads;
-// 2 tensor-core, one CTA per (tile, rank, K-split); 3 persistent stream-K
-// (TMA ring, tcgen05 engine or, for B <= kSkFfmaMaxBatch, FFMA engine).
-// The automatic choice is 3 whenever K > 0.
-constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3;
+// 2 tensor-core, one CTA per (tile, rank, K-split); 3 stream-K (TMA ring,
+// static partition of the K blocks); 4 persistent CTAs drawing (tile, rank)
+// units from a work counter (TMA ring, double-buffered accumulator).  Paths
+// 3 and 4 run the tcgen05 engine, or the FFMA engine for B <= kSkFfmaMaxBatch.
+// The automatic choice is 4 whenever K > 0 (1 for K = 0), with two CTAs per
+// SM and two 64-column slabs per stage: the fastest configuration measured on
+// the decode (B = 1), attention-projection (B = 8) and large (B = 16) shapes.
+constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3, kPathDyn = 4;
 constexpr int kSkFfmaMaxBatch = 2;
 
 int gemv_path(const symm_handle *h, int B, int Kr) {
     (void)B;
     if (h->opt_gemv_path != 0) return h->opt_gemv_path;
-    return Kr > 0 ? kPathSk : kPathFfma;
+    return Kr > 0 ? kPathDyn : kPathFfma;
 }
 
 int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
@@ -174,6 +183,7 @@ int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
         case kPathFfma: return ffma_rows_per_tile(B);
         case kPathTc: return kTcRows;
         case kPathSk: return kTcRows;
+        case kPathDyn: return kTcRows;
         default: return 0;
     }
 }
@@ -184,6 +194,7 @@ int sk_engine(const symm_handle *h, int B) {
 }
 
 int sk_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }
+int sk_cps(const symm_handle *h) { return h->opt_sk_cps > 0 ? h->opt_sk_cps : 2; }
 
 // CTA whose range holds block g (same arithmetic as the kernel).
 int sk_cta_of_block(long long g, long long total, int G) {
@@ -192,12 +203,15 @@ int sk_cta_of_block(long long g, long long total, int G) {
 
 // Stream-K geometry: G <= SM count CTAs over total = tiles * R * KB blocks,
 // shrunk until the parts per unit fit the scratch region and the signal pad.
-bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slabs, SkGeom *geo) {
+bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slabs, int cps, SkGeom *geo) {
     const long long KB = (Kr + sk_block_k(slabs) - 1) / sk_block_k(slabs);
     const long long units = (long long)tiles * h->R;
     const long long total = units * KB;
     if (total <= 0 || KB > (1LL << 30)) return false;
-    long long G = std::min<long long>(total, num_sms(h->device));
+    // Grid: SMs x CTAs-per-SM (persistent), S CTAs per unit (-S), or explicit.
+    long long G = h->opt_sk_grid == 0 ? (long long)num_sms(h->device) * cps
+                                      : (h->opt_sk_grid < 0 ? units * (long long)(-h->opt_sk_grid) : h->opt_sk_grid);
+    G = std::min<long long>(total, std::min<long long>(G, 1LL << 30));
     const size_t part_bytes = (size_t)B * N * 4;
     while (G >= 1) {
         int pmax = 1;
@@ -252,8 +266,9 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 
 // The kernel and launch geometry gemv_all_reduce would use.
 struct Plan {
-    int path = 0, engine = 0, slabs = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
+    int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
     SkGeom geo = {0, 0, 0, 1};
+    DynGeom dyn = {0, 1, 0, 0, 0, nullptr};
 };
 
 int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
@@ -272,9 +287,42 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the stream-K kernel needs K > 0");
         pl->engine = sk_engine(h, B);
         pl->slabs = sk_slabs(h);
-        if (!sk_geometry(h, pl->tiles, N, Kr, B, pl->slabs, &pl->geo))
+        pl->cps = sk_cps(h);
+        if (!sk_config_supported(pl->slabs, pl->cps))
+            return fail(SYMM_EINVAL, "stream-K has no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
+        if (!sk_geometry(h, pl->tiles, N, Kr, B, pl->slabs, pl->cps, &pl->geo))
             return fail(SYMM_ERANGE, "stream-K partials do not fit the scratch region or the signal pad");
         pl->grid = pl->geo.G;
+    }
+    if (pl->path == kPathDyn) {
+        if (Kr == 0) return fail(SYMM_EINVAL, "the persistent kernel needs K > 0");
+        pl->engine = sk_engine(h, B);
+        pl->slabs = sk_slabs(h);
+        pl->cps = sk_cps(h);
+        if (!sk_config_supported(pl->slabs, pl->cps))
+            return fail(SYMM_EINVAL, "no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
+        const long long pairs = (long long)pl->tiles * h->R;
+        const long long KB = (Kr + sk_block_k(pl->slabs) - 1) / sk_block_k(pl->slabs);
+        if (pairs > (1LL << 26)) return fail(SYMM_ERANGE, "too many row tiles");
+        long long G = h->opt_sk_grid > 0 ? h->opt_sk_grid : (long long)num_sms(h->device) * pl->cps;
+        // K splits: the requested count (option), else none; limited by the K
+        // blocks, the scratch region (one partial per split) and the pad.
+        long long S = h->opt_dyn_splits > 0 ? h->opt_dyn_splits : 1;
+        S = std::min<long long>(S, KB);
+        while (S > 1 && ((size_t)S * B * N * 4 > h->scratch_bytes || (long long)pl->tiles * S > h->max_tiles)) --S;
+        const long long KBs = (KB + S - 1) / S;
+        S = (KB + KBs - 1) / KBs;   // no empty split
+        const long long units = pairs * S;
+        G = std::max<long long>(1, std::min<long long>(G, units));
+        pl->dyn.units = (int)units;
+        pl->dyn.splits = (int)S;
+        pl->dyn.KB = (int)KB;
+        pl->dyn.KBs = (int)KBs;
+        pl->dyn.G = (int)G;
+        pl->splits = (int)S;
+        pl->dyn.work = pad_word(h, 0, kPadWorkOffset);
+        pl->grid = (int)G;
+        pl->geo.KB = (int)KB;
     }
     return SYMM_OK;
 }
@@ -390,8 +438,8 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     switch (option) {
         case SYMM_OPT_GEMV_PATH:
-            if (value < 0 || value > 3)
-                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 ffma, 2 tensor core, 3 stream-K)", value);
+            if (value < 0 || value > 4)
+                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1..4)", value);
             h->opt_gemv_path = value;
             return SYMM_OK;
         case SYMM_OPT_TILE_ORDER:
@@ -406,6 +454,18 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
         case SYMM_OPT_SK_ENGINE:
             if (value < -1 || value > 1) return fail(SYMM_EINVAL, "stream-K engine %d not in {-1 auto, 0, 1}", value);
             h->opt_sk_engine = value;
+            return SYMM_OK;
+        case SYMM_OPT_SK_GRID:
+            if (value < -16) return fail(SYMM_EINVAL, "stream-K grid %d: 0 auto, -S (S = 1..16 CTAs per unit) or > 0", value);
+            h->opt_sk_grid = value;
+            return SYMM_OK;
+        case SYMM_OPT_DYN_SPLITS:
+            if (value < 0 || value > 16) return fail(SYMM_EINVAL, "persistent-kernel splits %d not in 0..16", value);
+            h->opt_dyn_splits = value;
+            return SYMM_OK;
+        case SYMM_OPT_SK_CTAS_PER_SM:
+            if (value < 0 || value > 3) return fail(SYMM_EINVAL, "stream-K CTAs per SM %d not in 0..3", value);
+            h->opt_sk_cps = value;
             return SYMM_OK;
         default:
             return fail(SYMM_EINVAL, "unknown option %d", option);
@@ -428,6 +488,7 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
     out->grid = pl.grid;
     out->parts_max = pl.geo.Pmax;
     out->kblocks = pl.geo.KB;
+    out->ctas_per_sm = pl.cps;
     return SYMM_OK;
 }
 
@@ -477,8 +538,9 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     int rc = make_plan(h, N, Kr, B, &pl);
     if (rc != SYMM_OK) return rc;
     const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
-              slabs = pl.slabs;
+              slabs = pl.slabs, cps = pl.cps;
     const SkGeom geo = pl.geo;
+    const DynGeom dyn = pl.dyn;
     rc = check_device(h);
     if (rc != SYMM_OK) return rc;
 
@@ -486,10 +548,11 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
     // Tickets of launch e are (e-1)*C_t .. e*C_t-1 (C_t contributors of tile t,
     // at most R * max(splits, Pmax)): restart the pad when the geometry
     // changes or before the tickets would wrap.
-    const int cmax = h->R * std::max(splits, geo.Pmax);
+    const int cmax = std::max(h->R * std::max(std::max(splits, dyn.splits), geo.Pmax), dyn.units);
     uint64_t key = 1469598103934665603ull;
     for (long long v : {(long long)path, (long long)tiles, (long long)splits, (long long)geo.KB, (long long)geo.G,
-                        (long long)geo.Pmax, (long long)engine, (long long)slabs}) {
+                        (long long)geo.Pmax, (long long)engine, (long long)slabs, (long long)cps, (long long)geo.total,
+                        (long long)dyn.units, (long long)dyn.G, (long long)dyn.splits}) {
         key ^= (uint64_t)v;
         key *= 1099511628211ull;
     }
@@ -527,7 +590,8 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
             e = launch_gemv_ffma(a, s);
             break;
         case kPathTc:
-        case kPathSk: {
+        case kPathSk:
+        case kPathDyn: {
             if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
             int err = 0;
             const void *maps = tc_maps_for(h, a, &err);
@@ -537,9 +601,11 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
             }
             if (path == kPathTc) {
                 e = launch_gemv_tc(a, maps, s);
+            } else if (path == kPathDyn) {
+                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, s);
             } else {
                 a.partial_stride = (long long)B * N * 4;
-                e = launch_gemv_sk(a, geo, maps, engine, slabs, s);
+                e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
             }
             break;
         }

@@ -195,12 +195,16 @@ int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band);
 /* Per-handle options.  The kernel choice is automatic by default; the
  * others exist for tests and measurements. */
 enum {
-    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto (3 when K > 0, else 1); 1 CUDA-core kernel, one CTA per
-                                 (row tile, rank); 2 tensor-core kernel, one CTA per (tile, rank,
-                                 K-split); 3 persistent stream-K kernel (TMA ring, one CTA per SM) */
+    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto (4 when K > 0, else 1); 1 CUDA-core kernel, one CTA per (row tile, rank);
+                                 2 tensor-core kernel, one CTA per (tile, rank, K-split);
+                                 3 stream-K kernel (TMA ring, static partition of the K blocks);
+                                 4 persistent kernel drawing (tile, rank) units from a work counter */
     SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
-    SYMM_OPT_SK_SLABS = 3,    /* stream-K: 64-column slabs per pipeline stage, 0 auto (2), 1, 2 or 4 */
-    SYMM_OPT_SK_ENGINE = 4    /* stream-K: -1 auto (FFMA for B <= 2, else tcgen05), 0 tcgen05, 1 FFMA */
+    SYMM_OPT_SK_SLABS = 3,    /* paths 3, 4: 64-column slabs per pipeline stage, 0 auto (2), 1, 2 or 4 */
+    SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (FFMA for B <= 2, else tcgen05), 0 tcgen05, 1 FFMA */
+    SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: resident CTAs per SM, 0 auto (2), 1..3 (ring shrinks) */
+    SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
+    SYMM_OPT_DYN_SPLITS = 7   /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 
@@ -217,16 +221,17 @@ int symm_info(symm_handle_t *h, symm_info_t *info);
 /* The kernel and launch geometry gemv_all_reduce would use for (N, K, B) on
  * this handle, without launching anything (SYMM_EINVAL / SYMM_ERANGE exactly
  * as the call would return them).
- *   path           1 CUDA-core, 2 tensor-core per tile, 3 persistent stream-K
+ *   path           1 CUDA-core, 2 tensor-core per tile, 3 stream-K, 4 persistent dynamic
  *   engine         stream-K compute engine: 0 tcgen05, 1 FFMA
  *   slabs          stream-K 64-column slabs per pipeline stage
  *   rows_per_tile  output rows per tile; tiles = ceil(N / rows_per_tile)
- *   splits         K-splits per rank (path 2)
+ *   splits         K-splits per rank (paths 2 and 4)
  *   grid           CTAs launched
  *   parts_max      stream-K: most partials one (tile, rank) is cut into
- *   kblocks        stream-K: K blocks per (tile, rank) */
+ *   kblocks        stream-K: K blocks per (tile, rank)
+ *   ctas_per_sm    stream-K: resident CTAs per SM */
 typedef struct {
-    int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks;
+    int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks, ctas_per_sm;
 } symm_gemv_plan_t;
 int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out);
 

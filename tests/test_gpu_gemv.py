@@ -19,7 +19,7 @@ from helpers import f64_to_words_via_f32, tolerance_ratio, ulp_distance, words_t
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC, csg.GEMV_PATH_SK]
+PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC, csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -304,7 +304,7 @@ def test_shape_changes_on_one_handle(path):
         ws.close()
 
 
-@pytest.mark.parametrize("path", [csg.GEMV_PATH_FFMA, csg.GEMV_PATH_SK])
+@pytest.mark.parametrize("path", [csg.GEMV_PATH_FFMA, csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN])
 def test_many_launches_keep_tickets_consistent(path):
     R, N, K, B = 8, 1000, 8 * 512, 2
     W, x = _normal_case(R, N, K, B, seed=17)
@@ -317,7 +317,7 @@ def test_many_launches_keep_tickets_consistent(path):
         for _ in range(50):
             ws.run(s)
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
-        if path == csg.GEMV_PATH_FFMA:
+        if path in (csg.GEMV_PATH_FFMA, csg.GEMV_PATH_DYN):
             assert int(_counter_view(ws, 3).item()) == 50 * R   # one contributor per rank
         else:
             assert int(_counter_view(ws, 3).item()) % 50 == 0   # C_3 contributors per launch
@@ -328,17 +328,20 @@ def test_many_launches_keep_tickets_consistent(path):
 
 # ------------------------------------------------------ stream-K variants
 
-SK_VARIANTS = [(engine, slabs) for engine in (0, 1) for slabs in (1, 2, 4)]
-SK_SHAPES = [(8, 8192, 8 * 3584, 1), (8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1),
-             (3, 513, 3 * 4096, 2), (8, 8192, 8 * 512, 1)]
+SK_PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (1, 3)]   # (slabs, CTAs per SM)
+SK_VARIANTS = [(engine, slabs, cps) for engine in (0, 1) for slabs, cps in SK_PIPES]
+SK_SHAPES = [(8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1), (3, 513, 3 * 4096, 2),
+             (8, 2048, 8 * 512, 1)]
 
 
-@pytest.mark.parametrize("engine,slabs", SK_VARIANTS, ids=[f"eng{e}-slabs{s}" for e, s in SK_VARIANTS])
+@pytest.mark.parametrize("path", [csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN], ids=["streamk", "persistent"])
+@pytest.mark.parametrize("engine,slabs,cps", SK_VARIANTS,
+                         ids=[f"eng{e}-slabs{s}-cps{c}" for e, s, c in SK_VARIANTS])
 @pytest.mark.parametrize("shape", SK_SHAPES, ids=[f"R{a}N{b}K{c}B{d}" for a, b, c, d in SK_SHAPES])
-def test_stream_k_engines_and_slabs(engine, slabs, shape):
-    """Both stream-K engines at every pipeline depth: integer inputs bit-exact,
-    normal inputs within tolerance, replicas identical, reversed CTA order
-    identical."""
+def test_tma_kernels_engines_and_pipelines(path, engine, slabs, cps, shape):
+    """The stream-K and the persistent TMA kernels, both engines, every
+    pipeline shape: integer inputs bit-exact, normal inputs within tolerance,
+    replicas identical, reversed CTA / unit order identical."""
     R, N, K, B = shape
     for kind in ("int", "normal"):
         if kind == "int":
@@ -347,11 +350,13 @@ def test_stream_k_engines_and_slabs(engine, slabs, shape):
             W, x = _normal_case(R, N, K, B, seed=N + 7 * slabs)
         ws = GemvWorkspace(R, N, K, B)
         try:
-            csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_SK)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
             csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
             csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, slabs)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_CTAS_PER_SM, cps)
             plan = csg.symm_gemv_plan(ws.h, N, K, B)
-            assert plan["path"] == csg.GEMV_PATH_SK and plan["engine"] == engine and plan["slabs"] == slabs
+            assert plan["path"] == path and plan["engine"] == engine and plan["slabs"] == slabs
+            assert plan["ctas_per_sm"] == cps
             ws.load_W(W)
             ws.load_x(x)
             s = torch.cuda.current_stream()
@@ -368,3 +373,35 @@ def test_stream_k_engines_and_slabs(engine, slabs, shape):
         finally:
             ws.close()
         check_gemv(W, x, y0, exact=(kind == "int"))
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("splits", [2, 3, 5])
+@pytest.mark.parametrize("shape", [(8, 300, 8 * 1032, 2), (4, 513, 4 * 4096, 1), (2, 130, 2 * 520, 2)],
+                         ids=["R8N300", "R4N513", "R2N130"])
+def test_persistent_kernel_k_splits(engine, splits, shape):
+    """The persistent kernel with every (tile, rank) cut into K splits: more,
+    smaller units for the work counter; integer inputs stay bit-exact."""
+    R, N, K, B = shape
+    for kind in ("int", "normal"):
+        W, x = (_int_case(R, N, K // R, B, seed=splits + N) if kind == "int"
+                else _normal_case(R, N, K, B, seed=3 * splits + N))
+        ws = GemvWorkspace(R, N, K, B)
+        try:
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, splits)
+            plan = csg.symm_gemv_plan(ws.h, N, K, B)
+            assert plan["splits"] > 1
+            ws.load_W(W)
+            ws.load_x(x)
+            s = torch.cuda.current_stream()
+            for _ in range(2):
+                ws.fill_y(0xFF)
+                ws.run(s)
+                assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+            y = ws.read_y()
+            assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
+        finally:
+            ws.close()
+        check_gemv(W, x, y, exact=(kind == "int"))

@@ -3,26 +3,32 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mlp_down_decode]
 
-One step is one ``gemv_all_reduce`` call over the workload (default: the MLP
-down-projection decode, R=8 ranks as symmetric slots, N=8192, K=28672,
-K/R=3584, B=1).  Inputs are synthetic (seeded generator), resident in HBM when
-the timed region starts; W rotates over several copies so the bytes touched
-between two reads of the same W exceed the 129 MB L2 (no flush is needed).
+One step is one library call over the workload: ``gemv_all_reduce`` for the
+GEMV workloads (default: the MLP down-projection decode, R=8 ranks as
+symmetric slots, N=8192, K=28672, K/R=3584, B=1) and ``one_shot_all_reduce``
+for ``--workload allreduce`` (R=8 slots of 4,194,304 bf16).  Inputs are
+synthetic (seeded generator) and resident in HBM when the timed region
+starts; inputs rotate over enough copies that the bytes touched between two
+reads of the same data exceed the 129 MB L2, otherwise L2 is flushed between
+launches outside the per-launch events.
 
-``value`` is the algorithmic HBM throughput of the call in GB/s (bytes that
-the method must move: W_r and x_r of every rank, the fp32 partials written and
-read back, and the R bf16 output replicas) divided by the measured time;
-``ms_per_step`` gives the call latency.  The ``roofline`` object divides the
-same bytes by the kernel's average launch time (CUDA events around every
-launch on the launching stream) and by the measured copy bandwidth.
+``value`` is the algorithmic HBM throughput of the call in GB/s -- the bytes
+the method must move (GEMV: W_r and x_r of every rank, the fp32 partials
+written and read back, the R bf16 output replicas; all-reduce: R inputs read,
+R outputs written) over the measured time per step; ``ms_per_step`` is the
+call latency.  ``roofline`` divides the same bytes by the kernel's mean launch
+time (CUDA events around every launch on the launching stream) and by the
+measured copy bandwidth.  ``e2e`` is the same call with its per-step inputs
+copied from pinned host memory and its result read back every step.
 
 ``--impl reference`` times the CPU oracle (fp64, plain C, all host cores) on
-the same workload, each step a bounded sample of the rows; it is a deliberately
-slow baseline, not the target.
+the same workload, each step a bounded sample of it; a deliberately slow
+baseline, not the target.
 
-Under torchrun (N > 1) every rank runs an independent replica of the workload
-on its own GPU (the R ranks of the method are slots of one GPU; nothing
-crosses GPUs), timing is max over ranks, and ``value`` sums the ranks' bytes.
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the R ranks of the method are slots of one GPU;
+nothing crosses GPUs), timing is max over ranks and ``value`` sums the ranks'
+bytes.
 """
 from __future__ import annotations
 
@@ -44,6 +50,7 @@ METRIC = "gemv_all_reduce µs/call and achieved HBM GB/s (% of GB300 peak), R=8 
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+DATA = "synthetic (seeded SplitMix64 + Box-Muller, bf16 RNE)"
 
 
 def algorithmic_bytes(R, N, K, B):
@@ -53,13 +60,21 @@ def algorithmic_bytes(R, N, K, B):
     return N * K * 2 + B * K * 2 + 2 * R * B * N * 4 + R * B * N * 2
 
 
+def allreduce_bytes(R, n):
+    """One-shot all-reduce: R inputs of n bf16 read, R outputs written."""
+    return 2 * R * n * 2
+
+
 def workload(name):
     import synth
 
-    w = dict(synth.WORKLOADS[name])
-    if w["kind"] != "gemv":
-        raise SystemExit(f"bench workloads are GEMV + all-reduce cases, not {name}")
-    return w
+    return dict(synth.WORKLOADS[name])
+
+
+def workload_bytes(w):
+    if w["kind"] == "allreduce":
+        return allreduce_bytes(w["R"], w["n"])
+    return algorithmic_bytes(w["R"], w["N"], w["K"], w["B"])
 
 
 def host_cores():
@@ -67,6 +82,24 @@ def host_cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:  # pragma: no cover
         return os.cpu_count() or 1
+
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of a list of floats over all ranks (identity at N=1)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    if device is not None:
+        t = t.to(device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def throughput_gbs(nbytes, ms, world=1):
+    """Whole-job GB/s: every rank moved `nbytes` in `ms` (the max over ranks)."""
+    return world * nbytes / (ms * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------- clocks
@@ -79,8 +112,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: str):
-        self.gpu = gpu_index
+    def __init__(self, gpu: str):
+        self.gpu = gpu
         self.proc = None
         self.lines = []
         self.thread = None
@@ -135,7 +168,7 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
-# ------------------------------------------------------------- GPU arm
+# --------------------------------------------------------- GPU arm pieces
 
 
 def measured_hbm_peak():
@@ -150,7 +183,7 @@ def measured_hbm_peak():
 
 def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
     """DRAM bytes per launch from a committed ncu summary, only if it was taken
-    on the kernel source as it is now."""
+    on the kernel sources as they are now."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
@@ -160,6 +193,21 @@ def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
     except (OSError, ValueError, KeyError):
         pass
     return None
+
+
+def kernel_source_sha():
+    """Hash of the device-code sources (the host runtime, which only plans and
+    launches, is left out)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "collective_split_gemv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f == "symm_runtime.cu":
+            continue
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
 
 
 def kernel_name(plan):
@@ -172,84 +220,31 @@ def kernel_name(plan):
     return f"{name}<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
 
 
-def kernel_source_sha():
-    import hashlib
-
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "collective_split_gemv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
-    return h.hexdigest()[:16]
-
-
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id):
+    """Warm up, then time exactly n_steps calls of step(i) on `stream`, each
+    bracketed by CUDA events; clocks sampled during the region.  Returns
+    (step_ms, launch_ms list, clocks)."""
     import torch
 
-    import __graft_entry__
-    import collective_split_gemv_gb300 as csg
-    import synth
-    from collective_split_gemv_gb300.workspace import GemvWorkspace
-
-    if rank == 0:
-        __graft_entry__.build()
-    if world > 1:
-        torch.distributed.barrier()   # the other ranks load what rank 0 built
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = workload(args.workload)
-    R, N, K, B = w["R"], w["N"], w["K"], w["B"]
-    nbytes = algorithmic_bytes(R, N, K, B)
-    W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
-    w_total = W.nbytes
-    copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(w_total, 1))))
-    ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
-    paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
-             "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path])
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, args.sk_slabs)
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, args.sk_engine)
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps)
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_GRID, args.sk_grid)
-    csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits)
-    plan = csg.symm_gemv_plan(ws.h, N, K, B)
-    for c in range(copies):
-        ws.load_W(W, copy=c)
-    ws.load_x(x)
-    stream = torch.cuda.Stream(device=dev)
-    working_set = copies * w_total
-    flush = working_set < 2 * L2_BYTES
-    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
-
-    def step(i):
-        ws.run(stream, copy=i % copies)
-
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            if flush:
+        for i in range(n_warmup):
+            if flush_buf is not None:
                 flush_buf.fill_(i & 0xFF)
             step(i)
     stream.synchronize()
-    code, _, _ = csg.symm_status(ws.h, stream)
-    if code != csg.SYMM_OK:
-        raise SystemExit(f"protocol error during warm-up: {csg.symm_last_error()}")
-
-    # ---- timed region: K calls, CUDA events around each launch ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
-    sampler = ClockSampler(str(local_rank) if not visible else visible.split(",")[local_rank].strip())
+    sampler = ClockSampler(gpu_id)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for i in range(args.steps):
-            if flush:
+        for i in range(n_steps):
+            if flush_buf is not None:
                 flush_buf.fill_(i & 0xFF)
             starts[i].record(stream)
             step(i)
@@ -260,66 +255,136 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     clocks = sampler.stop()
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = t0.elapsed_time(t1)
+    # with L2 flushes inside the region, a step's time is its launch's own
+    step_ms = (sum(launch_ms) / len(launch_ms)) if flush_buf is not None else t0.elapsed_time(t1) / n_steps
+    return step_ms, launch_ms, clocks
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import collective_split_gemv_gb300 as csg
+    import synth
+    from collective_split_gemv_gb300.workspace import AllReduceWorkspace, GemvWorkspace
+
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()   # the other ranks load what rank 0 built
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_id = str(local_rank) if not visible else visible.split(",")[local_rank].strip()
+    w = workload(args.workload)
+    nbytes = workload_bytes(w)
+    stream = torch.cuda.Stream(device=dev)
+    R = w["R"]
+
+    if w["kind"] == "gemv":
+        N, K, B = w["N"], w["K"], w["B"]
+        W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
+        per_copy = W.nbytes
+        copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(per_copy, 1))))
+        ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
+        paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
+                 "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
+        for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
+                         (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
+                         (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits)):
+            csg.symm_set_option(ws.h, opt, val)
+        plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        kernel = kernel_name(plan)
+        for c in range(copies):
+            ws.load_W(W, copy=c)
+        ws.load_x(x)
+
+        def step(i):
+            ws.run(stream, copy=i % copies)
+
+        # e2e: per-step inputs are x_r (W_r are resident model weights); result y
+        in_host = [torch.from_numpy(np.ascontiguousarray(x[r])).view(torch.uint8).reshape(-1).pin_memory()
+                   for r in range(R)]
+        in_dev = [ws.x_view(r) for r in range(R)]
+        out_dev = ws.y_view(0)
+        out_bytes = ws.y_bytes
+        config_extra = {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan}
+    else:
+        n = w["n"]
+        inp = synth.allreduce_inputs(R, n, w["seed"])
+        per_copy = inp.nbytes * 2    # R inputs read + R outputs written, both rotated
+        copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(per_copy, 1))))
+        ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
+        for c in range(copies):
+            ws.load_in(inp, copy=c)
+        kernel = "one_shot_ar_kernel"
+
+        def step(i):
+            ws.run(stream, copy=i % copies)
+
+        in_host = [torch.from_numpy(np.ascontiguousarray(inp[r])).view(torch.uint8).reshape(-1).pin_memory()
+                   for r in range(R)]
+        in_dev = [ws.in_view(r, 0) for r in range(R)]
+        out_dev = ws.out_view(0, 0)
+        out_bytes = ws.bytes
+        config_extra = {"R": R, "n": n}
+
+    working_set = copies * per_copy
+    flush = working_set < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id)
     code, _, _ = csg.symm_status(ws.h, stream)
     if code != csg.SYMM_OK:
         raise SystemExit(f"protocol error in the timed region: {csg.symm_last_error()}")
-    # with L2 flushes inside the region, the per-step time is the kernels' own
-    step_ms = sum(launch_ms) / len(launch_ms) if flush else region_ms / args.steps
 
-    # ---- e2e: same call through the ABI with host buffers every step ----
-    x_host = [torch.from_numpy(np.ascontiguousarray(x[r])).view(torch.uint8).reshape(-1).pin_memory()
-              for r in range(R)]
-    y_host = torch.empty(ws.y_bytes, dtype=torch.uint8).pin_memory()
-    x_dev = [ws.x_view(r) for r in range(R)]
-    w_dev = [ws.w_view(r, 0) for r in range(R)]
-    y_dev = ws.y_view(0)
+    # ---- e2e: the same call through the ABI with host buffers every step ----
+    out_host = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     e2e_steps = max(3, min(args.steps, 200))
     torch.cuda.synchronize(dev)
     tt = time.perf_counter()
     for i in range(e2e_steps):
         with torch.cuda.stream(stream):
             for r in range(R):
-                x_dev[r].copy_(x_host[r], non_blocking=True)
-            step(i)
-            y_host.copy_(y_dev, non_blocking=True)
+                in_dev[r].copy_(in_host[r], non_blocking=True)
+            ws.run(stream, copy=0)
+            out_host.copy_(out_dev, non_blocking=True)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - tt) * 1e3 / e2e_steps
-    # weights streamed from the host as well (every step copies all W_r)
-    W_host = [torch.from_numpy(np.ascontiguousarray(W[r])).view(torch.uint8).reshape(-1).pin_memory()
-              for r in range(R)]
-    ew_steps = max(3, min(args.steps, 10))
-    torch.cuda.synchronize(dev)
-    tt = time.perf_counter()
-    for i in range(ew_steps):
-        with torch.cuda.stream(stream):
-            for r in range(R):
-                w_dev[r].copy_(W_host[r], non_blocking=True)
-                x_dev[r].copy_(x_host[r], non_blocking=True)
-            ws.run(stream, copy=0)
-            y_host.copy_(y_dev, non_blocking=True)
-        stream.synchronize()
-    ew_ms = (time.perf_counter() - tt) * 1e3 / ew_steps
+    h2d = sum(t.numel() for t in in_host)
+
+    ew = None
+    if w["kind"] == "gemv":
+        # weights streamed from the host as well (every step copies all W_r)
+        W_host = [torch.from_numpy(np.ascontiguousarray(W[r])).view(torch.uint8).reshape(-1).pin_memory()
+                  for r in range(R)]
+        w_dev = [ws.w_view(r, 0) for r in range(R)]
+        ew_steps = max(3, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        tt = time.perf_counter()
+        for i in range(ew_steps):
+            with torch.cuda.stream(stream):
+                for r in range(R):
+                    w_dev[r].copy_(W_host[r], non_blocking=True)
+                    in_dev[r].copy_(in_host[r], non_blocking=True)
+                ws.run(stream, copy=0)
+                out_host.copy_(out_dev, non_blocking=True)
+            stream.synchronize()
+        ew = (time.perf_counter() - tt) * 1e3 / ew_steps
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
 
-    # ---- max over ranks ----
-    vals = torch.tensor([step_ms, e2e_ms, ew_ms, statistics.mean(launch_ms)], dtype=torch.float64)
-    if world > 1:
-        t = vals.to(dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        vals = t.cpu()
-    step_ms, e2e_ms, ew_ms, mean_launch_ms = [float(v) for v in vals]
+    step_ms, e2e_ms, ew_ms, mean_launch_ms = max_over_ranks(
+        [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms)], world, dev)
     ws.close()
     if rank != 0:
         return None
 
     peak, peak_kind = measured_hbm_peak()
     achieved = nbytes / (mean_launch_ms * 1e-3) / 1e9
-    kernel = kernel_name(plan)
     line = {
         "metric": METRIC,
-        "value": round(world * nbytes / (step_ms * 1e-3) / 1e9, 2),
+        "value": round(throughput_gbs(nbytes, step_ms, world), 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -331,24 +396,23 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "accumulate": "f32",
-        "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16 RNE)",
+        "data": DATA,
         "config": {
-            "workload": args.workload, "R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B,
+            "workload": args.workload, **config_extra,
             "algorithmic_bytes_per_call": nbytes,
             "l2": (f"L2 flushed (2x{L2_BYTES // 10**6} MB write) between launches; step time = kernel time"
                    if flush else
-                   f"inputs larger than L2: {copies} rotating copies of W ({working_set / 1e9:.2f} GB)"),
+                   f"inputs larger than L2: {copies} rotating copies ({working_set / 1e9:.2f} GB)"),
             "parallelism": "R ranks as symmetric slots on one GPU" + (f"; {world} independent replicas"
                                                                      if world > 1 else ""),
-            "plan": plan,
         },
         "roofline": {
             "bound": "hbm",
             "kernel": kernel,
             "achieved": round(achieved, 1),
             "peak": peak,
-            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s",
+            "peak_kind": ("measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                          else "fallback 6.8 TB/s"),
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(kernel, args.workload, kernel_source_sha()),
@@ -357,19 +421,20 @@ def run_ours(args, rank, world, local_rank):
         },
         "clocks": clocks,
         "e2e": {
-            "value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "value": round(throughput_gbs(nbytes, e2e_ms, world), 2), "unit": "GB/s",
             "us_per_call": round(e2e_ms * 1e3, 2),
-            "h2d_bytes_per_step": R * B * (K // R) * 2, "d2h_bytes_per_step": B * N * 2,
-            "what": "x_r of every rank H2D from pinned memory, gemv_all_reduce, y (slot 0) D2H, "
-                    "stream synchronised every step; W_r resident (model weights)",
-        },
-        "e2e_weights_from_host": {
-            "value": round(nbytes / (ew_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "us_per_call": round(ew_ms * 1e3, 2),
-            "h2d_bytes_per_step": N * K * 2 + R * B * (K // R) * 2, "d2h_bytes_per_step": B * N * 2,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
+            "what": ("per-step inputs H2D from pinned memory, the call, the result (slot 0) D2H, stream "
+                     "synchronised every step" + ("; W_r resident (model weights)" if w["kind"] == "gemv" else "")),
         },
         "gpu_launches": args.steps,
     }
+    if ew is not None:
+        line["e2e_weights_from_host"] = {
+            "value": round(throughput_gbs(nbytes, ew_ms, world), 2), "unit": "GB/s",
+            "us_per_call": round(ew_ms * 1e3, 2),
+            "h2d_bytes_per_step": W.nbytes + h2d, "d2h_bytes_per_step": out_bytes,
+        }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     return line
@@ -378,53 +443,59 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------------ CPU oracle
 
 
-def _oracle_sample(name, rows):
-    """Inputs restricted to the first `rows` output rows of the workload."""
-    import synth
-
-    w = workload(name)
-    W, x = synth.gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
-    return w, W, x
-
-
 def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0):
-    """Time the oracle (as it is) on this host's cores on row samples of the
-    workload; returns the cpu_baseline object (value in GB/s of algorithmic
-    bytes, scaled to the rows processed)."""
+    """Time the oracle (as it is) on this host's cores on the workload: with
+    `steps` None, repeat the full call for about `budget_s` seconds; else run
+    exactly `steps` calls, each on a row sample sized so that all of them fit
+    in about `budget_s`.  Returns the cpu_baseline object (GB/s of algorithmic
+    bytes, the time scaled to a full call)."""
     import numpy as np
 
     import oracle
+    import synth
 
-    w, W, x = _oracle_sample(name, None)
-    R, N, K, B = w["R"], w["N"], w["K"], w["B"]
+    w = workload(name)
     threads = host_cores()
+    nbytes = workload_bytes(w)
+    if w["kind"] == "allreduce":
+        inp = synth.allreduce_inputs(w["R"], w["n"], w["seed"])
+        full = inp.shape[1]
+
+        def call(rows):
+            oracle.one_shot_all_reduce(np.ascontiguousarray(inp[:, :rows]), threads=threads)
+        unit = "elements per slot"
+    else:
+        W, x = synth.gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
+        full = w["N"]
+
+        def call(rows):
+            oracle.gemv_all_reduce(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
+        unit = "rows"
     t = time.perf_counter()
-    oracle.gemv_all_reduce(W[:, :64], x, threads=threads)
-    per_row = max((time.perf_counter() - t) / 64, 1e-9)
+    call(full)                                  # calibration: one full call
+    t_full = max(time.perf_counter() - t, 1e-6)
     if steps is None:
-        rows = N
-        reps = max(1, int(budget_s / (per_row * N)))
+        rows = full if t_full <= budget_s else max(1, int(full * budget_s / t_full))
+        reps = max(1, int(budget_s / (t_full * rows / full)))
     else:
         per_step = budget_s / max(1, steps + warmup)
-        rows = int(max(1, min(N, per_step / per_row)))
+        rows = max(1, min(full, int(full * per_step / t_full)))
         reps = steps
-    Ws = np.ascontiguousarray(W[:, :rows])
-    for _ in range(warmup):
-        oracle.gemv_all_reduce(Ws, x, threads=threads)
+        for _ in range(warmup):
+            call(rows)
     t = time.perf_counter()
     for _ in range(reps):
-        oracle.gemv_all_reduce(Ws, x, threads=threads)
+        call(rows)
     el = time.perf_counter() - t
-    frac = rows / N
-    sec_per_call = el / reps / frac
+    sec_per_call = el / reps * full / rows
     return {
-        "value": round(algorithmic_bytes(R, N, K, B) / sec_per_call / 1e9, 4),
+        "value": round(nbytes / sec_per_call / 1e9, 4),
         "unit": "GB/s",
         "us_per_call_equiv": round(sec_per_call * 1e6, 1),
         "cores": threads,
         "kind": "oracle",
-        "sample": f"{rows} of {N} rows of {name} (all R={R} ranks, full K={K}), {reps} repetitions, "
-                  f"{el:.1f} s; time scaled to the full call",
+        "sample": (f"{rows} of {full} {unit} of {name}, {reps} repetitions, {el:.1f} s of CPU time; "
+                   "time scaled to the full call"),
     }
 
 
@@ -432,24 +503,22 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = workload(args.workload)
-    R, N, K, B = w["R"], w["N"], w["K"], w["B"]
     cb = cpu_baseline(args.workload, budget_s=min(120.0, 2.0 * (args.steps + args.warmup)),
                       steps=args.steps, warmup=args.warmup)
     sec = cb["us_per_call_equiv"] * 1e-6
+    cfg = {k: w[k] for k in ("R", "N", "K", "B", "n") if k in w}
     return {
         "metric": METRIC, "impl": "reference", "value": cb["value"], "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16 RNE)",
-        "config": {"workload": args.workload, "R": R, "N": N, "K": K, "B": B,
-                   "algorithmic_bytes_per_call": algorithmic_bytes(R, N, K, B)},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": {"workload": args.workload, **cfg, "algorithmic_bytes_per_call": workload_bytes(w)},
         "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
 
 
-def main():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20000)
@@ -457,22 +526,27 @@ def main():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="mlp_down_decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk", "dyn"), default="auto",
                    help="force one kernel (measurement only)")
     p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 4),
-                   help="stream-K slabs per pipeline stage (0 = library default)")
+                   help="TMA kernels: slabs per pipeline stage (0 = library default)")
     p.add_argument("--sk-cps", type=int, default=0, choices=(0, 1, 2, 3),
-                   help="stream-K resident CTAs per SM (0 = library default)")
+                   help="TMA kernels: resident CTAs per SM (0 = library default)")
     p.add_argument("--sk-grid", type=int, default=0,
-                   help="stream-K grid: 0 library default, -1 one CTA per (tile, rank), or a count")
+                   help="stream-K grid: 0 library default, -S = S CTAs per (tile, rank), or a count")
     p.add_argument("--dyn-splits", type=int, default=0,
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
-                   help="stream-K engine: -1 auto, 0 tcgen05, 1 FFMA")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
-    args = p.parse_args()
+                   help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
+    args = p.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

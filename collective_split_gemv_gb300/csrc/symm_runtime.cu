@@ -171,15 +171,23 @@ int num_sms(int device) {
 constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3, kPathDyn = 4;
 constexpr int kSkFfmaMaxBatch = 2;
 
-int gemv_path(const symm_handle *h, int B, int Kr) {
-    (void)B;
+// Below this many bytes of W a call is latency-bound: the persistent
+// kernel's start-up costs more than it saves, and for narrow batches the
+// one-CTA-per-tile CUDA-core kernel returns first (measured on 0.3-17 MB).
+constexpr size_t kSmallWBytes = 24u << 20;
+constexpr int kSmallMaxBatch = 4;
+
+int gemv_path(const symm_handle *h, int N, int B, int Kr) {
     if (h->opt_gemv_path != 0) return h->opt_gemv_path;
-    return Kr > 0 ? kPathDyn : kPathFfma;
+    if (Kr == 0) return kPathFfma;
+    const size_t wbytes = (size_t)N * (size_t)Kr * 2 * (size_t)h->R;
+    if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) return kPathFfma;
+    return kPathDyn;
 }
 
-int rows_per_tile_for(const symm_handle *h, int B, int Kr) {
+int rows_per_tile_for(const symm_handle *h, int N, int B, int Kr) {
     if (B < 1 || B > SYMM_MAX_BATCH) return 0;
-    switch (gemv_path(h, B, Kr)) {
+    switch (gemv_path(h, N, B, Kr)) {
         case kPathFfma: return ffma_rows_per_tile(B);
         case kPathTc: return kTcRows;
         case kPathSk: return kTcRows;
@@ -275,8 +283,8 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
     if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
         return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
                     (size_t)B * (size_t)N * 4, h->scratch_bytes);
-    pl->path = gemv_path(h, B, Kr);
-    pl->rows = rows_per_tile_for(h, B, Kr);
+    pl->path = gemv_path(h, N, B, Kr);
+    pl->rows = rows_per_tile_for(h, N, B, Kr);
     if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     pl->tiles = (N + pl->rows - 1) / pl->rows;
     if (pl->tiles > h->max_tiles)
@@ -307,7 +315,13 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
         long long G = h->opt_sk_grid > 0 ? h->opt_sk_grid : (long long)num_sms(h->device) * pl->cps;
         // K splits: the requested count (option), else none; limited by the K
         // blocks, the scratch region (one partial per split) and the pad.
-        long long S = h->opt_dyn_splits > 0 ? h->opt_dyn_splits : 1;
+        // Automatic: split only when the (tile, rank) pairs fill at most a
+        // quarter of the grid, and then to about half of it -- splits cost a
+        // partial and a reduction input each, and measured slower whenever
+        // the pairs alone already kept most SMs streaming.
+        long long S = h->opt_dyn_splits > 0
+                          ? h->opt_dyn_splits
+                          : (4 * pairs > G ? 1 : std::min<long long>(8, (G + 2 * pairs - 1) / (2 * pairs)));
         S = std::min<long long>(S, KB);
         while (S > 1 && ((size_t)S * B * N * 4 > h->scratch_bytes || (long long)pl->tiles * S > h->max_tiles)) --S;
         const long long KBs = (KB + S - 1) / S;

@@ -127,36 +127,55 @@ class GemvWorkspace:
 
 
 class AllReduceWorkspace:
-    def __init__(self, R: int, n: int, device: int | None = None, separate_out: bool = True):
-        self.R, self.n = R, n
+    """R slots holding `copies` input arrays of n bf16 and one output array
+    (or, in place, each input array is its own output)."""
+
+    def __init__(self, R: int, n: int, device: int | None = None, separate_out: bool = True, copies: int = 1):
+        self.R, self.n, self.copies = R, n, copies
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.bytes = n * 2
-        self.in_off = 0
-        self.out_off = _up(max(self.bytes, 1)) if separate_out else 0
-        self.slot_bytes = self.out_off + _up(max(self.bytes, 1)) if separate_out else _up(max(self.bytes, 1))
+        per = _up(max(self.bytes, 1))
+        # copy c: input at in_offs[c], output at out_offs[c] (its own region, or
+        # the input itself in place) -- rotating both keeps writes out of L2 too
+        self.in_offs = [c * per for c in range(copies)]
+        self.in_off = self.in_offs[0]
+        self.separate_out = separate_out
+        self.out_offs = [(copies + c) * per for c in range(copies)] if separate_out else list(self.in_offs)
+        self.out_off = self.out_offs[0]
+        self.slot_bytes = (2 * copies if separate_out else copies) * per
         with torch.cuda.device(self.device):
             self.h = symm_alloc(R, self.slot_bytes, 0, 4096)
         self.slots, self.pads, self.stride = symm_rendezvous(self.h)
         self.base = self.slots[0]
 
+    def _out(self, copy: int) -> int:
+        return self.out_offs[copy]
+
     def view(self, rank: int, offset: int, nbytes: int) -> torch.Tensor:
         return torch.as_tensor(DeviceView(self.slots[rank] + offset, (nbytes,)), device=self.device)
 
-    def load_in(self, inp: np.ndarray) -> None:
-        assert inp.shape == (self.R, self.n) and inp.dtype == np.uint16
-        for r in range(self.R):
-            self.view(r, self.in_off, self.bytes).copy_(
-                torch.from_numpy(np.ascontiguousarray(inp[r])).view(torch.uint8))
+    def in_view(self, rank: int, copy: int = 0) -> torch.Tensor:
+        return self.view(rank, self.in_offs[copy], self.bytes)
 
-    def read_out(self) -> np.ndarray:
+    def out_view(self, rank: int, copy: int = 0) -> torch.Tensor:
+        return self.view(rank, self._out(copy), self.bytes)
+
+    def load_in(self, inp: np.ndarray, copy: int = 0) -> None:
+        assert inp.shape == (self.R, self.n) and inp.dtype == np.uint16
+        if self.bytes == 0:
+            return
+        for r in range(self.R):
+            self.in_view(r, copy).copy_(torch.from_numpy(np.ascontiguousarray(inp[r])).view(torch.uint8))
+
+    def read_out(self, copy: int = 0) -> np.ndarray:
         torch.cuda.synchronize(self.device)
         out = np.empty((self.R, self.n), dtype=np.uint16)
         for r in range(self.R):
-            out[r] = self.view(r, self.out_off, self.bytes).cpu().numpy().view(np.uint16)
+            out[r] = self.out_view(r, copy).cpu().numpy().view(np.uint16)
         return out
 
-    def run(self, stream=None) -> None:
-        one_shot_all_reduce(self.h, self.base + self.in_off, self.base + self.out_off, self.R, self.n,
+    def run(self, stream=None, copy: int = 0) -> None:
+        one_shot_all_reduce(self.h, self.base + self.in_offs[copy], self.base + self._out(copy), self.R, self.n,
                             stream)
 
     def close(self) -> None:

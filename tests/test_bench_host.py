@@ -1,0 +1,71 @@
+"""Host-side logic of bench.py, on the CPU: byte accounting against the
+hand-computed per-call figures of the five workloads, argument defaults, and
+the max-over-ranks aggregation of the multi-GPU replicas with two gloo ranks."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_algorithmic_bytes_match_hand_computed_values():
+    # W + x + partials written and read back + R replicated outputs
+    assert bench.algorithmic_bytes(2, 256, 512, 1) == 262_144 + 1_024 + 4_096 + 1_024
+    assert bench.algorithmic_bytes(4, 8192, 8192, 8) == 136_970_240
+    assert bench.algorithmic_bytes(8, 8192, 28672, 1) == 470_474_752
+    assert bench.algorithmic_bytes(8, 16384, 53248, 16) == 1_767_505_920
+    assert bench.allreduce_bytes(8, 4_194_304) == 134_217_728
+    for name in ("tiny", "allreduce", "attn_out_proj", "mlp_down_decode", "mlp_down_large"):
+        assert bench.workload_bytes(bench.workload(name)) > 0
+
+
+def test_throughput_is_whole_job():
+    assert bench.throughput_gbs(1e9, 1.0) == pytest.approx(1000.0)
+    assert bench.throughput_gbs(1e9, 1.0, world=4) == pytest.approx(4000.0)
+
+
+def test_default_arguments_time_the_decode_workload():
+    a = bench.parse_args([])
+    assert a.workload == "mlp_down_decode" and a.impl == "ours" and a.gpus == 1 and a.warmup >= 3
+    assert bench.parse_args(["--warmup", "1"]).warmup == 3
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.max_over_ranks([1.5, 2.0], 1) == [1.5, 2.0]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, queue):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        vals = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 3.0], world)
+        queue.put((rank, vals))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, queue)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = dict(queue.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert results[0] == results[1] == [2.0, 10.0, 3.0]

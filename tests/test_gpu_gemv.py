@@ -318,7 +318,9 @@ def test_many_launches_keep_tickets_consistent(path):
             ws.run(s)
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
         if path in (csg.GEMV_PATH_FFMA, csg.GEMV_PATH_DYN):
-            assert int(_counter_view(ws, 3).item()) == 50 * R   # one contributor per rank
+            # R * splits contributors per tile and launch
+            splits = csg.symm_gemv_plan(ws.h, N, K, B)["splits"]
+            assert int(_counter_view(ws, 3).item()) == 50 * R * splits
         else:
             assert int(_counter_view(ws, 3).item()) % 50 == 0   # C_3 contributors per launch
         check_gemv(W, x, ws.read_y())

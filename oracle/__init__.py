@@ -15,6 +15,16 @@ Every function follows the definitions stated in ``oracle.c``:
 * ``one_shot_all_reduce``: out[i] = sum_r in_r[i] in fp64, rank order, RNE to
   bf16 for every rank ("PyTorch Symmetric Memory" talk, one-shot segment;
   symmetric memory docs, ``one_shot_all_reduce``).
+* ``reduce_scatter``: rank s keeps block s of the flat sum; ``gemv_reduce_scatter``:
+  rank s keeps batch rows [s*B/R, (s+1)*B/R) of the fused layer's output
+  ("Bay.Area.AI: Tensor and 2D Parallelism", sequence-parallel passage).  The
+  two-shot all-reduce reaches the all-reduce definition, so its oracle is
+  ``one_shot_all_reduce``.
+* ``all_reduce_bias_rmsnorm`` / ``gemv_bias_rmsnorm``: all-reduce, plus bias, then
+  RMS normalisation per row with gain gamma and eps inside the square root
+  ("PyTorch Symmetric Memory" talk, fused-kernel segment).
+* ``tile_reduce``: 2-D strided tiles summed over ranks into one root's output
+  tile each (symmetric memory docs, ``tile_reduce`` / ``multi_root_tile_reduce``).
 * ``bf16_value`` / ``bf16_round``: the bf16 encoding, decoded from its fields
   and rounded from fp64 bit fields.
 
@@ -70,6 +80,21 @@ def _bind(lib):
     lib.oracle_one_shot_all_reduce.argtypes = [ctypes.c_int, ctypes.c_size_t, u16p, ip, f64p, u16p,
                                                ctypes.c_int]
     lib.oracle_one_shot_all_reduce.restype = ctypes.c_int
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    lib.oracle_reduce_scatter.argtypes = [ctypes.c_int, ctypes.c_size_t, u16p, f64p, u16p]
+    lib.oracle_reduce_scatter.restype = ctypes.c_int
+    lib.oracle_gemv_reduce_scatter.argtypes = [ctypes.c_int] * 4 + [u16p, u16p, f64p, u16p, ctypes.c_int]
+    lib.oracle_gemv_reduce_scatter.restype = ctypes.c_int
+    lib.oracle_all_reduce_bias_rmsnorm.argtypes = [ctypes.c_int] * 3 + [u16p, u16p, u16p, ctypes.c_double,
+                                                                        f64p, u16p]
+    lib.oracle_all_reduce_bias_rmsnorm.restype = ctypes.c_int
+    lib.oracle_gemv_bias_rmsnorm.argtypes = [ctypes.c_int] * 4 + [u16p, u16p, u16p, u16p, ctypes.c_double,
+                                                                  f64p, u16p, ctypes.c_int]
+    lib.oracle_gemv_bias_rmsnorm.restype = ctypes.c_int
+    lib.oracle_tile_reduce.argtypes = [ctypes.c_int, ctypes.c_size_t, u16p, u16p, ctypes.c_int, szp,
+                                       ctypes.c_size_t, ip, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
+                                       ctypes.c_size_t, f64p]
+    lib.oracle_tile_reduce.restype = ctypes.c_int
     return lib
 
 
@@ -146,9 +171,98 @@ class Oracle:
             raise ValueError(f"oracle_one_shot_all_reduce returned {rc}")
         return ref, out
 
+    def reduce_scatter(self, inp: np.ndarray):
+        """inp: (R, n) bf16 words, n % R == 0.  Returns (ref fp64 (n,), out
+        bf16 (R, n // R) -- rank s holds block s of the sum)."""
+        inp = np.ascontiguousarray(inp, dtype=np.uint16)
+        R, n = inp.shape
+        ref = np.empty(n, dtype=np.float64)
+        out = np.empty((R, n // R if R else 0), dtype=np.uint16)
+        rc = self.lib.oracle_reduce_scatter(R, n, _u16(inp), _f64(ref), _u16(out))
+        if rc != 0:
+            raise ValueError(f"oracle_reduce_scatter returned {rc}")
+        return ref, out
+
+    def gemv_reduce_scatter(self, W: np.ndarray, x: np.ndarray, threads: int | None = None):
+        """W (R, N, K_r), x (R, B, K_r), B % R == 0.  Returns (y_ref fp64
+        (B, N), out bf16 (R, B // R, N) -- rank s holds rows s*B/R ...)."""
+        W = np.ascontiguousarray(W, dtype=np.uint16)
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        R, N, Kr = W.shape
+        B = x.shape[1]
+        y_ref = np.empty((B, N), dtype=np.float64)
+        out = np.empty((R, B // R, N), dtype=np.uint16)
+        rc = self.lib.oracle_gemv_reduce_scatter(R, N, R * Kr, B, _u16(W), _u16(x), _f64(y_ref), _u16(out),
+                                                 threads or _threads())
+        if rc != 0:
+            raise ValueError(f"oracle_gemv_reduce_scatter returned {rc}")
+        return y_ref, out
+
+    def all_reduce_bias_rmsnorm(self, inp: np.ndarray, bias=None, gamma=None, eps: float = 1e-6):
+        """inp (R, rows, H) bf16 words; bias, gamma (H,) words or None.
+        Returns (ref fp64 (rows, H), out bf16 (R, rows, H))."""
+        inp = np.ascontiguousarray(inp, dtype=np.uint16)
+        R, rows, H = inp.shape
+        bp, gp = _opt_u16(bias, H), _opt_u16(gamma, H)
+        ref = np.empty((rows, H), dtype=np.float64)
+        out = np.empty((R, rows, H), dtype=np.uint16)
+        rc = self.lib.oracle_all_reduce_bias_rmsnorm(R, rows, H, _u16(inp), bp[1], gp[1], eps, _f64(ref),
+                                                     _u16(out))
+        if rc != 0:
+            raise ValueError(f"oracle_all_reduce_bias_rmsnorm returned {rc}")
+        return ref, out
+
+    def gemv_bias_rmsnorm(self, W: np.ndarray, x: np.ndarray, bias=None, gamma=None, eps: float = 1e-6,
+                          threads: int | None = None):
+        """The fused layer followed by bias + RMSNorm over each batch row's N
+        outputs.  Returns (y_ref fp64 (B, N), y bf16 (R, B, N))."""
+        W = np.ascontiguousarray(W, dtype=np.uint16)
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        R, N, Kr = W.shape
+        B = x.shape[1]
+        bp, gp = _opt_u16(bias, N), _opt_u16(gamma, N)
+        y_ref = np.empty((B, N), dtype=np.float64)
+        y = np.empty((R, B, N), dtype=np.uint16)
+        rc = self.lib.oracle_gemv_bias_rmsnorm(R, N, R * Kr, B, _u16(W), _u16(x), bp[1], gp[1], eps,
+                                               _f64(y_ref), _u16(y), threads or _threads())
+        if rc != 0:
+            raise ValueError(f"oracle_gemv_bias_rmsnorm returned {rc}")
+        return y_ref, y
+
+    def tile_reduce(self, slots_in: np.ndarray, slots_out: np.ndarray, in_offs, out_off: int, roots,
+                    rows: int, cols: int, ld_in: int, ld_out: int):
+        """slots_in, slots_out: (R, slot_elems) bf16 words; tile i starts at
+        element in_offs[i] of every slot and is summed into slot roots[i]'s
+        output tile at out_off.  Returns (ref fp64 (ntiles, rows, cols), the
+        updated copy of slots_out)."""
+        slots_in = np.ascontiguousarray(slots_in, dtype=np.uint16)
+        out = np.array(slots_out, dtype=np.uint16, copy=True, order="C")
+        R, slot_elems = slots_in.shape
+        offs = np.ascontiguousarray(in_offs, dtype=np.uint64)
+        rts = np.ascontiguousarray(roots, dtype=np.int32)
+        nt = len(offs)
+        ref = np.empty((nt, rows, cols), dtype=np.float64)
+        rc = self.lib.oracle_tile_reduce(R, slot_elems, _u16(slots_in), _u16(out), nt,
+                                         offs.ctypes.data_as(ctypes.POINTER(ctypes.c_size_t)), out_off,
+                                         rts.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), rows, cols, ld_in,
+                                         ld_out, _f64(ref))
+        if rc != 0:
+            raise ValueError(f"oracle_tile_reduce returned {rc}")
+        return ref, out
+
 
 def _u16(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def _opt_u16(a, n):
+    """(array kept alive, pointer) for an optional bf16 vector of length n."""
+    if a is None:
+        return None, None
+    v = np.ascontiguousarray(a, dtype=np.uint16)
+    if v.shape != (n,):
+        raise ValueError(f"expected a vector of {n} bf16 words, got shape {v.shape}")
+    return v, _u16(v)
 
 
 def _f64(a):
@@ -192,3 +306,24 @@ def bf16_value(words):
 
 def bf16_round(values):
     return load().bf16_round(values)
+
+
+def reduce_scatter(inp):
+    return load().reduce_scatter(inp)
+
+
+def gemv_reduce_scatter(W, x, threads=None):
+    return load().gemv_reduce_scatter(W, x, threads)
+
+
+def all_reduce_bias_rmsnorm(inp, bias=None, gamma=None, eps=1e-6):
+    return load().all_reduce_bias_rmsnorm(inp, bias, gamma, eps)
+
+
+def gemv_bias_rmsnorm(W, x, bias=None, gamma=None, eps=1e-6, threads=None):
+    return load().gemv_bias_rmsnorm(W, x, bias, gamma, eps, threads)
+
+
+def tile_reduce(slots_in, slots_out, in_offs, out_off, roots, rows, cols, ld_in, ld_out):
+    return load().tile_reduce(slots_in, slots_out, in_offs, out_off, roots, rows, cols, ld_in, ld_out)
+

@@ -36,11 +36,20 @@
  *
  * Every rank's output slot receives the same rounded value; the oracle writes
  * all R replicas and checks that they are identical.
+ *
+ * Further collectives on the same slots, each defined where it is written
+ * below: the reduce-scatter (flat, and along the batch rows of the fused
+ * layer), the all-reduce followed by a bias and RMS normalisation (alone and
+ * as the fused layer's epilogue), and the 2-D tile reduce to one or several
+ * roots.  A two-shot all-reduce reaches exactly the all-reduce definition
+ * (its two phases change where each sum is computed, not the sum), so its
+ * oracle is oracle_one_shot_all_reduce.
  */
 #include <math.h>
 #include <pthread.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------ bf16 words */
@@ -273,5 +282,173 @@ int oracle_one_shot_all_reduce(int R, size_t n, const uint16_t *in, const int *o
     for (int t = 0; t < threads; ++t)
         if (live[t]) pthread_join(tid[t], NULL);
     if (out && !replicas_identical(out, R, n)) return -2;
+    return 0;
+}
+
+/* ------------------------------------------------------- reduce-scatter */
+
+/* The sequence-parallel ending of the row-parallel layer: "Bay.Area.AI:
+ * Tensor and 2D Parallelism" (talk, sequence-parallel passage) -- after the
+ * row-wise sharded linear, a reduce-scatter instead of an all-reduce leaves
+ * each rank one shard of the summed tensor.  The shards are the R equal
+ * consecutive blocks of the flat tensor: rank s keeps elements
+ * [s*n/R, (s+1)*n/R) of the sum (n % R == 0).
+ *   ref[i]          fp64 sum over ranks in order 0..R-1, i < n
+ *   out[s][j]       bf16 RNE of ref[s*(n/R) + j]
+ * Returns 0, -1 on bad arguments. */
+int oracle_reduce_scatter(int R, size_t n, const uint16_t *in, double *ref, uint16_t *out) {
+    if (R < 1 || R > 64 || n % (size_t)R) return -1;
+    const double *val = bf16_table();
+    const size_t c = n / (size_t)R;
+    for (int s = 0; s < R; ++s) {
+        for (size_t j = 0; j < c; ++j) {
+            const size_t i = (size_t)s * c + j;
+            double acc = 0.0;
+            for (int r = 0; r < R; ++r) acc += val[in[(size_t)r * n + i]];
+            ref[i] = acc;
+            out[(size_t)s * c + j] = oracle_bf16_round(acc);
+        }
+    }
+    return 0;
+}
+
+/* Reduce-scatter of the fused layer's output along the token (batch)
+ * dimension, the dimension sequence parallelism shards: rank s keeps rows
+ * b in [s*B/R, (s+1)*B/R) of y = sum_r W_r x_r (B % R == 0).
+ *   y_ref[b][n]     the fp64 sum, as oracle_gemv_all_reduce computes it
+ *   out[s][i][n]    bf16 RNE of y_ref[s*B/R + i][n]
+ * Returns 0, -1 on bad arguments. */
+int oracle_gemv_reduce_scatter(int R, int N, int K, int B, const uint16_t *W, const uint16_t *x,
+                               double *y_ref, uint16_t *out, int threads) {
+    if (R < 1 || R > 64 || B % R) return -1;
+    int rc = oracle_gemv_all_reduce(R, N, K, B, W, x, NULL, y_ref, NULL, threads);
+    if (rc) return rc;
+    const int Bs = B / R;
+    for (int s = 0; s < R; ++s)
+        for (int i = 0; i < Bs; ++i)
+            for (int n = 0; n < N; ++n)
+                out[((size_t)s * Bs + i) * N + n] = oracle_bf16_round(y_ref[(size_t)(s * Bs + i) * N + n]);
+    return 0;
+}
+
+/* ------------------------------------------- all-reduce + bias + RMSNorm */
+
+/* "PyTorch Symmetric Memory: A New Programming Paradigm for Distributed AI"
+ * (talk, the fused kernel segment): an all-reduce, then a bias added to its
+ * result, then RMS normalisation, in one kernel.  Per row of H elements:
+ *     z[h]  = (sum_r in_r[h]) + bias[h]
+ *     ms    = (1/H) sum_h z[h]^2
+ *     y[h]  = z[h] / sqrt(ms + eps) * gamma[h]
+ * (RMS normalisation with a per-element gain and eps inside the square root;
+ * NULL bias means zeros, NULL gamma means ones).  Everything in fp64, one
+ * rounding to bf16 at the end, the same value for every rank. */
+static void bias_rmsnorm_row(double *z, int H, const uint16_t *bias, const uint16_t *gamma, double eps,
+                             double *y) {
+    const double *val = bf16_table();
+    double ss = 0.0;
+    for (int h = 0; h < H; ++h) {
+        if (bias) z[h] += val[bias[h]];
+        ss += z[h] * z[h];
+    }
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int h = 0; h < H; ++h) y[h] = z[h] * inv * (gamma ? val[gamma[h]] : 1.0);
+}
+
+/* in [R][rows][H]; ref [rows][H] (fp64 result before rounding);
+ * out [R][rows][H] or NULL.  Returns 0, -1 on bad arguments, -2 if the
+ * replicas differ. */
+int oracle_all_reduce_bias_rmsnorm(int R, int rows, int H, const uint16_t *in, const uint16_t *bias,
+                                   const uint16_t *gamma, double eps, double *ref, uint16_t *out) {
+    if (R < 1 || R > 64 || rows < 0 || H < 1 || !(eps >= 0.0)) return -1;
+    const double *val = bf16_table();
+    double *z = (double *)malloc((size_t)H * sizeof(double));
+    if (!z) return -1;
+    for (int i = 0; i < rows; ++i) {
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int r = 0; r < R; ++r) acc += val[in[((size_t)r * rows + i) * H + h]];
+            z[h] = acc;
+        }
+        bias_rmsnorm_row(z, H, bias, gamma, eps, ref + (size_t)i * H);
+        if (out)
+            for (int h = 0; h < H; ++h) {
+                const uint16_t w = oracle_bf16_round(ref[(size_t)i * H + h]);
+                for (int s = 0; s < R; ++s) out[((size_t)s * rows + i) * H + h] = w;
+            }
+    }
+    free(z);
+    if (out && !replicas_identical(out, R, (size_t)rows * H)) return -2;
+    return 0;
+}
+
+/* The same epilogue on the fused layer: y[b] = RMSNorm(W x[b] + bias) over
+ * the N outputs of each batch row, the GEMV sum as oracle_gemv_all_reduce
+ * computes it.  y_ref [B][N]; out [R][B][N] or NULL. */
+int oracle_gemv_bias_rmsnorm(int R, int N, int K, int B, const uint16_t *W, const uint16_t *x,
+                             const uint16_t *bias, const uint16_t *gamma, double eps, double *y_ref,
+                             uint16_t *out, int threads) {
+    if (N < 1 || !(eps >= 0.0)) return -1;
+    double *z = (double *)malloc((size_t)B * N * sizeof(double) + 1);
+    if (!z) return -1;
+    int rc = oracle_gemv_all_reduce(R, N, K, B, W, x, NULL, z, NULL, threads);
+    if (rc == 0) {
+        for (int b = 0; b < B; ++b) {
+            bias_rmsnorm_row(z + (size_t)b * N, N, bias, gamma, eps, y_ref + (size_t)b * N);
+            if (out)
+                for (int n = 0; n < N; ++n) {
+                    const uint16_t w = oracle_bf16_round(y_ref[(size_t)b * N + n]);
+                    for (int s = 0; s < R; ++s) out[((size_t)s * B + b) * N + n] = w;
+                }
+        }
+    }
+    free(z);
+    return rc;
+}
+
+/* ------------------------------------------------------------ tile reduce */
+
+/* PyTorch Symmetric Memory documentation, op reference `tile_reduce` and
+ * `multi_root_tile_reduce`, and the talk's tile-communication segment: a 2-D
+ * tile (rows x cols elements of a row-major tensor with leading dimension
+ * ld, i.e. not contiguous) is summed over all ranks and the sum is written
+ * into the output tile of one root rank only; with several tiles each goes
+ * to its own root, and no rank is root twice.
+ *
+ * The buffers are whole slots: in and out are [R][slot_elems] bf16 words;
+ * tile i starts at element in_off[i] of every slot, the output tile at
+ * element out_off.  For every tile i, element (a, c):
+ *     ref[i][a][c] = sum_r in[r][in_off[i] + a*ld_in + c]   (fp64, rank order)
+ *     out[roots[i]][out_off + a*ld_out + c] = bf16 RNE of ref[i][a][c]
+ * and nothing else of out changes.  Returns 0, -1 on bad arguments (root
+ * out of range or repeated, a tile outside the slot). */
+int oracle_tile_reduce(int R, size_t slot_elems, const uint16_t *in, uint16_t *out, int ntiles,
+                       const size_t *in_off, size_t out_off, const int *roots, int rows, int cols,
+                       size_t ld_in, size_t ld_out, double *ref) {
+    if (R < 1 || R > 64 || ntiles < 1 || ntiles > R || rows < 0 || cols < 0) return -1;
+    if (rows > 0 && cols > 0) {
+        if ((size_t)cols > ld_in || (size_t)cols > ld_out) return -1;
+        if (out_off + (size_t)(rows - 1) * ld_out + (size_t)cols > slot_elems) return -1;
+    }
+    int used[64];
+    memset(used, 0, sizeof used);
+    for (int i = 0; i < ntiles; ++i) {
+        if (roots[i] < 0 || roots[i] >= R || used[roots[i]]) return -1;
+        used[roots[i]] = 1;
+        if (rows > 0 && cols > 0 && in_off[i] + (size_t)(rows - 1) * ld_in + (size_t)cols > slot_elems)
+            return -1;
+    }
+    const double *val = bf16_table();
+    for (int i = 0; i < ntiles; ++i) {
+        for (int a = 0; a < rows; ++a) {
+            for (int c = 0; c < cols; ++c) {
+                double acc = 0.0;
+                for (int r = 0; r < R; ++r)
+                    acc += val[in[(size_t)r * slot_elems + in_off[i] + (size_t)a * ld_in + (size_t)c]];
+                if (ref) ref[((size_t)i * rows + a) * cols + c] = acc;
+                out[(size_t)roots[i] * slot_elems + out_off + (size_t)a * ld_out + (size_t)c] =
+                    oracle_bf16_round(acc);
+            }
+        }
+    }
     return 0;
 }

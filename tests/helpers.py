@@ -74,6 +74,10 @@ def load_golden(name: str) -> dict:
                 cur = cases.setdefault(line[5:].strip(), {})
                 continue
             key, val = line.split(":", 1)
-            rows = [[float(t) for t in r.split()] for r in val.split(";")]
+            if val.strip() == "none":
+                cur[key.strip()] = None
+                continue
+            # "-" marks an entry the case leaves unspecified (NaN here)
+            rows = [[float("nan") if t == "-" else float(t) for t in r.split()] for r in val.split(";")]
             cur[key.strip()] = rows[0][0] if len(rows) == 1 and len(rows[0]) == 1 else np.array(rows)
     return cases

@@ -8,7 +8,10 @@ import os
 import pytest
 
 import oracle
-from test_oracle_pins import PINS
+from test_oracle_pins import PINS as GEMV_PINS
+from test_oracle_pins_collectives import PINS as COLLECTIVE_PINS
+
+PINS = GEMV_PINS + COLLECTIVE_PINS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -28,6 +31,19 @@ MUTANTS = [
     ("ar_one_replica", "for (int r = 0; r < a->R; ++r) a->out", "for (int r = 0; r < 1; ++r) a->out"),
     ("gemv_one_replica", "for (int s = 0; s < g->R; ++s)\n                    g->y_out", "for (int s = 0; s < 1; ++s)\n                    g->y_out"),
     ("order_ignored", "y += rank_partial(g, g->order[i], b, n);", "y += rank_partial(g, i, b, n);"),
+    ("rs_wrong_block", "const size_t i = (size_t)s * c + j;", "const size_t i = (size_t)j * R + s;"),
+    ("rs_skip_last_rank", "for (int r = 0; r < R; ++r) acc += val[in[(size_t)r * n + i]];",
+     "for (int r = 0; r < R - 1; ++r) acc += val[in[(size_t)r * n + i]];"),
+    ("gemv_rs_rows_by_rank", "y_ref[(size_t)(s * Bs + i) * N + n]", "y_ref[(size_t)(i * R + s) * N + n]"),
+    ("rmsnorm_no_bias", "if (bias) z[h] += val[bias[h]];", "(void)bias;"),
+    ("rmsnorm_eps_outside", "1.0 / sqrt(ss / (double)H + eps)", "1.0 / (sqrt(ss / (double)H) + eps)"),
+    ("rmsnorm_sum_not_mean", "1.0 / sqrt(ss / (double)H + eps)", "1.0 / sqrt(ss + eps)"),
+    ("rmsnorm_no_gamma", "(gamma ? val[gamma[h]] : 1.0)", "1.0"),
+    ("rmsnorm_bias_after_norm_sum", "ss += z[h] * z[h];", "ss += (z[h] - (bias ? val[bias[h]] : 0.0)) * (z[h] - (bias ? val[bias[h]] : 0.0));"),
+    ("tile_root_ignored", "out[(size_t)roots[i] * slot_elems + out_off", "out[(size_t)0 * slot_elems + out_off"),
+    ("tile_ld_swapped", "(size_t)a * ld_in + (size_t)c]];", "(size_t)a * ld_out + (size_t)c]];"),
+    ("tile_transposed", "in_off[i] + (size_t)a * ld_in + (size_t)c]", "in_off[i] + (size_t)c * ld_in + (size_t)a]"),
+    ("tile_repeat_root_allowed", "used[roots[i]]) return -1;", "0) return -1;"),
 ]
 
 
@@ -43,6 +59,6 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     for pin in PINS:
         try:
             pin(orc)
-        except (AssertionError, ValueError) as e:  # noqa: PERF203
+        except (AssertionError, ValueError, pytest.fail.Exception) as e:  # noqa: PERF203
             caught.append((pin.__name__, type(e).__name__))
     assert caught, f"mutant {name} passed every pin"

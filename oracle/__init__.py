@@ -91,7 +91,7 @@ def _bind(lib):
     lib.oracle_gemv_bias_rmsnorm.argtypes = [ctypes.c_int] * 4 + [u16p, u16p, u16p, u16p, ctypes.c_double,
                                                                   f64p, u16p, ctypes.c_int]
     lib.oracle_gemv_bias_rmsnorm.restype = ctypes.c_int
-    lib.oracle_tile_reduce.argtypes = [ctypes.c_int, ctypes.c_size_t, u16p, u16p, ctypes.c_int, szp,
+    lib.oracle_tile_reduce.argtypes = [ctypes.c_int, ctypes.c_size_t, u16p, ctypes.c_size_t, u16p, ctypes.c_int, szp,
                                        ctypes.c_size_t, ip, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
                                        ctypes.c_size_t, f64p]
     lib.oracle_tile_reduce.restype = ctypes.c_int
@@ -231,18 +231,20 @@ class Oracle:
 
     def tile_reduce(self, slots_in: np.ndarray, slots_out: np.ndarray, in_offs, out_off: int, roots,
                     rows: int, cols: int, ld_in: int, ld_out: int):
-        """slots_in, slots_out: (R, slot_elems) bf16 words; tile i starts at
-        element in_offs[i] of every slot and is summed into slot roots[i]'s
-        output tile at out_off.  Returns (ref fp64 (ntiles, rows, cols), the
-        updated copy of slots_out)."""
+        """slots_in (R, in_slot), slots_out (R, out_slot): bf16 words; tile i
+        starts at element in_offs[i] of every input slot and is summed into
+        slot roots[i]'s output tile at out_off.  Returns (ref fp64 (ntiles,
+        rows, cols), the updated copy of slots_out)."""
         slots_in = np.ascontiguousarray(slots_in, dtype=np.uint16)
         out = np.array(slots_out, dtype=np.uint16, copy=True, order="C")
-        R, slot_elems = slots_in.shape
+        R, in_slot = slots_in.shape
+        if out.ndim != 2 or out.shape[0] != R:
+            raise ValueError(f"slots_out must be ({R}, out_slot), got {out.shape}")
         offs = np.ascontiguousarray(in_offs, dtype=np.uint64)
         rts = np.ascontiguousarray(roots, dtype=np.int32)
         nt = len(offs)
         ref = np.empty((nt, rows, cols), dtype=np.float64)
-        rc = self.lib.oracle_tile_reduce(R, slot_elems, _u16(slots_in), _u16(out), nt,
+        rc = self.lib.oracle_tile_reduce(R, in_slot, _u16(slots_in), out.shape[1], _u16(out), nt,
                                          offs.ctypes.data_as(ctypes.POINTER(ctypes.c_size_t)), out_off,
                                          rts.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), rows, cols, ld_in,
                                          ld_out, _f64(ref))

@@ -414,27 +414,27 @@ int oracle_gemv_bias_rmsnorm(int R, int N, int K, int B, const uint16_t *W, cons
  * into the output tile of one root rank only; with several tiles each goes
  * to its own root, and no rank is root twice.
  *
- * The buffers are whole slots: in and out are [R][slot_elems] bf16 words;
- * tile i starts at element in_off[i] of every slot, the output tile at
- * element out_off.  For every tile i, element (a, c):
+ * The buffers are whole slots: in is [R][in_slot] and out is [R][out_slot]
+ * bf16 words; tile i starts at element in_off[i] of every input slot, the
+ * output tile at element out_off of an output slot.  For every tile i, element (a, c):
  *     ref[i][a][c] = sum_r in[r][in_off[i] + a*ld_in + c]   (fp64, rank order)
  *     out[roots[i]][out_off + a*ld_out + c] = bf16 RNE of ref[i][a][c]
  * and nothing else of out changes.  Returns 0, -1 on bad arguments (root
  * out of range or repeated, a tile outside the slot). */
-int oracle_tile_reduce(int R, size_t slot_elems, const uint16_t *in, uint16_t *out, int ntiles,
+int oracle_tile_reduce(int R, size_t in_slot, const uint16_t *in, size_t out_slot, uint16_t *out, int ntiles,
                        const size_t *in_off, size_t out_off, const int *roots, int rows, int cols,
                        size_t ld_in, size_t ld_out, double *ref) {
     if (R < 1 || R > 64 || ntiles < 1 || ntiles > R || rows < 0 || cols < 0) return -1;
     if (rows > 0 && cols > 0) {
         if ((size_t)cols > ld_in || (size_t)cols > ld_out) return -1;
-        if (out_off + (size_t)(rows - 1) * ld_out + (size_t)cols > slot_elems) return -1;
+        if (out_off + (size_t)(rows - 1) * ld_out + (size_t)cols > out_slot) return -1;
     }
     int used[64];
     memset(used, 0, sizeof used);
     for (int i = 0; i < ntiles; ++i) {
         if (roots[i] < 0 || roots[i] >= R || used[roots[i]]) return -1;
         used[roots[i]] = 1;
-        if (rows > 0 && cols > 0 && in_off[i] + (size_t)(rows - 1) * ld_in + (size_t)cols > slot_elems)
+        if (rows > 0 && cols > 0 && in_off[i] + (size_t)(rows - 1) * ld_in + (size_t)cols > in_slot)
             return -1;
     }
     const double *val = bf16_table();
@@ -443,9 +443,9 @@ int oracle_tile_reduce(int R, size_t slot_elems, const uint16_t *in, uint16_t *o
             for (int c = 0; c < cols; ++c) {
                 double acc = 0.0;
                 for (int r = 0; r < R; ++r)
-                    acc += val[in[(size_t)r * slot_elems + in_off[i] + (size_t)a * ld_in + (size_t)c]];
+                    acc += val[in[(size_t)r * in_slot + in_off[i] + (size_t)a * ld_in + (size_t)c]];
                 if (ref) ref[((size_t)i * rows + a) * cols + c] = acc;
-                out[(size_t)roots[i] * slot_elems + out_off + (size_t)a * ld_out + (size_t)c] =
+                out[(size_t)roots[i] * out_slot + out_off + (size_t)a * ld_out + (size_t)c] =
                     oracle_bf16_round(acc);
             }
         }

@@ -40,7 +40,7 @@ MUTANTS = [
     ("rmsnorm_sum_not_mean", "1.0 / sqrt(ss / (double)H + eps)", "1.0 / sqrt(ss + eps)"),
     ("rmsnorm_no_gamma", "(gamma ? val[gamma[h]] : 1.0)", "1.0"),
     ("rmsnorm_bias_after_norm_sum", "ss += z[h] * z[h];", "ss += (z[h] - (bias ? val[bias[h]] : 0.0)) * (z[h] - (bias ? val[bias[h]] : 0.0));"),
-    ("tile_root_ignored", "out[(size_t)roots[i] * slot_elems + out_off", "out[(size_t)0 * slot_elems + out_off"),
+    ("tile_root_ignored", "out[(size_t)roots[i] * out_slot + out_off", "out[(size_t)0 * out_slot + out_off"),
     ("tile_ld_swapped", "(size_t)a * ld_in + (size_t)c]];", "(size_t)a * ld_out + (size_t)c]];"),
     ("tile_transposed", "in_off[i] + (size_t)a * ld_in + (size_t)c]", "in_off[i] + (size_t)c * ld_in + (size_t)a]"),
     ("tile_repeat_root_allowed", "used[roots[i]]) return -1;", "0) return -1;"),

@@ -254,6 +254,25 @@ def pin_tile_brute_force(orc):
         assert np.array_equal(out, want_out), (R, sr, sc)
 
 
+def pin_tile_separate_output_tensor(orc):
+    # the docs' quadrant example: a full n x n tensor per rank, the output a
+    # separate (n/2) x (n/2) tensor; quadrant q summed into rank q's output
+    rng = np.random.default_rng(27)
+    R, n = 4, 12
+    h = n // 2
+    vals, words = _int_words(rng, (R, n * n), -30, 30)
+    before = np.full((R, h * h), 0x7FC0, dtype=np.uint16)
+    offs = [0, h, h * n, h * n + h]
+    ref, out = orc.tile_reduce(words, before, offs, 0, [0, 1, 2, 3], h, h, n, h)
+    full = vals.reshape(R, n, n).sum(axis=0)
+    quads = [full[:h, :h], full[:h, h:], full[h:, :h], full[h:, h:]]
+    for q in range(4):
+        assert np.array_equal(ref[q], quads[q])
+        assert np.array_equal(out[q], _words(quads[q].reshape(-1)))
+    with pytest.raises(ValueError):    # the output tile must fit the output slot
+        orc.tile_reduce(words, before, offs, 1, [0, 1, 2, 3], h, h, n, h)
+
+
 def pin_tile_rejects_bad_roots_and_extents(orc):
     z = np.zeros((4, 64), dtype=np.uint16)
     for offs, roots, rows, cols, ld in (([0, 8], [1, 1], 2, 2, 8),     # root twice

@@ -60,9 +60,36 @@ def algorithmic_bytes(R, N, K, B):
     return N * K * 2 + B * K * 2 + 2 * R * B * N * 4 + R * B * N * 2
 
 
-def allreduce_bytes(R, n):
-    """One-shot all-reduce: R inputs of n bf16 read, R outputs written."""
+def allreduce_bytes(R, n, op="one_shot"):
+    """All-reduce (one- or two-shot): R inputs of n bf16 read, R outputs
+    written.  Reduce-scatter: R inputs read, one block of n / R written per
+    rank (n elements in all)."""
+    if op == "reduce_scatter":
+        return R * n * 2 + n * 2
     return 2 * R * n * 2
+
+
+def gemv_rs_bytes(R, N, K, B):
+    """Fused layer ending in a reduce-scatter: as algorithmic_bytes, but each
+    output row is stored once (in its owner's slot): B * N * 2."""
+    return N * K * 2 + B * K * 2 + 2 * R * B * N * 4 + B * N * 2
+
+
+def gemv_rmsnorm_bytes(R, N, K, B):
+    """Fused layer + bias + RMSNorm: algorithmic_bytes plus bias and gamma
+    (N bf16 each)."""
+    return algorithmic_bytes(R, N, K, B) + 2 * N * 2
+
+
+def ar_rmsnorm_bytes(R, rows, H):
+    """All-reduce + bias + RMSNorm: R inputs read, R outputs written, bias and
+    gamma read (H bf16 each)."""
+    return 2 * R * rows * H * 2 + 2 * H * 2
+
+
+def tile_bytes(R, rows, cols, ntiles):
+    """Tile reduce: per tile R input tiles read, one output tile written."""
+    return ntiles * (R + 1) * rows * cols * 2
 
 
 def workload(name):
@@ -71,9 +98,18 @@ def workload(name):
     return dict(synth.WORKLOADS[name])
 
 
-def workload_bytes(w):
-    if w["kind"] == "allreduce":
-        return allreduce_bytes(w["R"], w["n"])
+def workload_bytes(w, ar_op="one_shot"):
+    k = w["kind"]
+    if k == "allreduce":
+        return allreduce_bytes(w["R"], w["n"], ar_op)
+    if k == "gemv_rs":
+        return gemv_rs_bytes(w["R"], w["N"], w["K"], w["B"])
+    if k == "gemv_rmsnorm":
+        return gemv_rmsnorm_bytes(w["R"], w["N"], w["K"], w["B"])
+    if k == "ar_rmsnorm":
+        return ar_rmsnorm_bytes(w["R"], w["rows"], w["H"])
+    if k == "tile":
+        return tile_bytes(w["R"], w["rows"] // 2, w["cols"] // 2, 4)
     return algorithmic_bytes(w["R"], w["N"], w["K"], w["B"])
 
 
@@ -260,14 +296,131 @@ def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id):
     return step_ms, launch_ms, clocks
 
 
+def _pinned(a):
+    import numpy as np
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a)).view(torch.uint8).reshape(-1).pin_memory()
+
+
+def _copies_for(per_copy):
+    """Rotating input copies so that the bytes touched between two uses of a
+    copy exceed the L2 three times over (at most 8)."""
+    return max(1, min(8, math.ceil(3 * L2_BYTES / max(per_copy, 1))))
+
+
+def make_case(args, w, local_rank, stream):
+    """Workspace, inputs and the per-step call of one workload.  Returns a dict:
+    ws, step(i) (copy i % copies), run0() (copy 0, for the end-to-end leg),
+    in_host / in_dev (per-step inputs for the end-to-end copies), out_dev /
+    out_bytes (the result read back), kernel, config, per_copy, copies,
+    launches_per_step, W (GEMV weights, for the weights-from-host leg)."""
+    import collective_split_gemv_gb300 as csg
+    import synth
+    from collective_split_gemv_gb300.workspace import (AllReduceWorkspace, GemvWorkspace, RmsNormWorkspace,
+                                                       TileWorkspace)
+
+    kind, R = w["kind"], w["R"]
+    if kind in ("gemv", "gemv_rs", "gemv_rmsnorm"):
+        N, K, B = w["N"], w["K"], w["B"]
+        W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
+        copies = _copies_for(W.nbytes)
+        ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
+        paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
+                 "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
+        for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
+                         (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
+                         (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
+                         (csg.SYMM_OPT_NORM_PDL, args.norm_pdl)):
+            csg.symm_set_option(ws.h, opt, val)
+        plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        for c in range(copies):
+            ws.load_W(W, copy=c)
+        ws.load_x(x)
+        mode = {"gemv": "all_reduce", "gemv_rs": "reduce_scatter", "gemv_rmsnorm": "bias_rmsnorm"}[kind]
+        eps = w.get("eps", 1e-6)
+        if kind == "gemv_rmsnorm":
+            ws.load_vectors(*synth.norm_vectors(N, w["seed"]))
+            # the planner reserves z at the top of the scratch region; the plan
+            # shown is that of the all-reduce form of the same shape
+        kernel = kernel_name(plan) + ("+rmsnorm_rows_kernel<z>" if kind == "gemv_rmsnorm" else "")
+        out_rows = B // R if kind == "gemv_rs" else B
+        return {
+            "ws": ws, "W": W, "copies": copies, "per_copy": W.nbytes, "kernel": kernel,
+            "step": lambda i: ws.run(stream, copy=i % copies, mode=mode, eps=eps),
+            "run0": lambda: ws.run(stream, copy=0, mode=mode, eps=eps),
+            # e2e: per-step inputs are x_r (W_r are resident model weights); result y
+            "in_host": [_pinned(x[r]) for r in range(R)], "in_dev": [ws.x_view(r) for r in range(R)],
+            "out_dev": ws.view(0, ws.y_off, out_rows * N * 2), "out_bytes": out_rows * N * 2,
+            "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
+            "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
+                       **({"eps": eps, "norm_pdl": args.norm_pdl} if kind == "gemv_rmsnorm" else {})},
+        }
+    if kind == "allreduce":
+        n, op = w["n"], args.ar_op
+        inp = synth.allreduce_inputs(R, n, w["seed"])
+        copies = _copies_for(inp.nbytes * 2)    # R inputs read + R outputs written, both rotated
+        ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
+        for c in range(copies):
+            ws.load_in(inp, copy=c)
+        out_n = n // R if op == "reduce_scatter" else n
+        kernel = {"one_shot": "one_shot_ar_kernel", "reduce_scatter": "reduce_scatter_kernel",
+                  "two_shot": "reduce_scatter_kernel+all_gather_blocks_kernel"}[op]
+        return {
+            "ws": ws, "copies": copies, "per_copy": inp.nbytes * 2, "kernel": kernel,
+            "step": lambda i: ws.run(stream, copy=i % copies, op=op),
+            "run0": lambda: ws.run(stream, copy=0, op=op),
+            "in_host": [_pinned(inp[r]) for r in range(R)], "in_dev": [ws.in_view(r, 0) for r in range(R)],
+            "out_dev": ws.view(0, ws.out_offs[0], out_n * 2), "out_bytes": out_n * 2,
+            "launches_per_step": 2 if op == "two_shot" else 1,
+            "config": {"R": R, "n": n, "op": op},
+        }
+    if kind == "ar_rmsnorm":
+        rows, H, eps = w["rows"], w["H"], w["eps"]
+        inp, bias, gamma = synth.rmsnorm_inputs(R, rows, H, w["seed"])
+        copies = _copies_for(inp.nbytes * 2)
+        ws = RmsNormWorkspace(R, rows, H, copies=copies, device=local_rank)
+        for c in range(copies):
+            ws.load(inp, bias, gamma, copy=c)
+        return {
+            "ws": ws, "copies": copies, "per_copy": inp.nbytes * 2, "kernel": "rmsnorm_rows_kernel<slots>",
+            "step": lambda i: ws.run(stream, copy=i % copies, eps=eps),
+            "run0": lambda: ws.run(stream, copy=0, eps=eps),
+            "in_host": [_pinned(inp[r]) for r in range(R)],
+            "in_dev": [ws.view(r, ws.in_offs[0], ws.bytes) for r in range(R)],
+            "out_dev": ws.view(0, ws.out_offs[0], ws.bytes), "out_bytes": ws.bytes,
+            "launches_per_step": 1,
+            "config": {"R": R, "rows": rows, "H": H, "eps": eps},
+        }
+    if kind == "tile":
+        n = w["rows"]
+        h = n // 2
+        full = synth.tile_inputs(R, n, w["cols"], w["seed"])
+        copies = _copies_for(full.nbytes)
+        ws = TileWorkspace(R, n, w["cols"], h, w["cols"] // 2, copies=copies, device=local_rank)
+        for c in range(copies):
+            ws.load_in(full, copy=c)
+        tiles = [(0, 0), (0, h), (h, 0), (h, h)]
+        roots = [0, 1, 2, 3]
+        return {
+            "ws": ws, "copies": copies, "per_copy": full.nbytes, "kernel": "tile_reduce_kernel",
+            "step": lambda i: ws.run(tiles, roots, h, w["cols"] // 2, stream=stream, copy=i % copies),
+            "run0": lambda: ws.run(tiles, roots, h, w["cols"] // 2, stream=stream, copy=0),
+            "in_host": [_pinned(full[r]) for r in range(R)],
+            "in_dev": [ws.view(r, ws.in_offs[0], ws.in_bytes) for r in range(R)],
+            "out_dev": ws.view(0, ws.out_offs[0], ws.out_bytes), "out_bytes": ws.out_bytes,
+            "launches_per_step": 1,
+            "config": {"R": R, "tensor": [n, w["cols"]], "tiles": "four quadrants", "roots": roots},
+        }
+    raise SystemExit(f"unknown workload kind {kind!r}")
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
 
     import __graft_entry__
     import collective_split_gemv_gb300 as csg
-    import synth
-    from collective_split_gemv_gb300.workspace import AllReduceWorkspace, GemvWorkspace
 
     if rank == 0:
         __graft_entry__.build()
@@ -278,57 +431,14 @@ def run_ours(args, rank, world, local_rank):
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_id = str(local_rank) if not visible else visible.split(",")[local_rank].strip()
     w = workload(args.workload)
-    nbytes = workload_bytes(w)
+    nbytes = workload_bytes(w, args.ar_op)
     stream = torch.cuda.Stream(device=dev)
     R = w["R"]
 
-    if w["kind"] == "gemv":
-        N, K, B = w["N"], w["K"], w["B"]
-        W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
-        per_copy = W.nbytes
-        copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(per_copy, 1))))
-        ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
-        paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
-                 "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
-        for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
-                         (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
-                         (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits)):
-            csg.symm_set_option(ws.h, opt, val)
-        plan = csg.symm_gemv_plan(ws.h, N, K, B)
-        kernel = kernel_name(plan)
-        for c in range(copies):
-            ws.load_W(W, copy=c)
-        ws.load_x(x)
-
-        def step(i):
-            ws.run(stream, copy=i % copies)
-
-        # e2e: per-step inputs are x_r (W_r are resident model weights); result y
-        in_host = [torch.from_numpy(np.ascontiguousarray(x[r])).view(torch.uint8).reshape(-1).pin_memory()
-                   for r in range(R)]
-        in_dev = [ws.x_view(r) for r in range(R)]
-        out_dev = ws.y_view(0)
-        out_bytes = ws.y_bytes
-        config_extra = {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan}
-    else:
-        n = w["n"]
-        inp = synth.allreduce_inputs(R, n, w["seed"])
-        per_copy = inp.nbytes * 2    # R inputs read + R outputs written, both rotated
-        copies = max(1, min(8, math.ceil(3 * L2_BYTES / max(per_copy, 1))))
-        ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
-        for c in range(copies):
-            ws.load_in(inp, copy=c)
-        kernel = "one_shot_ar_kernel"
-
-        def step(i):
-            ws.run(stream, copy=i % copies)
-
-        in_host = [torch.from_numpy(np.ascontiguousarray(inp[r])).view(torch.uint8).reshape(-1).pin_memory()
-                   for r in range(R)]
-        in_dev = [ws.in_view(r, 0) for r in range(R)]
-        out_dev = ws.out_view(0, 0)
-        out_bytes = ws.bytes
-        config_extra = {"R": R, "n": n}
+    c = make_case(args, w, local_rank, stream)
+    ws, step, run0, kernel = c["ws"], c["step"], c["run0"], c["kernel"]
+    in_host, in_dev, out_dev, out_bytes = c["in_host"], c["in_dev"], c["out_dev"], c["out_bytes"]
+    config_extra, per_copy, copies, W = c["config"], c["per_copy"], c["copies"], c.get("W")
 
     working_set = copies * per_copy
     flush = working_set < 2 * L2_BYTES
@@ -345,16 +455,16 @@ def run_ours(args, rank, world, local_rank):
     tt = time.perf_counter()
     for i in range(e2e_steps):
         with torch.cuda.stream(stream):
-            for r in range(R):
-                in_dev[r].copy_(in_host[r], non_blocking=True)
-            ws.run(stream, copy=0)
+            for src, dst in zip(in_host, in_dev):
+                dst.copy_(src, non_blocking=True)
+            run0()
             out_host.copy_(out_dev, non_blocking=True)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - tt) * 1e3 / e2e_steps
     h2d = sum(t.numel() for t in in_host)
 
     ew = None
-    if w["kind"] == "gemv":
+    if w["kind"] in ("gemv", "gemv_rs", "gemv_rmsnorm"):
         # weights streamed from the host as well (every step copies all W_r)
         W_host = [torch.from_numpy(np.ascontiguousarray(W[r])).view(torch.uint8).reshape(-1).pin_memory()
                   for r in range(R)]
@@ -366,8 +476,9 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.stream(stream):
                 for r in range(R):
                     w_dev[r].copy_(W_host[r], non_blocking=True)
-                    in_dev[r].copy_(in_host[r], non_blocking=True)
-                ws.run(stream, copy=0)
+                for src, dst in zip(in_host, in_dev):
+                    dst.copy_(src, non_blocking=True)
+                run0()
                 out_host.copy_(out_dev, non_blocking=True)
             stream.synchronize()
         ew = (time.perf_counter() - tt) * 1e3 / ew_steps
@@ -425,9 +536,9 @@ def run_ours(args, rank, world, local_rank):
             "us_per_call": round(e2e_ms * 1e3, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
             "what": ("per-step inputs H2D from pinned memory, the call, the result (slot 0) D2H, stream "
-                     "synchronised every step" + ("; W_r resident (model weights)" if w["kind"] == "gemv" else "")),
+                     "synchronised every step" + ("; W_r resident (model weights)" if W is not None else "")),
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * c["launches_per_step"],
     }
     if ew is not None:
         line["e2e_weights_from_host"] = {
@@ -436,14 +547,14 @@ def run_ours(args, rank, world, local_rank):
             "h2d_bytes_per_step": W.nbytes + h2d, "d2h_bytes_per_step": out_bytes,
         }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op)
     return line
 
 
 # ------------------------------------------------------------ CPU oracle
 
 
-def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0):
+def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot"):
     """Time the oracle (as it is) on this host's cores on the workload: with
     `steps` None, repeat the full call for about `budget_s` seconds; else run
     exactly `steps` calls, each on a row sample sized so that all of them fit
@@ -456,20 +567,52 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0):
 
     w = workload(name)
     threads = host_cores()
-    nbytes = workload_bytes(w)
-    if w["kind"] == "allreduce":
-        inp = synth.allreduce_inputs(w["R"], w["n"], w["seed"])
+    nbytes = workload_bytes(w, ar_op)
+    kind, R = w["kind"], w["R"]
+    if kind == "allreduce":
+        inp = synth.allreduce_inputs(R, w["n"], w["seed"])
         full = inp.shape[1]
-
-        def call(rows):
-            oracle.one_shot_all_reduce(np.ascontiguousarray(inp[:, :rows]), threads=threads)
+        if ar_op == "reduce_scatter":
+            def call(rows):
+                m = max(R, rows // R * R)
+                oracle.reduce_scatter(np.ascontiguousarray(inp[:, :m]))
+        else:   # the two-shot all-reduce reaches the all-reduce definition
+            def call(rows):
+                oracle.one_shot_all_reduce(np.ascontiguousarray(inp[:, :rows]), threads=threads)
         unit = "elements per slot"
-    else:
-        W, x = synth.gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
-        full = w["N"]
+    elif kind == "ar_rmsnorm":
+        inp, bias, gamma = synth.rmsnorm_inputs(R, w["rows"], w["H"], w["seed"])
+        full = w["rows"]
 
         def call(rows):
-            oracle.gemv_all_reduce(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
+            oracle.all_reduce_bias_rmsnorm(np.ascontiguousarray(inp[:, :rows]), bias, gamma, w["eps"])
+        unit = "rows"
+    elif kind == "tile":
+        h = w["rows"] // 2
+        full_t = synth.tile_inputs(R, w["rows"], w["cols"], w["seed"])
+        flat = full_t.reshape(R, -1)
+        out = np.zeros((R, h * (w["cols"] // 2)), dtype=np.uint16)
+        offs = [0, h, h * w["cols"], h * w["cols"] + h]
+        full = h
+
+        def call(rows):
+            oracle.tile_reduce(flat, out, offs, 0, [0, 1, 2, 3], rows, w["cols"] // 2, w["cols"], w["cols"] // 2)
+        unit = "tile rows"
+    else:
+        W, x = synth.gemv_inputs(R, w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
+        full = w["N"]
+        if kind == "gemv_rs":
+            def call(rows):
+                oracle.gemv_reduce_scatter(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
+        elif kind == "gemv_rmsnorm":
+            bias, gamma = synth.norm_vectors(w["N"], w["seed"])
+
+            def call(rows):
+                oracle.gemv_bias_rmsnorm(np.ascontiguousarray(W[:, :rows]), x, bias[:rows], gamma[:rows],
+                                         w["eps"], threads=threads)
+        else:
+            def call(rows):
+                oracle.gemv_all_reduce(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
         unit = "rows"
     t = time.perf_counter()
     call(full)                                  # calibration: one full call
@@ -504,14 +647,16 @@ def run_reference(args, rank, world):
         return None
     w = workload(args.workload)
     cb = cpu_baseline(args.workload, budget_s=min(120.0, 2.0 * (args.steps + args.warmup)),
-                      steps=args.steps, warmup=args.warmup)
+                      steps=args.steps, warmup=args.warmup, ar_op=args.ar_op)
     sec = cb["us_per_call_equiv"] * 1e-6
-    cfg = {k: w[k] for k in ("R", "N", "K", "B", "n") if k in w}
+    cfg = {k: w[k] for k in ("R", "N", "K", "B", "n", "rows", "cols", "H") if k in w}
+    if w["kind"] == "allreduce":
+        cfg["op"] = args.ar_op
     return {
         "metric": METRIC, "impl": "reference", "value": cb["value"], "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-        "config": {"workload": args.workload, **cfg, "algorithmic_bytes_per_call": workload_bytes(w)},
+        "config": {"workload": args.workload, **cfg, "algorithmic_bytes_per_call": workload_bytes(w, args.ar_op)},
         "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -539,6 +684,10 @@ def parse_args(argv=None):
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
+    p.add_argument("--ar-op", choices=("one_shot", "two_shot", "reduce_scatter"), default="one_shot",
+                   help="allreduce workload: which collective one step calls")
+    p.add_argument("--norm-pdl", type=int, default=1, choices=(0, 1),
+                   help="bias + RMSNorm form: launch the normalisation stage as a programmatic dependent")
     args = p.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

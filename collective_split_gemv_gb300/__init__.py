@@ -38,12 +38,15 @@ SYMM_OPT_SK_ENGINE = 4
 SYMM_OPT_SK_CTAS_PER_SM = 5
 SYMM_OPT_SK_GRID = 6
 SYMM_OPT_DYN_SPLITS = 7
+SYMM_OPT_NORM_PDL = 8
 
 GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK, GEMV_PATH_DYN = 0, 1, 2, 3, 4
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
-            "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "symm_free",
+            "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "gemv_reduce_scatter",
+            "gemv_all_reduce_bias_rmsnorm", "reduce_scatter", "two_shot_all_reduce",
+            "all_reduce_bias_rmsnorm", "tile_reduce", "multi_root_tile_reduce", "symm_free",
             "symm_last_error")
 
 _lib = None
@@ -90,6 +93,15 @@ def lib() -> ctypes.CDLL:
         L.symm_info.argtypes = [vp, ctypes.POINTER(SymmInfo)]
         L.symm_gemv_plan.argtypes = [vp, i, i, i, ctypes.POINTER(GemvPlan)]
         L.gemv_all_reduce_noalloc.argtypes = [vp, vp, vp, sz, i, i, i, i, vp]
+        ll = ctypes.c_longlong
+        f32 = ctypes.c_float
+        L.gemv_reduce_scatter.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+        L.gemv_all_reduce_bias_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f32, vp]
+        L.reduce_scatter.argtypes = [vp, vp, vp, i, sz, vp]
+        L.two_shot_all_reduce.argtypes = [vp, vp, vp, i, sz, vp]
+        L.all_reduce_bias_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i, i, i, f32, vp]
+        L.tile_reduce.argtypes = [vp, vp, vp, i, i, i, ll, ll, vp]
+        L.multi_root_tile_reduce.argtypes = [vp, ctypes.POINTER(vp), vp, ctypes.POINTER(i), i, i, i, ll, ll, vp]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
         L.symm_last_error.restype = ctypes.c_char_p
@@ -154,6 +166,46 @@ def one_shot_all_reduce(h, inp: int, out: int, R: int, n: int, stream=None) -> N
 
 def gemv_all_reduce(h, W_r: int, x_r: int, y: int, R: int, N: int, K: int, B: int, stream=None) -> None:
     _check(lib().gemv_all_reduce(h, _vp(W_r), _vp(x_r), _vp(y), R, N, K, B, _stream(stream)))
+
+
+def gemv_reduce_scatter(h, W_r: int, x_r: int, y: int, R: int, N: int, K: int, B: int, stream=None) -> None:
+    _check(lib().gemv_reduce_scatter(h, _vp(W_r), _vp(x_r), _vp(y), R, N, K, B, _stream(stream)))
+
+
+def gemv_all_reduce_bias_rmsnorm(h, W_r: int, x_r: int, bias, gamma, y: int, R: int, N: int, K: int, B: int,
+                                 eps: float, stream=None) -> None:
+    _check(lib().gemv_all_reduce_bias_rmsnorm(h, _vp(W_r), _vp(x_r), _vp(bias), _vp(gamma), _vp(y), R, N, K, B,
+                                              float(eps), _stream(stream)))
+
+
+def reduce_scatter(h, inp: int, out: int, R: int, n: int, stream=None) -> None:
+    _check(lib().reduce_scatter(h, _vp(inp), _vp(out), R, n, _stream(stream)))
+
+
+def two_shot_all_reduce(h, inp: int, out: int, R: int, n: int, stream=None) -> None:
+    _check(lib().two_shot_all_reduce(h, _vp(inp), _vp(out), R, n, _stream(stream)))
+
+
+def all_reduce_bias_rmsnorm(h, inp: int, bias, gamma, out: int, R: int, rows: int, H: int, eps: float,
+                            stream=None) -> None:
+    _check(lib().all_reduce_bias_rmsnorm(h, _vp(inp), _vp(bias), _vp(gamma), _vp(out), R, rows, H, float(eps),
+                                         _stream(stream)))
+
+
+def tile_reduce(h, in_tile: int, out_tile: int, root: int, rows: int, cols: int, ld_in: int, ld_out: int,
+                stream=None) -> None:
+    _check(lib().tile_reduce(h, _vp(in_tile), _vp(out_tile), root, rows, cols, ld_in, ld_out, _stream(stream)))
+
+
+def multi_root_tile_reduce(h, in_tiles, out_tile: int, roots, rows: int, cols: int, ld_in: int, ld_out: int,
+                           stream=None) -> None:
+    nt = len(in_tiles)
+    if len(roots) != nt:
+        raise ValueError("in_tiles and roots differ in length")
+    tiles = (ctypes.c_void_p * max(nt, 1))(*[int(p) for p in in_tiles])
+    rts = (ctypes.c_int * max(nt, 1))(*[int(r) for r in roots])
+    _check(lib().multi_root_tile_reduce(h, tiles, _vp(out_tile), rts, nt, rows, cols, ld_in, ld_out,
+                                        _stream(stream)))
 
 
 def symm_status(h, stream=None):

@@ -35,6 +35,13 @@ __device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v) {
     acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
 }
 
+__device__ __forceinline__ void set8(float (&acc)[8], const uint4 &v) {
+    acc[0] = bf16lo(v.x); acc[1] = bf16hi(v.x);
+    acc[2] = bf16lo(v.y); acc[3] = bf16hi(v.y);
+    acc[4] = bf16lo(v.z); acc[5] = bf16hi(v.z);
+    acc[6] = bf16lo(v.w); acc[7] = bf16hi(v.w);
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half)
     return *reinterpret_cast<const uint32_t *>(&p);
@@ -99,7 +106,119 @@ __global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceAr
     }
 }
 
+// Reduce-scatter (and phase 1 of the two-shot all-reduce): element i belongs
+// to owner s = i / chunk, whose slot alone receives the sum of the R inputs
+// (fp32, rank order 0..R-1, RNE to bf16).  kVec: chunk % 8 == 0, so a
+// 16-byte vector never straddles two owners; otherwise one element per
+// thread.  A thread reads its element(s) in every slot before its one store,
+// so in == out is safe for the two-shot layout (shift = 1).
+template <int RT, bool kVec>
+__global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const ReduceScatterArgs a) {
+    const int R = RT > 0 ? RT : a.R;
+    const size_t step = (size_t)gridDim.x * kThreads;
+    const size_t first = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (kVec) {
+        const size_t nvec = a.n / 8;
+        for (size_t v = first; v < nvec; v += step) {
+            const size_t i = v * 8;
+            const size_t s = i / a.chunk;
+            const uint8_t *src = a.in + i * 2;
+            float acc[8];
+            if (RT > 0) {
+                uint4 x[RT > 0 ? RT : 1];
+#pragma unroll
+                for (int q = 0; q < (RT > 0 ? RT : 1); ++q) x[q] = ld_v4(src + (long long)q * a.stride);
+                set8(acc, x[0]);
+#pragma unroll
+                for (int q = 1; q < (RT > 0 ? RT : 1); ++q) add8(acc, x[q]);
+            } else {
+                set8(acc, ld_v4(src));
+                for (int q = 1; q < R; ++q) add8(acc, ld_v4(src + (long long)q * a.stride));
+            }
+            uint4 o;
+            o.x = pack2(acc[0], acc[1]);
+            o.y = pack2(acc[2], acc[3]);
+            o.z = pack2(acc[4], acc[5]);
+            o.w = pack2(acc[6], acc[7]);
+            const size_t j = i - s * a.chunk + (a.shift ? s * a.chunk : 0);
+            st_v4(a.out + (long long)s * a.stride + j * 2, o);
+        }
+    }
+    // Elements not covered by vectors: all of them (scalar layout) or the
+    // ragged tail n % 8.
+    const size_t e0 = kVec ? (a.n / 8) * 8 : 0;
+    for (size_t i = e0 + first; i < a.n; i += step) {
+        const size_t s = i / a.chunk;
+        float acc = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(a.in + i * 2));
+        for (int q = 1; q < R; ++q)
+            acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(a.in + i * 2 + (long long)q * a.stride));
+        const size_t j = i - s * a.chunk + (a.shift ? s * a.chunk : 0);
+        *reinterpret_cast<__nv_bfloat16 *>(a.out + (long long)s * a.stride + j * 2) = __float2bfloat16_rn(acc);
+    }
+}
+
+// Phase 2 of the two-shot all-reduce: every slot q copies each owner's block
+// from the owner's slot (out_q[i] = out_s[i], s = i / chunk, q != s).  The
+// owner's values were stored by phase 1, an earlier launch on the stream.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) all_gather_blocks_kernel(const ReduceScatterArgs a) {
+    const size_t step = (size_t)gridDim.x * kThreads;
+    const size_t first = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (kVec) {
+        const size_t nvec = a.n / 8;
+        for (size_t v = first; v < nvec; v += step) {
+            const size_t i = v * 8;
+            const int s = (int)(i / a.chunk);
+            const uint4 val = ld_v4(a.out + (long long)s * a.stride + i * 2);
+            for (int q = 0; q < a.R; ++q)
+                if (q != s) st_v4(a.out + (long long)q * a.stride + i * 2, val);
+        }
+    }
+    const size_t e0 = kVec ? (a.n / 8) * 8 : 0;
+    for (size_t i = e0 + first; i < a.n; i += step) {
+        const int s = (int)(i / a.chunk);
+        const uint16_t val = *reinterpret_cast<const uint16_t *>(a.out + (long long)s * a.stride + i * 2);
+        for (int q = 0; q < a.R; ++q)
+            if (q != s) *reinterpret_cast<uint16_t *>(a.out + (long long)q * a.stride + i * 2) = val;
+    }
+}
+
+unsigned grid_for(size_t work_items) {
+    int sms = 152;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    size_t blocks = (work_items + kThreads - 1) / kThreads;
+    const size_t cap = (size_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    return (unsigned)blocks;
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
+    const bool vec = a.chunk % 8 == 0;
+    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n);
+    if (vec) {
+        switch (a.R) {
+            case 2: reduce_scatter_kernel<2, true><<<g, kThreads, 0, s>>>(a); break;
+            case 4: reduce_scatter_kernel<4, true><<<g, kThreads, 0, s>>>(a); break;
+            case 8: reduce_scatter_kernel<8, true><<<g, kThreads, 0, s>>>(a); break;
+            default: reduce_scatter_kernel<0, true><<<g, kThreads, 0, s>>>(a); break;
+        }
+    } else {
+        reduce_scatter_kernel<0, false><<<g, kThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s) {
+    const bool vec = a.chunk % 8 == 0;
+    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n);
+    if (vec) all_gather_blocks_kernel<true><<<g, kThreads, 0, s>>>(a);
+    else all_gather_blocks_kernel<false><<<g, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s) {
     const size_t nvec = a.n / 8;

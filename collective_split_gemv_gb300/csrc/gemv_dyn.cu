@@ -196,6 +196,7 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemvArgs a, const DynGeom geo) {
+    allow_dependent_launch(a);
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;

@@ -54,6 +54,7 @@ __device__ __forceinline__ float dot8(const uint4 &w, const float4 &lo, const fl
 
 template <int B>
 __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a) {
+    allow_dependent_launch(a);
     constexpr int G = FfmaShape<B>::G;
     constexpr int U = FfmaShape<B>::U;
     extern __shared__ float4 xs4[];   // [B][2][kc_cap]

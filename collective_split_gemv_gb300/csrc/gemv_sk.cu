@@ -168,10 +168,8 @@ __device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeo
         for (int k = 0; k < kPer; ++k) {
             const int i = i0 + k * kGroupThreads;
             if (i < count) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(acc[k]);
-                const size_t yoff = off[k] / 2;
-                for (int q = 0; q < a.R; ++q)
-                    *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+                const int b = i / rows;
+                store_output(a, b, n0 + (i - b * rows), acc[k]);
             }
         }
     }
@@ -195,6 +193,7 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, const SkGeom geo) {
+    allow_dependent_launch(a);
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;

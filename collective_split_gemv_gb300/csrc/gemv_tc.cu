@@ -56,6 +56,7 @@ static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, int kb_total, int kb_per_split) {
+    allow_dependent_launch(a);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];

@@ -44,7 +44,18 @@ struct GemvArgs {
     int kc_cap;              // 16-byte chunks of x staged in shared memory per pass
     uint32_t epoch;          // this launch's epoch (>= 1)
     int reverse_order;       // 1: CTAs take work in reverse (arrival-order tests)
+    // What the tile reducer does with the fp32 sum of output (b, n):
+    //   kOutAllReduce      bf16 into y of every rank (y: [B][N] per slot);
+    //   kOutReduceScatter  bf16 into y of rank b / rs_rows only, at row
+    //                      b % rs_rows (y: [rs_rows][N] per slot);
+    //   kOutBiasZ          fp32 sum + bias[n] into z[b][n] (slot 0), for the
+    //                      RMS-normalisation stage that follows.
+    int out_mode;
+    int rs_rows;             // kOutReduceScatter: B / R
+    float *z;                // kOutBiasZ: fp32 [B][N]
+    const uint8_t *bias;     // kOutBiasZ: bf16 [N] (slot 0) or nullptr
 };
+constexpr int kOutAllReduce = 0, kOutReduceScatter = 1, kOutBiasZ = 2;
 
 // Sets the calling thread's last-error message (see symm_last_error) and
 // returns `code`.
@@ -60,6 +71,55 @@ struct AllReduceArgs {
 
 // Kernel launchers; return the launch's cudaError_t.
 cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s);
+
+// Reduce-scatter over the slots: element i (i < n) belongs to owner
+// i / chunk; its sum over the R slots goes to slot owner's out at element
+// (i - owner * chunk) + shift * owner * chunk.  shift = 0: the compact
+// reduce-scatter output (chunk elements per slot); shift = 1: the owner's
+// block of a full-length output (phase 1 of the two-shot all-reduce).
+struct ReduceScatterArgs {
+    const uint8_t *in;       // bf16 [n], slot 0
+    uint8_t *out;            // bf16, slot 0
+    long long stride;
+    int R;
+    size_t n;
+    size_t chunk;            // elements per owner
+    int shift;
+};
+cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s);
+// Phase 2 of the two-shot all-reduce: out_q[i] = out_owner(i)[i] for q != owner.
+cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s);
+
+// Sum of a 2-D tile over the R slots into one root slot's output tile.
+constexpr int kMaxTiles = 64;
+struct TileReduceArgs {
+    const uint8_t *in[kMaxTiles];  // tile i's first element, slot 0
+    int root[kMaxTiles];
+    uint8_t *out;                  // output tile's first element, slot 0
+    long long stride;
+    int R, ntiles, rows, cols;
+    long long ld_in, ld_out;       // elements
+};
+cudaError_t launch_tile_reduce(const TileReduceArgs &a, cudaStream_t s);
+
+// RMS normalisation of `rows` rows of H elements, one thread-block cluster
+// per row.  Source: either R bf16 slots plus an optional bf16 bias (the
+// all-reduce + bias + RMSNorm kernel), or one fp32 array that already holds
+// sum + bias (the fused layer's epilogue stage).  The result is stored as
+// bf16 into every slot's out.
+struct RmsNormArgs {
+    const uint8_t *in;       // bf16 [rows][H], slot 0 (source kind 0)
+    const float *z;          // fp32 [rows][H] (source kind 1)
+    const uint8_t *bias;     // bf16 [H], slot 0, or nullptr (kind 0 only)
+    const uint8_t *gamma;    // bf16 [H], slot 0, or nullptr
+    uint8_t *out;            // bf16 [rows][H], slot 0
+    long long stride;
+    int R, rows, H;
+    float eps;
+    int wait_prior;          // 1: launched as a dependent of the previous kernel (PDL)
+};
+int rmsnorm_max_h();
+cudaError_t launch_rmsnorm_rows(const RmsNormArgs &a, cudaStream_t s);
 
 // FFMA (CUDA-core) fused kernel: any B in 1..16.
 int ffma_rows_per_tile(int B);

@@ -92,10 +92,39 @@ __device__ __forceinline__ void latch_status(uint32_t *status, int code, int ran
     }
 }
 
+// Where the tile reducer puts the fp32 sum of output (b, n) (see
+// GemvArgs::out_mode): bf16 into every rank's y (all-reduce), bf16 into the
+// rank that owns batch row b (reduce-scatter along the batch rows, the
+// sequence-parallel ending of the row-parallel layer), or fp32 sum + bias
+// into z for the RMS-normalisation stage.
+__device__ __forceinline__ void store_output(const GemvArgs &a, int b, int n, float acc) {
+    if (a.out_mode == kOutAllReduce) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(acc);
+        const size_t yoff = ((size_t)b * a.N + n) * 2;
+        for (int q = 0; q < a.R; ++q) *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+    } else if (a.out_mode == kOutReduceScatter) {
+        const int q = b / a.rs_rows;
+        const size_t yoff = ((size_t)(b - q * a.rs_rows) * a.N + n) * 2;
+        *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = __float2bfloat16_rn(acc);
+    } else {
+        float v = acc;
+        if (a.bias) v += __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.bias)[n]);
+        __stcg(a.z + (size_t)b * a.N + n, v);
+    }
+}
+
+// In a bias + RMSNorm call the normalisation kernel is launched as a
+// programmatic dependent of the GEMV; this lets its CTAs be scheduled while
+// the GEMV still runs (they wait for the whole GEMV grid, and its memory, at
+// griddepcontrol.wait before reading z).  A no-op for the other modes.
+__device__ __forceinline__ void allow_dependent_launch(const GemvArgs &a) {
+    if (a.out_mode == kOutBiasZ) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The reduction of one tile by its last contributor: for each output (b, n)
 // of rows [n0, n0 + rows), sum the C contributors' fp32 partials in
 // contributor order j = 0..C-1 (contributor j's [B][N] array at
-// contributor_base(j)), round to bf16 (RNE) and store into every rank's y.
+// contributor_base(j)) and hand the sum to store_output.
 // The flags have been acquired and fenced, so plain L2 loads (.cg) see the
 // partials.  Each thread takes kPer outputs and loads kBatch contributors of
 // all of them before adding anything, so one L2 round trip serves
@@ -134,11 +163,10 @@ __device__ __forceinline__ void reduce_tile(const GemvArgs &a, int n0, int rows,
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            if (i0 + k * nthreads < count) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(acc[k]);
-                const size_t yoff = off[k] / 2;   // the same (b, n) in bf16
-                for (int q = 0; q < a.R; ++q)
-                    *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
+            const int i = i0 + k * nthreads;
+            if (i < count) {
+                const int b = i / rows;
+                store_output(a, b, n0 + (i - b * rows), acc[k]);
             }
         }
     }

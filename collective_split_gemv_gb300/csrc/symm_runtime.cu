@@ -47,6 +47,7 @@ struct symm_handle {
     int opt_sk_cps = 0;
     int opt_sk_grid = 0;
     int opt_dyn_splits = 0;
+    int opt_norm_pdl = 1;       // launch the RMSNorm stage as a programmatic dependent
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -211,7 +212,7 @@ int sk_cta_of_block(long long g, long long total, int G) {
 
 // Stream-K geometry: G <= SM count CTAs over total = tiles * R * KB blocks,
 // shrunk until the parts per unit fit the scratch region and the signal pad.
-bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slabs, int cps, SkGeom *geo) {
+bool sk_geometry(const symm_handle *h, size_t cap, int tiles, int N, int Kr, int B, int slabs, int cps, SkGeom *geo) {
     const long long KB = (Kr + sk_block_k(slabs) - 1) / sk_block_k(slabs);
     const long long units = (long long)tiles * h->R;
     const long long total = units * KB;
@@ -227,7 +228,7 @@ bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slab
             const int P = sk_cta_of_block((u + 1) * KB - 1, total, (int)G) - sk_cta_of_block(u * KB, total, (int)G) + 1;
             pmax = std::max(pmax, P);
         }
-        if ((size_t)pmax * part_bytes <= h->scratch_bytes && (long long)tiles * pmax <= h->max_tiles) {
+        if ((size_t)pmax * part_bytes <= cap && (long long)tiles * pmax <= h->max_tiles) {
             geo->total = total;
             geo->KB = (int)KB;
             geo->G = (int)G;
@@ -243,14 +244,14 @@ bool sk_geometry(const symm_handle *h, int tiles, int N, int Kr, int B, int slab
 
 // K-splits per rank for the tensor-core kernel: enough CTAs for two per SM
 // when the row tiles alone are too few, limited by K blocks, scratch and pad.
-int tc_splits(const symm_handle *h, int tiles, int N, int Kr, int B) {
+int tc_splits(const symm_handle *h, size_t cap, int tiles, int N, int Kr, int B) {
     const int kb_total = (Kr + kTcBlockK - 1) / kTcBlockK;
     const long long base = (long long)tiles * h->R;
     const int sms = num_sms(h->device);
     int S = 1;
     if (base < sms) S = (int)std::min<long long>((2LL * sms + base - 1) / base, 16);
     S = std::max(1, std::min(S, kb_total));
-    while (S > 1 && ((size_t)S * B * N * 4 > h->scratch_bytes || (long long)tiles * S > h->max_tiles)) --S;
+    while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)tiles * S > h->max_tiles)) --S;
     // no empty split: with kb_per = ceil(kb_total / S), use exactly ceil(kb_total / kb_per) splits
     const int kb_per = (kb_total + S - 1) / S;
     return std::max(1, (kb_total + kb_per - 1) / kb_per);
@@ -279,17 +280,19 @@ struct Plan {
     DynGeom dyn = {0, 1, 0, 0, 0, nullptr};
 };
 
-int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
-    if ((size_t)B * (size_t)N * 4 > h->scratch_bytes)
-        return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, handle has %zu",
-                    (size_t)B * (size_t)N * 4, h->scratch_bytes);
+// `cap`: scratch bytes per slot the partials may use (the whole region, or
+// less when part of it is reserved for the bias + RMSNorm stage's z).
+int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap) {
+    if ((size_t)B * (size_t)N * 4 > cap)
+        return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, %zu available",
+                    (size_t)B * (size_t)N * 4, cap);
     pl->path = gemv_path(h, N, B, Kr);
     pl->rows = rows_per_tile_for(h, N, B, Kr);
     if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     pl->tiles = (N + pl->rows - 1) / pl->rows;
     if (pl->tiles > h->max_tiles)
         return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", pl->tiles, h->max_tiles);
-    pl->splits = pl->path == kPathTc ? tc_splits(h, pl->tiles, N, Kr, B) : 1;
+    pl->splits = pl->path == kPathTc ? tc_splits(h, cap, pl->tiles, N, Kr, B) : 1;
     pl->grid = pl->tiles * h->R * pl->splits;
     if (pl->path == kPathSk) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the stream-K kernel needs K > 0");
@@ -298,7 +301,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
         pl->cps = sk_cps(h);
         if (!sk_config_supported(pl->slabs, pl->cps))
             return fail(SYMM_EINVAL, "stream-K has no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
-        if (!sk_geometry(h, pl->tiles, N, Kr, B, pl->slabs, pl->cps, &pl->geo))
+        if (!sk_geometry(h, cap, pl->tiles, N, Kr, B, pl->slabs, pl->cps, &pl->geo))
             return fail(SYMM_ERANGE, "stream-K partials do not fit the scratch region or the signal pad");
         pl->grid = pl->geo.G;
     }
@@ -323,7 +326,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl) {
                           ? h->opt_dyn_splits
                           : (4 * pairs > G ? 1 : std::min<long long>(8, (G + 2 * pairs - 1) / (2 * pairs)));
         S = std::min<long long>(S, KB);
-        while (S > 1 && ((size_t)S * B * N * 4 > h->scratch_bytes || (long long)pl->tiles * S > h->max_tiles)) --S;
+        while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;
         const long long KBs = (KB + S - 1) / S;
         S = (KB + KBs - 1) / KBs;   // no empty split
         const long long units = pairs * S;
@@ -347,6 +350,167 @@ namespace symm {
 // Lets other translation units of the library report through symm_last_error.
 int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace symm
+
+namespace {
+
+// What the fused call does after the tile sums (GemvArgs::out_mode) and the
+// extra arguments of each form.
+struct Epilogue {
+    int mode = kOutAllReduce;
+    const void *bias = nullptr;    // kOutBiasZ
+    const void *gamma = nullptr;   // kOutBiasZ
+    float eps = 0.f;               // kOutBiasZ
+};
+
+// The three public forms of the fused row-parallel layer share everything up
+// to the tile reducer's store: all-reduce (y [B][N] in every slot),
+// reduce-scatter along the batch rows (y [B/R][N] per slot), and all-reduce +
+// bias + RMSNorm (fp32 z stage, then the cluster normalisation kernel).
+int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,
+                symm_stream_t stream, const Epilogue &ep) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    if (N < 0 || K < 0) return fail(SYMM_EINVAL, "N=%d K=%d must be >= 0", N, K);
+    if (B < 0 || B > SYMM_MAX_BATCH) return fail(SYMM_EINVAL, "B=%d outside 0..%d", B, SYMM_MAX_BATCH);
+    if (K % R) return fail(SYMM_EINVAL, "K=%d is not a multiple of R=%d", K, R);
+    const int Kr = K / R;
+    if (Kr % 8) return fail(SYMM_EINVAL, "K/R=%d is not a multiple of 8", Kr);
+    if (ep.mode == kOutReduceScatter && B % R)
+        return fail(SYMM_EINVAL, "reduce-scatter along the batch rows needs B=%d to be a multiple of R=%d", B, R);
+    if (ep.mode == kOutBiasZ) {
+        if (N % 8) return fail(SYMM_EINVAL, "bias + RMSNorm needs N=%d to be a multiple of 8", N);
+        if (N > rmsnorm_max_h()) return fail(SYMM_EINVAL, "bias + RMSNorm supports N <= %d", rmsnorm_max_h());
+        if (!(ep.eps >= 0.f) || ep.eps > 3.0e38f) return fail(SYMM_EINVAL, "eps must be finite and >= 0");
+    }
+    if (N == 0 || B == 0) return SYMM_OK;
+    const size_t wbytes = (size_t)N * (size_t)Kr * 2;
+    const size_t xbytes = (size_t)B * (size_t)Kr * 2;
+    const size_t ybytes = (size_t)(ep.mode == kOutReduceScatter ? B / R : B) * (size_t)N * 2;
+    const size_t vbytes = (size_t)N * 2;
+    if (!in_user_region(h, W_r, wbytes)) return fail(SYMM_EINVAL, "W_r (N x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, x_r, xbytes)) return fail(SYMM_EINVAL, "x_r (B x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, y, ybytes)) return fail(SYMM_EINVAL, "y is not inside slot 0's user region");
+    if (!aligned16(W_r) || !aligned16(x_r) || !aligned16(y)) return fail(SYMM_EINVAL, "W_r, x_r and y must be 16-byte aligned");
+    if (overlaps(y, ybytes, W_r, wbytes) || overlaps(y, ybytes, x_r, xbytes))
+        return fail(SYMM_EINVAL, "y overlaps W_r or x_r");
+    for (const void *v : {ep.bias, ep.gamma}) {
+        if (!v) continue;
+        if (!in_user_region(h, v, vbytes) || !aligned16(v))
+            return fail(SYMM_EINVAL, "bias / gamma (N bf16) must be 16-byte aligned inside slot 0's user region");
+        if (overlaps(v, vbytes, y, ybytes)) return fail(SYMM_EINVAL, "bias / gamma overlaps y");
+    }
+    // The bias + RMSNorm form keeps z (fp32 [B][N]) at the top of slot 0's
+    // scratch region; the partials get the rest.
+    size_t cap = h->scratch_bytes;
+    size_t z_off = 0;
+    if (ep.mode == kOutBiasZ) {
+        const size_t zbytes = (size_t)B * N * 4;
+        if (zbytes > h->scratch_bytes) return fail(SYMM_ERANGE, "z needs %zu scratch bytes", zbytes);
+        z_off = (h->scratch_bytes - zbytes) / 256 * 256;
+        cap = z_off;
+    }
+    Plan pl;
+    int rc = make_plan(h, N, Kr, B, &pl, cap);
+    if (rc != SYMM_OK) return rc;
+    const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
+              slabs = pl.slabs, cps = pl.cps;
+    const SkGeom geo = pl.geo;
+    const DynGeom dyn = pl.dyn;
+    rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Tickets of launch e are (e-1)*C_t .. e*C_t-1 (C_t contributors of tile t,
+    // at most R * max(splits, Pmax)): restart the pad when the geometry
+    // changes or before the tickets would wrap.
+    const int cmax = std::max(h->R * std::max(std::max(splits, dyn.splits), geo.Pmax), dyn.units);
+    uint64_t key = 1469598103934665603ull;
+    for (long long v : {(long long)path, (long long)tiles, (long long)splits, (long long)geo.KB, (long long)geo.G,
+                        (long long)geo.Pmax, (long long)engine, (long long)slabs, (long long)cps, (long long)geo.total,
+                        (long long)dyn.units, (long long)dyn.G, (long long)dyn.splits}) {
+        key ^= (uint64_t)v;
+        key *= 1099511628211ull;
+    }
+    if (((uint64_t)h->epoch + 1) * (uint64_t)cmax > 0xFFFFFFFFull || h->epoch == 0 || key != h->geom_key) {
+        rc = reset_protocol(h, s);
+        if (rc != SYMM_OK) return rc;
+        h->geom_key = key;
+    }
+    h->epoch += 1;
+
+    GemvArgs a;
+    a.W = static_cast<const uint8_t *>(W_r);
+    a.x = static_cast<const uint8_t *>(x_r);
+    a.y = static_cast<uint8_t *>(y);
+    a.scratch = h->base + h->scratch_off;
+    a.flags = pad_word(h, 0, h->flags_off);
+    a.counters = pad_word(h, 0, h->counters_off);
+    a.status = pad_word(h, 0, 0);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.N = N;
+    a.Kr = Kr;
+    a.B = B;
+    a.rows_per_tile = rows;
+    a.num_tiles = tiles;
+    a.epoch = h->epoch;
+    a.reverse_order = h->opt_tile_order;
+    a.splits = splits;
+    a.partial_stride = (long long)B * N * 4;
+    a.kc_cap = 0;
+    a.out_mode = ep.mode;
+    a.rs_rows = ep.mode == kOutReduceScatter ? B / R : B;
+    a.z = ep.mode == kOutBiasZ ? reinterpret_cast<float *>(h->base + h->scratch_off + z_off) : nullptr;
+    a.bias = ep.mode == kOutBiasZ ? static_cast<const uint8_t *>(ep.bias) : nullptr;
+    cudaError_t e = cudaSuccess;
+    switch (path) {
+        case kPathFfma:
+            a.kc_cap = ffma_kc_cap(B, Kr);
+            e = launch_gemv_ffma(a, s);
+            break;
+        case kPathTc:
+        case kPathSk:
+        case kPathDyn: {
+            if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
+            int err = 0;
+            const void *maps = tc_maps_for(h, a, &err);
+            if (!maps) {
+                h->epoch -= 1;
+                return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
+            }
+            if (path == kPathTc) {
+                e = launch_gemv_tc(a, maps, s);
+            } else if (path == kPathDyn) {
+                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, s);
+            } else {
+                a.partial_stride = (long long)B * N * 4;
+                e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
+            }
+            break;
+        }
+        default:
+            return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "gemv_all_reduce launch");
+    if (ep.mode == kOutBiasZ) {
+        RmsNormArgs n = {};
+        n.z = a.z;
+        n.gamma = static_cast<const uint8_t *>(ep.gamma);
+        n.out = a.y;
+        n.stride = a.stride;
+        n.R = h->R;
+        n.rows = B;
+        n.H = N;
+        n.eps = ep.eps;
+        n.wait_prior = h->opt_norm_pdl;
+        e = launch_rmsnorm_rows(n, s);
+        if (e != cudaSuccess) return cuda_fail(e, "RMSNorm stage launch");
+    }
+    return SYMM_OK;
+}
+
+
+}  // namespace
 
 extern "C" {
 
@@ -477,6 +641,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 16) return fail(SYMM_EINVAL, "persistent-kernel splits %d not in 0..16", value);
             h->opt_dyn_splits = value;
             return SYMM_OK;
+        case SYMM_OPT_NORM_PDL:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "RMSNorm-stage PDL %d not in {0, 1}", value);
+            h->opt_norm_pdl = value;
+            return SYMM_OK;
         case SYMM_OPT_SK_CTAS_PER_SM:
             if (value < 0 || value > 3) return fail(SYMM_EINVAL, "stream-K CTAs per SM %d not in 0..3", value);
             h->opt_sk_cps = value;
@@ -491,7 +659,7 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
     if (N < 1 || K < 0 || B < 1 || B > SYMM_MAX_BATCH || K % h->R || (K / h->R) % 8)
         return fail(SYMM_EINVAL, "no plan for N=%d K=%d B=%d on %d ranks", N, K, B, h->R);
     Plan pl;
-    int rc = make_plan(h, N, K / h->R, B, &pl);
+    int rc = make_plan(h, N, K / h->R, B, &pl, h->scratch_bytes);
     if (rc != SYMM_OK) return rc;
     out->path = pl.path;
     out->engine = pl.engine;
@@ -531,103 +699,174 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
 
 int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,
                     symm_stream_t stream) {
+    return gemv_common(h, W_r, x_r, y, R, N, K, B, stream, Epilogue());
+}
+
+int gemv_reduce_scatter(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,
+                        symm_stream_t stream) {
+    Epilogue ep;
+    ep.mode = kOutReduceScatter;
+    return gemv_common(h, W_r, x_r, y, R, N, K, B, stream, ep);
+}
+
+int gemv_all_reduce_bias_rmsnorm(symm_handle_t *h, const void *W_r, const void *x_r, const void *bias,
+                                 const void *gamma, void *y, int R, int N, int K, int B, float eps,
+                                 symm_stream_t stream) {
+    Epilogue ep;
+    ep.mode = kOutBiasZ;
+    ep.bias = bias;
+    ep.gamma = gamma;
+    ep.eps = eps;
+    return gemv_common(h, W_r, x_r, y, R, N, K, B, stream, ep);
+}
+
+int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
-    if (N < 0 || K < 0) return fail(SYMM_EINVAL, "N=%d K=%d must be >= 0", N, K);
-    if (B < 0 || B > SYMM_MAX_BATCH) return fail(SYMM_EINVAL, "B=%d outside 0..%d", B, SYMM_MAX_BATCH);
-    if (K % R) return fail(SYMM_EINVAL, "K=%d is not a multiple of R=%d", K, R);
-    const int Kr = K / R;
-    if (Kr % 8) return fail(SYMM_EINVAL, "K/R=%d is not a multiple of 8", Kr);
-    if (N == 0 || B == 0) return SYMM_OK;
-    const size_t wbytes = (size_t)N * (size_t)Kr * 2;
-    const size_t xbytes = (size_t)B * (size_t)Kr * 2;
-    const size_t ybytes = (size_t)B * (size_t)N * 2;
-    if (!in_user_region(h, W_r, wbytes)) return fail(SYMM_EINVAL, "W_r (N x K/R bf16) is not inside slot 0's user region");
-    if (!in_user_region(h, x_r, xbytes)) return fail(SYMM_EINVAL, "x_r (B x K/R bf16) is not inside slot 0's user region");
-    if (!in_user_region(h, y, ybytes)) return fail(SYMM_EINVAL, "y (B x N bf16) is not inside slot 0's user region");
-    if (!aligned16(W_r) || !aligned16(x_r) || !aligned16(y)) return fail(SYMM_EINVAL, "W_r, x_r and y must be 16-byte aligned");
-    if (overlaps(y, ybytes, W_r, wbytes) || overlaps(y, ybytes, x_r, xbytes))
-        return fail(SYMM_EINVAL, "y overlaps W_r or x_r");
-    Plan pl;
-    int rc = make_plan(h, N, Kr, B, &pl);
+    if (n % (size_t)R) return fail(SYMM_EINVAL, "n=%zu is not a multiple of R=%d", n, R);
+    if (n == 0) return SYMM_OK;
+    if (n > SIZE_MAX / 2) return fail(SYMM_EINVAL, "n too large");
+    const size_t ib = n * 2, ob = n / (size_t)R * 2;
+    if (!in_user_region(h, in, ib)) return fail(SYMM_EINVAL, "in + n elements is not inside slot 0's user region");
+    if (!in_user_region(h, out, ob)) return fail(SYMM_EINVAL, "out + n/R elements is not inside slot 0's user region");
+    if (!aligned16(in) || !aligned16(out)) return fail(SYMM_EINVAL, "in/out must be 16-byte aligned");
+    if (overlaps(in, ib, out, ob)) return fail(SYMM_EINVAL, "in and out overlap");
+    int rc = check_device(h);
     if (rc != SYMM_OK) return rc;
-    const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
-              slabs = pl.slabs, cps = pl.cps;
-    const SkGeom geo = pl.geo;
-    const DynGeom dyn = pl.dyn;
-    rc = check_device(h);
-    if (rc != SYMM_OK) return rc;
-
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Tickets of launch e are (e-1)*C_t .. e*C_t-1 (C_t contributors of tile t,
-    // at most R * max(splits, Pmax)): restart the pad when the geometry
-    // changes or before the tickets would wrap.
-    const int cmax = std::max(h->R * std::max(std::max(splits, dyn.splits), geo.Pmax), dyn.units);
-    uint64_t key = 1469598103934665603ull;
-    for (long long v : {(long long)path, (long long)tiles, (long long)splits, (long long)geo.KB, (long long)geo.G,
-                        (long long)geo.Pmax, (long long)engine, (long long)slabs, (long long)cps, (long long)geo.total,
-                        (long long)dyn.units, (long long)dyn.G, (long long)dyn.splits}) {
-        key ^= (uint64_t)v;
-        key *= 1099511628211ull;
-    }
-    if (((uint64_t)h->epoch + 1) * (uint64_t)cmax > 0xFFFFFFFFull || h->epoch == 0 || key != h->geom_key) {
-        rc = reset_protocol(h, s);
-        if (rc != SYMM_OK) return rc;
-        h->geom_key = key;
-    }
-    h->epoch += 1;
-
-    GemvArgs a;
-    a.W = static_cast<const uint8_t *>(W_r);
-    a.x = static_cast<const uint8_t *>(x_r);
-    a.y = static_cast<uint8_t *>(y);
-    a.scratch = h->base + h->scratch_off;
-    a.flags = pad_word(h, 0, h->flags_off);
-    a.counters = pad_word(h, 0, h->counters_off);
-    a.status = pad_word(h, 0, 0);
+    ReduceScatterArgs a;
+    a.in = static_cast<const uint8_t *>(in);
+    a.out = static_cast<uint8_t *>(out);
     a.stride = (long long)h->stride;
     a.R = h->R;
-    a.N = N;
-    a.Kr = Kr;
-    a.B = B;
-    a.rows_per_tile = rows;
-    a.num_tiles = tiles;
-    a.epoch = h->epoch;
-    a.reverse_order = h->opt_tile_order;
-    a.splits = splits;
-    a.partial_stride = (long long)B * N * 4;
-    a.kc_cap = 0;
-    cudaError_t e = cudaSuccess;
-    switch (path) {
-        case kPathFfma:
-            a.kc_cap = ffma_kc_cap(B, Kr);
-            e = launch_gemv_ffma(a, s);
-            break;
-        case kPathTc:
-        case kPathSk:
-        case kPathDyn: {
-            if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
-            int err = 0;
-            const void *maps = tc_maps_for(h, a, &err);
-            if (!maps) {
-                h->epoch -= 1;
-                return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
-            }
-            if (path == kPathTc) {
-                e = launch_gemv_tc(a, maps, s);
-            } else if (path == kPathDyn) {
-                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, s);
-            } else {
-                a.partial_stride = (long long)B * N * 4;
-                e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
-            }
-            break;
-        }
-        default:
-            return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "gemv_all_reduce launch");
+    a.n = n;
+    a.chunk = n / (size_t)R;
+    a.shift = 0;
+    cudaError_t e = launch_reduce_scatter(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
     return SYMM_OK;
+}
+
+int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    if (n == 0) return SYMM_OK;
+    if (n > SIZE_MAX / 2) return fail(SYMM_EINVAL, "n too large");
+    const size_t bytes = n * 2;
+    if (!in_user_region(h, in, bytes)) return fail(SYMM_EINVAL, "in + n elements is not inside slot 0's user region");
+    if (!in_user_region(h, out, bytes)) return fail(SYMM_EINVAL, "out + n elements is not inside slot 0's user region");
+    if (!aligned16(in) || !aligned16(out)) return fail(SYMM_EINVAL, "in/out must be 16-byte aligned");
+    if (in != out && overlaps(in, bytes, out, bytes)) return fail(SYMM_EINVAL, "in and out partially overlap");
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+    // Owner s reduces elements [s*chunk, (s+1)*chunk); chunk is a multiple of
+    // 8 elements so that every owner's block starts on a 16-byte boundary.
+    const size_t per = (n + (size_t)R - 1) / (size_t)R;
+    ReduceScatterArgs a;
+    a.in = static_cast<const uint8_t *>(in);
+    a.out = static_cast<uint8_t *>(out);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.n = n;
+    a.chunk = (per + 7) / 8 * 8;
+    a.shift = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_reduce_scatter(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "two_shot_all_reduce reduce-scatter launch");
+    e = launch_all_gather_blocks(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "two_shot_all_reduce all-gather launch");
+    return SYMM_OK;
+}
+
+int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, const void *gamma, void *out, int R,
+                            int rows, int H, float eps, symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    if (rows < 0 || rows > 65535) return fail(SYMM_EINVAL, "rows=%d outside 0..65535", rows);
+    if (H < 8 || H % 8 || H > rmsnorm_max_h())
+        return fail(SYMM_EINVAL, "H=%d must be a multiple of 8 in 8..%d", H, rmsnorm_max_h());
+    if (!(eps >= 0.f) || eps > 3.0e38f) return fail(SYMM_EINVAL, "eps must be finite and >= 0");
+    if (rows == 0) return SYMM_OK;
+    const size_t bytes = (size_t)rows * H * 2, vb = (size_t)H * 2;
+    if (!in_user_region(h, in, bytes)) return fail(SYMM_EINVAL, "in (rows x H bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, out, bytes)) return fail(SYMM_EINVAL, "out (rows x H bf16) is not inside slot 0's user region");
+    if (!aligned16(in) || !aligned16(out)) return fail(SYMM_EINVAL, "in/out must be 16-byte aligned");
+    if (in != out && overlaps(in, bytes, out, bytes)) return fail(SYMM_EINVAL, "in and out partially overlap");
+    for (const void *v : {bias, gamma}) {
+        if (!v) continue;
+        if (!in_user_region(h, v, vb) || !aligned16(v))
+            return fail(SYMM_EINVAL, "bias / gamma (H bf16) must be 16-byte aligned inside slot 0's user region");
+        if (overlaps(v, vb, out, bytes)) return fail(SYMM_EINVAL, "bias / gamma overlaps out");
+    }
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+    RmsNormArgs a = {};
+    a.in = static_cast<const uint8_t *>(in);
+    a.bias = static_cast<const uint8_t *>(bias);
+    a.gamma = static_cast<const uint8_t *>(gamma);
+    a.out = static_cast<uint8_t *>(out);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.rows = rows;
+    a.H = H;
+    a.eps = eps;
+    a.wait_prior = 0;
+    cudaError_t e = launch_rmsnorm_rows(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "all_reduce_bias_rmsnorm launch");
+    return SYMM_OK;
+}
+
+int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *out_tile, const int *roots,
+                           int ntiles, int rows, int cols, long long ld_in, long long ld_out, symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (!in_tiles || !roots || !out_tile) return fail(SYMM_EINVAL, "NULL argument");
+    if (ntiles < 1 || ntiles > h->R || ntiles > kMaxTiles)
+        return fail(SYMM_EINVAL, "ntiles=%d outside 1..%d (one root per rank at most)", ntiles, std::min(h->R, kMaxTiles));
+    if (rows < 0 || cols < 0) return fail(SYMM_EINVAL, "rows=%d cols=%d must be >= 0", rows, cols);
+    if (rows > 0 && cols > 0 && (ld_in < cols || ld_out < cols))
+        return fail(SYMM_EINVAL, "leading dimensions (%lld, %lld) must be >= cols=%d", ld_in, ld_out, cols);
+    bool used[SYMM_MAX_RANKS] = {};
+    for (int i = 0; i < ntiles; ++i) {
+        if (roots[i] < 0 || roots[i] >= h->R) return fail(SYMM_EINVAL, "root %d outside 0..%d", roots[i], h->R - 1);
+        if (used[roots[i]]) return fail(SYMM_EINVAL, "rank %d is the root of more than one tile", roots[i]);
+        used[roots[i]] = true;
+    }
+    if (rows == 0 || cols == 0) return SYMM_OK;
+    const size_t in_ext = ((size_t)(rows - 1) * (size_t)ld_in + (size_t)cols) * 2;
+    const size_t out_ext = ((size_t)(rows - 1) * (size_t)ld_out + (size_t)cols) * 2;
+    if (!in_user_region(h, out_tile, out_ext) || (reinterpret_cast<uintptr_t>(out_tile) & 1))
+        return fail(SYMM_EINVAL, "the output tile is not inside slot 0's user region (or not 2-byte aligned)");
+    for (int i = 0; i < ntiles; ++i) {
+        if (!in_tiles[i] || !in_user_region(h, in_tiles[i], in_ext) || (reinterpret_cast<uintptr_t>(in_tiles[i]) & 1))
+            return fail(SYMM_EINVAL, "input tile %d is not inside slot 0's user region (or not 2-byte aligned)", i);
+        // the output tile is written while other threads still read inputs
+        if (overlaps(in_tiles[i], in_ext, out_tile, out_ext))
+            return fail(SYMM_EINVAL, "input tile %d overlaps the output tile", i);
+    }
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+    TileReduceArgs a;
+    for (int i = 0; i < ntiles; ++i) {
+        a.in[i] = static_cast<const uint8_t *>(in_tiles[i]);
+        a.root[i] = roots[i];
+    }
+    a.out = static_cast<uint8_t *>(out_tile);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.ntiles = ntiles;
+    a.rows = rows;
+    a.cols = cols;
+    a.ld_in = ld_in;
+    a.ld_out = ld_out;
+    cudaError_t e = launch_tile_reduce(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tile reduce launch");
+    return SYMM_OK;
+}
+
+int tile_reduce(symm_handle_t *h, const void *in_tile, void *out_tile, int root, int rows, int cols, long long ld_in,
+                long long ld_out, symm_stream_t stream) {
+    const void *tiles[1] = {in_tile};
+    const int roots[1] = {root};
+    return multi_root_tile_reduce(h, tiles, out_tile, roots, 1, rows, cols, ld_in, ld_out, stream);
 }
 
 int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile) {

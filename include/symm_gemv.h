@@ -192,6 +192,123 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
  */
 int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band);
 
+/*
+ * gemv_reduce_scatter -- the fused row-parallel layer ending in a
+ * reduce-scatter instead of an all-reduce: the sequence-parallel form
+ * ("Bay.Area.AI: Tensor and 2D Parallelism", sequence-parallel passage: the
+ * activations are sharded along the sequence, and after the row-wise sharded
+ * linear one reduce-scatter returns each rank its own tokens of the sum).
+ * With y_full = bf16_rne( sum_r W_r x_r ) (B x N, as gemv_all_reduce computes
+ * it), rank s receives batch rows [s*B/R, (s+1)*B/R):
+ *
+ *     y_s[i][n] = y_full[s*B/R + i][n]      i < B/R
+ *
+ *   y  symmetric bf16 pointer; (B/R) x N row-major per slot.
+ * B % R == 0 is required (else SYMM_EINVAL); every other argument, layout,
+ * requirement and error as for gemv_all_reduce.  Bitwise equal to the rows of
+ * gemv_all_reduce's result for the same inputs and options.
+ */
+int gemv_reduce_scatter(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K,
+                        int B, symm_stream_t stream);
+
+/*
+ * gemv_all_reduce_bias_rmsnorm -- the fused layer followed by a bias and RMS
+ * normalisation of each batch row's N outputs (the all-reduce + bias + RMSNorm
+ * kernel of the "PyTorch Symmetric Memory" talk, fused-kernel segment,
+ * applied to the fused GEMV):
+ *
+ *     z[b][n]   = sum_r (W_r x_r)[b][n] + bias[n]                 (fp32)
+ *     y_s[b][n] = bf16_rne( z[b][n] / sqrt(mean_n z[b][n]^2 + eps) * gamma[n] )
+ *
+ * for every rank s.  The tile reducers store z (fp32) at the top of slot 0's
+ * scratch region instead of y; a second kernel (one thread-block cluster per
+ * batch row) normalises.  It is launched right after the GEMV on the same
+ * stream, as a programmatic dependent unless SYMM_OPT_NORM_PDL is 0.
+ *   bias, gamma  symmetric bf16 pointers to N elements (slot 0's copy is
+ *                read), 16-byte aligned; NULL means zeros / ones.
+ *   eps          >= 0, finite.
+ * Requirements beyond gemv_all_reduce: N % 8 == 0, N <= 65536, and the
+ * scratch region holds the partials plus 4*B*N bytes of z (else
+ * SYMM_ERANGE).  Errors: SYMM_EINVAL, SYMM_ERANGE, SYMM_ECUDA.
+ */
+int gemv_all_reduce_bias_rmsnorm(symm_handle_t *h, const void *W_r, const void *x_r, const void *bias,
+                                 const void *gamma, void *y, int R, int N, int K, int B, float eps,
+                                 symm_stream_t stream);
+
+/*
+ * reduce_scatter -- out_s[j] = bf16_rne( sum_{r=0}^{R-1} in_r[s*n/R + j] ),
+ * j < n/R, for every rank s: each rank keeps its own block of the summed flat
+ * tensor ("Bay.Area.AI: Tensor and 2D Parallelism", sequence-parallel
+ * passage; the reduce-scatter of the PyTorch Symmetric Memory docs' NCCL
+ * symmetric-kernel list).  fp32 accumulation in rank order.
+ *   in   symmetric bf16 pointer, n elements; out  symmetric, n/R elements.
+ *   n % R == 0; in and out must not overlap; 16-byte aligned.
+ * Errors: SYMM_EINVAL, SYMM_ECUDA.
+ */
+int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream);
+
+/*
+ * two_shot_all_reduce -- the same result as one_shot_all_reduce, bit for bit,
+ * computed in two phases (PyTorch Symmetric Memory docs, op reference
+ * `two_shot_all_reduce_`): rank s reduces only its block of elements
+ * [s*c, (s+1)*c) (c = ceil(n/R) rounded up to 8) into its own out, then every
+ * rank gathers the other blocks from their owners.  The two phases are two
+ * launches on `stream` (stream order is the barrier between them).  in == out
+ * (in place, as the docs' op) is allowed; other arguments as for
+ * one_shot_all_reduce.
+ */
+int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream);
+
+/*
+ * all_reduce_bias_rmsnorm -- the all-reduce + bias + RMSNorm kernel of the
+ * "PyTorch Symmetric Memory" talk (fused-kernel segment: the bias is added in
+ * the reduction's element-wise loop and the RMS normalisation follows in the
+ * same launch).  For each of `rows` rows of H elements and every rank s:
+ *
+ *     z[h]    = (sum_{r=0}^{R-1} in_r[h]) + bias[h]               (fp32)
+ *     out_s[h] = bf16_rne( z[h] / sqrt(mean_h z[h]^2 + eps) * gamma[h] )
+ *
+ *   in, out      symmetric bf16 pointers, rows x H row-major; in == out is
+ *                allowed, partial overlap is not.
+ *   bias, gamma  symmetric bf16 pointers to H elements or NULL (zeros / ones).
+ *   rows 0..65535; H % 8 == 0, 8 <= H <= 65536; eps >= 0 finite.
+ * One thread-block cluster per row.  Errors: SYMM_EINVAL, SYMM_ECUDA.
+ */
+int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, const void *gamma, void *out,
+                            int R, int rows, int H, float eps, symm_stream_t stream);
+
+/*
+ * tile_reduce -- sum a 2-D tile over all ranks into the root's output tile
+ * (PyTorch Symmetric Memory docs, op reference `tile_reduce`, reduce op
+ * "sum"; the talk's tile-communication segment):
+ *
+ *     out_root[a][c] = bf16_rne( sum_{r=0}^{R-1} in_r[a][c] )   a < rows, c < cols
+ *
+ * where element (a, c) of a tile is at tile + (a * ld + c) * 2 bytes, i.e. a
+ * rows x cols block of a row-major tensor with leading dimension ld
+ * (elements), not contiguous.  Only the root's output tile is written.
+ *   in_tile, out_tile  symmetric bf16 pointers (2-byte aligned; rows whose
+ *                      starts are all 16-byte aligned use 16-byte loads);
+ *                      they must not overlap.
+ *   ld_in, ld_out >= cols.  rows == 0 or cols == 0 is a no-op.
+ * Errors: SYMM_EINVAL, SYMM_ECUDA.
+ */
+int tile_reduce(symm_handle_t *h, const void *in_tile, void *out_tile, int root, int rows, int cols,
+                long long ld_in, long long ld_out, symm_stream_t stream);
+
+/*
+ * multi_root_tile_reduce -- several tiles at once, tile i summed over all
+ * ranks into the output tile of rank roots[i] (PyTorch Symmetric Memory docs,
+ * op reference `multi_root_tile_reduce`: no rank is root of two tiles).  All
+ * tiles have the same shape and leading dimension; the output tile is the
+ * same symmetric address for every root.  One launch.
+ *   in_tiles [ntiles] host array of symmetric pointers; roots [ntiles] host
+ *   array of distinct ranks; 1 <= ntiles <= R.  Otherwise as tile_reduce.
+ */
+int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *out_tile, const int *roots,
+                           int ntiles, int rows, int cols, long long ld_in, long long ld_out,
+                           symm_stream_t stream);
+
 /* Per-handle options.  The kernel choice is automatic by default; the
  * others exist for tests and measurements. */
 enum {
@@ -204,7 +321,10 @@ enum {
     SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (FFMA for B <= 2, else tcgen05), 0 tcgen05, 1 FFMA */
     SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: resident CTAs per SM, 0 auto (2), 1..3 (ring shrinks) */
     SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
-    SYMM_OPT_DYN_SPLITS = 7   /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
+    SYMM_OPT_DYN_SPLITS = 7,  /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
+    SYMM_OPT_NORM_PDL = 8     /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
+                                 programmatic dependent of the GEMV so its launch overlaps the GEMV's
+                                 tail; 0 plain stream order */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

@@ -19,6 +19,16 @@ mlp_down_decode     R=8 N=8192 K=28672 B=1; W~N(0,0.01) x=SiLU(g)*u,
                     g,u~N(0,1); seed 3
 mlp_down_large      R=8 N=16384 K=53248 B=16; W~N(0,0.006) x~N(0,1) with
                     floor(0.01 K) channels scaled x20; seed 4
+ar_bias_rmsnorm     R=8 rows=1 H=8192; in_r~U[-1,1); bias~N(0,0.1),
+                    gamma~N(1,0.1); eps 1e-6; seed 5
+mlp_down_decode_rmsnorm
+                    mlp_down_decode's W and x (seed 3) + bias~N(0,0.1),
+                    gamma~N(1,0.1) over N; eps 1e-6
+mlp_down_large_rs   mlp_down_large's W and x (seed 4), reduce-scatter of
+                    the B=16 rows over R=8 ranks (2 rows each)
+multi_root_tile     R=4, an 8192 x 8192 tensor per rank, in~U[-1,1);
+                    its four 4096 x 4096 quadrants summed to roots 0..3;
+                    seed 6
 ==================  =====================================================
 
 "N(m, s)": s is the standard deviation.  W and x are generated as the global
@@ -40,6 +50,7 @@ _LIB_PATH = os.path.join(_HERE, "libsynth.so")
 _lib = None
 
 TAG_W, TAG_X, TAG_G, TAG_U, TAG_OUTLIER, TAG_AR = 1, 2, 3, 4, 5, 6
+TAG_BIAS, TAG_GAMMA, TAG_TILE = 7, 8, 9
 
 WORKLOADS = {
     "tiny": dict(kind="gemv", R=2, N=256, K=512, B=1, seed=0, w_std=0.02, x="normal"),
@@ -49,6 +60,11 @@ WORKLOADS = {
                             x="silu_mul"),
     "mlp_down_large": dict(kind="gemv", R=8, N=16384, K=53248, B=16, seed=4, w_std=0.006,
                            x="outliers"),
+    "ar_bias_rmsnorm": dict(kind="ar_rmsnorm", R=8, rows=1, H=8192, seed=5, eps=1e-6),
+    "mlp_down_decode_rmsnorm": dict(kind="gemv_rmsnorm", R=8, N=8192, K=28672, B=1, seed=3, w_std=0.01,
+                                    x="silu_mul", eps=1e-6),
+    "mlp_down_large_rs": dict(kind="gemv_rs", R=8, N=16384, K=53248, B=16, seed=4, w_std=0.006, x="outliers"),
+    "multi_root_tile": dict(kind="tile", R=4, rows=8192, cols=8192, seed=6),
 }
 
 
@@ -185,9 +201,38 @@ def allreduce_inputs(R: int, n: int, seed: int) -> np.ndarray:
     return uniform(seed, TAG_AR, R, n, lo=-1.0, hi=1.0)[0]
 
 
+def norm_vectors(n: int, seed: int):
+    """(bias, gamma) for a bias + RMSNorm over n elements: bias ~ N(0, 0.1),
+    gamma ~ N(1, 0.1), bf16 words of shape (n,)."""
+    bias = normal(seed, TAG_BIAS, 1, n, std=0.1)[0, 0]
+    gamma = normal(seed, TAG_GAMMA, 1, n, std=0.1, mean=1.0)[0, 0]
+    return bias, gamma
+
+
+def rmsnorm_inputs(R: int, rows: int, H: int, seed: int):
+    """(in (R, rows, H), bias (H,), gamma (H,)) bf16 words; in_r ~ U[-1, 1)."""
+    inp = uniform(seed, TAG_AR, R, rows * H, lo=-1.0, hi=1.0)[0].reshape(R, rows, H)
+    bias, gamma = norm_vectors(H, seed)
+    return inp, bias, gamma
+
+
+def tile_inputs(R: int, rows: int, cols: int, seed: int) -> np.ndarray:
+    """(R, rows, cols) bf16 words, U[-1, 1): each rank's full 2-D tensor."""
+    return uniform(seed, TAG_TILE, R, rows * cols, lo=-1.0, hi=1.0)[0].reshape(R, rows, cols)
+
+
 def workload_inputs(name: str):
-    """Inputs of a named workload: (W, x) for GEMV cases, in_r for allreduce."""
+    """Inputs of a named workload: (W, x) for GEMV cases (plus (bias, gamma)
+    for the RMSNorm form), in_r for allreduce, (in, bias, gamma) for the
+    all-reduce + bias + RMSNorm case, the full tensors for the tile case."""
     w = WORKLOADS[name]
     if w["kind"] == "allreduce":
         return allreduce_inputs(w["R"], w["n"], w["seed"])
-    return gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
+    if w["kind"] == "ar_rmsnorm":
+        return rmsnorm_inputs(w["R"], w["rows"], w["H"], w["seed"])
+    if w["kind"] == "tile":
+        return tile_inputs(w["R"], w["rows"], w["cols"], w["seed"])
+    Wx = gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
+    if w["kind"] == "gemv_rmsnorm":
+        return Wx + norm_vectors(w["N"], w["seed"])
+    return Wx

@@ -67,7 +67,14 @@ def test_null_handle_is_rejected(lib):
     for call in (lambda: csg.gemv_all_reduce(None, 0, 0, 0, 2, 8, 16, 1),
                  lambda: csg.one_shot_all_reduce(None, 0, 0, 2, 8),
                  lambda: csg.symm_status(None),
-                 lambda: csg.symm_set_option(None, 1, 0)):
+                 lambda: csg.symm_set_option(None, 1, 0),
+                 lambda: csg.gemv_reduce_scatter(None, 0, 0, 0, 2, 8, 16, 2),
+                 lambda: csg.gemv_all_reduce_bias_rmsnorm(None, 0, 0, None, None, 0, 2, 8, 16, 1, 1e-6),
+                 lambda: csg.reduce_scatter(None, 0, 0, 2, 8),
+                 lambda: csg.two_shot_all_reduce(None, 0, 0, 2, 8),
+                 lambda: csg.all_reduce_bias_rmsnorm(None, 0, None, None, 0, 2, 1, 8, 1e-6),
+                 lambda: csg.tile_reduce(None, 0, 0, 0, 4, 4, 4, 4),
+                 lambda: csg.multi_root_tile_reduce(None, [0], 0, [0], 4, 4, 4, 4)):
         with pytest.raises(csg.SymmError) as e:
             call()
         assert e.value.code == csg.SYMM_EINVAL

@@ -231,16 +231,36 @@ def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
     return None
 
 
-def kernel_source_sha():
-    """Hash of the device-code sources (the host runtime, which only plans and
-    launches, is left out)."""
+# Device-code files each kernel is built from (the host runtime, which only
+# plans and launches, is left out).
+KERNEL_SOURCES = {
+    "gemv_ar_ffma_kernel": ("gemv_ffma.cu",),
+    "gemv_ar_tc_kernel": ("gemv_tc.cu", "sm100.cuh"),
+    "gemv_ar_sk_kernel": ("gemv_sk.cu", "sm100.cuh"),
+    "gemv_ar_dyn_kernel": ("gemv_dyn.cu", "sm100.cuh"),
+    "one_shot_ar_kernel": ("allreduce.cu",),
+    "reduce_scatter_kernel": ("allreduce.cu",),
+    "all_gather_blocks_kernel": ("allreduce.cu",),
+    "rmsnorm_rows_kernel": ("rmsnorm.cu",),
+    "tile_reduce_kernel": ("tile_reduce.cu",),
+}
+
+
+def kernel_source_sha(kernel=None):
+    """Hash of the device code a kernel is built from: its own file plus the
+    shared headers (protocol.cuh, internal.h).  `kernel` is a kernel name as
+    the bench reports it (template arguments and '+second kernel' ignored);
+    None hashes every device-code file."""
     import hashlib
 
-    h = hashlib.sha256()
     csrc = os.path.join(ROOT, "collective_split_gemv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f == "symm_runtime.cu":
-            continue
+    if kernel is None:
+        files = sorted(f for f in os.listdir(csrc) if f != "symm_runtime.cu")
+    else:
+        base = kernel.split("+")[0].split("<")[0]
+        files = sorted(set(KERNEL_SOURCES.get(base, ())) | {"protocol.cuh", "internal.h"})
+    h = hashlib.sha256()
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -526,7 +546,7 @@ def run_ours(args, rank, world, local_rank):
                           else "fallback 6.8 TB/s"),
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(kernel, args.workload, kernel_source_sha()),
+            "traffic": profiled_traffic(kernel, args.workload, kernel_source_sha(kernel)),
             "mean_launch_us": round(mean_launch_ms * 1e3, 3),
             "median_launch_us": round(statistics.median(launch_ms) * 1e3, 3),
         },

@@ -228,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base_ticket = (a.epoch - 1u) * (uint32_t)U;
 
     if (threadIdx.x == 0) {
+        // The descriptors' fetch overlaps the set-up below (the first TMA
+        // load would otherwise wait for it).
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], kEngine == 0 ? 1 : 4);
@@ -254,8 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
             int issued = 0;
             // The first unit is the CTA's own index (G <= U); later ones are
             // drawn: ticket k names unit G + k.
@@ -283,8 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r = tr - t * a.R;
                 const int kb0 = sp * KBs;
                 const int kb1 = min(kb0 + KBs, KB);
-                // Draw the next unit now; its value is needed only after this one.
-                const uint32_t next = atom_add_relaxed_gpu(geo.work, 1u) - base_ticket + (uint32_t)geo.G;
+                // The next unit is drawn right after the loads of this unit's
+                // last K block are issued: late enough that a CTA on a slow SM
+                // does not take a unit a faster one would finish first (the
+                // draw decides who gets the remaining units), early enough that
+                // the atomic's latency hides behind the stages still in the
+                // ring.  The ticket -> unit arithmetic sits in an asm statement
+                // after the loop, so no instruction waits on the atomic early.
+                uint32_t next_raw = 0u;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const int st = issued % kStages;
                     const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
@@ -303,9 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int s = 0; s < kSlabs; ++s)
                         tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0,
                                     r);
+                    if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(geo.work, 1u);
                     ++issued;
                 }
-                tk = next;
+                asm volatile("sub.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"(base_ticket - (uint32_t)geo.G));
             }
             if (!ok) {
                 latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);

@@ -165,13 +165,8 @@ __device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeo
                 first = false;
             }
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = i0 + k * kGroupThreads;
-            if (i < count) {
-                const int b = i / rows;
-                store_output(a, b, n0 + (i - b * rows), acc[k]);
-            }
-        }
+        for (int k = 0; k < kPer; ++k)
+            if (i0 + k * kGroupThreads < count) store_output(a, off[k] / sizeof(float), acc[k]);
     }
 }
 

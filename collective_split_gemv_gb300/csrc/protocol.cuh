@@ -97,19 +97,24 @@ __device__ __forceinline__ void latch_status(uint32_t *status, int code, int ran
 // rank that owns batch row b (reduce-scatter along the batch rows, the
 // sequence-parallel ending of the row-parallel layer), or fp32 sum + bias
 // into z for the RMS-normalisation stage.
-__device__ __forceinline__ void store_output(const GemvArgs &a, int b, int n, float acc) {
+// `e` is the element index b * N + n of the output in a [B][N] array.
+__device__ __forceinline__ void store_output(const GemvArgs &a, size_t e, float acc) {
     if (a.out_mode == kOutAllReduce) {
         const __nv_bfloat16 h = __float2bfloat16_rn(acc);
-        const size_t yoff = ((size_t)b * a.N + n) * 2;
-        for (int q = 0; q < a.R; ++q) *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = h;
-    } else if (a.out_mode == kOutReduceScatter) {
+        for (int q = 0; q < a.R; ++q)
+            *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + e * 2) = h;
+        return;
+    }
+    const int b = (int)(e / (size_t)a.N);
+    const int n = (int)(e - (size_t)b * a.N);
+    if (a.out_mode == kOutReduceScatter) {
         const int q = b / a.rs_rows;
         const size_t yoff = ((size_t)(b - q * a.rs_rows) * a.N + n) * 2;
         *reinterpret_cast<__nv_bfloat16 *>(a.y + (long long)q * a.stride + yoff) = __float2bfloat16_rn(acc);
     } else {
         float v = acc;
         if (a.bias) v += __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.bias)[n]);
-        __stcg(a.z + (size_t)b * a.N + n, v);
+        __stcg(a.z + e, v);
     }
 }
 
@@ -162,13 +167,8 @@ __device__ __forceinline__ void reduce_tile(const GemvArgs &a, int n0, int rows,
                 }
         }
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = i0 + k * nthreads;
-            if (i < count) {
-                const int b = i / rows;
-                store_output(a, b, n0 + (i - b * rows), acc[k]);
-            }
-        }
+        for (int k = 0; k < kPer; ++k)
+            if (i0 + k * nthreads < count) store_output(a, off[k] / sizeof(float), acc[k]);
     }
 }
 

@@ -16,10 +16,14 @@
 // A row of H elements is split over the C CTAs of a cluster (C <= 8, grid
 // (C, rows)); every thread keeps its z values in registers.  The sum of
 // squares is reduced in a fixed tree (thread -> warp shuffle -> CTA in warp
-// order -> cluster in CTA-rank order through distributed shared memory), so
-// every CTA of the cluster derives the same scale and the result does not
-// depend on timing.  The two cluster barriers are hardware barriers among
-// CTAs that are co-scheduled by construction: no CTA spins on memory.
+// order -> cluster in CTA-rank order: each CTA pushes its sum into every
+// CTA's shared memory, then a cluster barrier), so every CTA derives the
+// same scale and the result does not depend on timing.  The cluster barriers
+// (one split into an arrive at entry and a wait before the first remote
+// store, so that no CTA writes into a CTA that has not started; one after the
+// stores) are hardware barriers among CTAs that are co-scheduled by
+// construction: no CTA spins on memory, and none touches another's shared
+// memory after the last barrier, so any may exit.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,13 +45,12 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t cta) {
+// Store v at the same shared-memory variable of CTA `cta` of the cluster.
+__device__ __forceinline__ void st_cluster_f32(float *local, uint32_t cta, float v) {
     const uint32_t addr = (uint32_t)__cvta_generic_to_shared(local);
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(cta));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
@@ -66,9 +69,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int kSrc, int kV>
 __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArgs a, int chunk) {
     __shared__ float s_warp[kWarps];
-    __shared__ float s_cta;
-    __shared__ float s_scale;
-    if (a.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float s_part[kMaxCluster];   // s_part[c]: CTA c's sum of squares
 
     uint32_t crank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
@@ -78,6 +79,26 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     const int H8 = a.H / 8;
     const int v0 = (int)crank * chunk;
     const int v1 = min(H8, v0 + chunk);
+
+    // Distributed shared memory may be written only once every CTA of the
+    // cluster runs: arrive now, wait just before the first remote store (the
+    // row loads in between hide the wait).
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+    // gamma and bias do not depend on the kernel this one may follow: load
+    // them first, so their latency hides under the wait and the row loads.
+    uint4 gv[kV], bv[kV];
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+        const int v = v0 + (int)threadIdx.x + j * kThreads;
+        gv[j] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);   // bf16 1.0 pairs
+        bv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (v < v1) {
+            if (a.gamma) gv[j] = ld_v4(a.gamma + (size_t)v * 16);
+            if (kSrc == 0 && a.bias) bv[j] = ld_v4(a.bias + (size_t)v * 16);
+        }
+    }
+    if (a.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float z[kV][8];
     float ss = 0.f;
@@ -106,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
                 }
                 if (a.bias) {
                     float f[8];
-                    unpack8(ld_v4(a.bias + (size_t)v * 16), f);
+                    unpack8(bv[j], f);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) z[j][k] += f[k];
                 }
@@ -125,26 +146,27 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    // Thread c < C of warp 0 pushes this CTA's sum (warps in order) into
+    // s_part[crank] of CTA c; one cluster barrier (release / acquire) makes
+    // all pushes visible, and no CTA touches another's memory after it.
+    if (threadIdx.x < csize) {
         float t = s_warp[0];
+#pragma unroll
         for (int w = 1; w < kWarps; ++w) t += s_warp[w];
-        s_cta = t;
+        st_cluster_f32(&s_part[crank], threadIdx.x, t);
     }
-    cluster_sync_all();            // every CTA's s_cta is written and visible
-    if (threadIdx.x == 0) {
-        float t = ld_cluster_f32(&s_cta, 0);
-        for (uint32_t c = 1; c < csize; ++c) t += ld_cluster_f32(&s_cta, c);
-        s_scale = 1.0f / sqrtf(t / (float)a.H + a.eps);
-    }
-    cluster_sync_all();            // no CTA leaves while another still reads its s_cta
-    const float scale = s_scale;   // written before the barrier by thread 0 of this CTA
+    cluster_sync_all();
+    float tot = s_part[0];
+    for (uint32_t c = 1; c < csize; ++c) tot += s_part[c];   // CTA-rank order: the same in every CTA
+    const float scale = 1.0f / sqrtf(tot / (float)a.H + a.eps);
 
 #pragma unroll
     for (int j = 0; j < kV; ++j) {
         const int v = v0 + (int)threadIdx.x + j * kThreads;
         if (v < v1) {
-            float g[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-            if (a.gamma) unpack8(ld_v4(a.gamma + (size_t)v * 16), g);
+            float g[8];
+            unpack8(gv[j], g);
             float y[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) y[k] = z[j][k] * scale * g[k];

@@ -257,8 +257,10 @@ def kernel_source_sha(kernel=None):
     if kernel is None:
         files = sorted(f for f in os.listdir(csrc) if f != "symm_runtime.cu")
     else:
-        base = kernel.split("+")[0].split("<")[0]
-        files = sorted(set(KERNEL_SOURCES.get(base, ())) | {"protocol.cuh", "internal.h"})
+        files = {"protocol.cuh", "internal.h"}
+        for part in kernel.split("+"):           # a step of two kernels hashes both
+            files |= set(KERNEL_SOURCES.get(part.split("<")[0], ()))
+        files = sorted(files)
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:

@@ -133,6 +133,11 @@ def max_over_ranks(values, world, device=None):
     return [float(v) for v in t.cpu()]
 
 
+def _p10_p90(values):
+    v = sorted(values)
+    return v[int(0.1 * (len(v) - 1))], v[int(0.9 * (len(v) - 1))]
+
+
 def throughput_gbs(nbytes, ms, world=1):
     """Whole-job GB/s: every rank moved `nbytes` in `ms` (the max over ranks)."""
     return world * nbytes / (ms * 1e-3) / 1e9
@@ -334,8 +339,9 @@ def _copies_for(per_copy):
 def make_case(args, w, local_rank, stream):
     """Workspace, inputs and the per-step call of one workload.  Returns a dict:
     ws, step(i) (copy i % copies), run0() (copy 0, for the end-to-end leg),
-    in_host / in_dev (per-step inputs for the end-to-end copies), out_dev /
-    out_bytes (the result read back), kernel, config, per_copy, copies,
+    in_host / in_dst / in_bytes (per-step inputs for the end-to-end leg: one
+    pinned buffer of R blocks, their symmetric destination and the bytes per
+    rank), out_src / out_bytes (the result in slot 0, read back), kernel, config, per_copy, copies,
     launches_per_step, W (GEMV weights, for the weights-from-host leg)."""
     import collective_split_gemv_gb300 as csg
     import synth
@@ -372,8 +378,8 @@ def make_case(args, w, local_rank, stream):
             "step": lambda i: ws.run(stream, copy=i % copies, mode=mode, eps=eps),
             "run0": lambda: ws.run(stream, copy=0, mode=mode, eps=eps),
             # e2e: per-step inputs are x_r (W_r are resident model weights); result y
-            "in_host": [_pinned(x[r]) for r in range(R)], "in_dev": [ws.x_view(r) for r in range(R)],
-            "out_dev": ws.view(0, ws.y_off, out_rows * N * 2), "out_bytes": out_rows * N * 2,
+            "in_host": _pinned(x), "in_dst": ws.x_ptr(), "in_bytes": ws.x_bytes,
+            "out_src": ws.y_ptr(), "out_bytes": out_rows * N * 2,
             "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
             "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
                        **({"eps": eps, "norm_pdl": args.norm_pdl} if kind == "gemv_rmsnorm" else {})},
@@ -392,8 +398,8 @@ def make_case(args, w, local_rank, stream):
             "ws": ws, "copies": copies, "per_copy": inp.nbytes * 2, "kernel": kernel,
             "step": lambda i: ws.run(stream, copy=i % copies, op=op),
             "run0": lambda: ws.run(stream, copy=0, op=op),
-            "in_host": [_pinned(inp[r]) for r in range(R)], "in_dev": [ws.in_view(r, 0) for r in range(R)],
-            "out_dev": ws.view(0, ws.out_offs[0], out_n * 2), "out_bytes": out_n * 2,
+            "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
+            "out_src": ws.base + ws.out_offs[0], "out_bytes": out_n * 2,
             "launches_per_step": 2 if op == "two_shot" else 1,
             "config": {"R": R, "n": n, "op": op},
         }
@@ -408,9 +414,8 @@ def make_case(args, w, local_rank, stream):
             "ws": ws, "copies": copies, "per_copy": inp.nbytes * 2, "kernel": "rmsnorm_rows_kernel<slots>",
             "step": lambda i: ws.run(stream, copy=i % copies, eps=eps),
             "run0": lambda: ws.run(stream, copy=0, eps=eps),
-            "in_host": [_pinned(inp[r]) for r in range(R)],
-            "in_dev": [ws.view(r, ws.in_offs[0], ws.bytes) for r in range(R)],
-            "out_dev": ws.view(0, ws.out_offs[0], ws.bytes), "out_bytes": ws.bytes,
+            "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
+            "out_src": ws.base + ws.out_offs[0], "out_bytes": ws.bytes,
             "launches_per_step": 1,
             "config": {"R": R, "rows": rows, "H": H, "eps": eps},
         }
@@ -428,9 +433,8 @@ def make_case(args, w, local_rank, stream):
             "ws": ws, "copies": copies, "per_copy": full.nbytes, "kernel": "tile_reduce_kernel",
             "step": lambda i: ws.run(tiles, roots, h, w["cols"] // 2, stream=stream, copy=i % copies),
             "run0": lambda: ws.run(tiles, roots, h, w["cols"] // 2, stream=stream, copy=0),
-            "in_host": [_pinned(full[r]) for r in range(R)],
-            "in_dev": [ws.view(r, ws.in_offs[0], ws.in_bytes) for r in range(R)],
-            "out_dev": ws.view(0, ws.out_offs[0], ws.out_bytes), "out_bytes": ws.out_bytes,
+            "in_host": _pinned(full), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.in_bytes,
+            "out_src": ws.base + ws.out_offs[0], "out_bytes": ws.out_bytes,
             "launches_per_step": 1,
             "config": {"R": R, "tensor": [n, w["cols"]], "tiles": "four quadrants", "roots": roots},
         }
@@ -459,7 +463,8 @@ def run_ours(args, rank, world, local_rank):
 
     c = make_case(args, w, local_rank, stream)
     ws, step, run0, kernel = c["ws"], c["step"], c["run0"], c["kernel"]
-    in_host, in_dev, out_dev, out_bytes = c["in_host"], c["in_dev"], c["out_dev"], c["out_bytes"]
+    in_host, in_dst, in_bytes = c["in_host"], c["in_dst"], c["in_bytes"]
+    out_src, out_bytes = c["out_src"], c["out_bytes"]
     config_extra, per_copy, copies, W = c["config"], c["per_copy"], c["copies"], c.get("W")
 
     working_set = copies * per_copy
@@ -471,38 +476,39 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit(f"protocol error in the timed region: {csg.symm_last_error()}")
 
     # ---- e2e: the same call through the ABI with host buffers every step ----
-    out_host = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    # Each step: one strided copy of the step's inputs from pinned host memory
+    # into the R slots, the call, one copy of the result (slot 0) back, and a
+    # stream synchronisation.
+    out_host = torch.empty(max(out_bytes, 1), dtype=torch.uint8).pin_memory()
     e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step(extra=None):
+        if extra is not None:
+            extra()
+        csg.symm_copy_to_slots(ws.h, in_dst, in_host.data_ptr(), in_bytes, R, stream)
+        run0()
+        csg.symm_copy_from_slots(ws.h, out_host.data_ptr(), out_src, out_bytes, 1, stream)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
     torch.cuda.synchronize(dev)
     tt = time.perf_counter()
     for i in range(e2e_steps):
-        with torch.cuda.stream(stream):
-            for src, dst in zip(in_host, in_dev):
-                dst.copy_(src, non_blocking=True)
-            run0()
-            out_host.copy_(out_dev, non_blocking=True)
-        stream.synchronize()
+        e2e_step()
     e2e_ms = (time.perf_counter() - tt) * 1e3 / e2e_steps
-    h2d = sum(t.numel() for t in in_host)
+    h2d = in_bytes * R
 
     ew = None
-    if w["kind"] in ("gemv", "gemv_rs", "gemv_rmsnorm"):
+    if W is not None:
         # weights streamed from the host as well (every step copies all W_r)
-        W_host = [torch.from_numpy(np.ascontiguousarray(W[r])).view(torch.uint8).reshape(-1).pin_memory()
-                  for r in range(R)]
-        w_dev = [ws.w_view(r, 0) for r in range(R)]
+        W_host = _pinned(W)
+        w_bytes = W.nbytes // R
         ew_steps = max(3, min(args.steps, 10))
         torch.cuda.synchronize(dev)
         tt = time.perf_counter()
         for i in range(ew_steps):
-            with torch.cuda.stream(stream):
-                for r in range(R):
-                    w_dev[r].copy_(W_host[r], non_blocking=True)
-                for src, dst in zip(in_host, in_dev):
-                    dst.copy_(src, non_blocking=True)
-                run0()
-                out_host.copy_(out_dev, non_blocking=True)
-            stream.synchronize()
+            e2e_step(lambda: csg.symm_copy_to_slots(ws.h, ws.W_ptr(0), W_host.data_ptr(), w_bytes, R, stream))
         ew = (time.perf_counter() - tt) * 1e3 / ew_steps
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
@@ -551,14 +557,16 @@ def run_ours(args, rank, world, local_rank):
             "traffic": profiled_traffic(kernel, args.workload, kernel_source_sha(kernel)),
             "mean_launch_us": round(mean_launch_ms * 1e3, 3),
             "median_launch_us": round(statistics.median(launch_ms) * 1e3, 3),
+            "p10_p90_launch_us": [round(q * 1e3, 3) for q in _p10_p90(launch_ms)],
         },
         "clocks": clocks,
         "e2e": {
             "value": round(throughput_gbs(nbytes, e2e_ms, world), 2), "unit": "GB/s",
             "us_per_call": round(e2e_ms * 1e3, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
-            "what": ("per-step inputs H2D from pinned memory, the call, the result (slot 0) D2H, stream "
-                     "synchronised every step" + ("; W_r resident (model weights)" if W is not None else "")),
+            "what": ("per step: the inputs H2D from pinned memory in one strided copy into the R slots "
+                     "(symm_copy_to_slots), the call, the result (slot 0) D2H (symm_copy_from_slots), stream "
+                     "synchronised" + ("; W_r resident (model weights)" if W is not None else "")),
         },
         "gpu_launches": args.steps * c["launches_per_step"],
     }

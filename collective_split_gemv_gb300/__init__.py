@@ -46,7 +46,8 @@ EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
             "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "gemv_reduce_scatter",
             "gemv_all_reduce_bias_rmsnorm", "reduce_scatter", "two_shot_all_reduce",
-            "all_reduce_bias_rmsnorm", "tile_reduce", "multi_root_tile_reduce", "symm_free",
+            "all_reduce_bias_rmsnorm", "tile_reduce", "multi_root_tile_reduce", "symm_copy_to_slots",
+            "symm_copy_from_slots", "symm_free",
             "symm_last_error")
 
 _lib = None
@@ -102,6 +103,8 @@ def lib() -> ctypes.CDLL:
         L.all_reduce_bias_rmsnorm.argtypes = [vp, vp, vp, vp, vp, i, i, i, f32, vp]
         L.tile_reduce.argtypes = [vp, vp, vp, i, i, i, ll, ll, vp]
         L.multi_root_tile_reduce.argtypes = [vp, ctypes.POINTER(vp), vp, ctypes.POINTER(i), i, i, i, ll, ll, vp]
+        L.symm_copy_to_slots.argtypes = [vp, vp, vp, sz, i, vp]
+        L.symm_copy_from_slots.argtypes = [vp, vp, vp, sz, i, vp]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
         L.symm_last_error.restype = ctypes.c_char_p
@@ -206,6 +209,16 @@ def multi_root_tile_reduce(h, in_tiles, out_tile: int, roots, rows: int, cols: i
     rts = (ctypes.c_int * max(nt, 1))(*[int(r) for r in roots])
     _check(lib().multi_root_tile_reduce(h, tiles, _vp(out_tile), rts, nt, rows, cols, ld_in, ld_out,
                                         _stream(stream)))
+
+
+def symm_copy_to_slots(h, dst: int, src: int, bytes_per_rank: int, nranks: int, stream=None) -> None:
+    """Block r of the contiguous buffer at `src` -> dst + r * stride (one strided copy)."""
+    _check(lib().symm_copy_to_slots(h, _vp(dst), _vp(src), bytes_per_rank, nranks, _stream(stream)))
+
+
+def symm_copy_from_slots(h, dst: int, src: int, bytes_per_rank: int, nranks: int, stream=None) -> None:
+    """src + r * stride -> block r of the contiguous buffer at `dst` (one strided copy)."""
+    _check(lib().symm_copy_from_slots(h, _vp(dst), _vp(src), bytes_per_rank, nranks, _stream(stream)))
 
 
 def symm_status(h, stream=None):

@@ -893,6 +893,33 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
     return SYMM_OK;
 }
 
+int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
+                       symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (nranks < 0 || nranks > h->R) return fail(SYMM_EINVAL, "nranks=%d outside 0..%d", nranks, h->R);
+    if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
+    if (!src) return fail(SYMM_EINVAL, "src is NULL");
+    if (!in_user_region(h, dst, bytes_per_rank)) return fail(SYMM_EINVAL, "dst is not inside slot 0's user region");
+    // One strided copy: rank r's bytes land at dst + r * stride.
+    cudaError_t e = cudaMemcpy2DAsync(dst, h->stride, src, bytes_per_rank, bytes_per_rank, (size_t)nranks,
+                                      cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync (to slots)");
+    return SYMM_OK;
+}
+
+int symm_copy_from_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
+                         symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (nranks < 0 || nranks > h->R) return fail(SYMM_EINVAL, "nranks=%d outside 0..%d", nranks, h->R);
+    if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
+    if (!dst) return fail(SYMM_EINVAL, "dst is NULL");
+    if (!in_user_region(h, src, bytes_per_rank)) return fail(SYMM_EINVAL, "src is not inside slot 0's user region");
+    cudaError_t e = cudaMemcpy2DAsync(dst, bytes_per_rank, src, h->stride, bytes_per_rank, (size_t)nranks,
+                                      cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync (from slots)");
+    return SYMM_OK;
+}
+
 int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     if (bad_rank) *bad_rank = -1;

@@ -185,6 +185,28 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
 int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile);
 
 /*
+ * symm_copy_to_slots / symm_copy_from_slots -- stage per-rank data between a
+ * contiguous buffer and the symmetric slots in one strided copy (the
+ * rendezvous handle's per-peer buffers addressed the same way: rank r's
+ * instance of a symmetric pointer p is p + r * stride).  A convenience of
+ * this library for feeding the calls above from host memory; the source
+ * pages have no counterpart.
+ *   to_slots:   dst symmetric pointer; src holds nranks consecutive blocks of
+ *               bytes_per_rank; block r goes to dst + r * stride.
+ *   from_slots: src symmetric pointer; block r of dst receives
+ *               src + r * stride.
+ *   The contiguous side may be host memory (pinned for an asynchronous copy)
+ *   or device memory.  nranks 0..R; 0 bytes or 0 ranks is a no-op.
+ * Stream-ordered; returns after enqueueing.  Errors: SYMM_EINVAL (NULL
+ * pointer, nranks out of range, the symmetric side outside slot 0's user
+ * region), SYMM_ECUDA.
+ */
+int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
+                       symm_stream_t stream);
+int symm_copy_from_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
+                         symm_stream_t stream);
+
+/*
  * symm_check_guards -- verify the guard bands around every slot's user
  * region, scratch region and signal pad (synchronises the device).
  * Returns SYMM_OK, or SYMM_ECORRUPT with *bad_rank / *bad_band set

@@ -74,7 +74,9 @@ def test_null_handle_is_rejected(lib):
                  lambda: csg.two_shot_all_reduce(None, 0, 0, 2, 8),
                  lambda: csg.all_reduce_bias_rmsnorm(None, 0, None, None, 0, 2, 1, 8, 1e-6),
                  lambda: csg.tile_reduce(None, 0, 0, 0, 4, 4, 4, 4),
-                 lambda: csg.multi_root_tile_reduce(None, [0], 0, [0], 4, 4, 4, 4)):
+                 lambda: csg.multi_root_tile_reduce(None, [0], 0, [0], 4, 4, 4, 4),
+                 lambda: csg.symm_copy_to_slots(None, 0, 0, 16, 1),
+                 lambda: csg.symm_copy_from_slots(None, 0, 0, 16, 1)):
         with pytest.raises(csg.SymmError) as e:
             call()
         assert e.value.code == csg.SYMM_EINVAL

@@ -397,3 +397,38 @@ def test_gemv_bias_rmsnorm_rejects_ragged_n():
     with pytest.raises(csg.SymmError) as e:
         _run_mode(W, x, csg.GEMV_PATH_AUTO, "bias_rmsnorm")
     assert e.value.code == csg.SYMM_EINVAL
+
+
+# ------------------------------------------------------- staging copies
+
+
+def test_copy_to_and_from_slots_round_trip():
+    R, n = 4, 1000
+    aw = AllReduceWorkspace(R, n)
+    try:
+        s = torch.cuda.current_stream()
+        host = torch.arange(R * n, dtype=torch.int16).view(torch.uint8).pin_memory()
+        csg.symm_copy_to_slots(aw.h, aw.base + aw.in_offs[0], host.data_ptr(), n * 2, R, s)
+        s.synchronize()
+        for r in range(R):
+            got = aw.in_view(r).cpu().view(torch.int16)
+            assert torch.equal(got, torch.arange(r * n, (r + 1) * n, dtype=torch.int16)), r
+        back = torch.zeros(R * n * 2, dtype=torch.uint8).pin_memory()
+        csg.symm_copy_from_slots(aw.h, back.data_ptr(), aw.base + aw.in_offs[0], n * 2, R, s)
+        s.synchronize()
+        assert torch.equal(back, host)
+        # the result of a call read back from slot 0 only
+        aw.run(s)
+        one = torch.zeros(n * 2, dtype=torch.uint8).pin_memory()
+        csg.symm_copy_from_slots(aw.h, one.data_ptr(), aw.base + aw.out_offs[0], n * 2, 1, s)
+        s.synchronize()
+        assert torch.equal(one, aw.out_view(0).cpu())
+        for args in ((aw.slots[1], host.data_ptr(), 16, 1),          # not a slot-0 pointer
+                     (aw.base, host.data_ptr(), 16, R + 1),          # too many ranks
+                     (aw.base, 0, 16, 1)):                           # NULL source
+            with pytest.raises(csg.SymmError) as e:
+                csg.symm_copy_to_slots(aw.h, *args, s)
+            assert e.value.code == csg.SYMM_EINVAL
+        _guards_ok(aw.h)
+    finally:
+        aw.close()

@@ -283,10 +283,11 @@ def kernel_name(plan):
     return f"{name}<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
 
 
-def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id):
+def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id, per_launch=True):
     """Warm up, then time exactly n_steps calls of step(i) on `stream`, each
-    bracketed by CUDA events; clocks sampled during the region.  Returns
-    (step_ms, launch_ms list, clocks)."""
+    bracketed by CUDA events (per_launch; otherwise only the region is timed,
+    so that nothing separates consecutive launches on the stream); clocks
+    sampled during the region.  Returns (step_ms, launch_ms list, clocks)."""
     import torch
 
     with torch.cuda.stream(stream):
@@ -309,14 +310,19 @@ def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id):
         for i in range(n_steps):
             if flush_buf is not None:
                 flush_buf.fill_(i & 0xFF)
-            starts[i].record(stream)
+            if per_launch:
+                starts[i].record(stream)
             step(i)
-            ends[i].record(stream)
+            if per_launch:
+                ends[i].record(stream)
         t1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
+    if not per_launch:
+        region = t0.elapsed_time(t1) / n_steps
+        return region, [region] * n_steps, clocks
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # with L2 flushes inside the region, a step's time is its launch's own
     step_ms = (sum(launch_ms) / len(launch_ms)) if flush_buf is not None else t0.elapsed_time(t1) / n_steps
@@ -359,7 +365,7 @@ def make_case(args, w, local_rank, stream):
         for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
                          (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
                          (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
-                         (csg.SYMM_OPT_NORM_PDL, args.norm_pdl)):
+                         (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain))):
             csg.symm_set_option(ws.h, opt, val)
         plan = csg.symm_gemv_plan(ws.h, N, K, B)
         for c in range(copies):
@@ -382,6 +388,7 @@ def make_case(args, w, local_rank, stream):
             "out_src": ws.y_ptr(), "out_bytes": out_rows * N * 2,
             "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
             "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
+                       "chain_option": bool(args.chain),
                        **({"eps": eps, "norm_pdl": args.norm_pdl} if kind == "gemv_rmsnorm" else {})},
         }
     if kind == "allreduce":
@@ -470,7 +477,21 @@ def run_ours(args, rank, world, local_rank):
     working_set = copies * per_copy
     flush = working_set < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id)
+    # Chaining applies to the persistent kernel (path 4); region timing is
+    # used only where no L2 flush sits between the launches.
+    chained = (args.chain and W is not None and flush_buf is None
+               and c["config"].get("plan", {}).get("path") == 4)
+    # Chained calls are timed over the region only: an event between two
+    # launches would separate them on the stream.
+    step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,
+                                            per_launch=not chained)
+    unchained = None
+    if chained:
+        # the same calls in plain stream order, each bracketed by events
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 0)
+        u_step, u_launch, _ = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 1)
+        unchained = (u_step, statistics.mean(u_launch), statistics.median(u_launch), _p10_p90(u_launch))
     code, _, _ = csg.symm_status(ws.h, stream)
     if code != csg.SYMM_OK:
         raise SystemExit(f"protocol error in the timed region: {csg.symm_last_error()}")
@@ -513,8 +534,9 @@ def run_ours(args, rank, world, local_rank):
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
 
-    step_ms, e2e_ms, ew_ms, mean_launch_ms = max_over_ranks(
-        [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms)], world, dev)
+    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms = max_over_ranks(
+        [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms),
+         unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0], world, dev)
     ws.close()
     if rank != 0:
         return None
@@ -558,6 +580,8 @@ def run_ours(args, rank, world, local_rank):
             "mean_launch_us": round(mean_launch_ms * 1e3, 3),
             "median_launch_us": round(statistics.median(launch_ms) * 1e3, 3),
             "p10_p90_launch_us": [round(q * 1e3, 3) for q in _p10_p90(launch_ms)],
+            "timing": ("chained calls: region time / steps (events around the region only)" if chained
+                       else "CUDA events around every launch on the launching stream"),
         },
         "clocks": clocks,
         "e2e": {
@@ -570,6 +594,15 @@ def run_ours(args, rank, world, local_rank):
         },
         "gpu_launches": args.steps * c["launches_per_step"],
     }
+    if unchained is not None:
+        line["unchained"] = {
+            "what": "the same calls in plain stream order (SYMM_OPT_CHAIN 0), events around every launch",
+            "us_per_call": round(u_step_ms * 1e3, 3), "mean_launch_us": round(u_launch_ms * 1e3, 3),
+            "median_launch_us": round(unchained[2] * 1e3, 3),
+            "p10_p90_launch_us": [round(q * 1e3, 3) for q in unchained[3]],
+            "achieved": round(nbytes / (u_launch_ms * 1e-3) / 1e9, 1),
+            "frac": round(nbytes / (u_launch_ms * 1e-3) / 1e9 / peak, 4),
+        }
     if ew is not None:
         line["e2e_weights_from_host"] = {
             "value": round(throughput_gbs(nbytes, ew_ms, world), 2), "unit": "GB/s",
@@ -716,6 +749,9 @@ def parse_args(argv=None):
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--ar-op", choices=("one_shot", "two_shot", "reduce_scatter"), default="one_shot",
                    help="allreduce workload: which collective one step calls")
+    p.add_argument("--no-chain", dest="chain", action="store_false",
+                   help="GEMV workloads: launch every call in plain stream order (SYMM_OPT_CHAIN 0) instead of "
+                        "as a programmatic dependent of the previous call (the library default)")
     p.add_argument("--norm-pdl", type=int, default=1, choices=(0, 1),
                    help="bias + RMSNorm form: launch the normalisation stage as a programmatic dependent")
     args = p.parse_args(argv)

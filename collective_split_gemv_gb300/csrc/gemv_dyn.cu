@@ -196,7 +196,10 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemvArgs a, const DynGeom geo) {
-    allow_dependent_launch(a);
+    // Dependents of this launch (the RMSNorm stage, or the next fused call
+    // when calls are chained) may be scheduled as CTAs of this one retire;
+    // they wait for this grid before touching anything it writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;
@@ -254,6 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = kEngine == 0 ? tmem_base_sh : 0u;
+    // Launched as a programmatic dependent of the previous fused call (calls
+    // chained on one stream), this grid may start while that one drains.
+    // Everything below except the producer's first W loads can depend on it
+    // (x, scratch, the pad, y), so every other thread waits for it here; the
+    // wait returns at once when the launch was not a programmatic dependent.
+    if (!(warp == 0 && lane == 0)) griddep_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
@@ -263,6 +272,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             // drawn: ticket k names unit G + k.
             uint32_t tk = blockIdx.x;
             bool ok = true;
+            // W of the first unit's first stages depends on nothing the
+            // previous call writes: its loads go out before the dependency
+            // wait, x's after it.
+            int pre = 0;
+            {
+                const int u = a.reverse_order ? U - 1 - (int)tk : (int)tk;
+                const int tr = u / S;
+                const int sp = u - tr * S;
+                const int t = tr / a.R;
+                const int r = tr - t * a.R;
+                const int kb0 = sp * KBs;
+                const int kb1 = min(kb0 + KBs, KB);
+                pre = min(kStages, kb1 - kb0);
+                for (int i = 0; i < pre; ++i) {   // the ring is empty: no wait
+                    const int kb = kb0 + i;
+                    stage_unit[i] = u;
+                    stage_flags[i] = (kb == kb0 ? 1 : 0) | (kb == kb1 - 1 ? 2 : 0);
+                    mbar_arrive_expect_tx(&full_bar[i], (uint32_t)kStageBytes);
+                    uint8_t *dst = smem + (size_t)i * kStageBytes;
+#pragma unroll
+                    for (int s = 0; s < kSlabs; ++s)
+                        tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[i], kb * kBK + s * 64, t * kM, r);
+                }
+                griddep_wait();
+                for (int i = 0; i < pre; ++i) {
+                    const int kb = kb0 + i;
+                    uint8_t *dst = smem + (size_t)i * kStageBytes;
+#pragma unroll
+                    for (int s = 0; s < kSlabs; ++s)
+                        tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[i], kb * kBK + s * 64, 0,
+                                    r);
+                }
+                issued = pre;
+            }
+            bool first = true;
             while (ok) {
                 const int st0 = issued % kStages;
                 const uint32_t ph0 = (uint32_t)(issued / kStages) & 1u;
@@ -292,8 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the atomic's latency hides behind the stages still in the
                 // ring.  The ticket -> unit arithmetic sits in an asm statement
                 // after the loop, so no instruction waits on the atomic early.
+                const int kb_from = first ? kb0 + pre : kb0;   // the first unit's first stages are out
+                first = false;
                 uint32_t next_raw = 0u;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                if (kb_from >= kb1) next_raw = atom_add_relaxed_gpu(geo.work, 1u);
+                for (int kb = kb_from; kb < kb1; ++kb) {
                     const int st = issued % kStages;
                     const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
                     if (!mbar_wait(&empty_bar[st], ph ^ 1u, &abort_sh)) {
@@ -535,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int kEngine, int kSlabs, int kB, int kCps>
-cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, cudaStream_t s) {
+cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, bool chained, cudaStream_t s) {
     auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps>;
     constexpr int smem = Ring<kSlabs, kCps>::kSmem;
     static bool attr = false;
@@ -544,20 +591,33 @@ cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap 
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);
-    return cudaGetLastError();
+    if (!chained) {
+        kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)geo.G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr1[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr1;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], a, geo);
 }
 
 template <int kEngine, int kB>
 cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, int slabs, int cps,
-                          cudaStream_t s) {
+                          bool chained, cudaStream_t s) {
     switch (cps * 10 + slabs) {
-        case 11: return launch_cfg<kEngine, 1, kB, 1>(a, geo, m, s);
-        case 12: return launch_cfg<kEngine, 2, kB, 1>(a, geo, m, s);
-        case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, s);
-        case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, s);
-        case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, s);
-        case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, s);
+        case 11: return launch_cfg<kEngine, 1, kB, 1>(a, geo, m, chained, s);
+        case 12: return launch_cfg<kEngine, 2, kB, 1>(a, geo, m, chained, s);
+        case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, chained, s);
+        case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, chained, s);
+        case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, chained, s);
+        case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, chained, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -565,11 +625,11 @@ cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorM
 }  // namespace
 
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,
-                            cudaStream_t s) {
+                            bool chained, cudaStream_t s) {
     const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
-    if (engine == 0) return launch_engine<0, 0>(a, geo, m, slabs, cps, s);
-    if (a.B == 1) return launch_engine<1, 1>(a, geo, m, slabs, cps, s);
-    if (a.B == 2) return launch_engine<1, 2>(a, geo, m, slabs, cps, s);
+    if (engine == 0) return launch_engine<0, 0>(a, geo, m, slabs, cps, chained, s);
+    if (a.B == 1) return launch_engine<1, 1>(a, geo, m, slabs, cps, chained, s);
+    if (a.B == 2) return launch_engine<1, 2>(a, geo, m, slabs, cps, chained, s);
     return cudaErrorInvalidValue;
 }
 

@@ -158,8 +158,10 @@ struct DynGeom {
     uint32_t *work;
 };
 constexpr size_t kPadWorkOffset = 64;   // byte offset of the work counter in slot 0's pad
+// chained: launch as a programmatic dependent of the previous kernel on the
+// stream (its CTAs may start while that one drains; see the kernel).
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,
-                            int ctas_per_sm, cudaStream_t s);
+                            int ctas_per_sm, bool chained, cudaStream_t s);
 
 int sk_block_k(int slabs);
 bool sk_config_supported(int slabs, int ctas_per_sm);

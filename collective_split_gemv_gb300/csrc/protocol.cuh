@@ -118,6 +118,10 @@ __device__ __forceinline__ void store_output(const GemvArgs &a, size_t e, float 
     }
 }
 
+// Waits until the grid this one was launched as a programmatic dependent of
+// has completed and its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // In a bias + RMSNorm call the normalisation kernel is launched as a
 // programmatic dependent of the GEMV; this lets its CTAs be scheduled while
 // the GEMV still runs (they wait for the whole GEMV grid, and its memory, at

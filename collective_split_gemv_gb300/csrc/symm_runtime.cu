@@ -48,6 +48,11 @@ struct symm_handle {
     int opt_sk_grid = 0;
     int opt_dyn_splits = 0;
     int opt_norm_pdl = 1;       // launch the RMSNorm stage as a programmatic dependent
+    int opt_chain = 1;          // launch the persistent kernel as a programmatic dependent
+    // y of the last persistent-kernel launch on the handle: a chained launch
+    // reads W before its predecessor has finished, so W must not overlap it.
+    const void *last_y = nullptr;
+    size_t last_y_bytes = 0;
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -481,7 +486,15 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             if (path == kPathTc) {
                 e = launch_gemv_tc(a, maps, s);
             } else if (path == kPathDyn) {
-                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, s);
+                const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_y, h->last_y_bytes);
+                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, chained, s);
+                if (ep.mode == kOutBiasZ) {
+                    h->last_y = nullptr;   // y is written by the norm stage, which its successor waits for
+                    h->last_y_bytes = 0;
+                } else {
+                    h->last_y = y;
+                    h->last_y_bytes = ybytes;
+                }
             } else {
                 a.partial_stride = (long long)B * N * 4;
                 e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
@@ -640,6 +653,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
         case SYMM_OPT_DYN_SPLITS:
             if (value < 0 || value > 16) return fail(SYMM_EINVAL, "persistent-kernel splits %d not in 0..16", value);
             h->opt_dyn_splits = value;
+            return SYMM_OK;
+        case SYMM_OPT_CHAIN:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "chain %d not in {0, 1}", value);
+            h->opt_chain = value;
             return SYMM_OK;
         case SYMM_OPT_NORM_PDL:
             if (value < 0 || value > 1) return fail(SYMM_EINVAL, "RMSNorm-stage PDL %d not in {0, 1}", value);

@@ -344,9 +344,19 @@ enum {
     SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: resident CTAs per SM, 0 auto (2), 1..3 (ring shrinks) */
     SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
     SYMM_OPT_DYN_SPLITS = 7,  /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
-    SYMM_OPT_NORM_PDL = 8     /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
+    SYMM_OPT_NORM_PDL = 8,    /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
                                  programmatic dependent of the GEMV so its launch overlaps the GEMV's
                                  tail; 0 plain stream order */
+    SYMM_OPT_CHAIN = 9        /* 1 (default): the persistent kernel (path 4) is launched as a programmatic
+                                 dependent of the previous kernel on the stream, so back-to-back fused calls
+                                 overlap one call's start-up with the previous call's end.  Only this
+                                 library's persistent kernel lets its successor start early, and a chained
+                                 call loads W for its first stages before that predecessor has finished;
+                                 x, y, scratch and the pad are touched only after it has finished.  A call
+                                 whose W overlaps the previous call's y on the same handle is launched in
+                                 plain stream order instead; W must not overlap the y of another handle's
+                                 call launched just before it (handles on overlapping memory).  0: plain
+                                 stream order always */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

@@ -114,6 +114,10 @@ __global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceAr
 // so in == out is safe for the two-shot layout (shift = 1).
 template <int RT, bool kVec>
 __global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const ReduceScatterArgs a) {
+    // As phase 1 of the two-shot all-reduce, let phase 2 (launched as a
+    // programmatic dependent; it waits for this grid before touching memory)
+    // be scheduled as this grid's CTAs retire.
+    if (a.shift) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int R = RT > 0 ? RT : a.R;
     const size_t step = (size_t)gridDim.x * kThreads;
     const size_t first = (size_t)blockIdx.x * kThreads + threadIdx.x;
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const ReduceSc
 // owner's values were stored by phase 1, an earlier launch on the stream.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) all_gather_blocks_kernel(const ReduceScatterArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // phase 1 has completed and is visible
     const size_t step = (size_t)gridDim.x * kThreads;
     const size_t first = (size_t)blockIdx.x * kThreads + threadIdx.x;
     if (kVec) {
@@ -215,9 +220,18 @@ cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
 cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s) {
     const bool vec = a.chunk % 8 == 0;
     const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n);
-    if (vec) all_gather_blocks_kernel<true><<<g, kThreads, 0, s>>>(a);
-    else all_gather_blocks_kernel<false><<<g, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    // A programmatic dependent of phase 1: its launch overlaps phase 1's end.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return vec ? cudaLaunchKernelEx(&cfg, all_gather_blocks_kernel<true>, a)
+               : cudaLaunchKernelEx(&cfg, all_gather_blocks_kernel<false>, a);
 }
 
 cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s) {

@@ -174,6 +174,10 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
 
 /*
  * symm_status -- synchronise `stream`, read the device status word, clear it.
+ * (The library's counterpart of a collective watchdog's error report: the
+ * "Bay.Area.AI: Tensor and 2D Parallelism" talk describes a watchdog that
+ * catches hung collectives and a desync report; here no kernel ever waits, so
+ * a protocol violation is recorded and reported instead of hanging.)
  *   code  out: SYMM_OK, or SYMM_EPROTO when a launch found a stale or missing
  *         tile flag or an out-of-range arrival ticket (e.g. two launches on
  *         the handle overlapped on different streams).

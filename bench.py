@@ -396,6 +396,7 @@ def make_case(args, w, local_rank, stream):
         inp = synth.allreduce_inputs(R, n, w["seed"])
         copies = _copies_for(inp.nbytes * 2)    # R inputs read + R outputs written, both rotated
         ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_AR_CTAS_PER_SM, args.ar_cps)
         for c in range(copies):
             ws.load_in(inp, copy=c)
         out_n = n // R if op == "reduce_scatter" else n
@@ -747,6 +748,8 @@ def parse_args(argv=None):
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
+    p.add_argument("--ar-cps", type=int, default=0,
+                   help="allreduce workload: grid cap in CTAs per SM (0 = library default)")
     p.add_argument("--ar-op", choices=("one_shot", "two_shot", "reduce_scatter"), default="one_shot",
                    help="allreduce workload: which collective one step calls")
     p.add_argument("--no-chain", dest="chain", action="store_false",

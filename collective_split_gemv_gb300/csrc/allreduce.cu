@@ -27,6 +27,11 @@ namespace symm {
 namespace {
 
 constexpr int kThreads = 256;
+// Grid cap per SM.  Twice the 8 CTAs an SM holds at once: the hardware then
+// starts a fresh CTA wherever one retires, which measured faster (R=8, 8 MiB
+// per rank: one-shot 26.7 -> 25.6 us, two-shot 29.0 -> 27.3 us) than eight
+// resident CTAs walking a grid-stride loop of uneven length.
+constexpr int kDefaultCtasPerSm = 16;
 
 __device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v) {
     acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x);
@@ -188,12 +193,12 @@ __global__ void __launch_bounds__(kThreads) all_gather_blocks_kernel(const Reduc
     }
 }
 
-unsigned grid_for(size_t work_items) {
+unsigned grid_for(size_t work_items, int ctas_per_sm) {
     int sms = 152;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     size_t blocks = (work_items + kThreads - 1) / kThreads;
-    const size_t cap = (size_t)sms * 8;
+    const size_t cap = (size_t)sms * (size_t)(ctas_per_sm > 0 ? ctas_per_sm : kDefaultCtasPerSm);
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     return (unsigned)blocks;
@@ -203,7 +208,7 @@ unsigned grid_for(size_t work_items) {
 
 cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
     const bool vec = a.chunk % 8 == 0;
-    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n);
+    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n, a.ctas_per_sm);
     if (vec) {
         switch (a.R) {
             case 2: reduce_scatter_kernel<2, true><<<g, kThreads, 0, s>>>(a); break;
@@ -219,7 +224,7 @@ cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
 
 cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s) {
     const bool vec = a.chunk % 8 == 0;
-    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n);
+    const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n, a.ctas_per_sm);
     // A programmatic dependent of phase 1: its launch overlaps phase 1's end.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g, 1, 1);
@@ -240,10 +245,10 @@ cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s) {
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // Enough CTAs for one vector per thread, capped at 8 resident CTAs per SM
+    // Enough CTAs for one vector per thread, capped at ctas_per_sm per SM
     // (grid-stride beyond that); at least one CTA for the ragged tail.
     size_t blocks = (nvec + kThreads - 1) / kThreads;
-    const size_t cap = (size_t)sms * 8;
+    const size_t cap = (size_t)sms * (size_t)(a.ctas_per_sm > 0 ? a.ctas_per_sm : kDefaultCtasPerSm);
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     switch (a.R) {

@@ -67,6 +67,7 @@ struct AllReduceArgs {
     long long stride;
     int R;
     size_t n;
+    int ctas_per_sm;         // grid cap per SM (grid-stride beyond it); 0 = the default
 };
 
 // Kernel launchers; return the launch's cudaError_t.
@@ -85,6 +86,7 @@ struct ReduceScatterArgs {
     size_t n;
     size_t chunk;            // elements per owner
     int shift;
+    int ctas_per_sm;         // grid cap per SM; 0 = the default
 };
 cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s);
 // Phase 2 of the two-shot all-reduce: out_q[i] = out_owner(i)[i] for q != owner.

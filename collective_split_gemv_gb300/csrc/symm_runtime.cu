@@ -49,6 +49,7 @@ struct symm_handle {
     int opt_dyn_splits = 0;
     int opt_norm_pdl = 1;       // launch the RMSNorm stage as a programmatic dependent
     int opt_chain = 1;          // launch the persistent kernel as a programmatic dependent
+    int opt_ar_cps = 0;         // all-reduce / reduce-scatter grid cap per SM (0 = the kernels' default)
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     const void *last_y = nullptr;
@@ -654,6 +655,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 16) return fail(SYMM_EINVAL, "persistent-kernel splits %d not in 0..16", value);
             h->opt_dyn_splits = value;
             return SYMM_OK;
+        case SYMM_OPT_AR_CTAS_PER_SM:
+            if (value < 0 || value > 64) return fail(SYMM_EINVAL, "all-reduce CTAs per SM %d not in 0..64", value);
+            h->opt_ar_cps = value;
+            return SYMM_OK;
         case SYMM_OPT_CHAIN:
             if (value < 0 || value > 1) return fail(SYMM_EINVAL, "chain %d not in {0, 1}", value);
             h->opt_chain = value;
@@ -709,6 +714,7 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.stride = (long long)h->stride;
     a.R = h->R;
     a.n = n;
+    a.ctas_per_sm = h->opt_ar_cps;
     cudaError_t e = launch_one_shot_all_reduce(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "one_shot_all_reduce launch");
     return SYMM_OK;
@@ -758,6 +764,7 @@ int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n,
     a.n = n;
     a.chunk = n / (size_t)R;
     a.shift = 0;
+    a.ctas_per_sm = h->opt_ar_cps;
     cudaError_t e = launch_reduce_scatter(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
     return SYMM_OK;
@@ -786,6 +793,7 @@ int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.n = n;
     a.chunk = (per + 7) / 8 * 8;
     a.shift = 1;
+    a.ctas_per_sm = h->opt_ar_cps;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_reduce_scatter(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "two_shot_all_reduce reduce-scatter launch");

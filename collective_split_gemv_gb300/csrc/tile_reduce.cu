@@ -95,8 +95,9 @@ cudaError_t launch_tile_reduce(const TileReduceArgs &a, cudaStream_t s) {
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long items = (long long)a.rows * (vec ? a.cols / 8 : a.cols);
     long long bx = (items + kThreads - 1) / kThreads;
-    // about 8 resident CTAs per SM over all tiles together, grid-stride beyond
-    const long long cap = std::max<long long>(1, (long long)sms * 8 / a.ntiles);
+    // up to 16 CTAs per SM over all tiles together (eight resident at a time;
+    // the hardware starts a fresh CTA wherever one retires), grid-stride beyond
+    const long long cap = std::max<long long>(1, (long long)sms * 16 / a.ntiles);
     if (bx > cap) bx = cap;
     if (bx < 1) bx = 1;
     const dim3 grid((unsigned)bx, (unsigned)a.ntiles);

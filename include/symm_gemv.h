@@ -351,7 +351,7 @@ enum {
     SYMM_OPT_NORM_PDL = 8,    /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
                                  programmatic dependent of the GEMV so its launch overlaps the GEMV's
                                  tail; 0 plain stream order */
-    SYMM_OPT_CHAIN = 9        /* 1 (default): the persistent kernel (path 4) is launched as a programmatic
+    SYMM_OPT_CHAIN = 9,       /* 1 (default): the persistent kernel (path 4) is launched as a programmatic
                                  dependent of the previous kernel on the stream, so back-to-back fused calls
                                  overlap one call's start-up with the previous call's end.  Only this
                                  library's persistent kernel lets its successor start early, and a chained
@@ -361,6 +361,8 @@ enum {
                                  plain stream order instead; W must not overlap the y of another handle's
                                  call launched just before it (handles on overlapping memory).  0: plain
                                  stream order always */
+    SYMM_OPT_AR_CTAS_PER_SM = 10 /* one_shot_all_reduce, two_shot_all_reduce, reduce_scatter: grid cap in CTAs
+                                 (256 threads) per SM, grid-stride beyond it; 0 auto (16) */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

@@ -585,11 +585,16 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, bool chained, cudaStream_t s) {
     auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps>;
     constexpr int smem = Ring<kSlabs, kCps>::kSmem;
-    static bool attr = false;
-    if (!attr) {
+    // The shared-memory attribute is per device: set it once for each device
+    // a launch happens on (devices past 63 set it every time).
+    static unsigned long long attr_devices = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit == 0 || !(attr_devices & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr_devices |= bit;
     }
     if (!chained) {
         kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);

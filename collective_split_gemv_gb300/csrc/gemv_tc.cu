@@ -230,12 +230,17 @@ int tc_encode_maps(const GemvArgs &a, void *maps) {
 cudaError_t launch_gemv_tc(const GemvArgs &a, const void *maps, cudaStream_t s) {
     const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
     const size_t smem = tc_smem_bytes();
-    static bool attr_set = false;
-    if (!attr_set) {
+    // The shared-memory attribute is per device: set it once for each device
+    // a launch happens on (devices past 63 set it every time).
+    static unsigned long long attr_devices = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit == 0 || !(attr_devices & bit)) {
         cudaError_t e = cudaFuncSetAttribute(gemv_ar_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_devices |= bit;
     }
     const int kb_total = (a.Kr + kBK - 1) / kBK;
     const int kb_per_split = (kb_total + a.splits - 1) / a.splits;

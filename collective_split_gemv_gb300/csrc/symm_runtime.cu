@@ -837,6 +837,7 @@ int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, 
     a.wait_prior = 0;
     cudaError_t e = launch_rmsnorm_rows(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "all_reduce_bias_rmsnorm launch");
+
     return SYMM_OK;
 }
 

@@ -141,3 +141,37 @@ def _weights_from_previous_output(chain: int):
 
 def test_weights_that_are_the_previous_output_are_not_read_early():
     assert np.array_equal(_weights_from_previous_output(1), _weights_from_previous_output(0))
+
+
+def _rmsnorm_chain(chain: int, steps: int = 8):
+    """R = 1, N = K: fused calls with the bias + RMSNorm epilogue, each
+    reading the previous call's normalised output as x; the norm kernel lets
+    the next fused call start early."""
+    N = K = 2048
+    B = 2
+    W, x = synth.gemv_inputs(1, N, K, B, seed=29, w_std=1.0 / np.sqrt(K), x="normal")
+    bias, gamma = synth.norm_vectors(N, 29)
+    ws = GemvWorkspace(1, N, K, B, copies=2)
+    try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, chain)
+        ws.load_W(W)
+        ws.load_vectors(bias, gamma)
+        vbytes = B * N * 2
+        vstep = (vbytes + 255) // 256 * 256
+        base = ws.W_ptr(1)
+        ws.view(0, ws.w_off[1], vbytes).copy_(torch.from_numpy(np.ascontiguousarray(x[0])).view(torch.uint8).reshape(-1))
+        s = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            csg.gemv_all_reduce_bias_rmsnorm(ws.h, ws.W_ptr(0), base + i * vstep, ws.base + ws.bias_off,
+                                             ws.base + ws.gamma_off, base + (i + 1) * vstep, 1, N, K, B, 1e-6, s)
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        region = ws.view(0, ws.w_off[1], (steps + 1) * vstep).cpu().numpy()
+        return np.stack([region[(i + 1) * vstep:(i + 1) * vstep + vbytes].view(np.uint16) for i in range(steps)])
+    finally:
+        ws.close()
+
+
+def test_rmsnorm_chain_matches_plain_stream_order():
+    assert np.array_equal(_rmsnorm_chain(1), _rmsnorm_chain(0))

@@ -738,7 +738,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk", "dyn"), default="auto",
                    help="force one kernel (measurement only)")
-    p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 4),
+    p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 3, 4),
                    help="TMA kernels: slabs per pipeline stage (0 = library default)")
     p.add_argument("--sk-cps", type=int, default=0, choices=(0, 1, 2, 3),
                    help="TMA kernels: resident CTAs per SM (0 = library default)")

@@ -622,6 +622,7 @@ cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorM
         case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, chained, s);
         case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, chained, s);
         case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, chained, s);
+        case 23: return launch_cfg<kEngine, 3, kB, 2>(a, geo, m, chained, s);
         case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, chained, s);
         default: return cudaErrorInvalidValue;
     }

@@ -442,7 +442,7 @@ int sk_block_k(int slabs) { return 64 * slabs; }
 // at least two stages.
 bool sk_config_supported(int slabs, int cps) {
     return (cps == 1 && (slabs == 1 || slabs == 2 || slabs == 4)) ||
-           (cps == 2 && (slabs == 1 || slabs == 2)) || (cps == 3 && slabs == 1);
+           (cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3)) || (cps == 3 && slabs == 1);
 }
 
 template <int kEngine, int kB>
@@ -454,6 +454,7 @@ cudaError_t launch_engine(const GemvArgs &a, const SkGeom &geo, const CUtensorMa
         case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, s);
         case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, s);
         case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, s);
+        case 23: return launch_cfg<kEngine, 3, kB, 2>(a, geo, m, s);
         case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, s);
         default: return cudaErrorInvalidValue;
     }

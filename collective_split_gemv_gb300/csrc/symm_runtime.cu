@@ -639,8 +639,8 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             h->opt_tile_order = value;
             return SYMM_OK;
         case SYMM_OPT_SK_SLABS:
-            if (value != 0 && value != 1 && value != 2 && value != 4)
-                return fail(SYMM_EINVAL, "stream-K slabs %d not in {0 auto, 1, 2, 4}", value);
+            if (value < 0 || value > 4)
+                return fail(SYMM_EINVAL, "stream-K slabs %d not in {0 auto, 1, 2, 3, 4}", value);
             h->opt_sk_slabs = value;
             return SYMM_OK;
         case SYMM_OPT_SK_ENGINE:

@@ -330,7 +330,7 @@ def test_many_launches_keep_tickets_consistent(path):
 
 # ------------------------------------------------------ stream-K variants
 
-SK_PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (1, 3)]   # (slabs, CTAs per SM)
+SK_PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (3, 2), (1, 3)]   # (slabs, CTAs per SM)
 SK_VARIANTS = [(engine, slabs, cps) for engine in (0, 1) for slabs, cps in SK_PIPES]
 SK_SHAPES = [(8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1), (3, 513, 3 * 4096, 2),
              (8, 2048, 8 * 512, 1)]

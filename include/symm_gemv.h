@@ -50,6 +50,11 @@
  *  - Device memory ownership: the library owns what symm_alloc allocates
  *    (backing == NULL) and frees it in symm_free; borrowed backing memory
  *    stays the caller's and must outlive the handle.
+ *  - CUDA graphs: the fused calls (gemv_*) pass the handle's launch epoch,
+ *    a host-side counter, to their kernel, so a captured call replayed
+ *    later would reuse a stale epoch; the protocol then reports SYMM_EPROTO
+ *    (symm_status) instead of writing y.  Issue them eagerly on a stream.
+ *    The other collectives keep no state between calls.
  */
 #ifndef SYMM_GEMV_H
 #define SYMM_GEMV_H

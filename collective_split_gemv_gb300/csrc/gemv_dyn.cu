@@ -17,11 +17,11 @@
 // drawn close together.  S > 1 only serves to make units small enough that
 // drawing them balances the SMs.
 //
-// Work counter: slot 0's signal pad holds one u32 that only grows.  CTA c
-// starts with unit c (G <= U) and then draws: launch `epoch` owns tickets
-// (epoch-1)*U .. epoch*U-1, ticket k naming unit G + k; U - G tickets name
-// units and each of the G CTAs draws exactly one ticket past the end, which
-// tells it to stop.  The host resets the pad when the geometry changes.
+// Work counter: slot 0's signal pad holds two; launch e draws from
+// work[e & 1], which starts at zero (the previous launch's last tile reducer
+// cleared it).  CTA c starts with unit c (G <= U) and then draws: ticket k
+// names unit G + k; U - G tickets name units and each of the G CTAs draws
+// exactly one ticket past the end, which tells it to stop.
 //
 // Roles (192 threads):
 //   warp 0, lane 0  draws units, issues the TMA loads of each unit's K blocks
@@ -103,81 +103,83 @@ __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v
 // Steps 2-4 of the protocol for contributor (r, s) of tile t (C = R * S
 // contributors: every rank's K range in S splits), run by the 128 threads of
 // warps 2-5 (gt = 0..127).  The caller has stored its partial.
-__device__ __forceinline__ void publish_reduce_unit(const GemvArgs &a, int S, int t, int r, int s, int gt,
-                                                    int *s_last, int *s_bad) {
+__device__ __forceinline__ void publish_reduce_unit(const GemvArgs &a, uint32_t epoch, int S, int t, int r, int s,
+                                                    int gt, int *s_last, int *s_bad) {
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;
+    uint32_t done = 0;   // gt == 0, reducer: tiles counted before this one
     __threadfence();
     named_barrier(kGroupBarrier, kGroupThreads);
     if (gt == 0) {
         uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
                                                       (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, a.epoch);
-        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
-        const uint32_t pos = ticket - (a.epoch - 1u) * C;
-        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
-        *s_last = (pos == C - 1u);
+        st_release_gpu(flag, epoch);
+        *s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
         *s_bad = 0;
     }
     named_barrier(kGroupBarrier, kGroupThreads);
     if (!*s_last) return;
-    __threadfence();
+    // The acquire loads of the flags (and the barrier after them) order the
+    // partial loads of the reduction after every contributor's stores.
     for (int i = gt; i < (int)C; i += kGroupThreads) {
         const int q = i / S;
         const int qs = i - q * S;
         const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
                                                                (long long)q * a.stride) + (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != a.epoch) {
-            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
+        if (ld_acquire_gpu(f) != epoch) {
+            latch_status(a.status, kProtoStaleFlag, q, t, epoch);
             *s_bad = 1;
         }
     }
     named_barrier(kGroupBarrier, kGroupThreads);
-    if (*s_bad) return;
-    // Contributors in order: rank 0..R-1, split 0..S-1.
-    reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
-                [&](int j) {
-                    const int q = j / S;
-                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                },
-                gt, kGroupThreads);
+    if (gt == 0) finish_launch_if_last(a, done, epoch, t);
+    if (!*s_bad) {
+        // Contributors in order: rank 0..R-1, split 0..S-1.
+        reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
+                    [&](int j) {
+                        const int q = j / S;
+                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                    },
+                    gt, kGroupThreads);
+    }
 }
 
 // The same protocol run by one warp (the FFMA engine's epilogue warp).
-__device__ __forceinline__ void publish_reduce_warp(const GemvArgs &a, int S, int t, int r, int s, int lane) {
+__device__ __forceinline__ void publish_reduce_warp(const GemvArgs &a, uint32_t epoch, int S, int t, int r, int s,
+                                                    int lane) {
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;
+    uint32_t done = 0;   // lane 0, reducer: tiles counted before this one
     __threadfence();
     __syncwarp();
     uint32_t last = 0;
     if (lane == 0) {
         uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
                                                       (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, a.epoch);
-        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
-        const uint32_t pos = ticket - (a.epoch - 1u) * C;
-        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
-        last = pos == C - 1u;
+        st_release_gpu(flag, epoch);
+        last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    __threadfence();
-    bool bad = false;
+    bool bad = false;   // acquire loads of the flags, then the partials (see above)
     for (int i = lane; i < (int)C; i += 32) {
         const int q = i / S;
         const int qs = i - q * S;
         const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
                                                                (long long)q * a.stride) + (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != a.epoch) {
-            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
+        if (ld_acquire_gpu(f) != epoch) {
+            latch_status(a.status, kProtoStaleFlag, q, t, epoch);
             bad = true;
         }
     }
-    if (__any_sync(0xffffffffu, bad)) return;
-    reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
-                [&](int j) {
-                    const int q = j / S;
-                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                },
-                lane, 32);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) finish_launch_if_last(a, done, epoch, t);
+    if (!bad) {
+        reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
+                    [&](int j) {
+                        const int q = j / S;
+                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                    },
+                    lane, 32);
+    }
 }
 
 __device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     __shared__ int s_last, s_bad;
+    __shared__ uint32_t epoch_sh;
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5;
@@ -228,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = geo.splits;
     const int KBs = geo.KBs;            // K blocks per split (the last split may have fewer)
     const int KB = geo.KB;
-    const uint32_t base_ticket = (a.epoch - 1u) * (uint32_t)U;
 
     if (threadIdx.x == 0) {
         // The descriptors' fetch overlaps the set-up below (the first TMA
@@ -262,50 +264,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Everything below except the producer's first W loads can depend on it
     // (x, scratch, the pad, y), so every other thread waits for it here; the
     // wait returns at once when the launch was not a programmatic dependent.
-    if (!(warp == 0 && lane == 0)) griddep_wait();
+    int pre = 0;   // producer: stages of the first unit issued here
+    if (warp == 0 && lane == 0) {
+        // W of the first unit's first stages depends on nothing the previous
+        // call writes: its loads go out before the dependency wait, x's
+        // after it.  The first unit is the CTA's own index (G <= U).
+        const int u = a.reverse_order ? U - 1 - (int)blockIdx.x : (int)blockIdx.x;
+        const int tr = u / S;
+        const int sp = u - tr * S;
+        const int t = tr / a.R;
+        const int r = tr - t * a.R;
+        const int kb0 = sp * KBs;
+        const int kb1 = min(kb0 + KBs, KB);
+        pre = min(kStages, kb1 - kb0);
+        for (int i = 0; i < pre; ++i) {   // the ring is empty: no wait
+            const int kb = kb0 + i;
+            stage_unit[i] = u;
+            stage_flags[i] = (kb == kb0 ? 1 : 0) | (kb == kb1 - 1 ? 2 : 0);
+            mbar_arrive_expect_tx(&full_bar[i], (uint32_t)kStageBytes);
+            uint8_t *dst = smem + (size_t)i * kStageBytes;
+#pragma unroll
+            for (int s = 0; s < kSlabs; ++s)
+                tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[i], kb * kBK + s * 64, t * kM, r);
+        }
+        griddep_wait();
+        for (int i = 0; i < pre; ++i) {
+            const int kb = kb0 + i;
+            uint8_t *dst = smem + (size_t)i * kStageBytes;
+#pragma unroll
+            for (int s = 0; s < kSlabs; ++s)
+                tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[i], kb * kBK + s * 64, 0, r);
+        }
+        // Step 0 of the protocol: the launch epoch, read once per CTA and
+        // shared through the barrier below (which orders the read before
+        // every publish of this CTA).  Its latency overlaps the loads above.
+        epoch_sh = read_launch_epoch(a);
+    } else {
+        griddep_wait();
+    }
+    __syncthreads();
+    const uint32_t epoch = epoch_sh;
+    uint32_t *const work = a.work + (epoch & 1u);
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int issued = 0;
-            // The first unit is the CTA's own index (G <= U); later ones are
-            // drawn: ticket k names unit G + k.
+            int issued = pre;
+            // Later units are drawn: ticket k names unit G + k.
             uint32_t tk = blockIdx.x;
             bool ok = true;
-            // W of the first unit's first stages depends on nothing the
-            // previous call writes: its loads go out before the dependency
-            // wait, x's after it.
-            int pre = 0;
-            {
-                const int u = a.reverse_order ? U - 1 - (int)tk : (int)tk;
-                const int tr = u / S;
-                const int sp = u - tr * S;
-                const int t = tr / a.R;
-                const int r = tr - t * a.R;
-                const int kb0 = sp * KBs;
-                const int kb1 = min(kb0 + KBs, KB);
-                pre = min(kStages, kb1 - kb0);
-                for (int i = 0; i < pre; ++i) {   // the ring is empty: no wait
-                    const int kb = kb0 + i;
-                    stage_unit[i] = u;
-                    stage_flags[i] = (kb == kb0 ? 1 : 0) | (kb == kb1 - 1 ? 2 : 0);
-                    mbar_arrive_expect_tx(&full_bar[i], (uint32_t)kStageBytes);
-                    uint8_t *dst = smem + (size_t)i * kStageBytes;
-#pragma unroll
-                    for (int s = 0; s < kSlabs; ++s)
-                        tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[i], kb * kBK + s * 64, t * kM, r);
-                }
-                griddep_wait();
-                for (int i = 0; i < pre; ++i) {
-                    const int kb = kb0 + i;
-                    uint8_t *dst = smem + (size_t)i * kStageBytes;
-#pragma unroll
-                    for (int s = 0; s < kSlabs; ++s)
-                        tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[i], kb * kBK + s * 64, 0,
-                                    r);
-                }
-                issued = pre;
-            }
             bool first = true;
             while (ok) {
                 const int st0 = issued % kStages;
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb_from = first ? kb0 + pre : kb0;   // the first unit's first stages are out
                 first = false;
                 uint32_t next_raw = 0u;
-                if (kb_from >= kb1) next_raw = atom_add_relaxed_gpu(geo.work, 1u);
+                if (kb_from >= kb1) next_raw = atom_add_relaxed_gpu(work, 1u);
                 for (int kb = kb_from; kb < kb1; ++kb) {
                     const int st = issued % kStages;
                     const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
@@ -358,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int s = 0; s < kSlabs; ++s)
                         tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0,
                                     r);
-                    if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(geo.work, 1u);
+                    if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(work, 1u);
                     ++issued;
                 }
-                asm volatile("sub.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"(base_ticket - (uint32_t)geo.G));
+                asm volatile("add.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"((uint32_t)geo.G));
             }
             if (!ok) {
-                latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                latch_status(a.status, kProtoTimeout, -1, -1, epoch);
                 abort_sh = 1;
                 volatile int never = 0;
                 for (int j = max(0, issued - kStages); j < issued; ++j)
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) {
-                    latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                    latch_status(a.status, kProtoTimeout, -1, -1, epoch);
                     abort_sh = 1;
                 }
                 tc_commit(&drain_bar);
@@ -455,11 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[j]);
-                publish_reduce_warp(a, S, t, r, sp, lane);
+                publish_reduce_warp(a, epoch, S, t, r, sp, lane);
                 ++seg;
             }
             if (!ok) {
-                latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                latch_status(a.status, kProtoTimeout, -1, -1, epoch);
                 abort_sh = 1;
             }
         }
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int b = 0; b < kNmma; ++b)
                         if (b < a.B) P[(size_t)b * a.N + n] = v[b];
                 }
-                publish_reduce_unit(a, S, t, r, sp, gt, &s_last, &s_bad);
+                publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last, &s_bad);
                 ++seg;
             }
         } else {
@@ -568,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) {
-            latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+            latch_status(a.status, kProtoTimeout, -1, -1, epoch);
             abort_sh = 1;
         }
     }

@@ -55,6 +55,8 @@ __device__ __forceinline__ float dot8(const uint4 &w, const float4 &lo, const fl
 template <int B>
 __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a) {
     allow_dependent_launch(a);
+    // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
+    const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
     constexpr int G = FfmaShape<B>::G;
     constexpr int U = FfmaShape<B>::U;
     extern __shared__ float4 xs4[];   // [B][2][kc_cap]
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a
         for (int b = 0; b < B; ++b)
             if (rowok[g] && lane == ((g * B + b) & 31)) P[(size_t)b * a.N + row0 + g] = acc[g][b];
 
-    publish_and_reduce(a, t, r, 0);
+    publish_and_reduce(a, epoch, t, r, 0);
 }
 
 template <int B>

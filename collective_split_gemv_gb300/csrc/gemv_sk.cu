@@ -95,48 +95,11 @@ __device__ __forceinline__ int parts_of_unit(long long u, const SkGeom &geo) {
     return cta_of_block((u + 1) * geo.KB - 1, geo.total, geo.G) - cta_of_block(u * geo.KB, geo.total, geo.G) + 1;
 }
 
-// Steps 2-4 of the protocol for one part (r, p) of tile t, run by the 128
-// threads of warps 2-5 (gt = 0..127).  The caller has stored its partial.
-__device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeom &geo, int t, int r, int p,
-                                                  int gt, int *s_last, int *s_bad, int *s_parts) {
-    __threadfence();
-    named_barrier(kGroupBarrier, kGroupThreads);
-    if (gt == 0) {
-        int C = 0;
-        for (int q = 0; q < a.R; ++q) {
-            const int P = parts_of_unit((long long)t * a.R + q, geo);
-            s_parts[q] = P;
-            C += P;
-        }
-        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
-                                                      (long long)r * a.stride) + (size_t)t * geo.Pmax + p;
-        st_release_gpu(flag, a.epoch);
-        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
-        const uint32_t pos = ticket - (a.epoch - 1u) * (uint32_t)C;
-        if (pos >= (uint32_t)C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
-        *s_last = (pos == (uint32_t)C - 1u);
-        *s_bad = 0;
-    }
-    named_barrier(kGroupBarrier, kGroupThreads);
-    if (!*s_last) return;
-    __threadfence();
-    for (int i = gt; i < a.R * geo.Pmax; i += kGroupThreads) {
-        const int q = i / geo.Pmax;
-        const int qp = i - q * geo.Pmax;
-        if (qp < s_parts[q]) {
-            const uint32_t *f = reinterpret_cast<const uint32_t *>(
-                                    reinterpret_cast<const uint8_t *>(a.flags) + (long long)q * a.stride) +
-                                (size_t)t * geo.Pmax + qp;
-            if (ld_acquire_gpu(f) != a.epoch) {
-                latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
-                *s_bad = 1;
-            }
-        }
-    }
-    named_barrier(kGroupBarrier, kGroupThreads);
-    if (*s_bad) return;
+// The reduction of tile t by its last contributor (flags acquired): the
+// tile's parts in fixed order, run by the 128 threads of warps 2-5.
+__device__ __forceinline__ void sk_reduce_tile(const GemvArgs &a, int t, int gt, const int *s_parts) {
     // Partials of the tile in fixed order (rank, then part): plain L2 loads
-    // after the acquire above.  Each thread owns up to kPer outputs and loads
+    // after the reducer's acquire of the flags.  Each thread owns up to kPer outputs and loads
     // all of them for one contributor before adding, so one L2 round trip
     // serves kPer outputs; contributions are added strictly in order.
     const int n0 = t * kM;
@@ -168,6 +131,52 @@ __device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeo
         for (int k = 0; k < kPer; ++k)
             if (i0 + k * kGroupThreads < count) store_output(a, off[k] / sizeof(float), acc[k]);
     }
+}
+
+// Steps 2-4 of the protocol for one part (r, p) of tile t, run by the 128
+// threads of warps 2-5 (gt = 0..127).  The caller has stored its partial;
+// `epoch` (step 0) is needed in gt == 0 only, which publishes.
+__device__ __forceinline__ void sk_publish_reduce(const GemvArgs &a, const SkGeom &geo, uint32_t epoch, int t,
+                                                  int r, int p, int gt, int *s_last, int *s_bad, int *s_parts,
+                                                  uint32_t *s_epoch) {
+    uint32_t done = 0;   // gt == 0, reducer: tiles counted before this one
+    __threadfence();
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (gt == 0) {
+        int C = 0;
+        for (int q = 0; q < a.R; ++q) {
+            const int P = parts_of_unit((long long)t * a.R + q, geo);
+            s_parts[q] = P;
+            C += P;
+        }
+        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
+                                                      (long long)r * a.stride) + (size_t)t * geo.Pmax + p;
+        st_release_gpu(flag, epoch);
+        *s_last = take_ticket(a, t, (uint32_t)C, r, epoch, &done) == (uint32_t)C - 1u;
+        *s_bad = 0;
+        *s_epoch = epoch;
+    }
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (!*s_last) return;
+    const uint32_t e = *s_epoch;
+    // The acquire loads of the flags (and the barrier after them) order the
+    // partial loads of the reduction after every contributor's stores.
+    for (int i = gt; i < a.R * geo.Pmax; i += kGroupThreads) {
+        const int q = i / geo.Pmax;
+        const int qp = i - q * geo.Pmax;
+        if (qp < s_parts[q]) {
+            const uint32_t *f = reinterpret_cast<const uint32_t *>(
+                                    reinterpret_cast<const uint8_t *>(a.flags) + (long long)q * a.stride) +
+                                (size_t)t * geo.Pmax + qp;
+            if (ld_acquire_gpu(f) != e) {
+                latch_status(a.status, kProtoStaleFlag, q, t, e);
+                *s_bad = 1;
+            }
+        }
+    }
+    named_barrier(kGroupBarrier, kGroupThreads);
+    if (gt == 0) finish_launch_if_last(a, done, e, t);
+    if (!*s_bad) sk_reduce_tile(a, t, gt, s_parts);
 }
 
 // 8 bf16 of W (one 16-byte chunk) times 8 bf16 of x, fp32, ascending order.
@@ -204,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     __shared__ int s_last, s_bad;
+    __shared__ uint32_t s_epoch;
     __shared__ int s_parts[kMaxRanks];
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = issued % kStages;
                 const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
                 if (!mbar_wait(&empty_bar[st], ph ^ 1u, &abort_sh)) {
-                    latch_status(a.status, kProtoTimeout, r, t, a.epoch);
+                    latch_status(a.status, kProtoTimeout, r, t, read_launch_epoch(a));
                     abort_sh = 1;
                     break;
                 }
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++seg;
             }
             if (!ok) {
-                latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+                latch_status(a.status, kProtoTimeout, -1, -1, read_launch_epoch(a));
                 abort_sh = 1;
             }
             // Every MMA issued by this thread has finished once this commit arrives.
@@ -332,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         const int gt = threadIdx.x - 64;
+        // gt == 0 publishes; its read of the launch epoch overlaps the streaming.
+        const uint32_t epoch = gt == 0 ? read_launch_epoch(a) : 0u;
         int i = 0, seg = 0;
         long long g = beg;
         while (g < end) {
@@ -398,11 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < (kEngine == 0 ? kNmma : kB); ++b)
                     if (b < a.B) P[(size_t)b * a.N + n] = v[b];
             }
-            sk_publish_reduce(a, geo, t, r, p, gt, &s_last, &s_bad, s_parts);
+            sk_publish_reduce(a, geo, epoch, t, r, p, gt, &s_last, &s_bad, s_parts, &s_epoch);
             ++seg;
         }
         if (g < end) {
-            latch_status(a.status, kProtoTimeout, -1, -1, a.epoch);
+            latch_status(a.status, kProtoTimeout, -1, -1, read_launch_epoch(a));
             abort_sh = 1;
         }
     }

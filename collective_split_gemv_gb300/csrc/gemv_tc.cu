@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, int kb_total, int kb_per_split) {
     allow_dependent_launch(a);
+    // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
+    const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = i % kStages;
                 const uint32_t ph = (uint32_t)(i / kStages) & 1u;
                 if (!mbar_wait(&empty_bar[st], ph ^ 1u, &abort_sh)) {
-                    latch_status(a.status, kProtoTimeout, r, t, a.epoch);
+                    latch_status(a.status, kProtoTimeout, r, t, read_launch_epoch(a));
                     abort_sh = 1;
                     break;
                 }
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = i % kStages;
                 const uint32_t ph = (uint32_t)(i / kStages) & 1u;
                 if (!mbar_wait(&full_bar[st], ph, &abort_sh)) {
-                    latch_status(a.status, kProtoTimeout, r, t, a.epoch);
+                    latch_status(a.status, kProtoTimeout, r, t, read_launch_epoch(a));
                     abort_sh = 1;
                     break;
                 }
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkb > 0) {
             ok = mbar_wait_sleepy(&accum_bar, 0, &abort_sh);
             if (!ok) {
-                latch_status(a.status, kProtoTimeout, r, t, a.epoch);
+                latch_status(a.status, kProtoTimeout, r, t, read_launch_epoch(a));
                 abort_sh = 1;
             }
             __syncwarp();
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
     if (abort_sh) return;
-    publish_and_reduce(a, t, r, s);
+    publish_and_reduce(a, epoch, t, r, s);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,

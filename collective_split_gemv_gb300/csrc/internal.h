@@ -9,10 +9,23 @@
 namespace symm {
 
 // Signal-pad layout of every slot (byte offsets from the pad start):
-//   [0, 128)                status words {code, rank, tile, epoch} (slot 0 only)
+//   [0, 16)                 status words {code, rank, tile, epoch} (slot 0 only)
+//   [64, 72)                work[2]      work counters of the persistent kernel,
+//                                        launch e uses work[e & 1] (slot 0 only)
+//   [96, 100)               epoch        epoch of the last finished fused launch
+//                                        (slot 0 only)
+//   [112, 116)              tiles_done   tiles of the running launch that have
+//                                        been reduced (slot 0 only)
 //   [128, 128 + 4*T)        flags[T]     tile t of rank r published (epoch)
 //   [cnt_off, cnt_off+4*T)  counters[T]  arrivals at tile t (slot 0 only)
+// Between launches every counter is zero; only the epoch and the flags carry
+// over.  So a launch needs no host-side state: the same launch replayed from
+// a CUDA graph, or launches of different geometries interleaved, see a
+// consistent pad.
 constexpr size_t kPadStatusBytes = 128;
+constexpr size_t kPadWorkOffset = 64;
+constexpr size_t kPadEpochOffset = 96;
+constexpr size_t kPadTilesDoneOffset = 112;
 constexpr int kStatusCode = 0, kStatusRank = 1, kStatusTile = 2, kStatusEpoch = 3;
 constexpr int kProtoStaleFlag = 1;    // device codes; host maps them to SYMM_EPROTO
 constexpr int kProtoBadTicket = 2;
@@ -42,7 +55,9 @@ struct GemvArgs {
     int rows_per_tile;
     int num_tiles;
     int kc_cap;              // 16-byte chunks of x staged in shared memory per pass
-    uint32_t epoch;          // this launch's epoch (>= 1)
+    uint32_t *epoch_word;    // slot 0: epoch of the last finished fused launch
+    uint32_t *tiles_done;    // slot 0: tiles reduced so far in this launch
+    uint32_t *work;          // slot 0: the persistent kernel's two work counters
     int reverse_order;       // 1: CTAs take work in reverse (arrival-order tests)
     // What the tile reducer does with the fp32 sum of output (b, n):
     //   kOutAllReduce      bf16 into y of every rank (y: [B][N] per slot);
@@ -150,16 +165,14 @@ struct SkGeom {
     int Pmax;
 };
 // Persistent dynamically scheduled kernel: G CTAs draw the U = T*R units (KB
-// K-blocks each) from the work counter `work` (slot 0's pad).
+// K-blocks each) from the work counter work[epoch & 1] (slot 0's pad).
 struct DynGeom {
     int units;      // T * R * splits
     int splits;     // K splits per (tile, rank)
     int KB;         // K blocks per (tile, rank)
     int KBs;        // K blocks per split
     int G;
-    uint32_t *work;
 };
-constexpr size_t kPadWorkOffset = 64;   // byte offset of the work counter in slot 0's pad
 // chained: launch as a programmatic dependent of the previous kernel on the
 // stream (its CTAs may start while that one drains; see the kernel).
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,

@@ -3,27 +3,40 @@
 //
 // Protocol (one row tile t, C = R * splits contributing CTAs: one per rank
 // and K-split):
+//  0. the launch's epoch e is one more than the epoch word of slot 0's pad,
+//     which holds the epoch of the last finished fused launch on the handle
+//     (read on the device, so a launch replayed from a CUDA graph gets a new
+//     epoch each time);
 //  1. every thread stores its share of the contributor's fp32 partial into
 //     the rank's scratch slot, then fences (gpu scope);
-//  2. after a CTA barrier, thread 0 release-stores the contributor's flag
-//     (epoch) and takes an arrival ticket with an acq_rel atomic add on
-//     counter[t];
-//  3. tickets are monotone across launches of one geometry (the host resets
-//     the pad when the tile count or C changes): launch `epoch` owns tickets
-//     (epoch-1)*C .. epoch*C-1 and the holder of the last one is the
-//     reducer.  A ticket outside that range latches a protocol error;
-//  4. the reducer acquires the C flags (each must equal epoch), sums the C
+//  2. after a CTA barrier, one thread release-stores the contributor's flag
+//     (= e) and takes an arrival ticket with an acq_rel atomic add on
+//     counter[t].  Tickets run 0..C-1 in every launch: the holder of C-1 is
+//     the tile's reducer and puts the counter back to zero (every contributor
+//     of this launch has arrived).  A ticket >= C latches a protocol error;
+//  3. the reducer acquires the C flags (each must equal e), sums the C
 //     partials in fixed order (rank 0..R-1, split 0..splits-1) in fp32,
 //     rounds to bf16 (RNE) and stores the value into every rank's output
-//     slot.
+//     slot;
+//  4. the reducer counts the tile on tiles_done (when it takes the ticket).
+//     The reducer of the last tile knows that every CTA of the launch has
+//     read e (each read it before publishing), so it stores e into the epoch
+//     word and clears tiles_done and the work counter the next launch will
+//     use.
 // No CTA ever waits for another: a tile whose contributors have not all
-// arrived is finished by whichever contributor arrives last.
+// arrived is finished by whichever contributor arrives last.  Between
+// launches every counter is zero and the flags hold older epochs, so a
+// launch depends on no host-side state and the geometry may change from one
+// launch to the next.
 //
 // This is the publish-as-soon-as-done / reduce-locally scheme of the fused
 // GEMV + AllReduce ("Overlapping Collective Communication with Dependent
 // Computation ...", Abstract) and the one-shot all-reduce ("PyTorch Symmetric
 // Memory" talk, one-shot segment), with the start/end signal-pad barriers of
-// the symmetric-memory kernels replaced by per-tile release flags.
+// the symmetric-memory kernels replaced by per-tile release flags; keeping
+// the synchronisation state in the signal pad is what makes the calls
+// replayable from a CUDA graph (the symmetric-memory pages' CUDA-graph
+// compatible synchronisation primitives).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -72,6 +85,22 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float ld_relaxed_gpu_f32(const float *p) {
     float v;
     asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
@@ -90,6 +119,46 @@ __device__ __forceinline__ void latch_status(uint32_t *status, int code, int ran
         status[kStatusTile] = (uint32_t)tile;
         status[kStatusEpoch] = epoch;
     }
+}
+
+// Step 0: this launch's epoch.  A thread that publishes must have read it
+// before its flag store (the release orders the read before the flag); the
+// last tile's reducer then knows the read happened before its update.
+__device__ __forceinline__ uint32_t read_launch_epoch(const GemvArgs &a) {
+    return ld_relaxed_gpu_u32(a.epoch_word) + 1u;
+}
+
+// Step 2's ticket for contributor (r, ...) of tile t among C.  Returns the
+// ticket; its holder is the reducer when it equals C - 1, and the reducer
+// has then also counted the tile on tiles_done (*done: the count before it,
+// used later so that the atomic's latency hides behind the flag check) and
+// put the tile's counter back to zero.  The count may come before the flag
+// check: the acq_rel ticket already orders every contributor's epoch read
+// before it, whatever the flags hold.
+__device__ __forceinline__ uint32_t take_ticket(const GemvArgs &a, int t, uint32_t C, int r, uint32_t epoch,
+                                                uint32_t *done) {
+    const uint32_t pos = atom_add_acq_rel_gpu(a.counters + t, 1u);
+    if (pos >= C) {
+        latch_status(a.status, kProtoBadTicket, r, t, epoch);
+    } else if (pos == C - 1u) {
+        *done = atom_add_release_gpu(a.tiles_done, 1u);
+        st_relaxed_gpu_u32(a.counters + t, 0u);
+    }
+    return pos;
+}
+
+// Step 4: the reducer of the last tile (every CTA of the launch has read the
+// epoch by then) publishes the epoch and clears the counters for the next
+// launch.  Run by the thread that took the ticket, before the reduction, so
+// that these stores are long done when the grid ends.
+__device__ __forceinline__ void finish_launch_if_last(const GemvArgs &a, uint32_t done, uint32_t epoch, int t) {
+    const uint32_t T = (uint32_t)a.num_tiles;
+    if (done >= T) latch_status(a.status, kProtoBadTicket, -1, t, epoch);
+    if (done != T - 1u) return;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    st_relaxed_gpu_u32(a.tiles_done, 0u);
+    st_relaxed_gpu_u32(a.work + ((epoch + 1u) & 1u), 0u);
+    st_relaxed_gpu_u32(a.epoch_word, epoch);
 }
 
 // Where the tile reducer puts the fp32 sum of output (b, n) (see
@@ -177,50 +246,54 @@ __device__ __forceinline__ void reduce_tile(const GemvArgs &a, int n0, int rows,
 }
 
 // Steps 2-4 of the protocol.  Called by ALL threads of the CTA after each
-// thread has stored its part of contributor (r, s)'s partial for tile t.
-__device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, int t, int r, int s) {
+// thread has stored its part of contributor (r, s)'s partial for tile t;
+// `epoch` (step 0) is needed in thread 0 only, which publishes.
+__device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, uint32_t epoch, int t, int r, int s) {
     __shared__ int s_last;
     __shared__ int s_bad;
+    __shared__ uint32_t s_epoch;
     const int S = a.splits;
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;   // contributors per tile
+    uint32_t done = 0;                                 // thread 0, reducer: tiles counted before this one
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
                                                       (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, a.epoch);
-        const uint32_t ticket = atom_add_acq_rel_gpu(a.counters + t, 1u);
-        const uint32_t pos = ticket - (a.epoch - 1u) * C;
-        if (pos >= C) latch_status(a.status, kProtoBadTicket, r, t, a.epoch);
-        s_last = (pos == C - 1u);
+        st_release_gpu(flag, epoch);
+        s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
         s_bad = 0;
+        s_epoch = epoch;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
+    const uint32_t e = s_epoch;
+    // The acquire loads of the flags (and the barrier after them) order the
+    // partial loads of the reduction after every contributor's stores.
     for (uint32_t i = threadIdx.x; i < C; i += blockDim.x) {
         const int q = (int)(i / (uint32_t)S);
         const int qs = (int)(i % (uint32_t)S);
         const uint32_t *f = reinterpret_cast<const uint32_t *>(
                                 reinterpret_cast<const uint8_t *>(a.flags) + (long long)q * a.stride) +
                             (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != a.epoch) {
-            latch_status(a.status, kProtoStaleFlag, q, t, a.epoch);
+        if (ld_acquire_gpu(f) != e) {
+            latch_status(a.status, kProtoStaleFlag, q, t, e);
             s_bad = 1;
         }
     }
     __syncthreads();
-    if (s_bad) return;
-
-    // Sum in fixed order: rank 0..R-1, and within a rank split 0..S-1.
-    const int n0 = t * a.rows_per_tile;
-    const int rows = min(a.rows_per_tile, a.N - n0);
-    reduce_tile(a, n0, rows, (int)C,
-                [&](int j) {
-                    const int q = j / S;
-                    return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                },
-                (int)threadIdx.x, (int)blockDim.x);
+    if (threadIdx.x == 0) finish_launch_if_last(a, done, e, t);
+    if (!s_bad) {
+        // Sum in fixed order: rank 0..R-1, and within a rank split 0..S-1.
+        const int n0 = t * a.rows_per_tile;
+        const int rows = min(a.rows_per_tile, a.N - n0);
+        reduce_tile(a, n0, rows, (int)C,
+                    [&](int j) {
+                        const int q = j / S;
+                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
+                    },
+                    (int)threadIdx.x, (int)blockDim.x);
+    }
 }
 
 }  // namespace symm

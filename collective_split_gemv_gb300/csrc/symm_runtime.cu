@@ -35,11 +35,6 @@ struct symm_handle {
     int max_tiles = 0;
     uint8_t *base = nullptr;
     bool owned = false;
-    uint32_t epoch = 0;                       // epoch of the last GEMV launch
-    // Geometry of the launches since the last pad reset: tickets of launch e
-    // are (e-1)*C_t .. e*C_t-1 only while every launch has the same tiles and
-    // contributors per tile.
-    uint64_t geom_key = 0;
     int opt_gemv_path = 0;
     int opt_tile_order = 0;
     int opt_sk_slabs = 0;
@@ -142,7 +137,8 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Zero flags, counters and the work counter (stream-ordered); restart epochs.
+// Zero flags, counters, the work counters and the launch epoch
+// (stream-ordered): the pad as symm_alloc leaves it.
 int reset_protocol(symm_handle *h, cudaStream_t s) {
     cudaError_t e0 = cudaMemsetAsync(slot(h, 0) + h->pad_off + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
     if (e0 != cudaSuccess) return cuda_fail(e0, "cudaMemsetAsync(work counter)");
@@ -151,8 +147,6 @@ int reset_protocol(symm_handle *h, cudaStream_t s) {
                                         h->pad_bytes - h->flags_off, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(signal pad)");
     }
-    h->epoch = 0;
-    h->geom_key = 0;
     return SYMM_OK;
 }
 
@@ -283,7 +277,7 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 struct Plan {
     int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
     SkGeom geo = {0, 0, 0, 1};
-    DynGeom dyn = {0, 1, 0, 0, 0, nullptr};
+    DynGeom dyn = {0, 1, 0, 0, 0};
 };
 
 // `cap`: scratch bytes per slot the partials may use (the whole region, or
@@ -343,7 +337,6 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap) 
         pl->dyn.KBs = (int)KBs;
         pl->dyn.G = (int)G;
         pl->splits = (int)S;
-        pl->dyn.work = pad_word(h, 0, kPadWorkOffset);
         pl->grid = (int)G;
         pl->geo.KB = (int)KB;
     }
@@ -426,24 +419,10 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     if (rc != SYMM_OK) return rc;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Tickets of launch e are (e-1)*C_t .. e*C_t-1 (C_t contributors of tile t,
-    // at most R * max(splits, Pmax)): restart the pad when the geometry
-    // changes or before the tickets would wrap.
-    const int cmax = std::max(h->R * std::max(std::max(splits, dyn.splits), geo.Pmax), dyn.units);
-    uint64_t key = 1469598103934665603ull;
-    for (long long v : {(long long)path, (long long)tiles, (long long)splits, (long long)geo.KB, (long long)geo.G,
-                        (long long)geo.Pmax, (long long)engine, (long long)slabs, (long long)cps, (long long)geo.total,
-                        (long long)dyn.units, (long long)dyn.G, (long long)dyn.splits}) {
-        key ^= (uint64_t)v;
-        key *= 1099511628211ull;
-    }
-    if (((uint64_t)h->epoch + 1) * (uint64_t)cmax > 0xFFFFFFFFull || h->epoch == 0 || key != h->geom_key) {
-        rc = reset_protocol(h, s);
-        if (rc != SYMM_OK) return rc;
-        h->geom_key = key;
-    }
-    h->epoch += 1;
-
+    // The launch epoch, the tickets and the work counter live in the signal
+    // pad and are advanced by the kernels themselves (every counter is back
+    // at zero when a launch ends), so nothing here depends on earlier calls:
+    // a captured call replays correctly and the geometry may change freely.
     GemvArgs a;
     a.W = static_cast<const uint8_t *>(W_r);
     a.x = static_cast<const uint8_t *>(x_r);
@@ -459,7 +438,9 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.B = B;
     a.rows_per_tile = rows;
     a.num_tiles = tiles;
-    a.epoch = h->epoch;
+    a.epoch_word = pad_word(h, 0, kPadEpochOffset);
+    a.tiles_done = pad_word(h, 0, kPadTilesDoneOffset);
+    a.work = pad_word(h, 0, kPadWorkOffset);
     a.reverse_order = h->opt_tile_order;
     a.splits = splits;
     a.partial_stride = (long long)B * N * 4;
@@ -480,10 +461,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
             int err = 0;
             const void *maps = tc_maps_for(h, a, &err);
-            if (!maps) {
-                h->epoch -= 1;
-                return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
-            }
+            if (!maps) return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
             if (path == kPathTc) {
                 e = launch_gemv_tc(a, maps, s);
             } else if (path == kPathDyn) {

@@ -50,11 +50,21 @@
  *  - Device memory ownership: the library owns what symm_alloc allocates
  *    (backing == NULL) and frees it in symm_free; borrowed backing memory
  *    stays the caller's and must outlive the handle.
- *  - CUDA graphs: the fused calls (gemv_*) pass the handle's launch epoch,
- *    a host-side counter, to their kernel, so a captured call replayed
- *    later would reuse a stale epoch; the protocol then reports SYMM_EPROTO
- *    (symm_status) instead of writing y.  Issue them eagerly on a stream.
- *    The other collectives keep no state between calls.
+ *  - CUDA graphs: every call may be captured into a CUDA graph and the
+ *    graph replayed any number of times ("PyTorch Symmetric Memory" docs:
+ *    the signal-pad synchronisation primitives are CUDA-graph compatible).
+ *    The fused calls keep their whole protocol state in the signal pad: the
+ *    launch epoch (advanced on the device by the last tile's reducer), the
+ *    per-tile arrival counters and the work counters are back at zero when a
+ *    launch ends, so a launch depends on no host-side state and eager calls
+ *    of any geometry may run on the handle between replays.  Make one eager
+ *    call of each kind before capturing it, so that one-time set-up (kernel
+ *    attributes, the no-allocation call's array address) happens outside
+ *    the capture.
+ *  - After a launch in which a CTA gave up (a bounded wait ran out, latched
+ *    in the status word), the epoch is not advanced and the results of later
+ *    fused calls are undefined until symm_status has reported the error and
+ *    reset the signal pad.
  */
 #ifndef SYMM_GEMV_H
 #define SYMM_GEMV_H
@@ -187,8 +197,8 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
  *         tile flag or an out-of-range arrival ticket (e.g. two launches on
  *         the handle overlapped on different streams).
  *   rank, tile  out: where it was detected (-1 if none).
- * After an error the signal pad's flags and counters are reset so the handle
- * is usable again.  Returns SYMM_OK if the status could be read (whatever
+ * After an error the signal pad's flags, counters and launch epoch are reset
+ * so the handle is usable again.  Returns SYMM_OK if the status could be read (whatever
  * `code` says), SYMM_ECUDA otherwise.
  */
 int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile);

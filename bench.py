@@ -245,6 +245,7 @@ KERNEL_SOURCES = {
     "gemv_ar_sk_kernel": ("gemv_sk.cu", "sm100.cuh"),
     "gemv_ar_dyn_kernel": ("gemv_dyn.cu", "sm100.cuh"),
     "one_shot_ar_kernel": ("allreduce.cu",),
+    "one_shot_ar_staged_kernel": ("allreduce.cu", "sm100.cuh"),
     "reduce_scatter_kernel": ("allreduce.cu",),
     "all_gather_blocks_kernel": ("allreduce.cu",),
     "rmsnorm_rows_kernel": ("rmsnorm.cu",),
@@ -398,10 +399,13 @@ def make_case(args, w, local_rank, stream):
         copies = _copies_for(inp.nbytes * 2)    # R inputs read + R outputs written, both rotated
         ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_AR_CTAS_PER_SM, args.ar_cps)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_AR_KERNEL, args.ar_kernel)
         for c in range(copies):
             ws.load_in(inp, copy=c)
         out_n = n // R if op == "reduce_scatter" else n
-        kernel = {"one_shot": "one_shot_ar_kernel", "reduce_scatter": "reduce_scatter_kernel",
+        staged = args.ar_kernel == csg.AR_KERNEL_STAGED   # the library's automatic choice is per-thread
+        kernel = {"one_shot": "one_shot_ar_staged_kernel" if staged else "one_shot_ar_kernel",
+                  "reduce_scatter": "reduce_scatter_kernel",
                   "two_shot": "reduce_scatter_kernel+all_gather_blocks_kernel"}[op]
         return {
             "ws": ws, "copies": copies, "per_copy": inp.nbytes * 2, "kernel": kernel,
@@ -410,7 +414,8 @@ def make_case(args, w, local_rank, stream):
             "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
             "out_src": ws.base + ws.out_offs[0], "out_bytes": out_n * 2,
             "launches_per_step": 2 if op == "two_shot" else 1,
-            "config": {"R": R, "n": n, "op": op},
+            "config": {"R": R, "n": n, "op": op, **({"ar_kernel": "staged" if staged else "per_thread"}
+                                                    if op == "one_shot" else {})},
         }
     if kind == "ar_rmsnorm":
         rows, H, eps = w["rows"], w["H"], w["eps"]
@@ -784,6 +789,9 @@ def parse_args(argv=None):
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--ar-cps", type=int, default=0,
                    help="allreduce workload: grid cap in CTAs per SM (0 = library default)")
+    p.add_argument("--ar-kernel", type=int, default=0, choices=(0, 1, 2),
+                   help="allreduce workload, one-shot: 0 library default, 1 per-thread loads/stores, "
+                        "2 staged through shared memory by bulk copies")
     p.add_argument("--ar-op", choices=("one_shot", "two_shot", "reduce_scatter"), default="one_shot",
                    help="allreduce workload: which collective one step calls")
     p.add_argument("--no-chain", dest="chain", action="store_false",

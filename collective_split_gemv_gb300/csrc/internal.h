@@ -83,10 +83,17 @@ struct AllReduceArgs {
     int R;
     size_t n;
     int ctas_per_sm;         // grid cap per SM (grid-stride beyond it); 0 = the default
+    int kernel;              // one-shot kernel: kArKernelAuto / PerThread / Staged
 };
+// The one-shot all-reduce has two kernels: per-thread 16-byte loads and
+// stores, and one staged through shared memory by bulk (TMA) copies.  Auto
+// takes the per-thread one: it measured faster at every size (R = 8, 32 KB
+// to 33.5 MB per rank).
+constexpr int kArKernelAuto = 0, kArKernelPerThread = 1, kArKernelStaged = 2;
 
 // Kernel launchers; return the launch's cudaError_t.
 cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s);
+bool one_shot_uses_staged(const AllReduceArgs &a);
 
 // Reduce-scatter over the slots: element i (i < n) belongs to owner
 // i / chunk; its sum over the R slots goes to slot owner's out at element

@@ -45,6 +45,7 @@ struct symm_handle {
     int opt_norm_pdl = 1;       // launch the RMSNorm stage as a programmatic dependent
     int opt_chain = 1;          // launch the persistent kernel as a programmatic dependent
     int opt_ar_cps = 0;         // all-reduce / reduce-scatter grid cap per SM (0 = the kernels' default)
+    int opt_ar_kernel = 0;      // one-shot all-reduce kernel (kArKernel*)
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     const void *last_y = nullptr;
@@ -637,6 +638,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 64) return fail(SYMM_EINVAL, "all-reduce CTAs per SM %d not in 0..64", value);
             h->opt_ar_cps = value;
             return SYMM_OK;
+        case SYMM_OPT_AR_KERNEL:
+            if (value < 0 || value > 2) return fail(SYMM_EINVAL, "all-reduce kernel %d not in {0 auto, 1, 2}", value);
+            h->opt_ar_kernel = value;
+            return SYMM_OK;
         case SYMM_OPT_CHAIN:
             if (value < 0 || value > 1) return fail(SYMM_EINVAL, "chain %d not in {0, 1}", value);
             h->opt_chain = value;
@@ -693,6 +698,7 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.R = h->R;
     a.n = n;
     a.ctas_per_sm = h->opt_ar_cps;
+    a.kernel = h->opt_ar_kernel;
     cudaError_t e = launch_one_shot_all_reduce(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "one_shot_all_reduce launch");
     return SYMM_OK;

@@ -377,8 +377,13 @@ enum {
                                  plain stream order instead; W must not overlap the y of another handle's
                                  call launched just before it (handles on overlapping memory).  0: plain
                                  stream order always */
-    SYMM_OPT_AR_CTAS_PER_SM = 10 /* one_shot_all_reduce, two_shot_all_reduce, reduce_scatter: grid cap in CTAs
-                                 (256 threads) per SM, grid-stride beyond it; 0 auto (16) */
+    SYMM_OPT_AR_CTAS_PER_SM = 10, /* one_shot_all_reduce (per-thread kernel), two_shot_all_reduce,
+                                 reduce_scatter: grid cap in CTAs (256 threads) per SM, grid-stride beyond
+                                 it; 0 auto (16) */
+    SYMM_OPT_AR_KERNEL = 11   /* one_shot_all_reduce: 0 auto (= 1), 1 per-thread 16-byte loads and
+                                 stores, 2 staged: each CTA reduces a contiguous range chunk by chunk in
+                                 shared memory, moved in and out by bulk (TMA) copies (measured slower
+                                 than 1 from 0.5 MB per rank up) */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

@@ -69,10 +69,11 @@ def check_gemv(W, x, y, y_ref=None, exact=False):
     return ratio, eq, ulp
 
 
-def run_allreduce(inp, in_place=False):
+def run_allreduce(inp, in_place=False, kernel=csg.AR_KERNEL_AUTO):
     R, n = inp.shape
     aw = AllReduceWorkspace(R, n, separate_out=not in_place)
     try:
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_AR_KERNEL, kernel)
         aw.load_in(inp)
         aw.run(torch.cuda.current_stream())
         out = aw.read_out()

@@ -1,4 +1,6 @@
-"""One-shot all-reduce on the GPU through the C ABI against the CPU oracle."""
+"""One-shot all-reduce on the GPU through the C ABI against the CPU oracle,
+for both kernels: per-thread loads and stores, and the one staged through
+shared memory by bulk (TMA) copies."""
 from __future__ import annotations
 
 import numpy as np
@@ -32,29 +34,46 @@ def _check(inp, out, exact=False):
         int(ulp_distance(out[0], want[0]).max()) if out.size else 0
 
 
-def test_full_size_workload():
+KERNELS = {"per_thread": csg.AR_KERNEL_PER_THREAD, "staged": csg.AR_KERNEL_STAGED}
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+def test_full_size_workload(kernel):
     inp = synth.workload_inputs("allreduce")
-    out = run_allreduce(inp)
+    out = run_allreduce(inp, kernel=KERNELS[kernel])
     eq, ulp = _check(inp, out)
-    print(f"allreduce: bit-equal {eq:.6f}, max ulp {ulp}")
+    print(f"allreduce ({kernel}): bit-equal {eq:.6f}, max ulp {ulp}")
     assert eq >= 0.999 and ulp <= 1
-    out2 = run_allreduce(inp)
+    out2 = run_allreduce(inp, kernel=KERNELS[kernel])
     assert np.array_equal(out, out2)
 
 
+def test_kernels_and_auto_choice_agree_bit_for_bit():
+    # the same sum order (fp32, rank 0..R-1, one rounding) in both kernels;
+    # small and large sizes, ragged
+    for R, n in ((8, 4096 * 64 + 5), (8, (1 << 19) + 3), (3, (1 << 20) + 11)):
+        inp = synth.allreduce_inputs(R, n, R + n)
+        outs = [run_allreduce(inp, kernel=k) for k in (csg.AR_KERNEL_AUTO, csg.AR_KERNEL_PER_THREAD,
+                                                        csg.AR_KERNEL_STAGED)]
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2]), (R, n)
+        _check(inp, outs[0])
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("R,n", [(1, 8), (2, 7), (3, 1003), (4, 1), (5, 4096 + 3), (8, 100000),
-                                 (16, 999), (64, 65)])
-def test_integer_inputs_bit_exact(R, n):
+                                 (16, 999), (64, 65), (64, 64 * 1024 + 1), (2, 3 * 1024 * 1024 + 8)])
+def test_integer_inputs_bit_exact(R, n, kernel):
     rng = np.random.default_rng(R * 7 + n)
     inp = f64_to_words_via_f32(rng.integers(-100, 101, size=(R, n)).astype(np.float64))
-    out = run_allreduce(inp)
+    out = run_allreduce(inp, kernel=KERNELS[kernel])
     _check(inp, out, exact=True)
 
 
-@pytest.mark.parametrize("R,n", [(2, 12345), (8, 1 << 16), (3, 17)])
-def test_in_place(R, n):
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("R,n", [(2, 12345), (8, 1 << 16), (3, 17), (8, (1 << 20) + 7)])
+def test_in_place(R, n, kernel):
     inp = synth.allreduce_inputs(R, n, 9)
-    out = run_allreduce(inp, in_place=True)
+    out = run_allreduce(inp, in_place=True, kernel=KERNELS[kernel])
     _check(inp, out)
 
 

@@ -400,6 +400,7 @@ def make_case(args, w, local_rank, stream):
         ws = AllReduceWorkspace(R, n, device=local_rank, copies=copies)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_AR_CTAS_PER_SM, args.ar_cps)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_AR_KERNEL, args.ar_kernel)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, int(args.chain))
         for c in range(copies):
             ws.load_in(inp, copy=c)
         out_n = n // R if op == "reduce_scatter" else n
@@ -414,6 +415,7 @@ def make_case(args, w, local_rank, stream):
             "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
             "out_src": ws.base + ws.out_offs[0], "out_bytes": out_n * 2,
             "launches_per_step": 2 if op == "two_shot" else 1,
+            "chainable": True,
             "config": {"R": R, "n": n, "op": op, **({"ar_kernel": "staged" if staged else "per_thread"}
                                                     if op == "one_shot" else {})},
         }
@@ -422,6 +424,7 @@ def make_case(args, w, local_rank, stream):
         inp, bias, gamma = synth.rmsnorm_inputs(R, rows, H, w["seed"])
         copies = _copies_for(inp.nbytes * 2)
         ws = RmsNormWorkspace(R, rows, H, copies=copies, device=local_rank)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, int(args.chain))
         for c in range(copies):
             ws.load(inp, bias, gamma, copy=c)
         return {
@@ -439,6 +442,7 @@ def make_case(args, w, local_rank, stream):
         full = synth.tile_inputs(R, n, w["cols"], w["seed"])
         copies = _copies_for(full.nbytes)
         ws = TileWorkspace(R, n, w["cols"], h, w["cols"] // 2, copies=copies, device=local_rank)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, int(args.chain))
         for c in range(copies):
             ws.load_in(full, copy=c)
         tiles = [(0, 0), (0, h), (h, 0), (h, h)]
@@ -450,6 +454,7 @@ def make_case(args, w, local_rank, stream):
             "in_host": _pinned(full), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.in_bytes,
             "out_src": ws.base + ws.out_offs[0], "out_bytes": ws.out_bytes,
             "launches_per_step": 1,
+            "chainable": True,
             "config": {"R": R, "tensor": [n, w["cols"]], "tiles": "four quadrants", "roots": roots},
         }
     raise SystemExit(f"unknown workload kind {kind!r}")
@@ -484,10 +489,10 @@ def run_ours(args, rank, world, local_rank):
     working_set = copies * per_copy
     flush = working_set < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    # Chaining applies to the persistent kernel (path 4); region timing is
-    # used only where no L2 flush sits between the launches.
-    chained = (args.chain and W is not None and flush_buf is None
-               and c["config"].get("plan", {}).get("path") == 4)
+    # Chaining applies to the persistent kernel (path 4) and the collectives;
+    # region timing is used only where no L2 flush sits between the launches.
+    chained = (args.chain and flush_buf is None
+               and (c["config"].get("plan", {}).get("path") == 4 if W is not None else c.get("chainable", False)))
     # Chained calls are timed over the region only: an event between two
     # launches would separate them on the stream.
     step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,

@@ -65,6 +65,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // RT > 0: rank count known at compile time; RT == 0: runtime a.R.
 template <int RT>
 __global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceArgs a) {
+    chain_entry();
     const int R = RT > 0 ? RT : a.R;
     const size_t nvec = a.n / 8;
     const size_t step = (size_t)gridDim.x * kThreads;
@@ -162,6 +163,7 @@ __host__ __device__ __forceinline__ int staged_chunk_vectors(int R) {
 // scalar code.
 template <int RT>
 __global__ void __launch_bounds__(kStagedThreads, 2) one_shot_ar_staged_kernel(const AllReduceArgs a) {
+    chain_entry();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[kStagedStages];
     __shared__ int abort_sh;
@@ -261,10 +263,10 @@ __global__ void __launch_bounds__(kStagedThreads, 2) one_shot_ar_staged_kernel(c
 // so in == out is safe for the two-shot layout (shift = 1).
 template <int RT, bool kVec>
 __global__ void __launch_bounds__(kThreads) reduce_scatter_kernel(const ReduceScatterArgs a) {
-    // As phase 1 of the two-shot all-reduce, let phase 2 (launched as a
-    // programmatic dependent; it waits for this grid before touching memory)
-    // be scheduled as this grid's CTAs retire.
-    if (a.shift) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Chained: wait for the previous kernel before reading; let the next one
+    // (phase 2 of the two-shot all-reduce, or the next chained call) be
+    // scheduled as this grid's CTAs retire.
+    chain_entry();
     const int R = RT > 0 ? RT : a.R;
     const size_t step = (size_t)gridDim.x * kThreads;
     const size_t first = (size_t)blockIdx.x * kThreads + threadIdx.x;
@@ -346,6 +348,28 @@ unsigned grid_for(size_t work_items, int ctas_per_sm) {
     return (unsigned)blocks;
 }
 
+// Plain launch, or (a.chained) a launch as a programmatic dependent of the
+// previous kernel on the stream.
+template <class Kern, class Args>
+cudaError_t launch_maybe_chained(Kern kern, const Args &a, unsigned grid, int threads, size_t smem,
+                                 cudaStream_t s) {
+    if (!a.chained) {
+        kern<<<grid, threads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 }  // namespace
 
 cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
@@ -353,15 +377,13 @@ cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s) {
     const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n, a.ctas_per_sm);
     if (vec) {
         switch (a.R) {
-            case 2: reduce_scatter_kernel<2, true><<<g, kThreads, 0, s>>>(a); break;
-            case 4: reduce_scatter_kernel<4, true><<<g, kThreads, 0, s>>>(a); break;
-            case 8: reduce_scatter_kernel<8, true><<<g, kThreads, 0, s>>>(a); break;
-            default: reduce_scatter_kernel<0, true><<<g, kThreads, 0, s>>>(a); break;
+            case 2: return launch_maybe_chained(reduce_scatter_kernel<2, true>, a, g, kThreads, 0, s);
+            case 4: return launch_maybe_chained(reduce_scatter_kernel<4, true>, a, g, kThreads, 0, s);
+            case 8: return launch_maybe_chained(reduce_scatter_kernel<8, true>, a, g, kThreads, 0, s);
+            default: return launch_maybe_chained(reduce_scatter_kernel<0, true>, a, g, kThreads, 0, s);
         }
-    } else {
-        reduce_scatter_kernel<0, false><<<g, kThreads, 0, s>>>(a);
     }
-    return cudaGetLastError();
+    return launch_maybe_chained(reduce_scatter_kernel<0, false>, a, g, kThreads, 0, s);
 }
 
 cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s) {
@@ -399,8 +421,7 @@ cudaError_t launch_staged(const AllReduceArgs &a, unsigned grid, cudaStream_t s)
     }
     const int chv = staged_chunk_vectors(a.R);
     const size_t smem = (size_t)(kStagedStages * a.R + 2) * (size_t)chv * 16;
-    kern<<<grid, kStagedThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_maybe_chained(kern, a, grid, kStagedThreads, smem, s);
 }
 
 }  // namespace
@@ -433,13 +454,12 @@ cudaError_t launch_one_shot_all_reduce(const AllReduceArgs &a, cudaStream_t s) {
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     switch (a.R) {
-        case 1: one_shot_ar_kernel<1><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
-        case 2: one_shot_ar_kernel<2><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
-        case 4: one_shot_ar_kernel<4><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
-        case 8: one_shot_ar_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
-        default: one_shot_ar_kernel<0><<<(unsigned)blocks, kThreads, 0, s>>>(a); break;
+        case 1: return launch_maybe_chained(one_shot_ar_kernel<1>, a, (unsigned)blocks, kThreads, 0, s);
+        case 2: return launch_maybe_chained(one_shot_ar_kernel<2>, a, (unsigned)blocks, kThreads, 0, s);
+        case 4: return launch_maybe_chained(one_shot_ar_kernel<4>, a, (unsigned)blocks, kThreads, 0, s);
+        case 8: return launch_maybe_chained(one_shot_ar_kernel<8>, a, (unsigned)blocks, kThreads, 0, s);
+        default: return launch_maybe_chained(one_shot_ar_kernel<0>, a, (unsigned)blocks, kThreads, 0, s);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace symm

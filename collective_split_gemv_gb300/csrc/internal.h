@@ -84,6 +84,7 @@ struct AllReduceArgs {
     size_t n;
     int ctas_per_sm;         // grid cap per SM (grid-stride beyond it); 0 = the default
     int kernel;              // one-shot kernel: kArKernelAuto / PerThread / Staged
+    int chained;             // one-shot: launch as a programmatic dependent of the previous kernel
 };
 // The one-shot all-reduce has two kernels: per-thread 16-byte loads and
 // stores, and one staged through shared memory by bulk (TMA) copies.  Auto
@@ -109,6 +110,7 @@ struct ReduceScatterArgs {
     size_t chunk;            // elements per owner
     int shift;
     int ctas_per_sm;         // grid cap per SM; 0 = the default
+    int chained;             // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_reduce_scatter(const ReduceScatterArgs &a, cudaStream_t s);
 // Phase 2 of the two-shot all-reduce: out_q[i] = out_owner(i)[i] for q != owner.
@@ -123,6 +125,7 @@ struct TileReduceArgs {
     long long stride;
     int R, ntiles, rows, cols;
     long long ld_in, ld_out;       // elements
+    int chained;                   // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_tile_reduce(const TileReduceArgs &a, cudaStream_t s);
 
@@ -141,6 +144,7 @@ struct RmsNormArgs {
     int R, rows, H;
     float eps;
     int wait_prior;          // 1: launched as a dependent of the previous kernel (PDL)
+    int release_next;        // 1: let the next kernel on the stream be scheduled early
 };
 int rmsnorm_max_h();
 cudaError_t launch_rmsnorm_rows(const RmsNormArgs &a, cudaStream_t s);

@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     const int v0 = (int)crank * chunk;
     const int v1 = min(H8, v0 + chunk);
 
+    // A standalone chained call lets the next kernel on the stream be
+    // scheduled as this one's clusters retire.
+    if (a.release_next) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Distributed shared memory may be written only once every CTA of the
     // cluster runs: arrive now, wait just before the first remote store (the
     // row loads in between hide the wait).

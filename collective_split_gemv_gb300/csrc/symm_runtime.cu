@@ -48,8 +48,11 @@ struct symm_handle {
     int opt_ar_kernel = 0;      // one-shot all-reduce kernel (kArKernel*)
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
-    const void *last_y = nullptr;
-    size_t last_y_bytes = 0;
+    // Slot-0 range written by the last kernel this handle launched (the same
+    // offsets in every slot): a chained persistent-kernel launch, which loads
+    // W before its predecessor has finished, must not read it.
+    const void *last_write = nullptr;
+    size_t last_write_bytes = 0;
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -137,6 +140,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void note_write(symm_handle *h, const void *p, size_t bytes) {
+    h->last_write = p;
+    h->last_write_bytes = bytes;
+}
 
 // Zero flags, counters, the work counters and the launch epoch
 // (stream-ordered): the pad as symm_alloc leaves it.
@@ -466,15 +474,8 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             if (path == kPathTc) {
                 e = launch_gemv_tc(a, maps, s);
             } else if (path == kPathDyn) {
-                const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_y, h->last_y_bytes);
+                const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_write, h->last_write_bytes);
                 e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, chained, s);
-                if (ep.mode == kOutBiasZ) {
-                    h->last_y = nullptr;   // y is written by the norm stage, which its successor waits for
-                    h->last_y_bytes = 0;
-                } else {
-                    h->last_y = y;
-                    h->last_y_bytes = ybytes;
-                }
             } else {
                 a.partial_stride = (long long)B * N * 4;
                 e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
@@ -485,6 +486,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     }
     if (e != cudaSuccess) return cuda_fail(e, "gemv_all_reduce launch");
+    note_write(h, y, ybytes);   // by the GEMV, or by the norm stage launched next
     if (ep.mode == kOutBiasZ) {
         RmsNormArgs n = {};
         n.z = a.z;
@@ -699,8 +701,10 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.n = n;
     a.ctas_per_sm = h->opt_ar_cps;
     a.kernel = h->opt_ar_kernel;
+    a.chained = h->opt_chain;
     cudaError_t e = launch_one_shot_all_reduce(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "one_shot_all_reduce launch");
+    note_write(h, out, bytes);
     return SYMM_OK;
 }
 
@@ -749,8 +753,10 @@ int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n,
     a.chunk = n / (size_t)R;
     a.shift = 0;
     a.ctas_per_sm = h->opt_ar_cps;
+    a.chained = h->opt_chain;
     cudaError_t e = launch_reduce_scatter(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "reduce_scatter launch");
+    note_write(h, out, ob);
     return SYMM_OK;
 }
 
@@ -778,11 +784,13 @@ int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.chunk = (per + 7) / 8 * 8;
     a.shift = 1;
     a.ctas_per_sm = h->opt_ar_cps;
+    a.chained = h->opt_chain;   // phase 1; phase 2 is always a programmatic dependent of phase 1
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_reduce_scatter(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "two_shot_all_reduce reduce-scatter launch");
     e = launch_all_gather_blocks(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "two_shot_all_reduce all-gather launch");
+    note_write(h, out, bytes);
     return SYMM_OK;
 }
 
@@ -818,9 +826,15 @@ int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, 
     a.rows = rows;
     a.H = H;
     a.eps = eps;
-    a.wait_prior = 0;
+    // Chained: gamma and bias are loaded before the wait for the previous
+    // kernel, so not when that kernel (the handle's last) wrote them.
+    const bool chained = h->opt_chain != 0 && !overlaps(bias, bias ? vb : 0, h->last_write, h->last_write_bytes) &&
+                         !overlaps(gamma, gamma ? vb : 0, h->last_write, h->last_write_bytes);
+    a.wait_prior = chained;
+    a.release_next = chained;
     cudaError_t e = launch_rmsnorm_rows(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "all_reduce_bias_rmsnorm launch");
+    note_write(h, out, bytes);
 
     return SYMM_OK;
 }
@@ -867,8 +881,10 @@ int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *
     a.cols = cols;
     a.ld_in = ld_in;
     a.ld_out = ld_out;
+    a.chained = h->opt_chain;
     cudaError_t e = launch_tile_reduce(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tile reduce launch");
+    note_write(h, out_tile, out_ext);
     return SYMM_OK;
 }
 

@@ -43,6 +43,7 @@ __device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v) {
 
 template <int RT, bool kVec>
 __global__ void __launch_bounds__(kThreads) tile_reduce_kernel(const TileReduceArgs a) {
+    chain_entry();
     const int R = RT > 0 ? RT : a.R;
     const int t = blockIdx.y;
     const uint8_t *in = a.in[t];
@@ -86,6 +87,26 @@ __global__ void __launch_bounds__(kThreads) tile_reduce_kernel(const TileReduceA
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Plain launch, or (a.chained) a launch as a programmatic dependent of the
+// previous kernel on the stream.
+template <class Kern>
+cudaError_t launch_tile(Kern kern, const TileReduceArgs &a, dim3 grid, cudaStream_t s) {
+    if (!a.chained) {
+        kern<<<grid, kThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 }  // namespace
 
 cudaError_t launch_tile_reduce(const TileReduceArgs &a, cudaStream_t s) {
@@ -103,15 +124,13 @@ cudaError_t launch_tile_reduce(const TileReduceArgs &a, cudaStream_t s) {
     const dim3 grid((unsigned)bx, (unsigned)a.ntiles);
     if (vec) {
         switch (a.R) {
-            case 2: tile_reduce_kernel<2, true><<<grid, kThreads, 0, s>>>(a); break;
-            case 4: tile_reduce_kernel<4, true><<<grid, kThreads, 0, s>>>(a); break;
-            case 8: tile_reduce_kernel<8, true><<<grid, kThreads, 0, s>>>(a); break;
-            default: tile_reduce_kernel<0, true><<<grid, kThreads, 0, s>>>(a); break;
+            case 2: return launch_tile(tile_reduce_kernel<2, true>, a, grid, s);
+            case 4: return launch_tile(tile_reduce_kernel<4, true>, a, grid, s);
+            case 8: return launch_tile(tile_reduce_kernel<8, true>, a, grid, s);
+            default: return launch_tile(tile_reduce_kernel<0, true>, a, grid, s);
         }
-    } else {
-        tile_reduce_kernel<0, false><<<grid, kThreads, 0, s>>>(a);
     }
-    return cudaGetLastError();
+    return launch_tile(tile_reduce_kernel<0, false>, a, grid, s);
 }
 
 }  // namespace symm

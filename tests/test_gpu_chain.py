@@ -1,10 +1,12 @@
-"""Chained fused calls (SYMM_OPT_CHAIN = 1): the persistent kernel launched as a
-programmatic dependent of the previous call may start while that call drains,
-loading W early and everything else only after the previous grid has
-finished.  Checked on the GPU, through the C ABI: a chain whose every call
-reads the previous call's output as x gives the same bits as the same chain
-in plain stream order, back-to-back calls on one handle never trip the
-protocol, and the first result matches the oracle."""
+"""Chained calls (SYMM_OPT_CHAIN = 1): the persistent kernel and the one-shot
+all-reduce launched as programmatic dependents of the previous call may start
+while that call drains; the fused call loads W early and everything else only
+after the previous grid has finished, the all-reduce reads nothing before.
+Checked on the GPU, through the C ABI: a chain whose every call reads the
+previous call's output gives the same bits as the same chain in plain stream
+order, back-to-back calls on one handle never trip the protocol, W written by
+the previous call (a fused call's y, an all-reduce's output) is not read
+early, and the first result matches the oracle."""
 from __future__ import annotations
 
 import numpy as np
@@ -12,8 +14,9 @@ import pytest
 import torch
 
 import collective_split_gemv_gb300 as csg
+import oracle
 import synth
-from collective_split_gemv_gb300.workspace import GemvWorkspace
+from collective_split_gemv_gb300.workspace import AllReduceWorkspace, GemvWorkspace, RmsNormWorkspace
 from gpu_common import check_gemv, require_gpu
 
 pytestmark = pytest.mark.gpu
@@ -175,3 +178,115 @@ def _rmsnorm_chain(chain: int, steps: int = 8):
 
 def test_rmsnorm_chain_matches_plain_stream_order():
     assert np.array_equal(_rmsnorm_chain(1), _rmsnorm_chain(0))
+
+
+def _allreduce_chain(chain: int, steps: int = 10, kernel=csg.AR_KERNEL_PER_THREAD):
+    """In-place one-shot all-reduces, each reading what the previous one
+    wrote: a chained launch that read its inputs before its predecessor had
+    finished would see stale values."""
+    R, n = 4, (1 << 18) + 24
+    aw = AllReduceWorkspace(R, n, separate_out=False)
+    try:
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_CHAIN, chain)
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_AR_KERNEL, kernel)
+        inp = synth.allreduce_inputs(R, n, 31)   # grows by about R per call: 10 calls stay finite
+        aw.load_in(inp)
+        s = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            aw.run(s, op="one_shot")
+        return aw.read_out()
+    finally:
+        aw.close()
+
+
+@pytest.mark.parametrize("kernel", [csg.AR_KERNEL_PER_THREAD, csg.AR_KERNEL_STAGED])
+def test_chained_allreduce_chain_matches_plain_stream_order(kernel):
+    plain = _allreduce_chain(0, kernel=kernel)
+    chained = _allreduce_chain(1, kernel=kernel)
+    assert np.array_equal(chained, plain)
+    # one call against the oracle
+    inp = synth.allreduce_inputs(4, (1 << 18) + 24, 31)
+    one = _allreduce_chain(1, steps=1, kernel=kernel)
+    _, want = oracle.one_shot_all_reduce(inp)
+    assert np.array_equal(one[0], want[0])
+
+
+def test_weights_written_by_an_allreduce_are_not_read_early():
+    """An all-reduce writes the region the next fused call reads as W; the
+    fused call must then launch in plain stream order (a chained launch
+    would load W before the all-reduce had finished)."""
+    R, N, K, B = 2, 256, 2 * 256, 2
+    W, x = synth.gemv_inputs(R, N, K, B, seed=37, w_std=0.05, x="normal")
+    ws = GemvWorkspace(R, N, K, B, copies=2)
+    try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 1)
+        ws.load_W(W, copy=0)
+        ws.load_W(W, copy=1)
+        ws.load_x(x)
+        s = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        n = N * (K // R)
+        ws.run(s, copy=0)                                       # an earlier fused call
+        csg.one_shot_all_reduce(ws.h, ws.W_ptr(1), ws.W_ptr(1), R, n, s)   # W copy 1 <- sum over ranks
+        ws.run(s, copy=1)                                       # reads the all-reduce's output as W
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        _, summed = oracle.one_shot_all_reduce(W.reshape(R, -1))
+        check_gemv(summed.reshape(R, N, K // R), x, ws.read_y())
+    finally:
+        ws.close()
+
+
+def _collective_chain(chain: int, rounds: int = 5):
+    """Two-shot (in place), reduce-scatter (reading the two-shot's output),
+    multi-root tile reduce (quadrants of the same tensor) and one-shot (in
+    place), repeated: every call reads what an earlier one wrote."""
+    R, side = 4, 256
+    n = side * side
+    aw = AllReduceWorkspace(R, n)
+    try:
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_CHAIN, chain)
+        aw.load_in(synth.allreduce_inputs(R, n, 41))
+        s = torch.cuda.current_stream()
+        inp, out = aw.base + aw.in_off, aw.base + aw.out_off
+        h = side // 2
+        quads = [inp + (a * side + b) * 2 for a in (0, h) for b in (0, h)]
+        torch.cuda.synchronize()
+        for _ in range(rounds):
+            csg.two_shot_all_reduce(aw.h, inp, inp, R, n, s)
+            csg.reduce_scatter(aw.h, inp, out, R, n, s)
+            csg.multi_root_tile_reduce(aw.h, quads, out + (n // R) * 2, [3, 2, 1, 0], h, h, side, side, s)
+            csg.one_shot_all_reduce(aw.h, inp, inp, R, n, s)
+        torch.cuda.synchronize()
+        return (np.stack([aw.view(r, aw.in_off, n * 2).cpu().numpy() for r in range(R)]),
+                np.stack([aw.view(r, aw.out_off, n * 2).cpu().numpy() for r in range(R)]))
+    finally:
+        aw.close()
+
+
+def test_chained_collectives_match_plain_stream_order():
+    plain = _collective_chain(0)
+    chained = _collective_chain(1)
+    assert np.array_equal(chained[0], plain[0]) and np.array_equal(chained[1], plain[1])
+
+
+def _rmsnorm_standalone_chain(chain: int, steps: int = 8):
+    """all_reduce_bias_rmsnorm in place, each call reading the previous
+    call's normalised output."""
+    R, rows, H = 8, 2, 8192
+    nw = RmsNormWorkspace(R, rows, H, in_place=True)
+    try:
+        csg.symm_set_option(nw.h, csg.SYMM_OPT_CHAIN, chain)
+        nw.load(*synth.rmsnorm_inputs(R, rows, H, 43))
+        s = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            nw.run(s)
+        return nw.read_out()
+    finally:
+        nw.close()
+
+
+def test_chained_standalone_rmsnorm_matches_plain_stream_order():
+    assert np.array_equal(_rmsnorm_standalone_chain(1), _rmsnorm_standalone_chain(0))

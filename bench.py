@@ -511,7 +511,10 @@ def run_ours(args, rank, world, local_rank):
     # ---- e2e: the same call through the ABI with host buffers every step ----
     # Each step: one strided copy of the step's inputs from pinned host memory
     # into the R slots, the call, one copy of the result (slot 0) back, and a
-    # stream synchronisation.
+    # stream synchronisation.  The library copies pinned buffers with a kernel
+    # (the SMs read and write host memory over the CPU-GPU link), so a step is
+    # a chain of three kernels; --copy-engine 1 takes copy-engine copies.
+    csg.symm_set_option(ws.h, csg.SYMM_OPT_COPY_ENGINE, args.copy_engine)
     out_host = torch.empty(max(out_bytes, 1), dtype=torch.uint8).pin_memory()
     e2e_steps = max(3, min(args.steps, 200))
 
@@ -626,9 +629,11 @@ def run_ours(args, rank, world, local_rank):
             "value": round(throughput_gbs(nbytes, e2e_ms, world), 2), "unit": "GB/s",
             "us_per_call": round(e2e_ms * 1e3, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
-            "what": ("per step: the inputs H2D from pinned memory in one strided copy into the R slots "
-                     "(symm_copy_to_slots), the call, the result (slot 0) D2H (symm_copy_from_slots), stream "
-                     "synchronised" + ("; W_r resident (model weights)" if W is not None else "")),
+            "what": ("per step: the inputs H2D from pinned memory into the R slots (symm_copy_to_slots), the "
+                     "call, the result (slot 0) D2H (symm_copy_from_slots), stream synchronised; the copies "
+                     + ("by the copy engine" if args.copy_engine else
+                        "by a kernel reading / writing the pinned buffers over the CPU-GPU link")
+                     + ("; W_r resident (model weights)" if W is not None else "")),
         },
         "e2e_graph": {
             "value": round(throughput_gbs(nbytes, e2e_graph_ms, world), 2), "unit": "GB/s",
@@ -794,6 +799,9 @@ def parse_args(argv=None):
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--ar-cps", type=int, default=0,
                    help="allreduce workload: grid cap in CTAs per SM (0 = library default)")
+    p.add_argument("--copy-engine", type=int, default=0, choices=(0, 1),
+                   help="end-to-end legs: 0 library default (pinned host buffers copied by a kernel), "
+                        "1 the copy engine (SYMM_OPT_COPY_ENGINE)")
     p.add_argument("--ar-kernel", type=int, default=0, choices=(0, 1, 2),
                    help="allreduce workload, one-shot: 0 library default, 1 per-thread loads/stores, "
                         "2 staged through shared memory by bulk copies")

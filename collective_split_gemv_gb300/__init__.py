@@ -42,6 +42,7 @@ SYMM_OPT_NORM_PDL = 8
 SYMM_OPT_CHAIN = 9
 SYMM_OPT_AR_CTAS_PER_SM = 10
 SYMM_OPT_AR_KERNEL = 11
+SYMM_OPT_COPY_ENGINE = 12
 AR_KERNEL_AUTO, AR_KERNEL_PER_THREAD, AR_KERNEL_STAGED = 0, 1, 2   # auto is the per-thread kernel
 
 GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK, GEMV_PATH_DYN = 0, 1, 2, 3, 4

@@ -149,6 +149,18 @@ struct RmsNormArgs {
 int rmsnorm_max_h();
 cudaError_t launch_rmsnorm_rows(const RmsNormArgs &a, cudaStream_t s);
 
+// Strided copy by the SMs: block r (bytes) from src + r * src_stride to
+// dst + r * dst_stride, r < nranks (copy_slots.cu).
+struct CopySlotsArgs {
+    const uint8_t *src;
+    uint8_t *dst;
+    long long src_stride, dst_stride;
+    size_t bytes;
+    int nranks;
+    int chained;             // launch as a programmatic dependent of the previous kernel
+};
+cudaError_t launch_copy_slots(const CopySlotsArgs &a, cudaStream_t s);
+
 // FFMA (CUDA-core) fused kernel: any B in 1..16.
 int ffma_rows_per_tile(int B);
 size_t ffma_smem_bytes(int B, int kc_cap);

@@ -46,6 +46,7 @@ struct symm_handle {
     int opt_chain = 1;          // launch the persistent kernel as a programmatic dependent
     int opt_ar_cps = 0;         // all-reduce / reduce-scatter grid cap per SM (0 = the kernels' default)
     int opt_ar_kernel = 0;      // one-shot all-reduce kernel (kArKernel*)
+    int opt_copy_engine = 0;    // symm_copy_*: 1 = always the copy engine, 0 = SMs where possible
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     // Slot-0 range written by the last kernel this handle launched (the same
@@ -640,6 +641,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 64) return fail(SYMM_EINVAL, "all-reduce CTAs per SM %d not in 0..64", value);
             h->opt_ar_cps = value;
             return SYMM_OK;
+        case SYMM_OPT_COPY_ENGINE:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "copy engine %d not in {0, 1}", value);
+            h->opt_copy_engine = value;
+            return SYMM_OK;
         case SYMM_OPT_AR_KERNEL:
             if (value < 0 || value > 2) return fail(SYMM_EINVAL, "all-reduce kernel %d not in {0 auto, 1, 2}", value);
             h->opt_ar_kernel = value;
@@ -919,6 +924,23 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
     return SYMM_OK;
 }
 
+// The handle's device can copy to or from [p, p + bytes) with its SMs: its
+// own device memory, or pinned host memory mapped into the device's address
+// space at the same address (both ends checked).
+bool sm_addressable(const symm_handle *h, const void *p, size_t bytes) {
+    for (const uint8_t *q : {static_cast<const uint8_t *>(p), static_cast<const uint8_t *>(p) + bytes - 1}) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+            cudaGetLastError();   // an unregistered host pointer is not an error here
+            return false;
+        }
+        if (at.type == cudaMemoryTypeDevice && at.device == h->device) continue;
+        if (at.type == cudaMemoryTypeHost && at.devicePointer == q) continue;
+        return false;
+    }
+    return true;
+}
+
 int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
                        symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
@@ -926,9 +948,26 @@ int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t byte
     if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
     if (!src) return fail(SYMM_EINVAL, "src is NULL");
     if (!in_user_region(h, dst, bytes_per_rank)) return fail(SYMM_EINVAL, "dst is not inside slot 0's user region");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h->opt_copy_engine == 0 && sm_addressable(h, src, bytes_per_rank * (size_t)nranks)) {
+        int rc = check_device(h);
+        if (rc != SYMM_OK) return rc;
+        CopySlotsArgs a;
+        a.src = static_cast<const uint8_t *>(src);
+        a.dst = static_cast<uint8_t *>(dst);
+        a.src_stride = (long long)bytes_per_rank;
+        a.dst_stride = (long long)h->stride;
+        a.bytes = bytes_per_rank;
+        a.nranks = nranks;
+        a.chained = h->opt_chain;
+        cudaError_t e = launch_copy_slots(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copy to slots launch");
+        note_write(h, dst, bytes_per_rank);
+        return SYMM_OK;
+    }
     // One strided copy: rank r's bytes land at dst + r * stride.
     cudaError_t e = cudaMemcpy2DAsync(dst, h->stride, src, bytes_per_rank, bytes_per_rank, (size_t)nranks,
-                                      cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+                                      cudaMemcpyDefault, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync (to slots)");
     return SYMM_OK;
 }
@@ -940,8 +979,24 @@ int symm_copy_from_slots(symm_handle_t *h, void *dst, const void *src, size_t by
     if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
     if (!dst) return fail(SYMM_EINVAL, "dst is NULL");
     if (!in_user_region(h, src, bytes_per_rank)) return fail(SYMM_EINVAL, "src is not inside slot 0's user region");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h->opt_copy_engine == 0 && sm_addressable(h, dst, bytes_per_rank * (size_t)nranks)) {
+        int rc = check_device(h);
+        if (rc != SYMM_OK) return rc;
+        CopySlotsArgs a;
+        a.src = static_cast<const uint8_t *>(src);
+        a.dst = static_cast<uint8_t *>(dst);
+        a.src_stride = (long long)h->stride;
+        a.dst_stride = (long long)bytes_per_rank;
+        a.bytes = bytes_per_rank;
+        a.nranks = nranks;
+        a.chained = h->opt_chain;
+        cudaError_t e = launch_copy_slots(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copy from slots launch");
+        return SYMM_OK;
+    }
     cudaError_t e = cudaMemcpy2DAsync(dst, bytes_per_rank, src, h->stride, bytes_per_rank, (size_t)nranks,
-                                      cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+                                      cudaMemcpyDefault, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy2DAsync (from slots)");
     return SYMM_OK;
 }

@@ -216,6 +216,12 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
  *               src + r * stride.
  *   The contiguous side may be host memory (pinned for an asynchronous copy)
  *   or device memory.  nranks 0..R; 0 bytes or 0 ranks is a no-op.
+ *   Device memory and pinned host memory the GPU addresses at the same
+ *   pointer (every pinned allocation on this platform) are copied by a
+ *   kernel -- the SMs read or write the host buffer over the CPU-GPU link --
+ *   which, like the other calls, chains with its neighbours on the stream
+ *   (SYMM_OPT_CHAIN); other host memory, or SYMM_OPT_COPY_ENGINE = 1, takes
+ *   one strided copy-engine copy.
  * Stream-ordered; returns after enqueueing.  Errors: SYMM_EINVAL (NULL
  * pointer, nranks out of range, the symmetric side outside slot 0's user
  * region), SYMM_ECUDA.
@@ -381,10 +387,14 @@ enum {
     SYMM_OPT_AR_CTAS_PER_SM = 10, /* one_shot_all_reduce (per-thread kernel), two_shot_all_reduce,
                                  reduce_scatter: grid cap in CTAs (256 threads) per SM, grid-stride beyond
                                  it; 0 auto (16) */
-    SYMM_OPT_AR_KERNEL = 11   /* one_shot_all_reduce: 0 auto (= 1), 1 per-thread 16-byte loads and
+    SYMM_OPT_AR_KERNEL = 11,  /* one_shot_all_reduce: 0 auto (= 1), 1 per-thread 16-byte loads and
                                  stores, 2 staged: each CTA reduces a contiguous range chunk by chunk in
                                  shared memory, moved in and out by bulk (TMA) copies (measured slower
                                  than 1 from 0.5 MB per rank up) */
+    SYMM_OPT_COPY_ENGINE = 12 /* symm_copy_to_slots / from_slots: 0 (default) copy with a kernel when the
+                                 contiguous side is device memory or pinned host memory mapped at the same
+                                 address (a link in the chain of programmatic dependent launches, see
+                                 SYMM_OPT_CHAIN), else with the copy engine; 1 always the copy engine */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

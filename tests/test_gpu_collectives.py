@@ -402,10 +402,13 @@ def test_gemv_bias_rmsnorm_rejects_ragged_n():
 # ------------------------------------------------------- staging copies
 
 
-def test_copy_to_and_from_slots_round_trip():
+@pytest.mark.parametrize("engine", [0, 1])
+def test_copy_to_and_from_slots_round_trip(engine):
+    # engine 0: pinned host memory copied by the SMs (a kernel); 1: the copy engine
     R, n = 4, 1000
     aw = AllReduceWorkspace(R, n)
     try:
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_COPY_ENGINE, engine)
         s = torch.cuda.current_stream()
         host = torch.arange(R * n, dtype=torch.int16).view(torch.uint8).pin_memory()
         csg.symm_copy_to_slots(aw.h, aw.base + aw.in_offs[0], host.data_ptr(), n * 2, R, s)
@@ -429,6 +432,41 @@ def test_copy_to_and_from_slots_round_trip():
             with pytest.raises(csg.SymmError) as e:
                 csg.symm_copy_to_slots(aw.h, *args, s)
             assert e.value.code == csg.SYMM_EINVAL
+        _guards_ok(aw.h)
+    finally:
+        aw.close()
+
+
+@pytest.mark.parametrize("kind", ["pinned", "pageable", "device", "ragged_pinned"])
+@pytest.mark.parametrize("engine", [0, 1])
+def test_copy_slots_sources(kind, engine):
+    """Every kind of contiguous buffer, both engines: pinned host and device
+    memory go through the SMs (engine 0), pageable host memory through the
+    copy engine whatever the option; block sizes that are not multiples of
+    16 bytes take the byte-wise kernel."""
+    R = 3
+    nbytes = 4093 if kind == "ragged_pinned" else 4096
+    aw = AllReduceWorkspace(R, 4096)
+    try:
+        csg.symm_set_option(aw.h, csg.SYMM_OPT_COPY_ENGINE, engine)
+        s = torch.cuda.current_stream()
+        data = torch.randint(0, 256, (R * nbytes,), dtype=torch.uint8)
+        if kind in ("pinned", "ragged_pinned"):
+            src = data.pin_memory()
+            dst = torch.zeros_like(data).pin_memory()
+        elif kind == "device":
+            src = data.to(aw.device)
+            dst = torch.zeros_like(src)
+        else:
+            src = data.clone()
+            dst = torch.zeros_like(data)
+        sym = aw.base + aw.in_offs[0]
+        csg.symm_copy_to_slots(aw.h, sym, src.data_ptr(), nbytes, R, s)
+        csg.symm_copy_from_slots(aw.h, dst.data_ptr(), sym, nbytes, R, s)
+        s.synchronize()
+        assert torch.equal(dst.cpu(), data)
+        for r in range(R):
+            assert torch.equal(aw.view(r, aw.in_offs[0], nbytes).cpu(), data[r * nbytes:(r + 1) * nbytes])
         _guards_ok(aw.h)
     finally:
         aw.close()

@@ -489,10 +489,9 @@ def run_ours(args, rank, world, local_rank):
     working_set = copies * per_copy
     flush = working_set < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    # Chaining applies to the persistent kernel (path 4) and the collectives;
-    # region timing is used only where no L2 flush sits between the launches.
-    chained = (args.chain and flush_buf is None
-               and (c["config"].get("plan", {}).get("path") == 4 if W is not None else c.get("chainable", False)))
+    # Every call chains (the library default); region timing is used only
+    # where no L2 flush sits between the launches.
+    chained = args.chain and flush_buf is None and (W is not None or c.get("chainable", False))
     # Chained calls are timed over the region only: an event between two
     # launches would separate them on the stream.
     step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,

@@ -353,21 +353,7 @@ unsigned grid_for(size_t work_items, int ctas_per_sm) {
 template <class Kern, class Args>
 cudaError_t launch_maybe_chained(Kern kern, const Args &a, unsigned grid, int threads, size_t smem,
                                  cudaStream_t s) {
-    if (!a.chained) {
-        kern<<<grid, threads, smem, s>>>(a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return launch_kernel(kern, dim3(grid), dim3((unsigned)threads), smem, s, a.chained != 0, a);
 }
 
 }  // namespace
@@ -390,17 +376,8 @@ cudaError_t launch_all_gather_blocks(const ReduceScatterArgs &a, cudaStream_t s)
     const bool vec = a.chunk % 8 == 0;
     const unsigned g = grid_for(vec ? a.n / 8 + (a.n % 8) : a.n, a.ctas_per_sm);
     // A programmatic dependent of phase 1: its launch overlaps phase 1's end.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(g, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return vec ? cudaLaunchKernelEx(&cfg, all_gather_blocks_kernel<true>, a)
-               : cudaLaunchKernelEx(&cfg, all_gather_blocks_kernel<false>, a);
+    return vec ? launch_kernel(all_gather_blocks_kernel<true>, dim3(g), dim3(kThreads), 0, s, true, a)
+               : launch_kernel(all_gather_blocks_kernel<false>, dim3(g), dim3(kThreads), 0, s, true, a);
 }
 
 namespace {

@@ -54,20 +54,7 @@ cudaError_t launch_copy_slots(const CopySlotsArgs &a, cudaStream_t s) {
     if (blocks > cap) blocks = cap;
     if (blocks == 0) blocks = 1;
     auto kern = vec ? copy_slots_kernel<true> : copy_slots_kernel<false>;
-    if (!a.chained) {
-        kern<<<(unsigned)blocks, kThreads, 0, s>>>(a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return launch_kernel(kern, dim3((unsigned)blocks), dim3(kThreads), 0, s, a.chained != 0, a);
 }
 
 }  // namespace symm

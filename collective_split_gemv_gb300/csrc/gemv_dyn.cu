@@ -603,21 +603,7 @@ cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap 
         if (e != cudaSuccess) return e;
         attr_devices |= bit;
     }
-    if (!chained) {
-        kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)geo.G, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr1[1];
-    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr1[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr1;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], a, geo);
+    return launch_kernel(kern, dim3((unsigned)geo.G), dim3(kThreads), (size_t)smem, s, chained, m[0], m[1], a, geo);
 }
 
 template <int kEngine, int kB>

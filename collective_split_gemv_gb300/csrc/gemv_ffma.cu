@@ -54,7 +54,7 @@ __device__ __forceinline__ float dot8(const uint4 &w, const float4 &lo, const fl
 
 template <int B>
 __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a) {
-    allow_dependent_launch(a);
+    chain_entry();
     // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
     const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
     constexpr int G = FfmaShape<B>::G;
@@ -171,8 +171,7 @@ cudaError_t launch_b(const GemvArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const unsigned grid = (unsigned)a.num_tiles * (unsigned)a.R;
-    kern<<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, s, a.chained != 0, a);
 }
 
 template <int B>

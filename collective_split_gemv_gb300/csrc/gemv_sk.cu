@@ -197,7 +197,7 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, const SkGeom geo) {
-    allow_dependent_launch(a);
+    chain_entry();
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;
@@ -442,8 +442,8 @@ cudaError_t launch_cfg(const GemvArgs &a, const SkGeom &geo, const CUtensorMap *
         if (e != cudaSuccess) return e;
         attr_devices |= bit;
     }
-    kern<<<geo.G, kThreads, smem, s>>>(m[0], m[1], a, geo);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3((unsigned)geo.G), dim3(kThreads), (size_t)smem, s, a.chained != 0, m[0], m[1], a,
+                         geo);
 }
 
 }  // namespace

@@ -56,7 +56,7 @@ static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const GemvArgs a, int kb_total, int kb_per_split) {
-    allow_dependent_launch(a);
+    chain_entry();
     // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
     const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
     extern __shared__ uint8_t smem_raw[];
@@ -247,8 +247,8 @@ cudaError_t launch_gemv_tc(const GemvArgs &a, const void *maps, cudaStream_t s) 
     const int kb_total = (a.Kr + kBK - 1) / kBK;
     const int kb_per_split = (kb_total + a.splits - 1) / a.splits;
     const unsigned grid = (unsigned)a.num_tiles * (unsigned)a.R * (unsigned)a.splits;
-    gemv_ar_tc_kernel<<<grid, kThreads, smem, s>>>(m[0], m[1], a, kb_total, kb_per_split);
-    return cudaGetLastError();
+    return launch_kernel(gemv_ar_tc_kernel, dim3(grid), dim3(kThreads), smem, s, a.chained != 0, m[0], m[1], a,
+                         kb_total, kb_per_split);
 }
 
 }  // namespace symm

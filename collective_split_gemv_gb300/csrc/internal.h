@@ -6,7 +6,33 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace symm {
+
+// Launches kern<<<grid, block, smem, s>>>(args...); when `chained`, as a
+// programmatic dependent of the previous kernel on the stream (its CTAs may
+// be scheduled while that kernel drains; the kernel itself waits for it with
+// griddepcontrol.wait before touching what it wrote).
+template <class... KArgs, class... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool chained, Args &&...args) {
+    if (!chained) {
+        kern<<<grid, block, smem, s>>>(std::forward<Args>(args)...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Signal-pad layout of every slot (byte offsets from the pad start):
 //   [0, 16)                 status words {code, rank, tile, epoch} (slot 0 only)
@@ -66,6 +92,7 @@ struct GemvArgs {
     //   kOutBiasZ          fp32 sum + bias[n] into z[b][n] (slot 0), for the
     //                      RMS-normalisation stage that follows.
     int out_mode;
+    int chained;             // per-tile kernels (paths 1-3): launch as a programmatic dependent
     int rs_rows;             // kOutReduceScatter: B / R
     float *z;                // kOutBiasZ: fp32 [B][N]
     const uint8_t *bias;     // kOutBiasZ: bf16 [N] (slot 0) or nullptr

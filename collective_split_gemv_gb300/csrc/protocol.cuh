@@ -191,22 +191,15 @@ __device__ __forceinline__ void store_output(const GemvArgs &a, size_t e, float 
 // has completed and its memory is visible; returns at once otherwise.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Entry of the collective kernels for chained calls (launched as
-// programmatic dependents of the previous kernel on the stream): a CTA may be
-// scheduled while that kernel drains, and waits for it, and for its memory,
-// before reading anything; it lets its own successor be scheduled likewise.
-// Both are no-ops in plain stream order.
+// Entry of the collective kernels and the per-tile fused kernels for chained
+// calls (launched as programmatic dependents of the previous kernel on the
+// stream): a CTA may be scheduled while that kernel drains, and waits for it,
+// and for its memory, before reading anything; it lets its own successor (the
+// next chained call, or the RMS-normalisation stage of a bias + RMSNorm call)
+// be scheduled likewise.  Both are no-ops in plain stream order.
 __device__ __forceinline__ void chain_entry() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     griddep_wait();
-}
-
-// In a bias + RMSNorm call the normalisation kernel is launched as a
-// programmatic dependent of the GEMV; this lets its CTAs be scheduled while
-// the GEMV still runs (they wait for the whole GEMV grid, and its memory, at
-// griddepcontrol.wait before reading z).  A no-op for the other modes.
-__device__ __forceinline__ void allow_dependent_launch(const GemvArgs &a) {
-    if (a.out_mode == kOutBiasZ) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // The reduction of one tile by its last contributor: for each output (b, n)

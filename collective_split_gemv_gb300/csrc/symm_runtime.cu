@@ -456,6 +456,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.partial_stride = (long long)B * N * 4;
     a.kc_cap = 0;
     a.out_mode = ep.mode;
+    a.chained = h->opt_chain;   // paths 1-3 (path 4 decides below)
     a.rs_rows = ep.mode == kOutReduceScatter ? B / R : B;
     a.z = ep.mode == kOutBiasZ ? reinterpret_cast<float *>(h->base + h->scratch_off + z_off) : nullptr;
     a.bias = ep.mode == kOutBiasZ ? static_cast<const uint8_t *>(ep.bias) : nullptr;

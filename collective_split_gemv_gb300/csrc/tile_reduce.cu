@@ -87,24 +87,9 @@ __global__ void __launch_bounds__(kThreads) tile_reduce_kernel(const TileReduceA
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Plain launch, or (a.chained) a launch as a programmatic dependent of the
-// previous kernel on the stream.
 template <class Kern>
 cudaError_t launch_tile(Kern kern, const TileReduceArgs &a, dim3 grid, cudaStream_t s) {
-    if (!a.chained) {
-        kern<<<grid, kThreads, 0, s>>>(a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return launch_kernel(kern, grid, dim3(kThreads), 0, s, a.chained != 0, a);
 }
 
 }  // namespace

@@ -373,17 +373,17 @@ enum {
     SYMM_OPT_NORM_PDL = 8,    /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
                                  programmatic dependent of the GEMV so its launch overlaps the GEMV's
                                  tail; 0 plain stream order */
-    SYMM_OPT_CHAIN = 9,       /* 1 (default): the persistent kernel (path 4) and the one-shot all-reduce are
-                                 launched as programmatic dependents of the previous kernel on the stream,
-                                 so back-to-back calls overlap one call's start-up with the previous
-                                 call's end; both let their successor be scheduled early.  A chained
-                                 all-reduce reads nothing before its predecessor has finished.  A chained
-                                 fused call loads W for its first stages before its predecessor has
-                                 finished; x, y, scratch and the pad are touched only after.  A fused call
-                                 whose W overlaps the output of the last call on the same handle (any
-                                 call) is launched in plain stream order instead; W must not be written
-                                 by any other kernel launched just before it on the stream.  0: plain
-                                 stream order always */
+    SYMM_OPT_CHAIN = 9,       /* 1 (default): every kernel of this library is launched as a programmatic
+                                 dependent of the previous kernel on the stream, so back-to-back calls
+                                 overlap one call's start-up with the previous call's end; each lets its
+                                 successor be scheduled early.  A chained kernel reads nothing before its
+                                 predecessor has finished, with two exceptions: the persistent fused
+                                 kernel (path 4) loads W for its first stages early, and the standalone
+                                 all-reduce + bias + RMSNorm loads gamma and bias early.  Such a call is
+                                 launched in plain stream order when those operands overlap the output
+                                 of the last call on the same handle (any call); they must not be
+                                 written by any other kernel launched just before it on the stream.
+                                 0: plain stream order always */
     SYMM_OPT_AR_CTAS_PER_SM = 10, /* one_shot_all_reduce (per-thread kernel), two_shot_all_reduce,
                                  reduce_scatter: grid cap in CTAs (256 threads) per SM, grid-stride beyond
                                  it; 0 auto (16) */

@@ -27,7 +27,7 @@ def _gpu():
     require_gpu()
 
 
-def _dependent_chain(chain: int, steps: int, B: int):
+def _dependent_chain(chain: int, steps: int, B: int, path=csg.GEMV_PATH_DYN):
     """R = 1, N = K: call i + 1 reads call i's y as its x, so a call that read
     x before its predecessor finished would see a stale vector.  The vectors
     v_0 = x, v_1, ..., v_steps live in the second W copy's region, so the calls
@@ -37,7 +37,7 @@ def _dependent_chain(chain: int, steps: int, B: int):
     W, x = synth.gemv_inputs(1, N, K, B, seed=17, w_std=1.0 / np.sqrt(K), x="normal")
     ws = GemvWorkspace(1, N, K, B, copies=2)
     try:
-        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, chain)
         ws.load_W(W)
         vbytes = B * N * 2
@@ -60,9 +60,11 @@ def _dependent_chain(chain: int, steps: int, B: int):
 
 
 @pytest.mark.parametrize("B", [1, 2, 8])
-def test_dependent_chain_matches_plain_stream_order(B):
-    W, x, plain = _dependent_chain(0, 12, B)
-    _, _, chained = _dependent_chain(1, 12, B)
+@pytest.mark.parametrize("path", ["dyn", "ffma", "tc", "sk"])
+def test_dependent_chain_matches_plain_stream_order(B, path):
+    p = {"dyn": csg.GEMV_PATH_DYN, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC, "sk": csg.GEMV_PATH_SK}[path]
+    W, x, plain = _dependent_chain(0, 12, B, p)
+    _, _, chained = _dependent_chain(1, 12, B, p)
     assert np.array_equal(chained, plain)
     # the first call against the oracle
     check_gemv(W, x, plain[0])

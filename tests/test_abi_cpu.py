@@ -42,6 +42,23 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in csg.EXPORTED, f"{name} has no Python binding"
 
 
+def _header_enum(prefix):
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(" + prefix + r"\w*)\s*=\s*(-?\d+)", src)}
+
+
+def test_option_and_status_codes_match_the_binding():
+    """The binding's option numbers and status codes are the header's."""
+    for prefix in ("SYMM_OPT_", "SYMM_E", "SYMM_OK"):
+        declared = _header_enum(prefix)
+        assert declared, prefix
+        for name, value in declared.items():
+            assert getattr(csg, name) == value, name
+    opts = _header_enum("SYMM_OPT_")
+    assert len(set(opts.values())) == len(opts)   # no two options share a number
+
+
 def test_layout_arithmetic(lib):
     stride, total = csg.symm_layout(8, 1000, 4096, 4096)
     assert stride % (2 << 20) == 0 and stride >= 1000 + 4096 + 4096 + 3 * 4096

@@ -69,3 +69,26 @@ def test_max_over_ranks_with_two_gloo_ranks():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert results[0] == results[1] == [2.0, 10.0, 3.0]
+
+
+def test_traffic_entries_name_known_kernels_and_workloads():
+    """Every profiled traffic entry names a kernel the bench reports and a
+    workload it runs, with positive bytes and a 16-hex-digit source hash."""
+    import json
+    import re
+    import synth
+    d = json.load(open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles",
+                                    "traffic.json")))
+    for kernel, per in d.items():
+        if kernel.startswith("_"):
+            continue
+        for part in kernel.split("+"):
+            assert part.split("<")[0] in bench.KERNEL_SOURCES, kernel
+        for workload, entry in per.items():
+            assert workload in synth.WORKLOADS, (kernel, workload)
+            assert entry["dram_bytes_per_launch"] > 0
+            assert re.fullmatch(r"[0-9a-f]{16}", entry["source_sha"])
+            # a stale entry is reported as null, a current one as its bytes
+            got = bench.profiled_traffic(kernel, workload, entry["source_sha"])
+            assert got == entry["dram_bytes_per_launch"]
+            assert bench.profiled_traffic(kernel, workload, "0" * 16) is None

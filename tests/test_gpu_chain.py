@@ -292,3 +292,47 @@ def _rmsnorm_standalone_chain(chain: int, steps: int = 8):
 
 def test_chained_standalone_rmsnorm_matches_plain_stream_order():
     assert np.array_equal(_rmsnorm_standalone_chain(1), _rmsnorm_standalone_chain(0))
+
+
+def _interleaved(chain: int):
+    """Two handles on one stream, their fused calls alternating, and a
+    PyTorch kernel rewriting one handle's x between its calls: chained
+    launches must read x only after the kernel before them has finished."""
+    R, N, K, B = 4, 1024, 4 * 1024, 2
+    Wa, xa = synth.gemv_inputs(R, N, K, B, seed=51, w_std=0.03, x="normal")
+    Wb, xb = synth.gemv_inputs(R, N, K, B, seed=52, w_std=0.03, x="normal")
+    _, xa2 = synth.gemv_inputs(R, N, K, B, seed=53, w_std=0.03, x="normal")
+    wa, wb = GemvWorkspace(R, N, K, B), GemvWorkspace(R, N, K, B)
+    try:
+        for ws, W, x in ((wa, Wa, xa), (wb, Wb, xb)):
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, chain)
+            ws.load_W(W)
+            ws.load_x(x)
+        x_new = [torch.from_numpy(np.ascontiguousarray(xa2[r])).view(torch.int16).reshape(-1).to(wa.device)
+                 for r in range(R)]
+        s = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        ys = []
+        for i in range(6):
+            wa.run(s)
+            wb.run(s)
+            if i == 2:
+                for r in range(R):   # a PyTorch kernel writes x of handle a right before its next call
+                    torch.bitwise_xor(x_new[r], 0, out=wa.x_view(r).view(torch.int16))
+            ys.append((wa.read_y(), wb.read_y()) if i in (2, 5) else None)
+        assert csg.symm_status(wa.h, s)[0] == csg.SYMM_OK and csg.symm_status(wb.h, s)[0] == csg.SYMM_OK
+        return [y for y in ys if y is not None], (Wa, xa, xa2, Wb, xb)
+    finally:
+        wa.close()
+        wb.close()
+
+
+def test_two_handles_and_foreign_writes_between_chained_calls():
+    plain, (Wa, xa, xa2, Wb, xb) = _interleaved(0)
+    chained, _ = _interleaved(1)
+    for (ya_p, yb_p), (ya_c, yb_c) in zip(plain, chained):
+        assert np.array_equal(ya_p, ya_c) and np.array_equal(yb_p, yb_c)
+    check_gemv(Wa, xa, chained[0][0])
+    check_gemv(Wa, xa2, chained[1][0])
+    check_gemv(Wb, xb, chained[1][1])

@@ -361,22 +361,39 @@ def make_case(args, w, local_rank, stream):
         N, K, B = w["N"], w["K"], w["B"]
         W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
         copies = _copies_for(W.nbytes)
-        ws = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank)
         paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
                  "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
-        for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
-                         (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
-                         (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
-                         (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain))):
-            csg.symm_set_option(ws.h, opt, val)
+
+        def gemv_ws(packed):
+            ws_ = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank, packed=packed)
+            for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
+                             (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
+                             (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
+                             (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain))):
+                csg.symm_set_option(ws_.h, opt, val)
+            return ws_
+
+        ws = gemv_ws(False)
         plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        # Packed weights (made once by symm_pack_w, as at model load) wherever
+        # the call runs on the persistent kernel, the only one that reads them;
+        # the row-major weights are kept and timed beside them.
+        ws_rm = None
+        if args.w_layout == "packed" and plan["path"] == csg.GEMV_PATH_DYN:
+            ws_rm, ws = ws, gemv_ws(True)
         for c in range(copies):
             ws.load_W(W, copy=c)
+            if ws_rm is not None:
+                ws_rm.load_W(W, copy=c)
         ws.load_x(x)
+        if ws_rm is not None:
+            ws_rm.load_x(x)
         mode = {"gemv": "all_reduce", "gemv_rs": "reduce_scatter", "gemv_rmsnorm": "bias_rmsnorm"}[kind]
         eps = w.get("eps", 1e-6)
         if kind == "gemv_rmsnorm":
             ws.load_vectors(*synth.norm_vectors(N, w["seed"]))
+            if ws_rm is not None:
+                ws_rm.load_vectors(*synth.norm_vectors(N, w["seed"]))
             # the planner reserves z at the top of the scratch region; the plan
             # shown is that of the all-reduce form of the same shape
         kernel = kernel_name(plan) + ("+rmsnorm_rows_kernel<z>" if kind == "gemv_rmsnorm" else "")
@@ -385,11 +402,15 @@ def make_case(args, w, local_rank, stream):
             "ws": ws, "W": W, "copies": copies, "per_copy": W.nbytes, "kernel": kernel,
             "step": lambda i: ws.run(stream, copy=i % copies, mode=mode, eps=eps),
             "run0": lambda: ws.run(stream, copy=0, mode=mode, eps=eps),
+            "ws_rm": ws_rm,
+            "rm_step": (None if ws_rm is None else lambda i: ws_rm.run(stream, copy=i % copies, mode=mode, eps=eps)),
             # e2e: per-step inputs are x_r (W_r are resident model weights); result y
             "in_host": _pinned(x), "in_dst": ws.x_ptr(), "in_bytes": ws.x_bytes,
             "out_src": ws.y_ptr(), "out_bytes": out_rows * N * 2,
             "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
             "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
+                       "w_layout": ("packed (symm_pack_w once at load, untimed; the same bytes per call)"
+                                    if ws.packed else "row-major N x K/R per slot"),
                        "chain_option": bool(args.chain),
                        **({"eps": eps, "norm_pdl": args.norm_pdl} if kind == "gemv_rmsnorm" else {})},
         }
@@ -506,6 +527,16 @@ def run_ours(args, rank, world, local_rank):
     code, _, _ = csg.symm_status(ws.h, stream)
     if code != csg.SYMM_OK:
         raise SystemExit(f"protocol error in the timed region: {csg.symm_last_error()}")
+    row_major = None
+    if c.get("rm_step") is not None:
+        # the same calls on the row-major weights (chained like the main leg)
+        rm_step_ms, rm_launch, _ = timed_loop(c["rm_step"], args.steps, args.warmup, stream, dev, world, flush_buf,
+                                              gpu_id, per_launch=not chained)
+        code, _, _ = csg.symm_status(c["ws_rm"].h, stream)
+        if code != csg.SYMM_OK:
+            raise SystemExit(f"protocol error in the row-major leg: {csg.symm_last_error()}")
+        row_major = statistics.mean(rm_launch)
+        c["ws_rm"].close()
 
     # ---- e2e: the same call through the ABI with host buffers every step ----
     # Each step: one strided copy of the step's inputs from pinned host memory
@@ -568,15 +599,23 @@ def run_ours(args, rank, world, local_rank):
         ew_steps = max(3, min(args.steps, 10))
         torch.cuda.synchronize(dev)
         tt = time.perf_counter()
+        if ws.packed:   # the row-major weights into the staging copy, then packed, every step
+            def put_w():
+                csg.symm_copy_to_slots(ws.h, ws.W_rowmajor_ptr(), W_host.data_ptr(), w_bytes, R, stream)
+                ws.pack(0, stream)
+        else:
+            def put_w():
+                csg.symm_copy_to_slots(ws.h, ws.W_ptr(0), W_host.data_ptr(), w_bytes, R, stream)
         for i in range(ew_steps):
-            e2e_step(lambda: csg.symm_copy_to_slots(ws.h, ws.W_ptr(0), W_host.data_ptr(), w_bytes, R, stream))
+            e2e_step(put_w)
         ew = (time.perf_counter() - tt) * 1e3 / ew_steps
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
 
-    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms = max_over_ranks(
+    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms, rm_ms = max_over_ranks(
         [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms),
-         unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0, e2e_graph_ms], world, dev)
+         unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0, e2e_graph_ms,
+         row_major if row_major is not None else 0.0], world, dev)
     ws.close()
     if rank != 0:
         return None
@@ -652,11 +691,20 @@ def run_ours(args, rank, world, local_rank):
             "achieved": round(nbytes / (u_launch_ms * 1e-3) / 1e9, 1),
             "frac": round(nbytes / (u_launch_ms * 1e-3) / 1e9 / peak, 4),
         }
+    if row_major is not None:
+        line["row_major_w"] = {
+            "what": "the same calls with W_r row-major (no symm_pack_w), timed like the main leg",
+            "us_per_call": round(rm_ms * 1e3, 3),
+            "achieved": round(nbytes / (rm_ms * 1e-3) / 1e9, 1),
+            "frac": round(nbytes / (rm_ms * 1e-3) / 1e9 / peak, 4),
+        }
     if ew is not None:
         line["e2e_weights_from_host"] = {
             "value": round(throughput_gbs(nbytes, ew_ms, world), 2), "unit": "GB/s",
             "us_per_call": round(ew_ms * 1e3, 2),
             "h2d_bytes_per_step": W.nbytes + h2d, "d2h_bytes_per_step": out_bytes,
+            "what": ("the e2e step with every rank's W_r copied from pinned host memory into the slots as well"
+                     + (", then packed (symm_pack_w)" if ws.packed else "")),
         }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op)
@@ -792,6 +840,9 @@ def parse_args(argv=None):
                    help="TMA kernels: resident CTAs per SM (0 = library default)")
     p.add_argument("--sk-grid", type=int, default=0,
                    help="stream-K grid: 0 library default, -S = S CTAs per (tile, rank), or a count")
+    p.add_argument("--w-layout", choices=("packed", "row_major"), default="packed",
+                   help="GEMV weights: packed (symm_pack_w, where the call runs on the persistent kernel) or "
+                        "row-major")
     p.add_argument("--dyn-splits", type=int, default=0,
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),

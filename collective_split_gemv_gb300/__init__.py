@@ -52,7 +52,7 @@ EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce
             "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "gemv_reduce_scatter",
             "gemv_all_reduce_bias_rmsnorm", "reduce_scatter", "two_shot_all_reduce",
             "all_reduce_bias_rmsnorm", "tile_reduce", "multi_root_tile_reduce", "symm_copy_to_slots",
-            "symm_copy_from_slots", "symm_free",
+            "symm_copy_from_slots", "symm_packed_w_bytes", "symm_pack_w", "symm_release_w", "symm_free",
             "symm_last_error")
 
 _lib = None
@@ -110,6 +110,9 @@ def lib() -> ctypes.CDLL:
         L.multi_root_tile_reduce.argtypes = [vp, ctypes.POINTER(vp), vp, ctypes.POINTER(i), i, i, i, ll, ll, vp]
         L.symm_copy_to_slots.argtypes = [vp, vp, vp, sz, i, vp]
         L.symm_copy_from_slots.argtypes = [vp, vp, vp, sz, i, vp]
+        L.symm_packed_w_bytes.argtypes = [i, i, i, ctypes.POINTER(sz)]
+        L.symm_pack_w.argtypes = [vp, vp, vp, i, i, i, vp]
+        L.symm_release_w.argtypes = [vp, vp]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
         L.symm_last_error.restype = ctypes.c_char_p
@@ -226,6 +229,22 @@ def symm_copy_from_slots(h, dst: int, src: int, bytes_per_rank: int, nranks: int
     _check(lib().symm_copy_from_slots(h, _vp(dst), _vp(src), bytes_per_rank, nranks, _stream(stream)))
 
 
+def symm_packed_w_bytes(R: int, N: int, K: int) -> int:
+    """Bytes per slot of the packed form of an N x (K/R) W_r."""
+    out = ctypes.c_size_t()
+    _check(lib().symm_packed_w_bytes(R, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def symm_pack_w(h, W_r: int, Wp: int, R: int, N: int, K: int, stream=None) -> None:
+    """Packs every slot's row-major W_r into Wp and registers Wp with the handle."""
+    _check(lib().symm_pack_w(h, _vp(W_r), _vp(Wp), R, N, K, _stream(stream)))
+
+
+def symm_release_w(h, Wp: int) -> None:
+    _check(lib().symm_release_w(h, _vp(Wp)))
+
+
 def symm_status(h, stream=None):
     """-> (code, rank, tile); code is SYMM_OK or SYMM_EPROTO."""
     code, rank, tile = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
@@ -258,7 +277,6 @@ def symm_gemv_plan(h, N: int, K: int, B: int) -> dict:
     plan = GemvPlan()
     _check(lib().symm_gemv_plan(h, N, K, B, ctypes.byref(plan)))
     return {k: getattr(plan, k) for k, _ in GemvPlan._fields_}
-
 
 
 def gemv_all_reduce_noalloc(W_r: int, x_r: int, y: int, stride: int, R: int, N: int, K: int, B: int,

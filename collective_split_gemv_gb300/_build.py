@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsymm_gemv.so")
 
 SOURCES = ["symm_runtime.cu", "allreduce.cu", "gemv_ffma.cu", "gemv_tc.cu", "gemv_sk.cu", "gemv_dyn.cu", "gemv_noalloc.cu",
-           "tile_reduce.cu", "rmsnorm.cu", "copy_slots.cu"]
+           "tile_reduce.cu", "rmsnorm.cu", "copy_slots.cu", "pack_w.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-Xptxas", "-warn-spills", "-I", INCLUDE]

@@ -26,7 +26,9 @@
 // Roles (192 threads):
 //   warp 0, lane 0  draws units, issues the TMA loads of each unit's K blocks
 //                   (W 128 rows x 64*kSlabs, x 16 rows x 64*kSlabs, 128-byte
-//                   swizzle) and tags every stage with (unit, block);
+//                   swizzle; W of a packed weight as kSlabs contiguous 16 KB
+//                   blocks already in that byte order) and tags every stage
+//                   with (unit, block);
 //   warp 1          tcgen05 engine: TMEM owner; lane 0 issues the MMAs of each
 //                   stage and, at a unit's last block, hands the accumulator
 //                   and the unit id to the epilogue;
@@ -194,6 +196,23 @@ __device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float
     return acc;
 }
 
+static_assert(kM == kPackRows && kSlabA == (int)kPackBlockBytes, "a stage slab is one block of the packed layout");
+
+// W slab j (64 columns) of row tile t, rank r, into one stage slab: a TMA box
+// of the row-major W_r, or the same bytes as one contiguous block of the
+// packed layout (past the last slab: the slot's zero block, as the tensor
+// map's fill would give).
+__device__ __forceinline__ void load_w_slab(uint8_t *dst, const CUtensorMap *tmW, const GemvArgs &a, uint64_t *bar,
+                                            int j, int t, int r) {
+    if (a.w_packed) {
+        const int J = (a.Kr + kPackCols - 1) / kPackCols;
+        const size_t blk = j < J ? (size_t)t * J + j : (size_t)a.num_tiles * J;
+        bulk_load(dst, a.W + (long long)r * a.stride + blk * kPackBlockBytes, (uint32_t)kPackBlockBytes, bar);
+    } else {
+        tma_load_3d(dst, tmW, bar, j * 64, t * kM, r);
+    }
+}
+
 template <int kEngine, int kSlabs, int kB, int kCps>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *dst = smem + (size_t)i * kStageBytes;
 #pragma unroll
             for (int s = 0; s < kSlabs; ++s)
-                tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[i], kb * kBK + s * 64, t * kM, r);
+                load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[i], kb * kSlabs + s, t, r);
         }
         griddep_wait();
         for (int i = 0; i < pre; ++i) {
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst = smem + (size_t)st * kStageBytes;
 #pragma unroll
                     for (int s = 0; s < kSlabs; ++s)
-                        tma_load_3d(dst + s * kSlabA, &tmW, &full_bar[st], kb * kBK + s * 64, t * kM, r);
+                        load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[st], kb * kSlabs + s, t, r);
 #pragma unroll
                     for (int s = 0; s < kSlabs; ++s)
                         tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0,

@@ -96,6 +96,7 @@ struct GemvArgs {
     int rs_rows;             // kOutReduceScatter: B / R
     float *z;                // kOutBiasZ: fp32 [B][N]
     const uint8_t *bias;     // kOutBiasZ: bf16 [N] (slot 0) or nullptr
+    int w_packed;            // persistent kernel: W is in the packed layout (below), not [N][Kr]
 };
 constexpr int kOutAllReduce = 0, kOutReduceScatter = 1, kOutBiasZ = 2;
 
@@ -187,6 +188,26 @@ struct CopySlotsArgs {
     int chained;             // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_copy_slots(const CopySlotsArgs &a, cudaStream_t s);
+
+// Packed weight layout (symm_pack_w): W_r cut into 128-row x 64-column
+// blocks, block (t, j) = rows 128t.., columns 64j.. stored as 16 KB at
+// ((t * J + j) * 16 KB), J = ceil(Kr / 64), in the byte order a TMA load with
+// 128-byte swizzle leaves the same box in shared memory: row i at i * 128,
+// its 16-byte chunk c at chunk position c ^ (i % 8).  Rows past N and
+// columns past Kr are zero, and one more all-zero block follows the last
+// (the persistent kernel reads it for the stage slabs past Kr).
+constexpr int kPackRows = 128, kPackCols = 64;
+constexpr size_t kPackBlockBytes = (size_t)kPackRows * kPackCols * 2;
+inline size_t packed_w_blocks(int N, int Kr) {
+    return (size_t)((N + kPackRows - 1) / kPackRows) * (size_t)((Kr + kPackCols - 1) / kPackCols) + 1;
+}
+struct PackWArgs {
+    const uint8_t *W;        // bf16 [N][Kr], slot 0
+    uint8_t *Wp;             // packed, slot 0
+    long long stride;
+    int R, N, Kr;
+};
+cudaError_t launch_pack_w(const PackWArgs &a, cudaStream_t s);
 
 // FFMA (CUDA-core) fused kernel: any B in 1..16.
 int ffma_rows_per_tile(int B);

@@ -1,5 +1,5 @@
 // Inline-PTX building blocks for sm_100-family kernels (GB300, sm_103a):
-// mbarriers with bounded waits, TMA tensor loads, TMEM allocation, tcgen05
+// mbarriers with bounded waits, TMA tensor and bulk loads, TMEM allocation, tcgen05
 // MMA / commit / load, and the shared-memory matrix descriptor for 128-byte
 // swizzled K-major operand tiles.
 #pragma once
@@ -62,6 +62,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "[%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Contiguous global -> shared copy completing on an mbarrier (both addresses
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst_smem)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t cols) {

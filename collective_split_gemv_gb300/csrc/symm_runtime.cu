@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "../../include/symm_gemv.h"
 #include "internal.h"
@@ -62,6 +63,13 @@ struct symm_handle {
     };
     MapEntry map_cache[8];
     int map_next = 0;
+    // Packed weights made by symm_pack_w: slot-0 address, shape, bytes per slot.
+    struct PackedW {
+        const void *p = nullptr;
+        int N = 0, Kr = 0;
+        size_t bytes = 0;
+    };
+    std::vector<PackedW> packed;
 };
 
 namespace {
@@ -147,6 +155,12 @@ void note_write(symm_handle *h, const void *p, size_t bytes) {
     h->last_write_bytes = bytes;
 }
 
+const symm_handle::PackedW *find_packed(const symm_handle *h, const void *p) {
+    for (const auto &e : h->packed)
+        if (e.p == p) return &e;
+    return nullptr;
+}
+
 // Zero flags, counters, the work counters and the launch epoch
 // (stream-ordered): the pad as symm_alloc leaves it.
 int reset_protocol(symm_handle *h, cudaStream_t s) {
@@ -196,9 +210,9 @@ int gemv_path(const symm_handle *h, int N, int B, int Kr) {
     return kPathDyn;
 }
 
-int rows_per_tile_for(const symm_handle *h, int N, int B, int Kr) {
+int rows_per_tile_for_path(int path, int B) {
     if (B < 1 || B > SYMM_MAX_BATCH) return 0;
-    switch (gemv_path(h, N, B, Kr)) {
+    switch (path) {
         case kPathFfma: return ffma_rows_per_tile(B);
         case kPathTc: return kTcRows;
         case kPathSk: return kTcRows;
@@ -292,12 +306,19 @@ struct Plan {
 
 // `cap`: scratch bytes per slot the partials may use (the whole region, or
 // less when part of it is reserved for the bias + RMSNorm stage's z).
-int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap) {
+// `packed`: W is a packed weight, which only the persistent kernel reads
+// (a call with K = 0 reads no W and keeps its path).
+int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, bool packed = false) {
     if ((size_t)B * (size_t)N * 4 > cap)
         return fail(SYMM_ERANGE, "partials need %zu scratch bytes per slot, %zu available",
                     (size_t)B * (size_t)N * 4, cap);
     pl->path = gemv_path(h, N, B, Kr);
-    pl->rows = rows_per_tile_for(h, N, B, Kr);
+    if (packed && Kr > 0) {
+        if (h->opt_gemv_path != 0 && h->opt_gemv_path != kPathDyn)
+            return fail(SYMM_EINVAL, "a packed weight is read by the persistent kernel (path 4) only");
+        pl->path = kPathDyn;
+    }
+    pl->rows = rows_per_tile_for_path(pl->path, B);
     if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     pl->tiles = (N + pl->rows - 1) / pl->rows;
     if (pl->tiles > h->max_tiles)
@@ -391,12 +412,17 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
         if (N > rmsnorm_max_h()) return fail(SYMM_EINVAL, "bias + RMSNorm supports N <= %d", rmsnorm_max_h());
         if (!(ep.eps >= 0.f) || ep.eps > 3.0e38f) return fail(SYMM_EINVAL, "eps must be finite and >= 0");
     }
+    const symm_handle::PackedW *pw = find_packed(h, W_r);
+    if (pw && (pw->N != N || pw->Kr != Kr))
+        return fail(SYMM_EINVAL, "W_r is a packed weight of N=%d K/R=%d, called with N=%d K/R=%d", pw->N, pw->Kr, N,
+                    Kr);
     if (N == 0 || B == 0) return SYMM_OK;
-    const size_t wbytes = (size_t)N * (size_t)Kr * 2;
+    const size_t wbytes = pw ? pw->bytes : (size_t)N * (size_t)Kr * 2;
     const size_t xbytes = (size_t)B * (size_t)Kr * 2;
     const size_t ybytes = (size_t)(ep.mode == kOutReduceScatter ? B / R : B) * (size_t)N * 2;
     const size_t vbytes = (size_t)N * 2;
-    if (!in_user_region(h, W_r, wbytes)) return fail(SYMM_EINVAL, "W_r (N x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, W_r, wbytes))
+        return fail(SYMM_EINVAL, "W_r (N x K/R bf16, or its packed layout) is not inside slot 0's user region");
     if (!in_user_region(h, x_r, xbytes)) return fail(SYMM_EINVAL, "x_r (B x K/R bf16) is not inside slot 0's user region");
     if (!in_user_region(h, y, ybytes)) return fail(SYMM_EINVAL, "y is not inside slot 0's user region");
     if (!aligned16(W_r) || !aligned16(x_r) || !aligned16(y)) return fail(SYMM_EINVAL, "W_r, x_r and y must be 16-byte aligned");
@@ -419,7 +445,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
         cap = z_off;
     }
     Plan pl;
-    int rc = make_plan(h, N, Kr, B, &pl, cap);
+    int rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
     if (rc != SYMM_OK) return rc;
     const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
               slabs = pl.slabs, cps = pl.cps;
@@ -460,6 +486,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.rs_rows = ep.mode == kOutReduceScatter ? B / R : B;
     a.z = ep.mode == kOutBiasZ ? reinterpret_cast<float *>(h->base + h->scratch_off + z_off) : nullptr;
     a.bias = ep.mode == kOutBiasZ ? static_cast<const uint8_t *>(ep.bias) : nullptr;
+    a.w_packed = pw != nullptr && path == kPathDyn;
     cudaError_t e = cudaSuccess;
     switch (path) {
         case kPathFfma:
@@ -717,6 +744,69 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
 int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,
                     symm_stream_t stream) {
     return gemv_common(h, W_r, x_r, y, R, N, K, B, stream, Epilogue());
+}
+
+int symm_packed_w_bytes(int R, int N, int K, size_t *bytes_out) {
+    if (!bytes_out) return fail(SYMM_EINVAL, "bytes_out is NULL");
+    if (R < 1 || R > SYMM_MAX_RANKS) return fail(SYMM_EINVAL, "R=%d outside 1..%d", R, SYMM_MAX_RANKS);
+    if (N < 0 || K < 0) return fail(SYMM_EINVAL, "N=%d K=%d must be >= 0", N, K);
+    if (K % R) return fail(SYMM_EINVAL, "K=%d is not a multiple of R=%d", K, R);
+    if ((K / R) % 8) return fail(SYMM_EINVAL, "K/R=%d is not a multiple of 8", K / R);
+    *bytes_out = packed_w_blocks(N, K / R) * kPackBlockBytes;
+    return SYMM_OK;
+}
+
+int symm_pack_w(symm_handle_t *h, const void *W_r, void *Wp, int R, int N, int K, symm_stream_t stream) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
+    size_t pbytes = 0;
+    int rc = symm_packed_w_bytes(R, N, K, &pbytes);
+    if (rc != SYMM_OK) return rc;
+    const int Kr = K / R;
+    const size_t wbytes = (size_t)N * (size_t)Kr * 2;
+    if (!in_user_region(h, W_r, wbytes)) return fail(SYMM_EINVAL, "W_r (N x K/R bf16) is not inside slot 0's user region");
+    if (!in_user_region(h, Wp, pbytes))
+        return fail(SYMM_EINVAL, "Wp (%zu packed bytes per slot) is not inside slot 0's user region", pbytes);
+    if (!aligned16(W_r) || !aligned16(Wp)) return fail(SYMM_EINVAL, "W_r and Wp must be 16-byte aligned");
+    if (overlaps(W_r, wbytes, Wp, pbytes)) return fail(SYMM_EINVAL, "W_r and Wp overlap");
+    if (find_packed(h, W_r) && wbytes > 0) return fail(SYMM_EINVAL, "W_r is itself a packed weight");
+    rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
+    PackWArgs a;
+    a.W = static_cast<const uint8_t *>(W_r);
+    a.Wp = static_cast<uint8_t *>(Wp);
+    a.stride = (long long)h->stride;
+    a.R = h->R;
+    a.N = N;
+    a.Kr = Kr;
+    cudaError_t e = launch_pack_w(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "symm_pack_w launch");
+    note_write(h, Wp, pbytes);
+    // Wp's bytes now belong to this weight alone: earlier packed weights it
+    // overlaps are gone.
+    auto &v = h->packed;
+    v.erase(std::remove_if(v.begin(), v.end(),
+                           [&](const symm_handle::PackedW &q) { return overlaps(q.p, q.bytes, Wp, pbytes); }),
+            v.end());
+    symm_handle::PackedW q;
+    q.p = Wp;
+    q.N = N;
+    q.Kr = Kr;
+    q.bytes = pbytes;
+    v.push_back(q);
+    return SYMM_OK;
+}
+
+int symm_release_w(symm_handle_t *h, const void *Wp) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    auto &v = h->packed;
+    for (auto it = v.begin(); it != v.end(); ++it) {
+        if (it->p == Wp) {
+            v.erase(it);
+            return SYMM_OK;
+        }
+    }
+    return fail(SYMM_EINVAL, "%p is not a packed weight of this handle", Wp);
 }
 
 int gemv_reduce_scatter(symm_handle_t *h, const void *W_r, const void *x_r, void *y, int R, int N, int K, int B,

@@ -3,8 +3,10 @@
 A workspace allocates one handle whose user region holds, at the same offsets
 in every rank's slot, ``copies`` instances of W_r (so that a timing loop can
 rotate through more bytes than L2 holds), x_r and y, and stages host data into
-and out of the slots with PyTorch copies.  The computation itself is the
-library call (``run``); PyTorch only moves bytes.
+and out of the slots with PyTorch copies.  With ``packed`` the instances of
+W_r are packed weights (``symm_pack_w``), made from one row-major staging
+copy.  The computation itself is the library call (``run``); PyTorch only
+moves bytes.
 """
 from __future__ import annotations
 
@@ -13,7 +15,7 @@ import torch
 
 from . import (DeviceView, all_reduce_bias_rmsnorm, gemv_all_reduce, gemv_all_reduce_bias_rmsnorm,
                gemv_reduce_scatter, multi_root_tile_reduce, one_shot_all_reduce, reduce_scatter, symm_alloc,
-               symm_free, symm_rendezvous, two_shot_all_reduce)
+               symm_free, symm_pack_w, symm_packed_w_bytes, symm_rendezvous, two_shot_all_reduce)
 
 ALIGN = 256
 
@@ -30,20 +32,28 @@ def pad_bytes_for(N: int, min_rows: int = 8) -> int:
 
 
 class GemvWorkspace:
-    def __init__(self, R: int, N: int, K: int, B: int, copies: int = 1, device: int | None = None):
+    def __init__(self, R: int, N: int, K: int, B: int, copies: int = 1, device: int | None = None,
+                 packed: bool = False):
         if K % R:
             raise ValueError("K must be a multiple of R")
         self.R, self.N, self.K, self.B, self.Kr = R, N, K, B, K // R
         self.copies = copies
+        self.packed = packed
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.w_bytes = N * self.Kr * 2
+        self.wp_bytes = symm_packed_w_bytes(R, N, K) if packed else 0
         self.x_bytes = B * self.Kr * 2
         self.y_bytes = B * N * 2
         off = 0
+        # row-major W_r: the instances, or (packed) the one staging copy
         self.w_off = []
-        for _ in range(copies):
+        for _ in range(1 if packed else copies):
             self.w_off.append(off)
             off += _up(max(self.w_bytes, 1))
+        self.wp_off = []
+        for _ in range(copies if packed else 0):
+            self.wp_off.append(off)
+            off += _up(self.wp_bytes)
         self.x_off = off
         off += _up(max(self.x_bytes, 1))
         self.y_off = off
@@ -82,11 +92,19 @@ class GemvWorkspace:
         return torch.from_numpy(np.ascontiguousarray(a)).view(torch.uint8).reshape(-1)
 
     def load_W(self, W: np.ndarray, copy: int = 0) -> None:
+        """W (R, N, K/R) bf16 words into instance `copy` (packed: through the
+        staging copy, then symm_pack_w on the current stream)."""
         assert W.shape == (self.R, self.N, self.Kr) and W.dtype == np.uint16
-        if self.w_bytes == 0:
-            return
-        for r in range(self.R):
-            self.w_view(r, copy).copy_(self._bytes(W[r]))
+        if self.w_bytes > 0:
+            for r in range(self.R):
+                self.w_view(r, 0 if self.packed else copy).copy_(self._bytes(W[r]))
+        if self.packed:
+            self.pack(copy)
+
+    def pack(self, copy: int = 0, stream=None) -> None:
+        """Packs the row-major staging copy into packed instance `copy`."""
+        symm_pack_w(self.h, self.base + self.w_off[0], self.base + self.wp_off[copy], self.R, self.N, self.K,
+                    torch.cuda.current_stream(self.device) if stream is None else stream)
 
     def load_x(self, x: np.ndarray) -> None:
         assert x.shape == (self.R, self.B, self.Kr) and x.dtype == np.uint16
@@ -116,7 +134,12 @@ class GemvWorkspace:
 
     # --------------------------------------------------------------- run
     def W_ptr(self, copy: int = 0) -> int:
-        return self.base + self.w_off[copy]
+        """Instance `copy` of W_r as the fused calls take it (packed or row-major)."""
+        return self.base + (self.wp_off[copy] if self.packed else self.w_off[copy])
+
+    def W_rowmajor_ptr(self) -> int:
+        """The row-major W_r (packed workspaces: the staging copy)."""
+        return self.base + self.w_off[0]
 
     def x_ptr(self) -> int:
         return self.base + self.x_off

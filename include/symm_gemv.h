@@ -170,7 +170,10 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
  *     y_s[b][n] = bf16_rne( sum_{r=0}^{R-1} sum_{k<K/R} W_r[n][k] x_r[b][k] )
  *
  * for every rank s, fp32 accumulation, ranks summed in order 0..R-1.
- *   W_r  symmetric bf16 pointer; rank r's N x (K/R) row-major column block.
+ *   W_r  symmetric bf16 pointer; rank r's N x (K/R) row-major column block,
+ *        or a packed weight of this N and K made by symm_pack_w (the same
+ *        values in the layout the fused kernel streams fastest; the call's
+ *        results are bitwise those of the row-major form).
  *   x_r  symmetric bf16 pointer; rank r's B x (K/R) row-major activations.
  *   y    symmetric bf16 pointer; B x N row-major output, written in every slot.
  *   R    must equal the handle's rank count.
@@ -230,6 +233,43 @@ int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t byte
                        symm_stream_t stream);
 int symm_copy_from_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
                          symm_stream_t stream);
+
+/*
+ * Packed weights -- a second layout for the W_r of the fused calls
+ * (gemv_all_reduce, gemv_reduce_scatter, gemv_all_reduce_bias_rmsnorm), made
+ * once when the weights are loaded.  The pages fix no layout for the weight
+ * shards; this one lets the fused kernel stream each 128-row x 64-column
+ * block of W_r as one contiguous 16 KB read instead of 128 rows of 128 bytes
+ * (measured faster on every shape; the bytes read per call are the same).
+ *
+ * symm_packed_w_bytes -- bytes per slot of the packed form of an N x (K/R)
+ * W_r: (ceil(N/128) * ceil((K/R)/64) + 1) * 16384.  Same K, R rules as
+ * gemv_all_reduce.  Errors: SYMM_EINVAL.
+ *
+ * symm_pack_w -- for every slot r, writes the packed form of the row-major
+ * W_r (+ r * stride) into Wp (+ r * stride) and registers Wp with the handle
+ * for this N and K.  Layout: block (t, j) covers rows 128t.. and columns
+ * 64j.. and sits at byte (t * ceil((K/R)/64) + j) * 16384; inside it, row i
+ * starts at i * 128 and its 16-byte chunk c (elements 8c..8c+7) is stored at
+ * chunk position c XOR (i mod 8); rows past N and columns past K/R are zero;
+ * one all-zero block follows the last.
+ *   W_r, Wp  symmetric pointers, 16-byte aligned inside slot 0's user region;
+ *            they must not overlap; W_r must not itself be a packed weight.
+ * A fused call whose W_r equals a registered Wp reads it packed; it must use
+ * the same N and K (else SYMM_EINVAL) and runs on the persistent kernel
+ * (SYMM_OPT_GEMV_PATH 0 or 4, else SYMM_EINVAL).  The registration ends with
+ * symm_release_w, with a later symm_pack_w whose Wp range overlaps it, or with
+ * symm_free; writing other data into Wp does not end it.
+ * Stream-ordered (the W_r it reads may be written by earlier work on the
+ * stream); returns after enqueueing.  Errors: SYMM_EINVAL, SYMM_ECUDA.
+ *
+ * symm_release_w -- forget the packed weight registered at Wp (its bytes are
+ * untouched; a later fused call with W_r == Wp reads them row-major).
+ * Errors: SYMM_EINVAL (no packed weight registered at Wp).
+ */
+int symm_packed_w_bytes(int R, int N, int K, size_t *bytes_out);
+int symm_pack_w(symm_handle_t *h, const void *W_r, void *Wp, int R, int N, int K, symm_stream_t stream);
+int symm_release_w(symm_handle_t *h, const void *Wp);
 
 /*
  * symm_check_guards -- verify the guard bands around every slot's user

@@ -93,11 +93,29 @@ def test_null_handle_is_rejected(lib):
                  lambda: csg.tile_reduce(None, 0, 0, 0, 4, 4, 4, 4),
                  lambda: csg.multi_root_tile_reduce(None, [0], 0, [0], 4, 4, 4, 4),
                  lambda: csg.symm_copy_to_slots(None, 0, 0, 16, 1),
-                 lambda: csg.symm_copy_from_slots(None, 0, 0, 16, 1)):
+                 lambda: csg.symm_copy_from_slots(None, 0, 0, 16, 1),
+                 lambda: csg.symm_pack_w(None, 0, 0, 2, 8, 16),
+                 lambda: csg.symm_release_w(None, 0)):
         with pytest.raises(csg.SymmError) as e:
             call()
         assert e.value.code == csg.SYMM_EINVAL
     csg.symm_free(None)   # freeing NULL is a no-op
+
+
+@pytest.mark.parametrize("R,N,K", [(1, 1, 8), (2, 128, 128), (2, 129, 144), (8, 8192, 28672), (4, 0, 64),
+                                   (3, 7, 0), (8, 16384, 53248)])
+def test_packed_weight_size(lib, R, N, K):
+    # one 16 KB block per 128 rows x 64 columns of W_r, rounded up, plus the zero block
+    Kr = K // R
+    blocks = ((N + 127) // 128) * ((Kr + 63) // 64) + 1
+    assert csg.symm_packed_w_bytes(R, N, K) == blocks * 16384
+
+
+@pytest.mark.parametrize("args", [(0, 8, 8), (65, 8, 8), (2, -1, 16), (2, 8, -2), (2, 8, 9), (2, 8, 12)])
+def test_packed_weight_size_rejects(lib, args):
+    with pytest.raises(csg.SymmError) as e:
+        csg.symm_packed_w_bytes(*args)
+    assert e.value.code == csg.SYMM_EINVAL
 
 
 def test_alloc_without_gpu_reports_cuda_error(lib):

@@ -449,8 +449,10 @@ typedef struct {
 int symm_info(symm_handle_t *h, symm_info_t *info);
 
 /* The kernel and launch geometry gemv_all_reduce would use for (N, K, B) on
- * this handle, without launching anything (SYMM_EINVAL / SYMM_ERANGE exactly
- * as the call would return them).
+ * this handle with a row-major W_r, without launching anything (SYMM_EINVAL /
+ * SYMM_ERANGE exactly as the call would return them).  A call on a packed
+ * weight (symm_pack_w) runs path 4 with the plan reported while
+ * SYMM_OPT_GEMV_PATH is 4.
  *   path           1 CUDA-core, 2 tensor-core per tile, 3 stream-K, 4 persistent dynamic
  *   engine         stream-K compute engine: 0 tcgen05, 1 FFMA
  *   slabs          stream-K 64-column slabs per pipeline stage

@@ -47,6 +47,10 @@
  *    are shared by every launch on the handle.  Overlapping launches on the
  *    same handle are detected (SYMM_EPROTO in symm_status) rather than hung:
  *    no kernel in this library waits on another CTA.
+ *  - A handle's host-side state (options, the output range of the last call,
+ *    packed-weight registrations, cached tensor maps) is not locked: use a
+ *    handle from one host thread at a time.  Different handles are
+ *    independent.
  *  - Device memory ownership: the library owns what symm_alloc allocates
  *    (backing == NULL) and frees it in symm_free; borrowed backing memory
  *    stays the caller's and must outlive the handle.

@@ -707,32 +707,41 @@ def run_ours(args, rank, world, local_rank):
                      + (", then packed (symm_pack_w)" if ws.packed else "")),
         }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op)
+        cb = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op)
+        if cb["cores"] > 1:   # the same oracle on one core, a shorter sample
+            one = cpu_baseline(args.workload, budget_s=min(args.cpu_seconds, 4.0), ar_op=args.ar_op, threads=1)
+            cb["one_thread"] = {k: one[k] for k in ("value", "unit", "us_per_call_equiv", "cores", "sample")}
+        line["cpu_baseline"] = cb
     return line
 
 
 # ------------------------------------------------------------ CPU oracle
 
 
-def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot"):
+def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", threads=None):
     """Time the oracle (as it is) on this host's cores on the workload: with
     `steps` None, repeat the full call for about `budget_s` seconds; else run
     exactly `steps` calls, each on a row sample sized so that all of them fit
     in about `budget_s`.  Returns the cpu_baseline object (GB/s of algorithmic
-    bytes, the time scaled to a full call)."""
+    bytes, the time scaled to a full call).  `threads`: the oracle's threads
+    where it is multithreaded (None: every host core); `cores` in the result
+    is what the call actually used."""
     import numpy as np
 
     import oracle
     import synth
 
     w = workload(name)
-    threads = host_cores()
+    threads = host_cores() if threads is None else threads
+    used = threads
     nbytes = workload_bytes(w, ar_op)
     kind, R = w["kind"], w["R"]
     if kind == "allreduce":
         inp = synth.allreduce_inputs(R, w["n"], w["seed"])
         full = inp.shape[1]
         if ar_op == "reduce_scatter":
+            used = 1    # single-threaded oracle function
+
             def call(rows):
                 m = max(R, rows // R * R)
                 oracle.reduce_scatter(np.ascontiguousarray(inp[:, :m]))
@@ -743,11 +752,13 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot"):
     elif kind == "ar_rmsnorm":
         inp, bias, gamma = synth.rmsnorm_inputs(R, w["rows"], w["H"], w["seed"])
         full = w["rows"]
+        used = 1
 
         def call(rows):
             oracle.all_reduce_bias_rmsnorm(np.ascontiguousarray(inp[:, :rows]), bias, gamma, w["eps"])
         unit = "rows"
     elif kind == "tile":
+        used = 1
         h = w["rows"] // 2
         full_t = synth.tile_inputs(R, w["rows"], w["cols"], w["seed"])
         flat = full_t.reshape(R, -1)
@@ -795,7 +806,7 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot"):
         "value": round(nbytes / sec_per_call / 1e9, 4),
         "unit": "GB/s",
         "us_per_call_equiv": round(sec_per_call * 1e6, 1),
-        "cores": threads,
+        "cores": used,
         "kind": "oracle",
         "sample": (f"{rows} of {full} {unit} of {name}, {reps} repetitions, {el:.1f} s of CPU time; "
                    "time scaled to the full call"),

@@ -1,7 +1,8 @@
 // Persistent, dynamically scheduled fused GEMV + one-shot all-reduce: one or
 // more CTAs per SM draw whole (row tile, rank) units from an atomic work
 // counter and stream them through a TMA ring into the tcgen05 tensor cores
-// (wider batches) or into CUDA-core FFMA (B <= 2).
+// (the automatic choice at every batch width) or into CUDA-core FFMA (an
+// option for B <= 2).
 //
 // Why this shape: W is read exactly once, so the kernel is bound by HBM, and
 // what costs time besides bytes is (a) a CTA's start-up and wind-down, which

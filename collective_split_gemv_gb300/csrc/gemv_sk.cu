@@ -1,5 +1,5 @@
 // Persistent stream-K fused GEMV + one-shot all-reduce: a TMA ring feeding
-// either the tcgen05 tensor cores (wider batches) or CUDA-core FFMA (B <= 2),
+// either the tcgen05 tensor cores or (an option for B <= 2) CUDA-core FFMA,
 // one CTA per SM.
 //
 // Work decomposition.  A unit is one (row tile t of 128 rows, rank r) pair,

@@ -189,10 +189,13 @@ int num_sms(int device) {
 // 2 tensor-core, one CTA per (tile, rank, K-split); 3 stream-K (TMA ring,
 // static partition of the K blocks); 4 persistent CTAs drawing (tile, rank)
 // units from a work counter (TMA ring, double-buffered accumulator).  Paths
-// 3 and 4 run the tcgen05 engine, or the FFMA engine for B <= kSkFfmaMaxBatch.
-// The automatic choice is 4 whenever K > 0 (1 for K = 0), with two CTAs per
-// SM and two 64-column slabs per stage: the fastest configuration measured on
-// the decode (B = 1), attention-projection (B = 8) and large (B = 16) shapes.
+// 3 and 4 run the tcgen05 engine, or (as an option) the FFMA engine for
+// B <= kSkFfmaMaxBatch.  The automatic choice is 4 whenever K > 0 (1 for
+// K = 0, and for small W, below), with two CTAs per SM, two 64-column slabs
+// per stage and the tcgen05 engine at every batch width: the fastest
+// configuration measured on the decode (B = 1), attention-projection (B = 8)
+// and large (B = 16) shapes, and tcgen05 beat FFMA at B = 1 and 2 on every
+// shape measured (34 MB to 1.7 GB of W, packed or row-major).
 constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3, kPathDyn = 4;
 constexpr int kSkFfmaMaxBatch = 2;
 
@@ -223,7 +226,7 @@ int rows_per_tile_for_path(int path, int B) {
 
 int sk_engine(const symm_handle *h, int B) {
     if (h->opt_sk_engine >= 0) return (h->opt_sk_engine == 1 && B > kSkFfmaMaxBatch) ? 0 : h->opt_sk_engine;
-    return B <= kSkFfmaMaxBatch ? 1 : 0;
+    return 0;
 }
 
 int sk_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }

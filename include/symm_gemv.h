@@ -410,7 +410,8 @@ enum {
     SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
     SYMM_OPT_SK_SLABS = 3,    /* paths 3, 4: 64-column slabs per pipeline stage, 0 auto (2), 1..4 (the
                                  instantiated pipelines: 1, 2, 4 slabs at 1 CTA per SM; 1, 2, 3 at 2; 1 at 3) */
-    SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (FFMA for B <= 2, else tcgen05), 0 tcgen05, 1 FFMA */
+    SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (tcgen05), 0 tcgen05, 1 FFMA (B <= 2; wider batches run
+                                 tcgen05) */
     SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: resident CTAs per SM, 0 auto (2), 1..3 (ring shrinks) */
     SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
     SYMM_OPT_DYN_SPLITS = 7,  /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */

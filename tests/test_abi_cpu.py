@@ -2,7 +2,6 @@
 validation works without a GPU (no compute calls here)."""
 from __future__ import annotations
 
-import ctypes
 import os
 import re
 

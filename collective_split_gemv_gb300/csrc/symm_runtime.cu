@@ -332,7 +332,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         if (Kr == 0) return fail(SYMM_EINVAL, "the stream-K kernel needs K > 0");
         pl->engine = sk_engine(h, B);
         pl->slabs = sk_slabs(h);
-        pl->cps = sk_cps(h);
+        pl->cps = h->opt_sk_cps > 0 ? h->opt_sk_cps : 1;   // stream-K: 2 CTAs do not fit the registers
         if (!sk_config_supported(pl->slabs, pl->cps))
             return fail(SYMM_EINVAL, "stream-K has no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
         if (!sk_geometry(h, cap, pl->tiles, N, Kr, B, pl->slabs, pl->cps, &pl->geo))

@@ -412,7 +412,11 @@ enum {
                                  instantiated pipelines: 1, 2, 4 slabs at 1 CTA per SM; 1, 2, 3 at 2; 1 at 3) */
     SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (tcgen05), 0 tcgen05, 1 FFMA (B <= 2; wider batches run
                                  tcgen05) */
-    SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: resident CTAs per SM, 0 auto (2), 1..3 (ring shrinks) */
+    SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: CTAs per SM the ring is sized for, 0 auto (2 for path 4,
+                                 1 for path 3), 1..3 (the ring shrinks).  By their registers the
+                                 kernels hold fewer CTAs per SM than that in some configurations
+                                 (path 4 at 3; path 3 at 2 or 3): the grid then runs in two waves,
+                                 correctly but slower */
     SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
     SYMM_OPT_DYN_SPLITS = 7,  /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
     SYMM_OPT_NORM_PDL = 8,    /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a

@@ -92,3 +92,23 @@ def test_traffic_entries_name_known_kernels_and_workloads():
             got = bench.profiled_traffic(kernel, workload, entry["source_sha"])
             assert got == entry["dram_bytes_per_launch"]
             assert bench.profiled_traffic(kernel, workload, "0" * 16) is None
+
+
+@pytest.mark.parametrize("workload,threads", [("tiny", None), ("ar_bias_rmsnorm", 1)])
+def test_reference_arm_line_follows_the_contract(workload, threads):
+    """`bench.py --impl reference` (the oracle on the host cores): the keys of
+    the JSON line, a zero-copy e2e object, no GPU launches, and `cores` as the
+    threads the oracle function used (the RMSNorm oracle is single-threaded)."""
+    args = bench.parse_args(["--impl", "reference", "--workload", workload, "--steps", "2", "--warmup", "1"])
+    line = bench.run_reference(args, 0, 1)
+    for key in ("metric", "impl", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["gpu_launches"] == 0
+    assert line["config"]["workload"] == workload and line["value"] > 0
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["sample"]
+    assert cb["cores"] == (threads if threads is not None else bench.host_cores())
+    assert bench.run_reference(args, 1, 2) is None   # other ranks print nothing

@@ -10,15 +10,18 @@ for ``--workload allreduce`` (R=8 slots of 4,194,304 bf16).  Inputs are
 synthetic (seeded generator) and resident in HBM when the timed region
 starts; inputs rotate over enough copies that the bytes touched between two
 reads of the same data exceed the 129 MB L2, otherwise L2 is flushed between
-launches outside the per-launch events.
+launches outside the per-launch events.  Where the call runs on the
+persistent kernel its weights are packed once before timing (``symm_pack_w``,
+as at model load; the same bytes per call), and the same calls on the
+row-major weights are timed after the main leg (``row_major_w``).
 
 ``value`` is the algorithmic HBM throughput of the call in GB/s -- the bytes
 the method must move (GEMV: W_r and x_r of every rank, the fp32 partials
 written and read back, the R bf16 output replicas; all-reduce: R inputs read,
 R outputs written) over the measured time per step; ``ms_per_step`` is the
 call latency.  ``roofline`` divides the same bytes by the kernel's mean launch
-time (CUDA events around every launch on the launching stream) and by the
-measured copy bandwidth.  ``e2e`` is the same call with its per-step inputs
+time (CUDA events on the launching stream: around every launch, or around the
+whole region when calls are chained) and by the measured copy bandwidth.  ``e2e`` is the same call with its per-step inputs
 copied from pinned host memory and its result read back every step;
 ``e2e_graph`` is that step captured once into a CUDA graph and replayed.
 

@@ -244,9 +244,8 @@ def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
 # plans and launches, is left out).
 KERNEL_SOURCES = {
     "gemv_ar_ffma_kernel": ("gemv_ffma.cu",),
-    "gemv_ar_tc_kernel": ("gemv_tc.cu", "sm100.cuh"),
-    "gemv_ar_sk_kernel": ("gemv_sk.cu", "sm100.cuh"),
     "gemv_ar_dyn_kernel": ("gemv_dyn.cu", "sm100.cuh"),
+    "gemv_ar_cluster_kernel": ("gemv_cluster.cu",),
     "one_shot_ar_kernel": ("allreduce.cu",),
     "one_shot_ar_staged_kernel": ("allreduce.cu", "sm100.cuh"),
     "reduce_scatter_kernel": ("allreduce.cu",),
@@ -281,11 +280,10 @@ def kernel_source_sha(kernel=None):
 def kernel_name(plan):
     if plan["path"] == 1:
         return "gemv_ar_ffma_kernel"
-    if plan["path"] == 2:
-        return "gemv_ar_tc_kernel"
+    if plan["path"] == 5:
+        return "gemv_ar_cluster_kernel"
     engine = "tcgen05" if plan["engine"] == 0 else "ffma"
-    name = "gemv_ar_sk_kernel" if plan["path"] == 3 else "gemv_ar_dyn_kernel"
-    return f"{name}<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
+    return f"gemv_ar_dyn_kernel<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
 
 
 def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id, per_launch=True):
@@ -334,6 +332,29 @@ def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id, p
     return step_ms, launch_ms, clocks
 
 
+def chunked_spread(step, n_steps, stream, dev, world, chunk=None):
+    """The same n_steps chained calls once more, with an event after every
+    `chunk` calls (each event ends one chain: the call after it starts in
+    plain stream order).  Returns the per-call time of every chunk (ms), from
+    which the bench reports median and p10 / p90 of chained calls."""
+    import torch
+
+    chunk = chunk or max(5, n_steps // 10)
+    bounds = list(range(0, n_steps, chunk)) + [n_steps]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in bounds]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for j in range(1, len(bounds)):
+            for i in range(bounds[j - 1], bounds[j]):
+                step(i)
+            evs[j].record(stream)
+    torch.cuda.synchronize(dev)
+    return [evs[j - 1].elapsed_time(evs[j]) / (bounds[j] - bounds[j - 1]) for j in range(1, len(bounds))], chunk
+
+
 def _pinned(a):
     import numpy as np
     import torch
@@ -364,8 +385,8 @@ def make_case(args, w, local_rank, stream):
         N, K, B = w["N"], w["K"], w["B"]
         W, x = synth.gemv_inputs(R, N, K, B, w["seed"], w["w_std"], w["x"])
         copies = _copies_for(W.nbytes)
-        paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC,
-                 "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
+        paths = {"auto": csg.GEMV_PATH_AUTO, "ffma": csg.GEMV_PATH_FFMA, "dyn": csg.GEMV_PATH_DYN,
+                 "cluster": csg.GEMV_PATH_CLUSTER}
 
         def gemv_ws(packed):
             ws_ = GemvWorkspace(R, N, K, B, copies=copies, device=local_rank, packed=packed)
@@ -521,7 +542,11 @@ def run_ours(args, rank, world, local_rank):
     step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,
                                             per_launch=not chained)
     unchained = None
+    spread = None
     if chained:
+        # the spread of chained calls: the same calls timed in chunks
+        chunk_ms, chunk = chunked_spread(step, args.steps, stream, dev, world)
+        spread = (max_over_ranks(chunk_ms, world, dev), chunk)
         # the same calls in plain stream order, each bracketed by events
         csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 0)
         u_step, u_launch, _ = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id)
@@ -540,6 +565,20 @@ def run_ours(args, rank, world, local_rank):
             raise SystemExit(f"protocol error in the row-major leg: {csg.symm_last_error()}")
         row_major = statistics.mean(rm_launch)
         c["ws_rm"].close()
+    unfused = None
+    if w["kind"] == "gemv" and c.get("ws") is not None and csg.symm_gemv_plan(ws.h, w["N"], w["K"], w["B"])["path"] == \
+            csg.GEMV_PATH_DYN:
+        # What fusion buys: the same calls unfused (the GEMV storing every
+        # rank's fp32 partials, then a separate all-reduce kernel of them),
+        # timed like the main leg.
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, 1)
+        uf_step, uf_launch, _ = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,
+                                           per_launch=not chained)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, 0)
+        code, _, _ = csg.symm_status(ws.h, stream)
+        if code != csg.SYMM_OK:
+            raise SystemExit(f"protocol error in the unfused leg: {csg.symm_last_error()}")
+        unfused = statistics.mean(uf_launch)
 
     # ---- e2e: the same call through the ABI with host buffers every step ----
     # Each step: one strided copy of the step's inputs from pinned host memory
@@ -615,10 +654,10 @@ def run_ours(args, rank, world, local_rank):
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
 
-    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms, rm_ms = max_over_ranks(
+    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms, rm_ms, uf_ms = max_over_ranks(
         [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms),
          unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0, e2e_graph_ms,
-         row_major if row_major is not None else 0.0], world, dev)
+         row_major if row_major is not None else 0.0, unfused if unfused is not None else 0.0], world, dev)
     ws.close()
     if rank != 0:
         return None
@@ -660,9 +699,11 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(kernel, args.workload, kernel_source_sha(kernel)),
             "mean_launch_us": round(mean_launch_ms * 1e3, 3),
-            "median_launch_us": round(statistics.median(launch_ms) * 1e3, 3),
-            "p10_p90_launch_us": [round(q * 1e3, 3) for q in _p10_p90(launch_ms)],
-            "timing": ("chained calls: region time / steps (events around the region only)" if chained
+            "median_launch_us": round(statistics.median(spread[0] if spread else launch_ms) * 1e3, 3),
+            "p10_p90_launch_us": [round(q * 1e3, 3) for q in _p10_p90(spread[0] if spread else launch_ms)],
+            "timing": ((f"chained calls: region time / steps (events around the region only); median and "
+                        f"p10 / p90 over {len(spread[0])} chunks of {spread[1]} chained calls timed again "
+                        f"(an event after each chunk)") if chained
                        else "CUDA events around every launch on the launching stream"),
         },
         "clocks": clocks,
@@ -700,6 +741,14 @@ def run_ours(args, rank, world, local_rank):
             "us_per_call": round(rm_ms * 1e3, 3),
             "achieved": round(nbytes / (rm_ms * 1e-3) / 1e9, 1),
             "frac": round(nbytes / (rm_ms * 1e-3) / 1e9 / peak, 4),
+        }
+    if unfused is not None:
+        line["unfused"] = {
+            "what": ("the same calls unfused (SYMM_OPT_UNFUSED: the GEMV kernel storing every rank's fp32 partials, "
+                     "then a separate all-reduce kernel over them; the same bits), timed like the main leg"),
+            "us_per_call": round(uf_ms * 1e3, 3),
+            "fused_saving_pct": round(100.0 * (uf_ms - mean_launch_ms) / uf_ms, 2),
+            "pages_claim": "13-22 % lower execution time for the fused GEMV + AllReduce (hardware not named)",
         }
     if ew is not None:
         line["e2e_weights_from_host"] = {
@@ -846,14 +895,14 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="mlp_down_decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--gemv-path", choices=("auto", "ffma", "tc", "sk", "dyn"), default="auto",
+    p.add_argument("--gemv-path", choices=("auto", "ffma", "dyn", "cluster"), default="auto",
                    help="force one kernel (measurement only)")
     p.add_argument("--sk-slabs", type=int, default=0, choices=(0, 1, 2, 3, 4),
                    help="TMA kernels: slabs per pipeline stage (0 = library default)")
     p.add_argument("--sk-cps", type=int, default=0, choices=(0, 1, 2, 3),
                    help="TMA kernels: resident CTAs per SM (0 = library default)")
     p.add_argument("--sk-grid", type=int, default=0,
-                   help="stream-K grid: 0 library default, -S = S CTAs per (tile, rank), or a count")
+                   help="persistent kernel: grid in CTAs (0 = library default)")
     p.add_argument("--w-layout", choices=("packed", "row_major"), default="packed",
                    help="GEMV weights: packed (symm_pack_w, where the call runs on the persistent kernel) or "
                         "row-major")

@@ -12,13 +12,17 @@ default stream.
 
 There is no fallback: if the library has not been built, importing works but
 the first call raises.  Build it with ``__graft_entry__.build()``.
+
+``SYMM_GEMV_VARIANT=timeline`` in the environment loads the timeline build of
+the same library instead (kernels with %globaltimer phase stamps, see
+``symm_set_timeline``); it is built by ``_build.build(variant="timeline")``.
 """
 from __future__ import annotations
 
 import ctypes
 import os
 
-from ._build import LIB_PATH
+from ._build import lib_path as _lib_path
 
 SYMM_OK = 0
 SYMM_EINVAL = -1
@@ -43,17 +47,19 @@ SYMM_OPT_CHAIN = 9
 SYMM_OPT_AR_CTAS_PER_SM = 10
 SYMM_OPT_AR_KERNEL = 11
 SYMM_OPT_COPY_ENGINE = 12
+SYMM_OPT_UNFUSED = 13
 AR_KERNEL_AUTO, AR_KERNEL_PER_THREAD, AR_KERNEL_STAGED = 0, 1, 2   # auto is the per-thread kernel
 
-GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_TC, GEMV_PATH_SK, GEMV_PATH_DYN = 0, 1, 2, 3, 4
+GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_DYN, GEMV_PATH_CLUSTER = 0, 1, 4, 5   # paths 2 and 3 were retired
+TIMELINE_SLOTS = 16   # 64-bit words per CTA row of a timeline buffer
 
 EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
             "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "gemv_reduce_scatter",
             "gemv_all_reduce_bias_rmsnorm", "reduce_scatter", "two_shot_all_reduce",
             "all_reduce_bias_rmsnorm", "tile_reduce", "multi_root_tile_reduce", "symm_copy_to_slots",
-            "symm_copy_from_slots", "symm_packed_w_bytes", "symm_pack_w", "symm_release_w", "symm_free",
-            "symm_last_error")
+            "symm_copy_from_slots", "symm_packed_w_bytes", "symm_pack_w", "symm_release_w", "symm_set_timeline",
+            "symm_free", "symm_last_error")
 
 _lib = None
 
@@ -75,18 +81,25 @@ class GemvPlan(ctypes.Structure):
                                             "grid", "parts_max", "kblocks", "ctas_per_sm")]
 
 
+def library_variant() -> str:
+    """'' for the product library, 'timeline' for the stamped build."""
+    v = os.environ.get("SYMM_GEMV_VARIANT", "")
+    return "timeline" if v == "timeline" else ""
+
+
 def library_path() -> str:
-    return LIB_PATH
+    return _lib_path(library_variant())
 
 
 def lib() -> ctypes.CDLL:
     """The loaded ``libsymm_gemv.so``; raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: the CUDA library has not been built "
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: the CUDA library has not been built "
                                "(run __graft_entry__.build()); there is no CPU fallback")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         L.symm_layout.argtypes = [i, sz, sz, sz, ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.symm_alloc.argtypes = [i, sz, sz, sz, vp, sz, ctypes.POINTER(vp)]
@@ -113,6 +126,7 @@ def lib() -> ctypes.CDLL:
         L.symm_packed_w_bytes.argtypes = [i, i, i, ctypes.POINTER(sz)]
         L.symm_pack_w.argtypes = [vp, vp, vp, i, i, i, vp]
         L.symm_release_w.argtypes = [vp, vp]
+        L.symm_set_timeline.argtypes = [vp, vp, sz]
         L.symm_free.argtypes = [vp]
         L.symm_last_error.argtypes = []
         L.symm_last_error.restype = ctypes.c_char_p
@@ -243,6 +257,13 @@ def symm_pack_w(h, W_r: int, Wp: int, R: int, N: int, K: int, stream=None) -> No
 
 def symm_release_w(h, Wp: int) -> None:
     _check(lib().symm_release_w(h, _vp(Wp)))
+
+
+def symm_set_timeline(h, buf, nbytes: int) -> None:
+    """Diagnostics: per-CTA phase stamps of later calls into `buf` (device
+    pointer, rows of TIMELINE_SLOTS uint64); the timeline build only.  None
+    switches it off."""
+    _check(lib().symm_set_timeline(h, _vp(buf) if buf else None, nbytes if buf else 0))
 
 
 def symm_status(h, stream=None):

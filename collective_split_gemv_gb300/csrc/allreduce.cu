@@ -378,17 +378,9 @@ namespace {
 template <int RT>
 cudaError_t launch_staged(const AllReduceArgs &a, unsigned grid, cudaStream_t s) {
     auto kern = one_shot_ar_staged_kernel<RT>;
-    // The shared-memory attribute is per device: set it once for each device
-    // a launch happens on (devices past 63 set it every time).
-    static unsigned long long attr_devices = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
-    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    if (bit == 0 || !(attr_devices & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr_devices |= bit;
-    }
+    static std::atomic<unsigned long long> attr_devices{0};
+    cudaError_t e = set_smem_once(kern, kStagedSmemBudget, attr_devices);
+    if (e != cudaSuccess) return e;
     const int chv = staged_chunk_vectors(a.R);
     const size_t smem = (size_t)(kStagedStages * a.R + 2) * (size_t)chv * 16;
     return launch_maybe_chained(kern, a, grid, kStagedThreads, smem, s);

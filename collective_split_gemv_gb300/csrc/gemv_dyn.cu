@@ -55,6 +55,15 @@
 // steer the group's named barrier are made uniform with bar.red.and; a CTA
 // that gave up latches a status code, waits (bounded) for its copies and MMAs
 // in flight, frees TMEM and exits without publishing.
+//
+// Timeline slots (timeline build only, timeline.cuh), one row per CTA:
+//   0 entry                      1 set-up done (barriers, TMEM)
+//   2 first W load issued        3 dependency wait passed (producer)
+//   4 first stage full (MMA)     5 first accumulator ready (epilogue)
+//   6 last accumulator ready     7 last unit published
+//   8 last tile reduction done   9 exit
+//  10 units computed (count)    11 tile reductions (count)
+//  12 last stage issued         13 producer saw the end of the work
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,12 +71,13 @@
 #include "internal.h"
 #include "protocol.cuh"
 #include "sm100.cuh"
+#include "timeline.cuh"
 
 namespace symm {
 
 namespace {
 
-constexpr int kM = 128;
+constexpr int kM = kDynRows;
 constexpr int kNmma = 16;
 constexpr int kSlabA = kM * 64 * 2;
 constexpr int kSlabX = kNmma * 64 * 2;
@@ -105,45 +115,42 @@ __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v
 
 // Steps 2-4 of the protocol for contributor (r, s) of tile t (C = R * S
 // contributors: every rank's K range in S splits), run by the 128 threads of
-// warps 2-5 (gt = 0..127).  The caller has stored its partial.
-__device__ __forceinline__ void publish_reduce_unit(const GemvArgs &a, uint32_t epoch, int S, int t, int r, int s,
-                                                    int gt, int *s_last, int *s_bad) {
+// warps 2-5 (gt = 0..127).  The caller has stored its partial; the flag goes
+// out with it, before the fence, and the reducer checks the flags in the
+// same round of loads as its first partials (protocol.cuh).  Returns whether
+// this group reduced the tile.
+__device__ __forceinline__ bool publish_reduce_unit(const GemvArgs &a, uint32_t epoch, int S, int t, int r, int s,
+                                                    int gt, int *s_last) {
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;
     uint32_t done = 0;   // gt == 0, reducer: tiles counted before this one
+    if (gt == 0) st_relaxed_gpu_u32(flag_of(a, r, t, S, s), epoch);
     __threadfence();
     named_barrier(kGroupBarrier, kGroupThreads);
-    if (gt == 0) {
-        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
-                                                      (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, epoch);
-        *s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
-        *s_bad = 0;
-    }
+    if (gt == 0) *s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
     named_barrier(kGroupBarrier, kGroupThreads);
-    if (!*s_last) return;
-    // The acquire loads of the flags (and the barrier after them) order the
-    // partial loads of the reduction after every contributor's stores.
-    for (int i = gt; i < (int)C; i += kGroupThreads) {
-        const int q = i / S;
-        const int qs = i - q * S;
-        const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
-                                                               (long long)q * a.stride) + (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != epoch) {
-            latch_status(a.status, kProtoStaleFlag, q, t, epoch);
-            *s_bad = 1;
-        }
-    }
-    named_barrier(kGroupBarrier, kGroupThreads);
-    if (gt == 0) finish_launch_if_last(a, done, epoch, t);
-    if (!*s_bad) {
-        // Contributors in order: rank 0..R-1, split 0..S-1.
-        reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
-                    [&](int j) {
-                        const int q = j / S;
-                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                    },
-                    gt, kGroupThreads);
-    }
+    if (!*s_last) return false;
+    reduce_tile(a, t, epoch, t * kM, min(kM, a.N - t * kM), (int)C,
+                [&](int j) { return contributor_partials(a, j); }, [](bool ok) { return group_all(ok); },
+                [&]() {
+                    if (gt == 0) finish_launch_if_last(a, done, epoch, t);
+                },
+                gt, kGroupThreads);
+    return true;
+}
+
+// Unfused form (kOutPartials): no tile protocol.  One thread counts the unit
+// on tiles_done; the thread that counts the last of the U units finishes the
+// launch as the last tile reducer does in the fused form (every CTA read the
+// epoch before it counted a unit, and the acq_rel count orders those reads
+// before the epoch store).
+__device__ __forceinline__ void count_unit_partials(const GemvArgs &a, uint32_t epoch, uint32_t U) {
+    const uint32_t done = atom_add_acq_rel_gpu(a.tiles_done, 1u);
+    if (done >= U) latch_status(a.status, kProtoBadTicket, -1, -1, epoch);
+    if (done != U - 1u) return;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    st_relaxed_gpu_u32(a.tiles_done, 0u);
+    st_relaxed_gpu_u32(a.work + ((epoch + 1u) & 1u), 0u);
+    st_relaxed_gpu_u32(a.epoch_word, epoch);
 }
 
 // The same protocol run by one warp (the FFMA engine's epilogue warp).
@@ -151,38 +158,20 @@ __device__ __forceinline__ void publish_reduce_warp(const GemvArgs &a, uint32_t 
                                                     int lane) {
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;
     uint32_t done = 0;   // lane 0, reducer: tiles counted before this one
+    if (lane == 0) st_relaxed_gpu_u32(flag_of(a, r, t, S, s), epoch);
     __threadfence();
     __syncwarp();
     uint32_t last = 0;
-    if (lane == 0) {
-        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
-                                                      (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, epoch);
-        last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
-    }
+    if (lane == 0) last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) return;
-    bool bad = false;   // acquire loads of the flags, then the partials (see above)
-    for (int i = lane; i < (int)C; i += 32) {
-        const int q = i / S;
-        const int qs = i - q * S;
-        const uint32_t *f = reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(a.flags) +
-                                                               (long long)q * a.stride) + (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != epoch) {
-            latch_status(a.status, kProtoStaleFlag, q, t, epoch);
-            bad = true;
-        }
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) finish_launch_if_last(a, done, epoch, t);
-    if (!bad) {
-        reduce_tile(a, t * kM, min(kM, a.N - t * kM), (int)C,
-                    [&](int j) {
-                        const int q = j / S;
-                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                    },
-                    lane, 32);
-    }
+    reduce_tile(a, t, epoch, t * kM, min(kM, a.N - t * kM), (int)C,
+                [&](int j) { return contributor_partials(a, j); },
+                [](bool ok) { return __all_sync(0xffffffffu, ok) != 0; },
+                [&]() {
+                    if (lane == 0) finish_launch_if_last(a, done, epoch, t);
+                },
+                lane, 32);
 }
 
 __device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
@@ -222,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // when calls are chained) may be scheduled as CTAs of this one retire;
     // they wait for this grid before touching anything it writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     constexpr int kStages = RingT::kStages;
@@ -241,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float part_buf[2][kM * 2];   // FFMA engine: [buffer][b * 128 + row] partials, B <= 2
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
-    __shared__ int s_last, s_bad;
+    __shared__ int s_last;
     __shared__ uint32_t epoch_sh;
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -278,17 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 1);
     const uint32_t tmem = kEngine == 0 ? tmem_base_sh : 0u;
-    // Launched as a programmatic dependent of the previous fused call (calls
+    // Launched as a programmatic dependent of the previous kernel (calls
     // chained on one stream), this grid may start while that one drains.
-    // Everything below except the producer's first W loads can depend on it
-    // (x, scratch, the pad, y), so every other thread waits for it here; the
-    // wait returns at once when the launch was not a programmatic dependent.
+    // Everything below except, for a packed weight, the producer's first W
+    // loads can depend on it (x, scratch, the pad, y, a row-major W), so every
+    // other thread waits for it here; the wait returns at once when the
+    // launch was not a programmatic dependent.
     int pre = 0;   // producer: stages of the first unit issued here
     if (warp == 0 && lane == 0) {
-        // W of the first unit's first stages depends on nothing the previous
-        // call writes: its loads go out before the dependency wait, x's
-        // after it.  The first unit is the CTA's own index (G <= U).
+        // A packed weight is written once, by symm_pack_w (which the host
+        // never chains into a call that reads it), so the W loads of the first
+        // unit's first stages go out before the dependency wait and x's after
+        // it.  A row-major W may be the output of the kernel just before (any
+        // kernel, not only this library's): it is loaded after the wait.
+        // The first unit is the CTA's own index (G <= U).
         const int u = a.reverse_order ? U - 1 - (int)blockIdx.x : (int)blockIdx.x;
         const int tr = u / S;
         const int sp = u - tr * S;
@@ -297,6 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb0 = sp * KBs;
         const int kb1 = min(kb0 + KBs, KB);
         pre = min(kStages, kb1 - kb0);
+        if (!a.w_early) griddep_wait();
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 2);
         for (int i = 0; i < pre; ++i) {   // the ring is empty: no wait
             const int kb = kb0 + i;
             stage_unit[i] = u;
@@ -307,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kSlabs; ++s)
                 load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[i], kb * kSlabs + s, t, r);
         }
-        griddep_wait();
+        if (a.w_early) griddep_wait();
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 3);
         for (int i = 0; i < pre; ++i) {
             const int kb = kb0 + i;
             uint8_t *dst = smem + (size_t)i * kStageBytes;
@@ -338,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st0 = issued % kStages;
                 const uint32_t ph0 = (uint32_t)(issued / kStages) & 1u;
                 if (tk >= (uint32_t)U) {
+                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 13);
                     // End of the stream: an empty stage tagged -1.
                     if (!mbar_wait(&empty_bar[st0], ph0 ^ 1u, &abort_sh)) {
                         ok = false;
@@ -387,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     r);
                     if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(work, 1u);
                     ++issued;
+                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 12);
                 }
                 asm volatile("add.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"((uint32_t)geo.G));
             }
@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (i == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 4);
                     const int u = stage_unit[st];
                     const int fl = stage_flags[st];
                     const int j = seg & 1;
@@ -482,7 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[j]);
-                publish_reduce_warp(a, epoch, S, t, r, sp, lane);
+                if (a.out_mode == kOutPartials) {
+                    if (lane == 0) count_unit_partials(a, epoch, (uint32_t)U);
+                } else {
+                    publish_reduce_warp(a, epoch, S, t, r, sp, lane);
+                }
                 ++seg;
             }
             if (!ok) {
@@ -498,6 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         if constexpr (kEngine == 0) {
             int seg = 0;
+            int n_reduced = 0;   // timeline only
+            (void)n_reduced;
             while (true) {
                 const int j = seg & 1;
                 const uint32_t use = (uint32_t)(seg >> 1);
@@ -507,6 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) break;
                 ok = group_all(mbar_wait_sleepy(&acc_full[j], use & 1u, &abort_sh));
                 if (!ok) break;
+                if (gt == 0) {
+                    if (seg == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 5);
+                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 6);
+                }
                 tc_fence_after();
                 float v[16];
                 tmem_ld_16(tmem + (uint32_t)(j * kNmma) + ((uint32_t)(q4 * 32) << 16), v);
@@ -525,8 +536,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int b = 0; b < kNmma; ++b)
                         if (b < a.B) P[(size_t)b * a.N + n] = v[b];
                 }
-                publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last, &s_bad);
+                bool reduced = false;
+                if (a.out_mode == kOutPartials) {
+                    if (gt == 0) count_unit_partials(a, epoch, (uint32_t)U);
+                } else {
+                    reduced = publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last);
+                }
                 ++seg;
+                if (gt == 0) {
+                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, reduced ? 8 : 7);
+                    if (reduced) tl_value(a.tl, a.tl_ctas, blockIdx.x, 11, (unsigned long long)++n_reduced);
+                    tl_value(a.tl, a.tl_ctas, blockIdx.x, 10, (unsigned long long)seg);
+                }
             }
         } else {
             int i = 0, seg = 0;
@@ -602,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 9);
     if (kEngine == 0 && warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -612,17 +634,9 @@ template <int kEngine, int kSlabs, int kB, int kCps>
 cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, bool chained, cudaStream_t s) {
     auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps>;
     constexpr int smem = Ring<kSlabs, kCps>::kSmem;
-    // The shared-memory attribute is per device: set it once for each device
-    // a launch happens on (devices past 63 set it every time).
-    static unsigned long long attr_devices = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
-    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    if (bit == 0 || !(attr_devices & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_devices |= bit;
-    }
+    static std::atomic<unsigned long long> attr_devices{0};
+    cudaError_t e = set_smem_once(kern, smem, attr_devices);
+    if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3((unsigned)geo.G), dim3(kThreads), (size_t)smem, s, chained, m[0], m[1], a, geo);
 }
 
@@ -641,7 +655,57 @@ cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorM
     }
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); looked up once, thread-safe.
+EncodeTiledFn encode_fn() {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return nullptr;
+    }();
+    return fn;
+}
+
+// A 3-D view [R][rows][Kr] of bf16 with the slot stride as the rank stride;
+// boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill outside.
+int encode_3d(CUtensorMap *m, const void *base, int Kr, int rows, int R, long long stride, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return -1;
+    const cuuint64_t dims[3] = {(cuuint64_t)Kr, (cuuint64_t)rows, (cuuint64_t)R};
+    const cuuint64_t strides[2] = {(cuuint64_t)Kr * 2, (cuuint64_t)stride};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS ? 0 : (int)rc;
+}
+
 }  // namespace
+
+int dyn_encode_maps(const GemvArgs &a, void *maps) {
+    CUtensorMap *m = static_cast<CUtensorMap *>(maps);
+    int rc = encode_3d(&m[0], a.W, a.Kr, a.N, a.R, a.stride, kM);
+    if (rc != 0) return rc;
+    return encode_3d(&m[1], a.x, a.Kr, a.B, a.R, a.stride, kNmma);
+}
+
+int dyn_block_k(int slabs) { return 64 * slabs; }
+
+// Pipeline shapes that are instantiated: (slabs, CTAs per SM) with a ring of
+// at least two stages.
+bool dyn_config_supported(int slabs, int cps) {
+    return (cps == 1 && (slabs == 1 || slabs == 2 || slabs == 4)) ||
+           (cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3)) || (cps == 3 && slabs == 1);
+}
 
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,
                             bool chained, cudaStream_t s) {

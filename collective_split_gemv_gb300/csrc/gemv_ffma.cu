@@ -19,6 +19,9 @@
 //    then a fixed xor-shuffle tree across the warp;
 //  - the fp32 partial goes to the rank's scratch slot and the CTA enters the
 //    publish / last-arriver protocol (protocol.cuh).
+//
+// Timeline slots (timeline build only, timeline.cuh): 0 entry, 1 x staged
+// (first pass), 2 dot products done; 3-8 are the protocol's.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -53,7 +56,8 @@ __device__ __forceinline__ float dot8(const uint4 &w, const float4 &lo, const fl
 }
 
 template <int B>
-__global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) gemv_ar_ffma_kernel(const GemvArgs a) {
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
     chain_entry();
     // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
     const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a
             xs4[(b * 2 + 1) * kc_cap + c] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
         }
         __syncthreads();
+        if (c0 == 0 && threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 1);
 
         for (int c = lane; c < kc; c += 32 * U) {
             if (c != lane || c0 > 0) {
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(kThreads) gemv_ar_ffma_kernel(const GemvArgs a
             for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
             acc[g][b] = v;
         }
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 2);
 
     float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride);
 #pragma unroll

@@ -6,9 +6,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace symm {
+
+// Sets kern's dynamic shared-memory limit to `bytes` once per device (the
+// attribute is per device).  Host threads may launch concurrently: the
+// devices already set form an atomic bit mask, and setting the attribute
+// twice is harmless.  Devices past 63 set it on every call.
+template <class... KArgs>
+cudaError_t set_smem_once(void (*kern)(KArgs...), int bytes, std::atomic<unsigned long long> &done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
 
 // Launches kern<<<grid, block, smem, s>>>(args...); when `chained`, as a
 // programmatic dependent of the previous kernel on the stream (its CTAs may
@@ -77,7 +94,7 @@ struct GemvArgs {
     long long stride;        // bytes between slots
     long long partial_stride;  // bytes between the splits' partial arrays (4 * B * N)
     int R, N, Kr, B;
-    int splits;              // K-splits per rank (1 for the FFMA kernel)
+    int splits;              // K-splits per rank (1 for the per-tile kernel)
     int rows_per_tile;
     int num_tiles;
     int kc_cap;              // 16-byte chunks of x staged in shared memory per pass
@@ -90,15 +107,37 @@ struct GemvArgs {
     //   kOutReduceScatter  bf16 into y of rank b / rs_rows only, at row
     //                      b % rs_rows (y: [rs_rows][N] per slot);
     //   kOutBiasZ          fp32 sum + bias[n] into z[b][n] (slot 0), for the
-    //                      RMS-normalisation stage that follows.
+    //                      RMS-normalisation stage that follows;
+    //   kOutPartials       no tile reduction (persistent kernel only): the
+    //                      partials stay in scratch for the separate
+    //                      all-reduce kernel of the unfused form.
     int out_mode;
-    int chained;             // per-tile kernels (paths 1-3): launch as a programmatic dependent
+    int chained;             // per-tile and cluster kernels (paths 1, 5): launch as a programmatic dependent
     int rs_rows;             // kOutReduceScatter: B / R
     float *z;                // kOutBiasZ: fp32 [B][N]
     const uint8_t *bias;     // kOutBiasZ: bf16 [N] (slot 0) or nullptr
     int w_packed;            // persistent kernel: W is in the packed layout (below), not [N][Kr]
+    // Persistent kernel, chained launch: the first stages' W loads may go out
+    // before the wait for the previous kernel (packed weights only: they are
+    // written once, by symm_pack_w, never by the kernel a call follows).
+    int w_early;
+    unsigned long long *tl;  // timeline rows (timeline build only; nullptr: none), see timeline.cuh
+    int tl_ctas;             // CTAs the timeline buffer has rows for
 };
-constexpr int kOutAllReduce = 0, kOutReduceScatter = 1, kOutBiasZ = 2;
+constexpr int kOutAllReduce = 0, kOutReduceScatter = 1, kOutBiasZ = 2, kOutPartials = 3;
+
+// The unfused form's second kernel: y_s = bf16(sum of the R * splits fp32
+// partials in contributor order) for every slot s (partials_ar.cu).
+struct PartialsArArgs {
+    const uint8_t *scratch;  // fp32 [splits][B][N] partials of rank q at + q * stride
+    uint8_t *y;              // bf16 [B][N], slot 0
+    long long stride;
+    long long partial_stride;  // bytes between a rank's split partials (4 * B * N)
+    int R, splits, B, N;
+    int vec;                 // 1: B * N % 4 == 0 (16-byte loads, 8-byte stores)
+    int chained;             // launch as a programmatic dependent of the GEMV
+};
+cudaError_t launch_partials_ar(const PartialsArArgs &a, cudaStream_t s);
 
 // Sets the calling thread's last-error message (see symm_last_error) and
 // returns `code`.
@@ -173,6 +212,8 @@ struct RmsNormArgs {
     float eps;
     int wait_prior;          // 1: launched as a dependent of the previous kernel (PDL)
     int release_next;        // 1: let the next kernel on the stream be scheduled early
+    unsigned long long *tl;  // timeline rows (timeline build only; nullptr: none), see timeline.cuh
+    int tl_ctas;
 };
 int rmsnorm_max_h();
 cudaError_t launch_rmsnorm_rows(const RmsNormArgs &a, cudaStream_t s);
@@ -209,34 +250,25 @@ struct PackWArgs {
 };
 cudaError_t launch_pack_w(const PackWArgs &a, cudaStream_t s);
 
+// Cluster fused kernel for small layers (gemv_cluster.cu): one thread-block
+// cluster of R CTAs per 16-row tile, partials exchanged through distributed
+// shared memory; R <= kMaxClusterRanks, B <= 4.
+constexpr int kClusterRows = 16;
+constexpr int kMaxClusterRanks = 8;
+constexpr int kClusterMaxBatch = 4;
+cudaError_t launch_gemv_cluster(const GemvArgs &a, cudaStream_t s);
+
 // FFMA (CUDA-core) fused kernel: any B in 1..16.
 int ffma_rows_per_tile(int B);
 size_t ffma_smem_bytes(int B, int kc_cap);
 int ffma_kc_cap(int B, int Kr);
 cudaError_t launch_gemv_ffma(const GemvArgs &a, cudaStream_t s);
 
-// Tensor-core (tcgen05 + TMA) fused kernel: 128-row tiles, batch padded to 16.
-constexpr int kTcRows = 128;
-constexpr int kTcBlockK = 64;
-// Encodes the TMA descriptors for this launch (cached by the caller) and
-// launches.  `maps` points at two CUtensorMap objects (W, x), 64-byte aligned.
-int tc_encode_maps(const GemvArgs &a, void *maps);
-cudaError_t launch_gemv_tc(const GemvArgs &a, const void *maps, cudaStream_t s);
-size_t tc_smem_bytes();
-
-// Persistent stream-K kernel (TMA ring; tcgen05 or FFMA engine).  The U = T*R
-// units of KB K-blocks each form one sequence of total = U*KB blocks, cut into
-// G equal contiguous ranges (one per CTA).  Pmax bounds the parts a unit is
-// cut into; partial p of unit (t, r) lives at scratch_r + p * partial_stride
-// and its flag at flags_r[t * Pmax + p].
-struct SkGeom {
-    long long total;
-    int KB;
-    int G;
-    int Pmax;
-};
-// Persistent dynamically scheduled kernel: G CTAs draw the U = T*R units (KB
-// K-blocks each) from the work counter work[epoch & 1] (slot 0's pad).
+// Persistent dynamically scheduled kernel (TMA ring into tcgen05, or an FFMA
+// engine for B <= 2): 128-row tiles, batch padded to 16.  G CTAs draw the
+// U = T*R*splits units (KB K-blocks each) from the work counter
+// work[epoch & 1] (slot 0's pad).
+constexpr int kDynRows = 128;
 struct DynGeom {
     int units;      // T * R * splits
     int splits;     // K splits per (tile, rank)
@@ -244,14 +276,15 @@ struct DynGeom {
     int KBs;        // K blocks per split
     int G;
 };
+// Encodes the TMA descriptors of a launch (cached by the caller): `maps`
+// points at two CUtensorMap objects (W, x), 64-byte aligned.
+int dyn_encode_maps(const GemvArgs &a, void *maps);
+// K elements per ring stage, and the (slabs, CTAs per SM) pipelines built.
+int dyn_block_k(int slabs);
+bool dyn_config_supported(int slabs, int ctas_per_sm);
 // chained: launch as a programmatic dependent of the previous kernel on the
 // stream (its CTAs may start while that one drains; see the kernel).
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,
                             int ctas_per_sm, bool chained, cudaStream_t s);
-
-int sk_block_k(int slabs);
-bool sk_config_supported(int slabs, int ctas_per_sm);
-cudaError_t launch_gemv_sk(const GemvArgs &a, const SkGeom &geo, const void *maps, int engine, int slabs,
-                           int ctas_per_sm, cudaStream_t s);
 
 }  // namespace symm

@@ -8,14 +8,17 @@
 //     (read on the device, so a launch replayed from a CUDA graph gets a new
 //     epoch each time);
 //  1. every thread stores its share of the contributor's fp32 partial into
-//     the rank's scratch slot, then fences (gpu scope);
-//  2. after a CTA barrier, one thread release-stores the contributor's flag
-//     (= e) and takes an arrival ticket with an acq_rel atomic add on
-//     counter[t].  Tickets run 0..C-1 in every launch: the holder of C-1 is
-//     the tile's reducer and puts the counter back to zero (every contributor
-//     of this launch has arrived).  A ticket >= C latches a protocol error;
-//  3. the reducer acquires the C flags (each must equal e), sums the C
-//     partials in fixed order (rank 0..R-1, split 0..splits-1) in fp32,
+//     the rank's scratch slot, one thread also the contributor's flag (= e),
+//     then every thread fences (gpu scope);
+//  2. after a CTA barrier, one thread takes an arrival ticket with an acq_rel
+//     atomic add on counter[t].  Tickets run 0..C-1 in every launch: the
+//     holder of C-1 is the tile's reducer and puts the counter back to zero
+//     (every contributor of this launch has arrived).  A ticket >= C latches
+//     a protocol error;
+//  3. the reducer (its acq_rel ticket orders its loads after every
+//     contributor's fenced stores) loads the C flags together with the first
+//     partials -- each flag must equal e, else nothing is stored -- sums the
+//     C partials in fixed order (rank 0..R-1, split 0..splits-1) in fp32,
 //     rounds to bf16 (RNE) and stores the value into every rank's output
 //     slot;
 //  4. the reducer counts the tile on tiles_done (when it takes the ticket).
@@ -42,7 +45,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
+#include "timeline.cuh"
 
 namespace symm {
 
@@ -187,6 +193,38 @@ __device__ __forceinline__ void store_output(const GemvArgs &a, size_t e, float 
     }
 }
 
+// The same for the four outputs e .. e + 3 (e % 4 == 0, all in one row b,
+// which holds when N % 4 == 0): one 8-byte bf16 store per slot, or one
+// 16-byte fp32 store of z.  Each value is rounded or biased exactly as
+// store_output does it.
+__device__ __forceinline__ void store_output4(const GemvArgs &a, size_t e, float4 acc) {
+    if (a.out_mode == kOutBiasZ) {
+        if (a.bias) {
+            const int n = (int)(e % (size_t)a.N);
+            const uint2 bb = *reinterpret_cast<const uint2 *>(a.bias + (size_t)n * 2);
+            acc.x += bf16lo(bb.x);
+            acc.y += bf16hi(bb.x);
+            acc.z += bf16lo(bb.y);
+            acc.w += bf16hi(bb.y);
+        }
+        __stcg(reinterpret_cast<float4 *>(a.z + e), acc);
+        return;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t *>(&lo);
+    o.y = *reinterpret_cast<const uint32_t *>(&hi);
+    if (a.out_mode == kOutAllReduce) {
+        for (int q = 0; q < a.R; ++q) *reinterpret_cast<uint2 *>(a.y + (long long)q * a.stride + e * 2) = o;
+        return;
+    }
+    const int b = (int)(e / (size_t)a.N);
+    const int n = (int)(e - (size_t)b * a.N);
+    const int q = b / a.rs_rows;
+    *reinterpret_cast<uint2 *>(a.y + (long long)q * a.stride + ((size_t)(b - q * a.rs_rows) * a.N + n) * 2) = o;
+}
+
 // Waits until the grid this one was launched as a programmatic dependent of
 // has completed and its memory is visible; returns at once otherwise.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -202,100 +240,185 @@ __device__ __forceinline__ void chain_entry() {
     griddep_wait();
 }
 
+// Contributor (r, s)'s flag for tile t (S splits per rank) in rank r's pad.
+__device__ __forceinline__ uint32_t *flag_of(const GemvArgs &a, int r, int t, int S, int s) {
+    return reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) + (long long)r * a.stride) +
+           (size_t)t * S + s;
+}
+
 // The reduction of one tile by its last contributor: for each output (b, n)
 // of rows [n0, n0 + rows), sum the C contributors' fp32 partials in
-// contributor order j = 0..C-1 (contributor j's [B][N] array at
-// contributor_base(j)) and hand the sum to store_output.
-// The flags have been acquired and fenced, so plain L2 loads (.cg) see the
-// partials.  Each thread takes kPer outputs and loads kBatch contributors of
-// all of them before adding anything, so one L2 round trip serves
-// kPer * kBatch values; the additions stay in contributor order.
-template <class BaseFn>
-__device__ __forceinline__ void reduce_tile(const GemvArgs &a, int n0, int rows, int C, BaseFn contributor_base,
-                                            int tid, int nthreads) {
-    constexpr int kPer = 4;
-    constexpr int kBatch = 8;
-    const int count = rows * a.B;
-    for (int i0 = tid; i0 < count; i0 += nthreads * kPer) {
-        size_t off[kPer];
-        float acc[kPer];
+// contributor order j = 0..C-1 (contributor j = (rank j / S, split j % S),
+// its [B][N] array at contributor_base(j)) and hand the sum to store_output.
+// The caller holds the tile's last ticket (an acq_rel atomic that every
+// contributor took after fencing its partial and its flag), and the group
+// has passed a barrier since, so plain L2 loads (.cg) see every partial and
+// every flag.
+// Each thread takes kPer items -- vectors of four consecutive outputs (for
+// N % 4 == 0, when then n0 and rows are multiples of 4, and C <= 4), else
+// single outputs -- and loads up to kBatch contributors of all of them before
+// adding anything, so one L2 round trip serves up to kPer * kBatch loads
+// (32 registers either way); the additions stay in contributor order,
+// element by element, so vector and scalar items give the same bits.
+// The flags are checked in the same round trip as the first partials: thread
+// i loads the flags of contributors i, i + nthreads, ... and the group agrees
+// (all_ok, called exactly once by every thread of the group) before anything
+// is stored.  A flag that does not hold `epoch` latches kProtoStaleFlag and
+// the tile is left unwritten (returns false).  `issued` runs in every thread
+// once its first round of loads is out (the caller's launch bookkeeping,
+// whose atomic result it waits for, then overlaps those loads).
+template <int kW, class BaseFn, class AllFn, class IssuedFn>
+__device__ __forceinline__ bool reduce_items(const GemvArgs &a, int t, uint32_t epoch, int n0, int rows, int C,
+                                             BaseFn contributor_base, AllFn all_ok, IssuedFn issued, int tid,
+                                             int nthreads) {
+    // kW: outputs per item (4: float4 vectors, 1: scalars)
+    constexpr int kPer = kW == 4 ? 2 : 4;
+    constexpr int kBatch = kW == 4 ? 4 : 8;
+    using V = typename std::conditional<kW == 4, float4, float>::type;
+    const int S = a.splits;
+    const int per_row = rows / kW;           // items per batch row
+    const int count = per_row * a.B;         // items of the tile
+    bool checked = false;
+    for (int i0 = tid; i0 < count || !checked; i0 += nthreads * kPer) {
+        const bool active = i0 < count;
+        size_t off[kPer];                    // element offset b * N + n of the item's first output
+        V acc[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int i = min(i0 + k * nthreads, count - 1);
-            const int b = i / rows;
-            const int n = n0 + (i - b * rows);
-            off[k] = ((size_t)b * a.N + n) * sizeof(float);
-            acc[k] = 0.f;
+            const int i = min(i0 + k * nthreads, max(count - 1, 0));
+            const int b = per_row > 0 ? i / per_row : 0;
+            const int n = n0 + (i - b * per_row) * kW;
+            off[k] = (size_t)b * a.N + n;
         }
         for (int j0 = 0; j0 < C; j0 += kBatch) {
-            float v[kBatch][kPer];
+            // First round: this thread's flag (the common case, C <= nthreads:
+            // one load) goes out with the partial loads.
+            uint32_t f0 = epoch;
+            const bool first = !checked;
+            if (first && tid < C) f0 = ld_relaxed_gpu_u32(flag_of(a, tid / S, t, S, tid % S));
+            V v[kBatch][kPer];
+            if (active) {
 #pragma unroll
-            for (int c = 0; c < kBatch; ++c) {
-                const uint8_t *base = contributor_base(min(j0 + c, C - 1));
+                for (int c = 0; c < kBatch; ++c) {
+                    if (j0 + c < C) {
+                        const float *base = reinterpret_cast<const float *>(contributor_base(j0 + c));
 #pragma unroll
-                for (int k = 0; k < kPer; ++k) v[c][k] = __ldcg(reinterpret_cast<const float *>(base + off[k]));
-            }
-#pragma unroll
-            for (int c = 0; c < kBatch; ++c)
-                if (j0 + c < C) {
-#pragma unroll
-                    for (int k = 0; k < kPer; ++k) acc[k] = (j0 + c == 0) ? v[c][k] : acc[k] + v[c][k];
+                        for (int k = 0; k < kPer; ++k) v[c][k] = __ldcg(reinterpret_cast<const V *>(base + off[k]));
+                    }
                 }
-        }
+            }
+            if (first) {
+                issued();
+                checked = true;
+                bool ok = true;
+                for (int j = tid; j < C; j += nthreads) {
+                    const int q = j / S;
+                    const uint32_t f = j == tid ? f0 : ld_relaxed_gpu_u32(flag_of(a, q, t, S, j - q * S));
+                    if (f != epoch) {
+                        latch_status(a.status, kProtoStaleFlag, q, t, epoch);
+                        ok = false;
+                    }
+                }
+                if (!all_ok(ok)) return false;
+            }
+            if (active) {
 #pragma unroll
-        for (int k = 0; k < kPer; ++k)
-            if (i0 + k * nthreads < count) store_output(a, off[k] / sizeof(float), acc[k]);
+                for (int c = 0; c < kBatch; ++c) {
+                    if (j0 + c < C) {
+#pragma unroll
+                        for (int k = 0; k < kPer; ++k) {
+                            if (j0 + c == 0) {
+                                acc[k] = v[c][k];
+                            } else if constexpr (kW == 4) {
+                                acc[k].x += v[c][k].x;
+                                acc[k].y += v[c][k].y;
+                                acc[k].z += v[c][k].z;
+                                acc[k].w += v[c][k].w;
+                            } else {
+                                acc[k] += v[c][k];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                if (i0 + k * nthreads < count) {
+                    if constexpr (kW == 4) {
+                        store_output4(a, off[k], acc[k]);
+                    } else {
+                        store_output(a, off[k], acc[k]);
+                    }
+                }
+            }
+        }
     }
+    return true;
+}
+
+template <class BaseFn, class AllFn, class IssuedFn>
+__device__ __forceinline__ bool reduce_tile(const GemvArgs &a, int t, uint32_t epoch, int n0, int rows, int C,
+                                            BaseFn contributor_base, AllFn all_ok, IssuedFn issued, int tid,
+                                            int nthreads) {
+    if ((a.N & 3) == 0 && C <= 4)
+        return reduce_items<4>(a, t, epoch, n0, rows, C, contributor_base, all_ok, issued, tid, nthreads);
+    return reduce_items<1>(a, t, epoch, n0, rows, C, contributor_base, all_ok, issued, tid, nthreads);
+}
+
+// Contributor order: rank 0..R-1, and within a rank split 0..S-1.
+__device__ __forceinline__ const uint8_t *contributor_partials(const GemvArgs &a, int j) {
+    const int q = j / a.splits;
+    return a.scratch + (long long)q * a.stride + (long long)(j - q * a.splits) * a.partial_stride;
 }
 
 // Steps 2-4 of the protocol.  Called by ALL threads of the CTA after each
 // thread has stored its part of contributor (r, s)'s partial for tile t;
 // `epoch` (step 0) is needed in thread 0 only, which publishes.
+// Thread 0 stores the contributor's flag next to the partial stores, so one
+// fence orders both before the ticket: the flag is a record of which launch
+// the partial belongs to, checked by the reducer, while the ticket (an
+// acq_rel atomic) is what orders the reducer's loads after every
+// contributor's stores.
+// Timeline slots of the per-tile kernel (timeline build only): 3 partial
+// fenced, 4 ticket taken, 5 reducer: first loads out and launch bookkeeping
+// done, 6 reduction stored (reducer), 7 exit, 8 1 if this CTA reduced its
+// tile.
 __device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, uint32_t epoch, int t, int r, int s) {
     __shared__ int s_last;
-    __shared__ int s_bad;
     __shared__ uint32_t s_epoch;
     const int S = a.splits;
     const uint32_t C = (uint32_t)a.R * (uint32_t)S;   // contributors per tile
     uint32_t done = 0;                                 // thread 0, reducer: tiles counted before this one
+    if (threadIdx.x == 0) st_relaxed_gpu_u32(flag_of(a, r, t, S, s), epoch);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t *flag = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(a.flags) +
-                                                      (long long)r * a.stride) + (size_t)t * S + s;
-        st_release_gpu(flag, epoch);
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 3);
         s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
-        s_bad = 0;
         s_epoch = epoch;
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 4);
+        tl_value(a.tl, a.tl_ctas, blockIdx.x, 8, s_last ? 1ull : 0ull);
+        if (!s_last) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 7);
     }
     __syncthreads();
     if (!s_last) return;
     const uint32_t e = s_epoch;
-    // The acquire loads of the flags (and the barrier after them) order the
-    // partial loads of the reduction after every contributor's stores.
-    for (uint32_t i = threadIdx.x; i < C; i += blockDim.x) {
-        const int q = (int)(i / (uint32_t)S);
-        const int qs = (int)(i % (uint32_t)S);
-        const uint32_t *f = reinterpret_cast<const uint32_t *>(
-                                reinterpret_cast<const uint8_t *>(a.flags) + (long long)q * a.stride) +
-                            (size_t)t * S + qs;
-        if (ld_acquire_gpu(f) != e) {
-            latch_status(a.status, kProtoStaleFlag, q, t, e);
-            s_bad = 1;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) finish_launch_if_last(a, done, e, t);
-    if (!s_bad) {
-        // Sum in fixed order: rank 0..R-1, and within a rank split 0..S-1.
-        const int n0 = t * a.rows_per_tile;
-        const int rows = min(a.rows_per_tile, a.N - n0);
-        reduce_tile(a, n0, rows, (int)C,
-                    [&](int j) {
-                        const int q = j / S;
-                        return a.scratch + (long long)q * a.stride + (long long)(j - q * S) * a.partial_stride;
-                    },
-                    (int)threadIdx.x, (int)blockDim.x);
+    const int n0 = t * a.rows_per_tile;
+    const int rows = min(a.rows_per_tile, a.N - n0);
+    reduce_tile(a, t, e, n0, rows, (int)C, [&](int j) { return contributor_partials(a, j); },
+                [](bool ok) { return __syncthreads_and(ok) != 0; },
+                [&]() {
+                    if (threadIdx.x == 0) {
+                        finish_launch_if_last(a, done, e, t);
+                        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 5);
+                    }
+                },
+                (int)threadIdx.x, (int)blockDim.x);
+    if (threadIdx.x == 0) {
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 6);
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 7);
     }
 }
 

@@ -24,6 +24,11 @@
 // stores) are hardware barriers among CTAs that are co-scheduled by
 // construction: no CTA spins on memory, and none touches another's shared
 // memory after the last barrier, so any may exit.
+//
+// Timeline slots (timeline build only, timeline.cuh; row = blockIdx.y * C +
+// cluster rank): 0 entry, 1 gamma / bias loads issued, 2 dependency wait
+// passed, 3 row loaded and squared, 4 first cluster barrier passed, 5 second
+// cluster barrier passed, 6 stores issued.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,6 +36,7 @@
 
 #include "internal.h"
 #include "protocol.cuh"
+#include "timeline.cuh"
 
 namespace symm {
 
@@ -76,6 +82,8 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     uint32_t csize;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
     const int row = blockIdx.y;
+    const int tl_cta = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 0);
     const int H8 = a.H / 8;
     const int v0 = (int)crank * chunk;
     const int v1 = min(H8, v0 + chunk);
@@ -101,7 +109,9 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
             if (kSrc == 0 && a.bias) bv[j] = ld_v4(a.bias + (size_t)v * 16);
         }
     }
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 1);
     if (a.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 2);
 
     float z[kV][8];
     float ss = 0.f;
@@ -149,7 +159,9 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
     __syncthreads();
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 3);
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 4);
     // Thread c < C of warp 0 pushes this CTA's sum (warps in order) into
     // s_part[crank] of CTA c; one cluster barrier (release / acquire) makes
     // all pushes visible, and no CTA touches another's memory after it.
@@ -160,6 +172,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
         st_cluster_f32(&s_part[crank], threadIdx.x, t);
     }
     cluster_sync_all();
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 5);
     float tot = s_part[0];
     for (uint32_t c = 1; c < csize; ++c) tot += s_part[c];   // CTA-rank order: the same in every CTA
     const float scale = 1.0f / sqrtf(tot / (float)a.H + a.eps);
@@ -182,6 +195,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
             for (int q = 0; q < a.R; ++q) st_v4(dst + (long long)q * a.stride, o);
         }
     }
+    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 6);
 }
 
 template <int kSrc, int kV>

@@ -23,6 +23,7 @@
 
 #include "../../include/symm_gemv.h"
 #include "internal.h"
+#include "timeline.cuh"
 
 using namespace symm;
 
@@ -48,6 +49,7 @@ struct symm_handle {
     int opt_ar_cps = 0;         // all-reduce / reduce-scatter grid cap per SM (0 = the kernels' default)
     int opt_ar_kernel = 0;      // one-shot all-reduce kernel (kArKernel*)
     int opt_copy_engine = 0;    // symm_copy_*: 1 = always the copy engine, 0 = SMs where possible
+    int opt_unfused = 0;        // gemv_all_reduce as two kernels (GEMV partials, then their all-reduce)
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     // Slot-0 range written by the last kernel this handle launched (the same
@@ -55,6 +57,9 @@ struct symm_handle {
     // W before its predecessor has finished, must not read it.
     const void *last_write = nullptr;
     size_t last_write_bytes = 0;
+    // Timeline rows registered by symm_set_timeline (timeline build only).
+    unsigned long long *tl = nullptr;
+    int tl_ctas = 0;
     // TMA descriptors of recent tensor-core launches (two CUtensorMap each).
     struct MapEntry {
         const void *W = nullptr, *x = nullptr;
@@ -174,42 +179,56 @@ int reset_protocol(symm_handle *h, cudaStream_t s) {
     return SYMM_OK;
 }
 
+// SM count of a device, cached per device ordinal (atomics: host threads may
+// plan launches concurrently).
 int num_sms(int device) {
-    static int cached_dev = -1, cached = 0;
-    if (device != cached_dev) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
-        cached = v;
-        cached_dev = device;
+    static std::atomic<int> cached[64];
+    if (device >= 0 && device < 64) {
+        const int c = cached[device].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    if (device >= 0 && device < 64) cached[device].store(v, std::memory_order_relaxed);
+    return v;
 }
 
-// Kernels: 1 CUDA-core, one CTA per (tile, rank), 128-bit loads;
-// 2 tensor-core, one CTA per (tile, rank, K-split); 3 stream-K (TMA ring,
-// static partition of the K blocks); 4 persistent CTAs drawing (tile, rank)
-// units from a work counter (TMA ring, double-buffered accumulator).  Paths
-// 3 and 4 run the tcgen05 engine, or (as an option) the FFMA engine for
-// B <= kSkFfmaMaxBatch.  The automatic choice is 4 whenever K > 0 (1 for
-// K = 0, and for small W, below), with two CTAs per SM, two 64-column slabs
-// per stage and the tcgen05 engine at every batch width: the fastest
-// configuration measured on the decode (B = 1), attention-projection (B = 8)
-// and large (B = 16) shapes, and tcgen05 beat FFMA at B = 1 and 2 on every
-// shape measured (34 MB to 1.7 GB of W, packed or row-major).
-constexpr int kPathFfma = 1, kPathTc = 2, kPathSk = 3, kPathDyn = 4;
-constexpr int kSkFfmaMaxBatch = 2;
+// Kernels: 1 CUDA-core, one CTA per (tile, rank), 128-bit loads; 4
+// persistent CTAs drawing (tile, rank) units from a work counter (TMA ring,
+// double-buffered accumulator; the tcgen05 engine, or as an option the FFMA
+// engine for B <= kDynFfmaMaxBatch).  The automatic choice is 4 whenever
+// K > 0 (1 for K = 0, and for small W, below), with two CTAs per SM, two
+// 64-column slabs per stage and the tcgen05 engine at every batch width: the
+// fastest configuration measured on the decode (B = 1), attention-projection
+// (B = 8) and large (B = 16) shapes, and tcgen05 beat FFMA at B = 1 and 2 on
+// every shape measured (34 MB to 1.7 GB of W, packed or row-major).  Paths 2
+// (one tensor-core CTA per tile) and 3 (static stream-K partition) were
+// retired: neither won on any shape measured.  5 is the cluster kernel for
+// small layers: one thread-block cluster of R CTAs per row tile, the partials
+// exchanged through distributed shared memory instead of the global-memory
+// protocol (R <= 8, B <= 4).
+constexpr int kPathFfma = 1, kPathDyn = 4, kPathCluster = 5;
+constexpr int kDynFfmaMaxBatch = 2;
 
 // Below this many bytes of W a call is latency-bound: the persistent
-// kernel's start-up costs more than it saves, and for narrow batches the
-// one-CTA-per-tile CUDA-core kernel returns first (measured on 0.3-17 MB).
+// kernel's start-up costs more than it saves, and for narrow batches a
+// per-tile kernel returns first (measured on 0.3-17 MB): the cluster kernel
+// where R and B allow it, else the CUDA-core one.
 constexpr size_t kSmallWBytes = 24u << 20;
 constexpr int kSmallMaxBatch = 4;
+
+bool cluster_ok(const symm_handle *h, int N, int B) {
+    return h->R <= kMaxClusterRanks && B <= kClusterMaxBatch && (N + kClusterRows - 1) / kClusterRows <= 65535;
+}
 
 int gemv_path(const symm_handle *h, int N, int B, int Kr) {
     if (h->opt_gemv_path != 0) return h->opt_gemv_path;
     if (Kr == 0) return kPathFfma;
     const size_t wbytes = (size_t)N * (size_t)Kr * 2 * (size_t)h->R;
-    if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) return kPathFfma;
+    if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) return cluster_ok(h, N, B) ? kPathCluster : kPathFfma;
     return kPathDyn;
 }
 
@@ -217,72 +236,19 @@ int rows_per_tile_for_path(int path, int B) {
     if (B < 1 || B > SYMM_MAX_BATCH) return 0;
     switch (path) {
         case kPathFfma: return ffma_rows_per_tile(B);
-        case kPathTc: return kTcRows;
-        case kPathSk: return kTcRows;
-        case kPathDyn: return kTcRows;
+        case kPathDyn: return kDynRows;
+        case kPathCluster: return kClusterRows;
         default: return 0;
     }
 }
 
-int sk_engine(const symm_handle *h, int B) {
-    if (h->opt_sk_engine >= 0) return (h->opt_sk_engine == 1 && B > kSkFfmaMaxBatch) ? 0 : h->opt_sk_engine;
+int dyn_engine(const symm_handle *h, int B) {
+    if (h->opt_sk_engine >= 0) return (h->opt_sk_engine == 1 && B > kDynFfmaMaxBatch) ? 0 : h->opt_sk_engine;
     return 0;
 }
 
-int sk_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }
-int sk_cps(const symm_handle *h) { return h->opt_sk_cps > 0 ? h->opt_sk_cps : 2; }
-
-// CTA whose range holds block g (same arithmetic as the kernel).
-int sk_cta_of_block(long long g, long long total, int G) {
-    return (int)(((g + 1) * (long long)G + total - 1) / total) - 1;
-}
-
-// Stream-K geometry: G <= SM count CTAs over total = tiles * R * KB blocks,
-// shrunk until the parts per unit fit the scratch region and the signal pad.
-bool sk_geometry(const symm_handle *h, size_t cap, int tiles, int N, int Kr, int B, int slabs, int cps, SkGeom *geo) {
-    const long long KB = (Kr + sk_block_k(slabs) - 1) / sk_block_k(slabs);
-    const long long units = (long long)tiles * h->R;
-    const long long total = units * KB;
-    if (total <= 0 || KB > (1LL << 30)) return false;
-    // Grid: SMs x CTAs-per-SM (persistent), S CTAs per unit (-S), or explicit.
-    long long G = h->opt_sk_grid == 0 ? (long long)num_sms(h->device) * cps
-                                      : (h->opt_sk_grid < 0 ? units * (long long)(-h->opt_sk_grid) : h->opt_sk_grid);
-    G = std::min<long long>(total, std::min<long long>(G, 1LL << 30));
-    const size_t part_bytes = (size_t)B * N * 4;
-    while (G >= 1) {
-        int pmax = 1;
-        for (long long u = 0; u < units; ++u) {
-            const int P = sk_cta_of_block((u + 1) * KB - 1, total, (int)G) - sk_cta_of_block(u * KB, total, (int)G) + 1;
-            pmax = std::max(pmax, P);
-        }
-        if ((size_t)pmax * part_bytes <= cap && (long long)tiles * pmax <= h->max_tiles) {
-            geo->total = total;
-            geo->KB = (int)KB;
-            geo->G = (int)G;
-            geo->Pmax = pmax;
-            return true;
-        }
-        if (G == 1) break;
-        G = std::max<long long>(1, G * 3 / 4);
-    }
-    return false;
-}
-
-
-// K-splits per rank for the tensor-core kernel: enough CTAs for two per SM
-// when the row tiles alone are too few, limited by K blocks, scratch and pad.
-int tc_splits(const symm_handle *h, size_t cap, int tiles, int N, int Kr, int B) {
-    const int kb_total = (Kr + kTcBlockK - 1) / kTcBlockK;
-    const long long base = (long long)tiles * h->R;
-    const int sms = num_sms(h->device);
-    int S = 1;
-    if (base < sms) S = (int)std::min<long long>((2LL * sms + base - 1) / base, 16);
-    S = std::max(1, std::min(S, kb_total));
-    while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)tiles * S > h->max_tiles)) --S;
-    // no empty split: with kb_per = ceil(kb_total / S), use exactly ceil(kb_total / kb_per) splits
-    const int kb_per = (kb_total + S - 1) / S;
-    return std::max(1, (kb_total + kb_per - 1) / kb_per);
-}
+int dyn_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }
+int dyn_cps(const symm_handle *h) { return h->opt_sk_cps > 0 ? h->opt_sk_cps : 2; }
 
 const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
     for (auto &e : h->map_cache)
@@ -290,7 +256,7 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
     auto &e = h->map_cache[h->map_next];
     h->map_next = (h->map_next + 1) % 8;
     e.W = nullptr;
-    *err = tc_encode_maps(a, e.maps);
+    *err = dyn_encode_maps(a, e.maps);
     if (*err != 0) return nullptr;
     e.W = a.W;
     e.x = a.x;
@@ -303,7 +269,6 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 // The kernel and launch geometry gemv_all_reduce would use.
 struct Plan {
     int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
-    SkGeom geo = {0, 0, 0, 1};
     DynGeom dyn = {0, 1, 0, 0, 0};
 };
 
@@ -321,33 +286,30 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
             return fail(SYMM_EINVAL, "a packed weight is read by the persistent kernel (path 4) only");
         pl->path = kPathDyn;
     }
+    if (h->opt_unfused) {
+        if (Kr == 0 || (h->opt_gemv_path != 0 && h->opt_gemv_path != kPathDyn))
+            return fail(SYMM_EINVAL, "the unfused form runs on the persistent kernel (path 4, K > 0) only");
+        pl->path = kPathDyn;
+    }
+    if (pl->path == kPathCluster && !cluster_ok(h, N, B))
+        return fail(SYMM_EINVAL, "the cluster kernel (path 5) needs R <= %d, B <= %d and at most 65535 row tiles",
+                    kMaxClusterRanks, kClusterMaxBatch);
     pl->rows = rows_per_tile_for_path(pl->path, B);
     if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     pl->tiles = (N + pl->rows - 1) / pl->rows;
     if (pl->tiles > h->max_tiles)
         return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", pl->tiles, h->max_tiles);
-    pl->splits = pl->path == kPathTc ? tc_splits(h, cap, pl->tiles, N, Kr, B) : 1;
-    pl->grid = pl->tiles * h->R * pl->splits;
-    if (pl->path == kPathSk) {
-        if (Kr == 0) return fail(SYMM_EINVAL, "the stream-K kernel needs K > 0");
-        pl->engine = sk_engine(h, B);
-        pl->slabs = sk_slabs(h);
-        pl->cps = h->opt_sk_cps > 0 ? h->opt_sk_cps : 1;   // stream-K: 2 CTAs do not fit the registers
-        if (!sk_config_supported(pl->slabs, pl->cps))
-            return fail(SYMM_EINVAL, "stream-K has no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
-        if (!sk_geometry(h, cap, pl->tiles, N, Kr, B, pl->slabs, pl->cps, &pl->geo))
-            return fail(SYMM_ERANGE, "stream-K partials do not fit the scratch region or the signal pad");
-        pl->grid = pl->geo.G;
-    }
+    pl->splits = 1;
+    pl->grid = pl->tiles * h->R;
     if (pl->path == kPathDyn) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the persistent kernel needs K > 0");
-        pl->engine = sk_engine(h, B);
-        pl->slabs = sk_slabs(h);
-        pl->cps = sk_cps(h);
-        if (!sk_config_supported(pl->slabs, pl->cps))
+        pl->engine = dyn_engine(h, B);
+        pl->slabs = dyn_slabs(h);
+        pl->cps = dyn_cps(h);
+        if (!dyn_config_supported(pl->slabs, pl->cps))
             return fail(SYMM_EINVAL, "no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
         const long long pairs = (long long)pl->tiles * h->R;
-        const long long KB = (Kr + sk_block_k(pl->slabs) - 1) / sk_block_k(pl->slabs);
+        const long long KB = (Kr + dyn_block_k(pl->slabs) - 1) / dyn_block_k(pl->slabs);
         if (pairs > (1LL << 26)) return fail(SYMM_ERANGE, "too many row tiles");
         long long G = h->opt_sk_grid > 0 ? h->opt_sk_grid : (long long)num_sms(h->device) * pl->cps;
         // K splits: the requested count (option), else none; limited by the K
@@ -372,7 +334,6 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         pl->dyn.G = (int)G;
         pl->splits = (int)S;
         pl->grid = (int)G;
-        pl->geo.KB = (int)KB;
     }
     return SYMM_OK;
 }
@@ -447,12 +408,13 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
         z_off = (h->scratch_bytes - zbytes) / 256 * 256;
         cap = z_off;
     }
+    if (h->opt_unfused && ep.mode != kOutAllReduce)
+        return fail(SYMM_EINVAL, "the unfused form (SYMM_OPT_UNFUSED) is a form of gemv_all_reduce only");
     Plan pl;
     int rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
     if (rc != SYMM_OK) return rc;
     const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
               slabs = pl.slabs, cps = pl.cps;
-    const SkGeom geo = pl.geo;
     const DynGeom dyn = pl.dyn;
     rc = check_device(h);
     if (rc != SYMM_OK) return rc;
@@ -485,33 +447,33 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.partial_stride = (long long)B * N * 4;
     a.kc_cap = 0;
     a.out_mode = ep.mode;
-    a.chained = h->opt_chain;   // paths 1-3 (path 4 decides below)
+    a.chained = h->opt_chain;   // path 1 (path 4 decides below)
     a.rs_rows = ep.mode == kOutReduceScatter ? B / R : B;
     a.z = ep.mode == kOutBiasZ ? reinterpret_cast<float *>(h->base + h->scratch_off + z_off) : nullptr;
     a.bias = ep.mode == kOutBiasZ ? static_cast<const uint8_t *>(ep.bias) : nullptr;
     a.w_packed = pw != nullptr && path == kPathDyn;
+    // Early W loads (before the wait for the previous kernel) only for a
+    // packed weight: it is written by symm_pack_w alone, and a call whose
+    // packed weight the handle's last kernel wrote is not chained (below).
+    a.w_early = a.w_packed;
+    if (h->opt_unfused) a.out_mode = kOutPartials;
+    a.tl = h->tl;
+    a.tl_ctas = h->tl_ctas;
     cudaError_t e = cudaSuccess;
     switch (path) {
         case kPathFfma:
             a.kc_cap = ffma_kc_cap(B, Kr);
             e = launch_gemv_ffma(a, s);
             break;
-        case kPathTc:
-        case kPathSk:
+        case kPathCluster:
+            e = launch_gemv_cluster(a, s);
+            break;
         case kPathDyn: {
-            if (Kr == 0) return fail(SYMM_EINVAL, "the tensor-core kernel needs K > 0");
             int err = 0;
             const void *maps = tc_maps_for(h, a, &err);
             if (!maps) return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
-            if (path == kPathTc) {
-                e = launch_gemv_tc(a, maps, s);
-            } else if (path == kPathDyn) {
-                const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_write, h->last_write_bytes);
-                e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, chained, s);
-            } else {
-                a.partial_stride = (long long)B * N * 4;
-                e = launch_gemv_sk(a, geo, maps, engine, slabs, cps, s);
-            }
+            const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_write, h->last_write_bytes);
+            e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, chained, s);
             break;
         }
         default:
@@ -519,6 +481,24 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     }
     if (e != cudaSuccess) return cuda_fail(e, "gemv_all_reduce launch");
     note_write(h, y, ybytes);   // by the GEMV, or by the norm stage launched next
+    if (h->opt_unfused) {
+        // The unfused form's all-reduce of the partials, a programmatic
+        // dependent of the GEMV (it waits for the GEMV before reading).
+        PartialsArArgs pa;
+        pa.scratch = a.scratch;
+        pa.y = a.y;
+        pa.stride = a.stride;
+        pa.partial_stride = a.partial_stride;
+        pa.R = h->R;
+        pa.splits = splits;
+        pa.B = B;
+        pa.N = N;
+        pa.vec = ((size_t)B * (size_t)N) % 4 == 0;
+        pa.chained = 1;
+        e = launch_partials_ar(pa, s);
+        if (e != cudaSuccess) return cuda_fail(e, "unfused all-reduce launch");
+        return SYMM_OK;
+    }
     if (ep.mode == kOutBiasZ) {
         RmsNormArgs n = {};
         n.z = a.z;
@@ -643,8 +623,11 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
     switch (option) {
         case SYMM_OPT_GEMV_PATH:
-            if (value < 0 || value > 4)
-                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1..4)", value);
+            if (value == 2 || value == 3)
+                return fail(SYMM_EINVAL, "GEMV path %d was retired (0 auto, 1 CUDA-core, 4 persistent, 5 cluster)",
+                            value);
+            if (value < 0 || value > 5)
+                return fail(SYMM_EINVAL, "GEMV path %d unknown (0 auto, 1 CUDA-core, 4 persistent, 5 cluster)", value);
             h->opt_gemv_path = value;
             return SYMM_OK;
         case SYMM_OPT_TILE_ORDER:
@@ -653,15 +636,15 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             return SYMM_OK;
         case SYMM_OPT_SK_SLABS:
             if (value < 0 || value > 4)
-                return fail(SYMM_EINVAL, "stream-K slabs %d not in {0 auto, 1, 2, 3, 4}", value);
+                return fail(SYMM_EINVAL, "persistent-kernel slabs %d not in {0 auto, 1, 2, 3, 4}", value);
             h->opt_sk_slabs = value;
             return SYMM_OK;
         case SYMM_OPT_SK_ENGINE:
-            if (value < -1 || value > 1) return fail(SYMM_EINVAL, "stream-K engine %d not in {-1 auto, 0, 1}", value);
+            if (value < -1 || value > 1) return fail(SYMM_EINVAL, "persistent-kernel engine %d not in {-1 auto, 0, 1}", value);
             h->opt_sk_engine = value;
             return SYMM_OK;
         case SYMM_OPT_SK_GRID:
-            if (value < -16) return fail(SYMM_EINVAL, "stream-K grid %d: 0 auto, -S (S = 1..16 CTAs per unit) or > 0", value);
+            if (value < 0) return fail(SYMM_EINVAL, "persistent grid %d: 0 auto or a CTA count > 0", value);
             h->opt_sk_grid = value;
             return SYMM_OK;
         case SYMM_OPT_DYN_SPLITS:
@@ -688,8 +671,12 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 1) return fail(SYMM_EINVAL, "RMSNorm-stage PDL %d not in {0, 1}", value);
             h->opt_norm_pdl = value;
             return SYMM_OK;
+        case SYMM_OPT_UNFUSED:
+            if (value < 0 || value > 1) return fail(SYMM_EINVAL, "unfused %d not in {0, 1}", value);
+            h->opt_unfused = value;
+            return SYMM_OK;
         case SYMM_OPT_SK_CTAS_PER_SM:
-            if (value < 0 || value > 3) return fail(SYMM_EINVAL, "stream-K CTAs per SM %d not in 0..3", value);
+            if (value < 0 || value > 3) return fail(SYMM_EINVAL, "persistent-kernel CTAs per SM %d not in 0..3", value);
             h->opt_sk_cps = value;
             return SYMM_OK;
         default:
@@ -711,8 +698,8 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
     out->tiles = pl.tiles;
     out->splits = pl.splits;
     out->grid = pl.grid;
-    out->parts_max = pl.geo.Pmax;
-    out->kblocks = pl.geo.KB;
+    out->parts_max = 1;
+    out->kblocks = pl.dyn.KB;
     out->ctas_per_sm = pl.cps;
     return SYMM_OK;
 }
@@ -931,6 +918,8 @@ int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, 
                          !overlaps(gamma, gamma ? vb : 0, h->last_write, h->last_write_bytes);
     a.wait_prior = chained;
     a.release_next = chained;
+    a.tl = h->tl;
+    a.tl_ctas = h->tl_ctas;
     cudaError_t e = launch_rmsnorm_rows(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "all_reduce_bias_rmsnorm launch");
     note_write(h, out, bytes);
@@ -992,6 +981,20 @@ int tile_reduce(symm_handle_t *h, const void *in_tile, void *out_tile, int root,
     const void *tiles[1] = {in_tile};
     const int roots[1] = {root};
     return multi_root_tile_reduce(h, tiles, out_tile, roots, 1, rows, cols, ld_in, ld_out, stream);
+}
+
+int symm_set_timeline(symm_handle_t *h, void *buf, size_t bytes) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (!buf || bytes == 0) {
+        h->tl = nullptr;
+        h->tl_ctas = 0;
+        return SYMM_OK;
+    }
+    if (!kTimeline) return fail(SYMM_EINVAL, "this library was built without timeline stamps (-DSYMM_TIMELINE)");
+    if (reinterpret_cast<uintptr_t>(buf) % 8) return fail(SYMM_EINVAL, "the timeline buffer must be 8-byte aligned");
+    h->tl = static_cast<unsigned long long *>(buf);
+    h->tl_ctas = (int)std::min<size_t>(bytes / (sizeof(unsigned long long) * kTlSlots), 1u << 30);
+    return SYMM_OK;
 }
 
 int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile) {

@@ -404,21 +404,24 @@ int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *
 /* Per-handle options.  The kernel choice is automatic by default; the
  * others exist for tests and measurements. */
 enum {
-    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto (4 when K > 0, else 1); 1 CUDA-core kernel, one CTA per (row tile, rank);
-                                 2 tensor-core kernel, one CTA per (tile, rank, K-split);
-                                 3 stream-K kernel (TMA ring, static partition of the K blocks);
-                                 4 persistent kernel drawing (tile, rank) units from a work counter */
+    SYMM_OPT_GEMV_PATH = 1,   /* 0 auto: 4 when K > 0 and W_r of all ranks is over 24 MB or B > 4; else 5
+                                 when R <= 8 and B <= 4; else 1.  1 CUDA-core kernel, one CTA per (row
+                                 tile, rank); 4 persistent kernel drawing (tile, rank) units from a work
+                                 counter; 5 cluster kernel for small layers, one thread-block cluster of R
+                                 CTAs per 16-row tile, the partials exchanged through distributed shared
+                                 memory (R <= 8, B <= 4, else SYMM_EINVAL; it uses no scratch and no
+                                 signal pad).  2 and 3 (a tensor-core kernel per tile and a static
+                                 stream-K partition) were retired: neither won on any shape measured;
+                                 they return SYMM_EINVAL */
     SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
-    SYMM_OPT_SK_SLABS = 3,    /* paths 3, 4: 64-column slabs per pipeline stage, 0 auto (2), 1..4 (the
+    SYMM_OPT_SK_SLABS = 3,    /* path 4: 64-column slabs per pipeline stage, 0 auto (2), 1..4 (the
                                  instantiated pipelines: 1, 2, 4 slabs at 1 CTA per SM; 1, 2, 3 at 2; 1 at 3) */
-    SYMM_OPT_SK_ENGINE = 4,   /* paths 3, 4: -1 auto (tcgen05), 0 tcgen05, 1 FFMA (B <= 2; wider batches run
+    SYMM_OPT_SK_ENGINE = 4,   /* path 4: -1 auto (tcgen05), 0 tcgen05, 1 FFMA (B <= 2; wider batches run
                                  tcgen05) */
-    SYMM_OPT_SK_CTAS_PER_SM = 5, /* paths 3, 4: CTAs per SM the ring is sized for, 0 auto (2 for path 4,
-                                 1 for path 3), 1..3 (the ring shrinks).  By their registers the
-                                 kernels hold fewer CTAs per SM than that in some configurations
-                                 (path 4 at 3; path 3 at 2 or 3): the grid then runs in two waves,
-                                 correctly but slower */
-    SYMM_OPT_SK_GRID = 6,     /* stream-K: 0 auto, -S = S CTAs per (tile, rank) (S = 1..16), or a CTA count */
+    SYMM_OPT_SK_CTAS_PER_SM = 5, /* path 4: CTAs per SM the ring is sized for, 0 auto (2), 1..3 (the ring
+                                 shrinks).  By its registers the kernel holds fewer CTAs per SM than 3:
+                                 at 3 the grid runs in two waves, correctly but slower */
+    SYMM_OPT_SK_GRID = 6,     /* path 4: persistent grid, 0 auto (CTAs per SM x SMs) or a CTA count */
     SYMM_OPT_DYN_SPLITS = 7,  /* persistent kernel: K splits per (tile, rank), 0 auto, 1..16 */
     SYMM_OPT_NORM_PDL = 8,    /* gemv_all_reduce_bias_rmsnorm: 1 (default) launches the RMSNorm stage as a
                                  programmatic dependent of the GEMV so its launch overlaps the GEMV's
@@ -428,12 +431,14 @@ enum {
                                  overlap one call's start-up with the previous call's end; each lets its
                                  successor be scheduled early.  A chained kernel reads nothing before its
                                  predecessor has finished, with two exceptions: the persistent fused
-                                 kernel (path 4) loads W for its first stages early, and the standalone
-                                 all-reduce + bias + RMSNorm loads gamma and bias early.  Such a call is
-                                 launched in plain stream order when those operands overlap the output
-                                 of the last call on the same handle (any call); they must not be
-                                 written by any other kernel launched just before it on the stream.
-                                 0: plain stream order always */
+                                 kernel (path 4) loads a packed weight (symm_pack_w) for its first stages
+                                 early (a row-major W_r is loaded after the wait, like x), and the
+                                 standalone all-reduce + bias + RMSNorm loads gamma and bias early.  Such
+                                 a call is launched in plain stream order when those operands overlap
+                                 the output of the last call on the same handle (any call, symm_pack_w
+                                 included).  A packed weight is written by symm_pack_w only; gamma and
+                                 bias must not be written by any other kernel launched just before the
+                                 call on the stream.  0: plain stream order always */
     SYMM_OPT_AR_CTAS_PER_SM = 10, /* one_shot_all_reduce (per-thread kernel), two_shot_all_reduce,
                                  reduce_scatter: grid cap in CTAs (256 threads) per SM, grid-stride beyond
                                  it; 0 auto (16) */
@@ -441,10 +446,16 @@ enum {
                                  stores, 2 staged: each CTA reduces a contiguous range chunk by chunk in
                                  shared memory, moved in and out by bulk (TMA) copies (measured slower
                                  than 1 from 0.5 MB per rank up) */
-    SYMM_OPT_COPY_ENGINE = 12 /* symm_copy_to_slots / from_slots: 0 (default) copy with a kernel when the
+    SYMM_OPT_COPY_ENGINE = 12, /* symm_copy_to_slots / from_slots: 0 (default) copy with a kernel when the
                                  contiguous side is device memory or pinned host memory mapped at the same
                                  address (a link in the chain of programmatic dependent launches, see
                                  SYMM_OPT_CHAIN), else with the copy engine; 1 always the copy engine */
+    SYMM_OPT_UNFUSED = 13     /* gemv_all_reduce only, for measuring what fusion buys: 1 runs the call
+                                 unfused, as two kernels -- the persistent GEMV (path 4) storing every
+                                 rank's fp32 partials, then a separate all-reduce kernel that sums them in
+                                 the fused reducer's order and stores bf16 into every slot (the same
+                                 bits as the fused call); 0 (default) fused.  The other forms, path 1
+                                 and K == 0 return SYMM_EINVAL while it is set */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 
@@ -463,15 +474,15 @@ int symm_info(symm_handle_t *h, symm_info_t *info);
  * SYMM_ERANGE exactly as the call would return them).  A call on a packed
  * weight (symm_pack_w) runs path 4 with the plan reported while
  * SYMM_OPT_GEMV_PATH is 4.
- *   path           1 CUDA-core, 2 tensor-core per tile, 3 stream-K, 4 persistent dynamic
- *   engine         stream-K compute engine: 0 tcgen05, 1 FFMA
- *   slabs          stream-K 64-column slabs per pipeline stage
+ *   path           1 CUDA-core per tile, 4 persistent dynamic, 5 cluster per tile
+ *   engine         path 4 compute engine: 0 tcgen05, 1 FFMA
+ *   slabs          path 4: 64-column slabs per pipeline stage
  *   rows_per_tile  output rows per tile; tiles = ceil(N / rows_per_tile)
- *   splits         K-splits per rank (paths 2 and 4)
+ *   splits         K-splits per rank (path 4)
  *   grid           CTAs launched
- *   parts_max      stream-K: most partials one (tile, rank) is cut into
- *   kblocks        stream-K: K blocks per (tile, rank)
- *   ctas_per_sm    stream-K: resident CTAs per SM */
+ *   parts_max      1 (kept for layout compatibility)
+ *   kblocks        path 4: K blocks per (tile, rank)
+ *   ctas_per_sm    path 4: resident CTAs per SM the ring is sized for */
 typedef struct {
     int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks, ctas_per_sm;
 } symm_gemv_plan_t;
@@ -513,6 +524,19 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
  */
 int gemv_all_reduce_noalloc(const void *W_r, const void *x_r, void *y, size_t stride, int R, int N, int K,
                             int B, symm_stream_t stream);
+
+/*
+ * symm_set_timeline -- diagnostics: register a device buffer that the
+ * kernels of later calls on this handle fill with per-CTA %globaltimer
+ * stamps at their phase boundaries (one row of 16 unsigned 64-bit words per
+ * CTA, row = the CTA's linear index; which slot holds which phase is listed
+ * in each kernel's source).  Only the timeline build of this library
+ * (-DSYMM_TIMELINE) writes stamps; the product build returns SYMM_EINVAL for a
+ * non-NULL buffer.  CTAs whose row does not fit in `bytes` write nothing.
+ * buf == NULL (or bytes == 0) switches the timeline off.  The buffer is
+ * borrowed: it must stay valid while calls that may write it run.  No counterpart on the pages.
+ */
+int symm_set_timeline(symm_handle_t *h, void *buf, size_t bytes);
 
 /* Release the handle; frees owned memory (synchronises the device first). */
 int symm_free(symm_handle_t *h);

@@ -4,12 +4,13 @@
 //
 // R threads play the R ranks.  A launch reads its epoch e from the epoch
 // word (one more than the last finished launch).  Each rank, for every tile t
-// of the launch in its own (shuffled) order, writes its partial of tile t,
-// release-stores its flag flags[r][t] = e and takes an arrival ticket with an
-// acq_rel fetch_add on counters[t].  Tickets run 0..R-1 in every launch; the
-// holder of R-1 counts the tile on tiles_done, puts the counter back to zero,
-// acquires the R flags (each must equal e), sums the R partials in rank order
-// 0..R-1 and writes y[t]; the reducer of the last tile stores e into the
+// of the launch in its own (shuffled) order, writes its partial of tile t and
+// its flag flags[r][t] = e (relaxed), fences, and takes an arrival ticket
+// with an acq_rel fetch_add on counters[t].  Tickets run 0..R-1 in every
+// launch; the holder of R-1 counts the tile on tiles_done, puts the counter
+// back to zero, reads the R flags (each must equal e; the acq_rel ticket
+// orders these loads after every rank's fenced stores), sums the R partials
+// in rank order 0..R-1 and writes y[t]; the reducer of the last tile stores e into the
 // epoch word and clears tiles_done.  No thread waits for another; a ticket out of
 // range or a stale flag latches a status code, and a rank made to skip a tile
 // latches the code of a CTA that gave up (as the kernels' bounded waits do).
@@ -39,7 +40,7 @@ struct Shared {
     std::vector<std::atomic<uint32_t>> counters;  // [T]
     std::atomic<uint32_t> epoch_word{0};          // epoch of the last finished launch
     std::atomic<uint32_t> tiles_done{0};
-    std::vector<double> partial;                  // [R][T] (plain: ordered by the flag release / acquire)
+    std::vector<double> partial;                  // [R][T] (plain: ordered by the fence and the acq_rel ticket)
     std::vector<double> y;                        // [T]
     std::atomic<int> status{0};
     std::atomic<int> bad_tile{-1};
@@ -77,7 +78,8 @@ void rank_launch(int r, int tiles, const double *values, unsigned seed, int skip
         }
         if (max_sleep_us > 0) std::this_thread::sleep_for(std::chrono::microseconds(pause(rng)));
         g->partial[(size_t)r * g->T + t] = values[(size_t)r * g->T + t];
-        g->flags[(size_t)r * g->T + t].store(t == stale_tile ? epoch - 1 : epoch, std::memory_order_release);
+        g->flags[(size_t)r * g->T + t].store(t == stale_tile ? epoch - 1 : epoch, std::memory_order_relaxed);
+        std::atomic_thread_fence(std::memory_order_release);
         const uint32_t pos = g->counters[(size_t)t].fetch_add(1u, std::memory_order_acq_rel);
         if (pos >= C) {
             latch(2, t);   // bad ticket: launches overlapped or the pad was not reset
@@ -91,7 +93,7 @@ void rank_launch(int r, int tiles, const double *values, unsigned seed, int skip
         g->counters[(size_t)t].store(0u, std::memory_order_relaxed);
         bool ok = true;
         for (int q = 0; q < g->R; ++q)
-            if (g->flags[(size_t)q * g->T + t].load(std::memory_order_acquire) != epoch) ok = false;
+            if (g->flags[(size_t)q * g->T + t].load(std::memory_order_relaxed) != epoch) ok = false;
         if (done >= (uint32_t)tiles) latch(2, t);
         if (done == (uint32_t)tiles - 1u) {   // the last tile: every rank has read the epoch
             std::atomic_thread_fence(std::memory_order_acquire);

@@ -290,7 +290,7 @@ def test_all_reduce_bias_rmsnorm_bad_arguments():
 
 # ------------------------------------- the fused layer's other two endings
 
-PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC, csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN]
+PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_DYN]
 
 
 def _gemv_ws(W, x, path):

@@ -19,7 +19,7 @@ from helpers import f64_to_words_via_f32, tolerance_ratio, ulp_distance, words_t
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_TC, csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN]
+PATHS = [csg.GEMV_PATH_AUTO, csg.GEMV_PATH_FFMA, csg.GEMV_PATH_DYN]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -251,6 +251,10 @@ def test_corrupted_counter_is_reported_and_recovered():
     y_ref, y_or = oracle.gemv_all_reduce(W, x)
     ws = GemvWorkspace(R, N, K, B)
     try:
+        # the per-tile kernel of the global-memory protocol (the automatic
+        # choice for so small a layer is the cluster kernel, which keeps no
+        # state in the pad)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_FFMA)
         ws.load_W(W)
         ws.load_x(x)
         s = torch.cuda.current_stream()
@@ -304,7 +308,7 @@ def test_shape_changes_on_one_handle(path):
         ws.close()
 
 
-@pytest.mark.parametrize("path", [csg.GEMV_PATH_FFMA, csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN])
+@pytest.mark.parametrize("path", [csg.GEMV_PATH_FFMA, csg.GEMV_PATH_DYN])
 def test_many_launches_leave_the_pad_consistent(path):
     R, N, K, B = 8, 1000, 8 * 512, 2
     W, x = _normal_case(R, N, K, B, seed=17)
@@ -328,7 +332,7 @@ def test_many_launches_leave_the_pad_consistent(path):
         ws.close()
 
 
-# ------------------------------------------------------ stream-K variants
+# ------------------------------------------- persistent-kernel variants
 
 SK_PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (3, 2), (1, 3)]   # (slabs, CTAs per SM)
 SK_VARIANTS = [(engine, slabs, cps) for engine in (0, 1) for slabs, cps in SK_PIPES]
@@ -336,13 +340,12 @@ SK_SHAPES = [(8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1), (3
              (8, 2048, 8 * 512, 1)]
 
 
-@pytest.mark.parametrize("path", [csg.GEMV_PATH_SK, csg.GEMV_PATH_DYN], ids=["streamk", "persistent"])
+@pytest.mark.parametrize("path", [csg.GEMV_PATH_DYN], ids=["persistent"])
 @pytest.mark.parametrize("engine,slabs,cps", SK_VARIANTS,
                          ids=[f"eng{e}-slabs{s}-cps{c}" for e, s, c in SK_VARIANTS])
 @pytest.mark.parametrize("shape", SK_SHAPES, ids=[f"R{a}N{b}K{c}B{d}" for a, b, c, d in SK_SHAPES])
 def test_tma_kernels_engines_and_pipelines(path, engine, slabs, cps, shape):
-    """The stream-K and the persistent TMA kernels, both engines, every
-    pipeline shape: integer inputs bit-exact, normal inputs within tolerance,
+    """The persistent TMA kernel, both engines, every pipeline shape: integer inputs bit-exact, normal inputs within tolerance,
     replicas identical, reversed CTA / unit order identical."""
     R, N, K, B = shape
     for kind in ("int", "normal"):

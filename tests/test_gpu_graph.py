@@ -22,7 +22,7 @@ from gpu_common import check_gemv, require_gpu
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"ffma": csg.GEMV_PATH_FFMA, "tc": csg.GEMV_PATH_TC, "sk": csg.GEMV_PATH_SK, "dyn": csg.GEMV_PATH_DYN}
+PATHS = {"ffma": csg.GEMV_PATH_FFMA, "dyn": csg.GEMV_PATH_DYN}
 WORK_OFF, EPOCH_OFF, DONE_OFF = 64, 96, 112   # slot 0's pad: work[2], epoch, tiles_done
 
 
@@ -218,29 +218,3 @@ def test_captured_collectives(op):
     finally:
         aw.close()
         nw.close()
-
-
-def test_captured_noalloc_call():
-    """The allocation-free entry point after its first (eager) call."""
-    R, N, K, B = 4, 576, 2048, 2
-    W, x = _case(R, N, K, B, seed=67)
-    ws = GemvWorkspace(R, N, K, B)
-    try:
-        ws.load_W(W)
-        ws.load_x(x)
-        s = torch.cuda.current_stream()
-        args = (ws.W_ptr(), ws.x_ptr(), ws.y_ptr(), ws.stride, R, N, K, B)
-        csg.gemv_all_reduce_noalloc(*args, s)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            csg.gemv_all_reduce_noalloc(*args, torch.cuda.current_stream())
-        for i in range(3):
-            _, x = synth.gemv_inputs(R, N, K, B, seed=70 + i, w_std=1.0, x="normal")
-            ws.load_x(x)
-            ws.fill_y(0xFF)
-            g.replay()
-            check_gemv(W, x, ws.read_y())
-        del g
-    finally:
-        ws.close()

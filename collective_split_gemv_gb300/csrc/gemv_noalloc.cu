@@ -29,7 +29,12 @@
 // Set-up: the first call on each device, with that device current, looks up
 // the array's device address with cudaGetSymbolAddress (host code cannot use
 // the array's name as a device pointer).  Make that first call before any
-// stream capture.
+// stream capture.  The address is cached per device together with the
+// identity of the CUDA context it was looked up in: after the context is torn
+// down and created again (cudaDeviceReset, or the primary context released
+// and retained anew) the array may have moved, and the next call on that
+// device looks the address up again.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -221,9 +226,42 @@ cudaError_t launch(const NoAllocArgs &a, cudaStream_t s) {
 
 std::mutex g_setup_mu;
 void *g_scratch_ptr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];   // context ID the address was looked up in
 
-// Device address of the fixed array on the current device (looked up once
-// per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Unique ID of the calling thread's current CUDA context (the driver's
+// cuCtxGetId, reached through the runtime's entry-point query); 0 if it
+// cannot be had.  Called with a device current, after the runtime has
+// initialised it.
+unsigned long long current_context_id() {
+    static const CtxGetCurrentFn get_current = []() -> CtxGetCurrentFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(p);
+        return nullptr;
+    }();
+    static const CtxGetIdFn get_id = []() -> CtxGetIdFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetIdFn>(p);
+        return nullptr;
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the fixed array on the current device: looked up once
+// per device and context (a context created anew may hold the array
+// elsewhere).
 int scratch_address(void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -233,8 +271,21 @@ int scratch_address(void **out) {
         return report_error(SYMM_ECUDA, msg);
     }
     if (dev < 0 || dev >= kMaxDevices) return report_error(SYMM_EINVAL, "device ordinal out of range");
+    unsigned long long ctx = current_context_id();
+    if (ctx == 0) {
+        // No context is current on this thread yet: cudaSetDevice on the
+        // current device makes the runtime create or bind that device's
+        // primary context (it allocates nothing), the one the launch will run
+        // in.
+        e = cudaSetDevice(dev);
+        if (e != cudaSuccess) {
+            snprintf(msg, sizeof msg, "initialising the device's context: %s", cudaGetErrorString(e));
+            return report_error(SYMM_ECUDA, msg);
+        }
+        ctx = current_context_id();
+    }
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) {
@@ -242,6 +293,7 @@ int scratch_address(void **out) {
             return report_error(SYMM_ECUDA, msg);
         }
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return SYMM_OK;

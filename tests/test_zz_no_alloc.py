@@ -18,7 +18,7 @@ import oracle
 import synth
 from collective_split_gemv_gb300.workspace import GemvWorkspace
 from gpu_common import require_gpu
-from helpers import tolerance_ratio, words_to_f64
+from helpers import f64_to_words_via_f32, tolerance_ratio, words_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,7 @@ def test_noalloc_matches_gemv_all_reduce(R, N, K, B):
         ws.run(s)
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
         y_existing = words_to_f64(ws.read_y()[0])
+        outs = []
         for _ in range(2):   # two calls in a row share (and reuse) the fixed array
             ws.fill_y(0xFF)
             csg.gemv_all_reduce_noalloc(ws.W_ptr(), ws.x_ptr(), ws.y_ptr(), ws.stride, R, N, K, B, s)
@@ -63,6 +64,47 @@ def test_noalloc_matches_gemv_all_reduce(R, N, K, B):
             got = words_to_f64(y[0])
             assert tolerance_ratio(got, y_existing) <= 1.0
             assert tolerance_ratio(got, y_oracle) <= 1.0
+            outs.append(y)
+        # the second call, on an array the first one left behind, gives the
+        # first call's bits
+        assert np.array_equal(outs[1], outs[0]), "the second call's bits differ from the first's"
+        assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
+    finally:
+        ws.close()
+
+
+INT_CASES = [(2, 256, 2 * 256, 1), (3, 77, 3 * 40, 5), (8, 300, 8 * 24, 16)]
+
+
+@pytest.mark.parametrize("R,N,K,B", INT_CASES, ids=[f"R{c[0]}N{c[1]}K{c[2]}B{c[3]}" for c in INT_CASES])
+def test_noalloc_small_integers_bit_exact(R, N, K, B):
+    """Small-integer inputs make every product and partial sum an exact
+    integer in fp32, so the allocation-free call must give the oracle's bf16
+    words exactly, on two calls in a row (the second reuses the shared array
+    the first one left behind), and the same words as gemv_all_reduce."""
+    rng = np.random.default_rng(N + B)
+    W = f64_to_words_via_f32(rng.integers(-8, 9, size=(R, N, K // R)).astype(np.float64))
+    x = f64_to_words_via_f32(rng.integers(-8, 9, size=(R, B, K // R)).astype(np.float64))
+    _, y_or = oracle.gemv_all_reduce(W, x)
+    ws = GemvWorkspace(R, N, K, B)
+    try:
+        ws.load_W(W)
+        ws.load_x(x)
+        s = torch.cuda.current_stream()
+        ws.fill_y(0xFF)
+        ws.run(s)
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        y_existing = ws.read_y()
+        outs = []
+        for _ in range(2):
+            ws.fill_y(0xFF)
+            csg.gemv_all_reduce_noalloc(ws.W_ptr(), ws.x_ptr(), ws.y_ptr(), ws.stride, R, N, K, B, s)
+            y = ws.read_y()
+            for r in range(R):
+                assert np.array_equal(y[r], y_or[0]), f"rank {r}'s y differs from the oracle's words"
+            outs.append(y)
+        assert np.array_equal(outs[1], outs[0])
+        assert np.array_equal(outs[0], y_existing), "differs from gemv_all_reduce"
         assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
     finally:
         ws.close()

@@ -332,6 +332,27 @@ def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id, p
     return step_ms, launch_ms, clocks
 
 
+def empty_launch_floor(stream, dev, flush_buf, n=50):
+    """CUDA-event time of an empty kernel (torch.cuda._sleep(0)) launched in
+    the per-launch pattern of timed_loop (events around each launch, the L2
+    flush between launches where there is one): the launch and completion
+    cost that every per-launch figure carries whatever the kernel does."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            if flush_buf is not None:
+                flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            torch.cuda._sleep(0)
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+
 def chunked_spread(step, n_steps, stream, dev, world, chunk=None):
     """The same n_steps chained calls once more, with an event after every
     `chunk` calls (each event ends one chain: the call after it starts in
@@ -541,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
     # launches would separate them on the stream.
     step_ms, launch_ms, clocks = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,
                                             per_launch=not chained)
+    floor_ms = empty_launch_floor(stream, dev, flush_buf)
     unchained = None
     spread = None
     if chained:
@@ -701,6 +723,7 @@ def run_ours(args, rank, world, local_rank):
             "mean_launch_us": round(mean_launch_ms * 1e3, 3),
             "median_launch_us": round(statistics.median(spread[0] if spread else launch_ms) * 1e3, 3),
             "p10_p90_launch_us": [round(q * 1e3, 3) for q in _p10_p90(spread[0] if spread else launch_ms)],
+            "empty_launch_us": round(floor_ms * 1e3, 3),
             "timing": ((f"chained calls: region time / steps (events around the region only); median and "
                         f"p10 / p90 over {len(spread[0])} chunks of {spread[1]} chained calls timed again "
                         f"(an event after each chunk)") if chained

@@ -192,19 +192,24 @@ static_assert(kM == kPackRows && kSlabA == (int)kPackBlockBytes, "a stage slab i
 // of the row-major W_r, or the same bytes as one contiguous block of the
 // packed layout (past the last slab: the slot's zero block, as the tensor
 // map's fill would give).
+// W is read once per call: its lines are marked evict-first in L2, so that
+// the stream does not push out what is read again soon (x, the partials).
 __device__ __forceinline__ void load_w_slab(uint8_t *dst, const CUtensorMap *tmW, const GemvArgs &a, uint64_t *bar,
-                                            int j, int t, int r) {
+                                            int j, int t, int r, uint64_t policy) {
     if (a.w_packed) {
         const int J = (a.Kr + kPackCols - 1) / kPackCols;
         const size_t blk = j < J ? (size_t)t * J + j : (size_t)a.num_tiles * J;
-        bulk_load(dst, a.W + (long long)r * a.stride + blk * kPackBlockBytes, (uint32_t)kPackBlockBytes, bar);
+        bulk_load_hint(dst, a.W + (long long)r * a.stride + blk * kPackBlockBytes, (uint32_t)kPackBlockBytes, bar,
+                       policy);
     } else {
-        tma_load_3d(dst, tmW, bar, j * 64, t * kM, r);
+        tma_load_3d_hint(dst, tmW, bar, j * 64, t * kM, r, policy);
     }
 }
 
+// At two CTAs per SM the register file must hold both (at most 168
+// registers a thread); the three-CTA rings do not fit it and run in two waves.
 template <int kEngine, int kSlabs, int kB, int kCps>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemvArgs a, const DynGeom geo) {
     // Dependents of this launch (the RMSNorm stage, or the next fused call
@@ -277,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // other thread waits for it here; the wait returns at once when the
     // launch was not a programmatic dependent.
     int pre = 0;   // producer: stages of the first unit issued here
+    // Producer's L2 policies: W streamed once (evict first); x_r re-read by
+    // every unit of rank r (evict last).
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
     if (warp == 0 && lane == 0) {
         // A packed weight is written once, by symm_pack_w (which the host
         // never chains into a call that reads it), so the W loads of the first
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *dst = smem + (size_t)i * kStageBytes;
 #pragma unroll
             for (int s = 0; s < kSlabs; ++s)
-                load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[i], kb * kSlabs + s, t, r);
+                load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[i], kb * kSlabs + s, t, r, pol_w);
         }
         if (a.w_early) griddep_wait();
         tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 3);
@@ -311,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *dst = smem + (size_t)i * kStageBytes;
 #pragma unroll
             for (int s = 0; s < kSlabs; ++s)
-                tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[i], kb * kBK + s * 64, 0, r);
+                tma_load_3d_hint(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[i], kb * kBK + s * 64, 0, r,
+                                 pol_x);
         }
         // Step 0 of the protocol: the launch epoch, read once per CTA and
         // shared through the barrier below (which orders the read before
@@ -379,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst = smem + (size_t)st * kStageBytes;
 #pragma unroll
                     for (int s = 0; s < kSlabs; ++s)
-                        load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[st], kb * kSlabs + s, t, r);
+                        load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[st], kb * kSlabs + s, t, r, pol_w);
 #pragma unroll
                     for (int s = 0; s < kSlabs; ++s)
-                        tma_load_3d(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64, 0,
-                                    r);
+                        tma_load_3d_hint(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64,
+                                         0, r, pol_x);
                     if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(work, 1u);
                     ++issued;
                     tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 12);

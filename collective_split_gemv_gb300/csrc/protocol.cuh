@@ -255,11 +255,11 @@ __device__ __forceinline__ uint32_t *flag_of(const GemvArgs &a, int r, int t, in
 // has passed a barrier since, so plain L2 loads (.cg) see every partial and
 // every flag.
 // Each thread takes kPer items -- vectors of four consecutive outputs (for
-// N % 4 == 0, when then n0 and rows are multiples of 4, and C <= 4), else
+// N % 4 == 0, when then n0 and rows are multiples of 4, and C <= 8), else
 // single outputs -- and loads up to kBatch contributors of all of them before
-// adding anything, so one L2 round trip serves up to kPer * kBatch loads
-// (32 registers either way); the additions stay in contributor order,
-// element by element, so vector and scalar items give the same bits.
+// adding anything, so one L2 round trip serves up to kPer * kBatch loads; the
+// additions stay in contributor order, element by element, so vector and
+// scalar items give the same bits.
 // The flags are checked in the same round trip as the first partials: thread
 // i loads the flags of contributors i, i + nthreads, ... and the group agrees
 // (all_ok, called exactly once by every thread of the group) before anything
@@ -273,7 +273,7 @@ __device__ __forceinline__ bool reduce_items(const GemvArgs &a, int t, uint32_t 
                                              int nthreads) {
     // kW: outputs per item (4: float4 vectors, 1: scalars)
     constexpr int kPer = kW == 4 ? 2 : 4;
-    constexpr int kBatch = kW == 4 ? 4 : 8;
+    constexpr int kBatch = 8;
     using V = typename std::conditional<kW == 4, float4, float>::type;
     const int S = a.splits;
     const int per_row = rows / kW;           // items per batch row
@@ -362,7 +362,7 @@ template <class BaseFn, class AllFn, class IssuedFn>
 __device__ __forceinline__ bool reduce_tile(const GemvArgs &a, int t, uint32_t epoch, int n0, int rows, int C,
                                             BaseFn contributor_base, AllFn all_ok, IssuedFn issued, int tid,
                                             int nthreads) {
-    if ((a.N & 3) == 0 && C <= 4)
+    if ((a.N & 3) == 0 && C <= 8)
         return reduce_items<4>(a, t, epoch, n0, rows, C, contributor_base, all_ok, issued, tid, nthreads);
     return reduce_items<1>(a, t, epoch, n0, rows, C, contributor_base, all_ok, issued, tid, nthreads);
 }

@@ -53,7 +53,7 @@ AR_KERNEL_AUTO, AR_KERNEL_PER_THREAD, AR_KERNEL_STAGED = 0, 1, 2   # auto is the
 GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_DYN, GEMV_PATH_CLUSTER = 0, 1, 4, 5   # paths 2 and 3 were retired
 TIMELINE_SLOTS = 16   # 64-bit words per CTA row of a timeline buffer
 
-EXPORTED = ("symm_layout", "symm_alloc", "symm_rendezvous", "one_shot_all_reduce",
+EXPORTED = ("symm_layout", "symm_alloc", "symm_mp_alloc", "symm_mp_import", "symm_rendezvous", "one_shot_all_reduce",
             "gemv_all_reduce", "symm_status", "symm_check_guards", "symm_set_option",
             "symm_info", "symm_gemv_plan", "gemv_all_reduce_noalloc", "gemv_reduce_scatter",
             "gemv_all_reduce_bias_rmsnorm", "reduce_scatter", "two_shot_all_reduce",
@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         L.symm_layout.argtypes = [i, sz, sz, sz, ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.symm_alloc.argtypes = [i, sz, sz, sz, vp, sz, ctypes.POINTER(vp)]
+        L.symm_mp_alloc.argtypes = [i, i, sz, sz, sz, ctypes.POINTER(vp), ctypes.POINTER(i)]
+        L.symm_mp_import.argtypes = [vp, i, i]
         L.symm_rendezvous.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(sz)]
         L.one_shot_all_reduce.argtypes = [vp, vp, vp, i, sz, vp]
         L.gemv_all_reduce.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
@@ -172,6 +174,23 @@ def symm_alloc(R: int, slot_bytes: int, scratch_bytes: int, signal_pad_bytes: in
     _check(lib().symm_alloc(R, slot_bytes, scratch_bytes, signal_pad_bytes, _vp(backing),
                             backing_bytes, ctypes.byref(h)))
     return h
+
+
+def symm_mp_alloc(R: int, rank: int, slot_bytes: int, scratch_bytes: int, signal_pad_bytes: int):
+    """This process's rank of a multi-process handle: its slot allocated and
+    mapped, the others not yet.  -> (handle, fd): fd is the POSIX descriptor
+    of the slot's allocation, to be sent to every other rank's process (see
+    ``multiproc.exchange_fds``) and closed by this process once they have it."""
+    h = ctypes.c_void_p()
+    fd = ctypes.c_int(-1)
+    _check(lib().symm_mp_alloc(R, rank, slot_bytes, scratch_bytes, signal_pad_bytes, ctypes.byref(h),
+                               ctypes.byref(fd)))
+    return h, fd.value
+
+
+def symm_mp_import(h, peer: int, fd: int) -> None:
+    """Maps rank `peer`'s slot (its process's descriptor, received by this one)."""
+    _check(lib().symm_mp_import(h, peer, fd))
 
 
 def symm_rendezvous(h):

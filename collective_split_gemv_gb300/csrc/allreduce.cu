@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceAr
         o.z = pack2(acc[4], acc[5]);
         o.w = pack2(acc[6], acc[7]);
         uint8_t *dst = a.out + i * 16;
+        if (a.my_rank >= 0) {   // multi-process handle: this rank's output only
+            st_v4(dst + (long long)a.my_rank * a.stride, o);
+            continue;
+        }
 #pragma unroll 8
         for (int s = 0; s < R; ++s) st_v4(dst + (long long)s * a.stride, o);
     }
@@ -118,7 +122,8 @@ __global__ void __launch_bounds__(kThreads) one_shot_ar_kernel(const AllReduceAr
                 reinterpret_cast<const uint8_t *>(src) + (long long)q * a.stride));
         const __nv_bfloat16 v = __float2bfloat16_rn(acc);
         for (int s = 0; s < R; ++s)
-            *reinterpret_cast<__nv_bfloat16 *>(a.out + e * 2 + (long long)s * a.stride) = v;
+            if (a.my_rank < 0 || s == a.my_rank)
+                *reinterpret_cast<__nv_bfloat16 *>(a.out + e * 2 + (long long)s * a.stride) = v;
     }
 }
 

@@ -138,19 +138,19 @@ __device__ __forceinline__ bool publish_reduce_unit(const GemvArgs &a, uint32_t 
     return true;
 }
 
-// Unfused form (kOutPartials): no tile protocol.  One thread counts the unit
-// on tiles_done; the thread that counts the last of the U units finishes the
-// launch as the last tile reducer does in the fused form (every CTA read the
-// epoch before it counted a unit, and the acq_rel count orders those reads
-// before the epoch store).
-__device__ __forceinline__ void count_unit_partials(const GemvArgs &a, uint32_t epoch, uint32_t U) {
-    const uint32_t done = atom_add_acq_rel_gpu(a.tiles_done, 1u);
-    if (done >= U) latch_status(a.status, kProtoBadTicket, -1, -1, epoch);
-    if (done != U - 1u) return;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    st_relaxed_gpu_u32(a.tiles_done, 0u);
-    st_relaxed_gpu_u32(a.work + ((epoch + 1u) & 1u), 0u);
-    st_relaxed_gpu_u32(a.epoch_word, epoch);
+// Unit u of this launch: (tile t, rank r, K split s).  Units are numbered
+// tile-major, u = (t * R + r) * S + s; a multi-process handle's launch
+// covers its own rank only, u = t * S + s.
+__device__ __forceinline__ void unit_of(const GemvArgs &a, int u, int S, int *t, int *r, int *s) {
+    const int tr = u / S;
+    *s = u - tr * S;
+    if (a.my_rank >= 0) {
+        *t = tr;
+        *r = a.my_rank;
+    } else {
+        *t = tr / a.R;
+        *r = tr - *t * a.R;
+    }
 }
 
 // The same protocol run by one warp (the FFMA engine's epilogue warp).
@@ -294,10 +294,8 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         // kernel, not only this library's): it is loaded after the wait.
         // The first unit is the CTA's own index (G <= U).
         const int u = a.reverse_order ? U - 1 - (int)blockIdx.x : (int)blockIdx.x;
-        const int tr = u / S;
-        const int sp = u - tr * S;
-        const int t = tr / a.R;
-        const int r = tr - t * a.R;
+        int t, r, sp;
+        unit_of(a, u, S, &t, &r, &sp);
         const int kb0 = sp * KBs;
         const int kb1 = min(kb0 + KBs, KB);
         pre = min(kStages, kb1 - kb0);
@@ -359,10 +357,8 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                     break;
                 }
                 const int u = a.reverse_order ? U - 1 - (int)tk : (int)tk;
-                const int tr = u / S;
-                const int sp = u - tr * S;
-                const int t = tr / a.R;
-                const int r = tr - t * a.R;
+                int t, r, sp;
+                unit_of(a, u, S, &t, &r, &sp);
                 const int kb0 = sp * KBs;
                 const int kb1 = min(kb0 + KBs, KB);
                 // The next unit is drawn right after the loads of this unit's
@@ -480,10 +476,8 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 if (!ok) break;
                 const int u = acc_unit[j];
                 if (u < 0) break;
-                const int tr = u / S;
-                const int sp = u - tr * S;
-                const int t = tr / a.R;
-                const int r = tr - t * a.R;
+                int t, r, sp;
+                unit_of(a, u, S, &t, &r, &sp);
                 float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
                                                      (long long)sp * a.partial_stride);
                 for (int idx = lane; idx < kM * kB; idx += 32) {
@@ -494,9 +488,10 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[j]);
                 if (a.out_mode == kOutPartials) {
-                    if (lane == 0) count_unit_partials(a, epoch, (uint32_t)U);
+                    if (lane == 0) count_unit(a, a.tiles_done, epoch, (uint32_t)U);
                 } else {
                     publish_reduce_warp(a, epoch, S, t, r, sp, lane);
+                    if (a.my_rank >= 0 && lane == 0) count_unit(a, a.units_done, epoch, (uint32_t)U);
                 }
                 ++seg;
             }
@@ -534,10 +529,8 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[j]);
-                const int tr = u / S;
-                const int sp = u - tr * S;
-                const int t = tr / a.R;
-                const int r = tr - t * a.R;
+                int t, r, sp;
+                unit_of(a, u, S, &t, &r, &sp);
                 const int n = t * kM + row;
                 if (n < a.N) {
                     float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
@@ -548,9 +541,10 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 }
                 bool reduced = false;
                 if (a.out_mode == kOutPartials) {
-                    if (gt == 0) count_unit_partials(a, epoch, (uint32_t)U);
+                    if (gt == 0) count_unit(a, a.tiles_done, epoch, (uint32_t)U);
                 } else {
                     reduced = publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last);
+                    if (a.my_rank >= 0 && gt == 0) count_unit(a, a.units_done, epoch, (uint32_t)U);
                 }
                 ++seg;
                 if (gt == 0) {

@@ -66,8 +66,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_ffma_kernel(const GemvArg
     extern __shared__ float4 xs4[];   // [B][2][kc_cap]
 
     const int bid = a.reverse_order ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-    const int t = bid / a.R;
-    const int r = bid - t * a.R;
+    // CTA (tile, rank); a multi-process handle's launch covers its own rank.
+    const int t = a.my_rank >= 0 ? bid : bid / a.R;
+    const int r = a.my_rank >= 0 ? a.my_rank : bid - t * a.R;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nchunk = a.Kr >> 3;
@@ -176,7 +177,7 @@ cudaError_t launch_b(const GemvArgs &a, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const unsigned grid = (unsigned)a.num_tiles * (unsigned)a.R;
+    const unsigned grid = (unsigned)a.num_tiles * (a.my_rank >= 0 ? 1u : (unsigned)a.R);
     return launch_kernel(kern, dim3(grid), dim3(kThreads), smem, s, a.chained != 0, a);
 }
 

@@ -123,6 +123,12 @@ struct GemvArgs {
     int w_early;
     unsigned long long *tl;  // timeline rows (timeline build only; nullptr: none), see timeline.cuh
     int tl_ctas;             // CTAs the timeline buffer has rows for
+    // Multi-process handle: this launch computes rank my_rank's units only
+    // (-1: every rank's).  tiles_done is then nullptr and the launch is
+    // finished by the CTA that counts the last of its units on units_done
+    // (the own slot's pad).
+    int my_rank;
+    uint32_t *units_done;
 };
 constexpr int kOutAllReduce = 0, kOutReduceScatter = 1, kOutBiasZ = 2, kOutPartials = 3;
 
@@ -152,6 +158,7 @@ struct AllReduceArgs {
     int ctas_per_sm;         // grid cap per SM (grid-stride beyond it); 0 = the default
     int kernel;              // one-shot kernel: kArKernelAuto / PerThread / Staged
     int chained;             // one-shot: launch as a programmatic dependent of the previous kernel
+    int my_rank;             // multi-process handle: store the result into this rank's slot only (-1: all)
 };
 // The one-shot all-reduce has two kernels: per-thread 16-byte loads and
 // stores, and one staged through shared memory by bulk (TMA) copies.  Auto
@@ -247,6 +254,7 @@ struct PackWArgs {
     uint8_t *Wp;             // packed, slot 0
     long long stride;
     int R, N, Kr;
+    int r0;                  // first rank packed (R ranks from it; a multi-process handle packs its own)
 };
 cudaError_t launch_pack_w(const PackWArgs &a, cudaStream_t s);
 

@@ -20,7 +20,7 @@ constexpr int kPackThreads = 256;
 constexpr int kChunksPerBlock = (int)(kPackBlockBytes / 16);   // 1024
 
 __global__ void __launch_bounds__(kPackThreads) pack_w_kernel(const PackWArgs a) {
-    const int r = blockIdx.y;
+    const int r = a.r0 + (int)blockIdx.y;
     const int J = (a.Kr + kPackCols - 1) / kPackCols;
     const int T = (a.N + kPackRows - 1) / kPackRows;
     const long long b = blockIdx.x;   // block of this slot; b == T * J is the zero block

@@ -147,7 +147,7 @@ __device__ __forceinline__ uint32_t take_ticket(const GemvArgs &a, int t, uint32
     if (pos >= C) {
         latch_status(a.status, kProtoBadTicket, r, t, epoch);
     } else if (pos == C - 1u) {
-        *done = atom_add_release_gpu(a.tiles_done, 1u);
+        if (a.tiles_done) *done = atom_add_release_gpu(a.tiles_done, 1u);
         st_relaxed_gpu_u32(a.counters + t, 0u);
     }
     return pos;
@@ -158,11 +158,29 @@ __device__ __forceinline__ uint32_t take_ticket(const GemvArgs &a, int t, uint32
 // launch.  Run by the thread that took the ticket, before the reduction, so
 // that these stores are long done when the grid ends.
 __device__ __forceinline__ void finish_launch_if_last(const GemvArgs &a, uint32_t done, uint32_t epoch, int t) {
+    if (!a.tiles_done) return;   // a launch counted in units (count_unit)
     const uint32_t T = (uint32_t)a.num_tiles;
     if (done >= T) latch_status(a.status, kProtoBadTicket, -1, t, epoch);
     if (done != T - 1u) return;
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
     st_relaxed_gpu_u32(a.tiles_done, 0u);
+    st_relaxed_gpu_u32(a.work + ((epoch + 1u) & 1u), 0u);
+    st_relaxed_gpu_u32(a.epoch_word, epoch);
+}
+
+// Step 4 for a launch that is counted in units instead of reduced tiles (the
+// unfused form's GEMV, whose partials no tile reducer sums; and one rank's
+// launch on a multi-process handle, whose tiles the other ranks' launches may
+// finish): the thread that counts the last of the launch's U units on
+// `counter` stores the epoch and clears the counter and the work counter the
+// next launch uses.  Every unit is counted after its CTA read the epoch, and
+// the acq_rel count orders those reads before the epoch store.
+__device__ __forceinline__ void count_unit(const GemvArgs &a, uint32_t *counter, uint32_t epoch, uint32_t U) {
+    const uint32_t done = atom_add_acq_rel_gpu(counter, 1u);
+    if (done >= U) latch_status(a.status, kProtoBadTicket, -1, -1, epoch);
+    if (done != U - 1u) return;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    st_relaxed_gpu_u32(counter, 0u);
     st_relaxed_gpu_u32(a.work + ((epoch + 1u) & 1u), 0u);
     st_relaxed_gpu_u32(a.epoch_word, epoch);
 }
@@ -398,6 +416,7 @@ __device__ __forceinline__ void publish_and_reduce(const GemvArgs &a, uint32_t e
         tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 3);
         s_last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
         s_epoch = epoch;
+        if (a.my_rank >= 0) count_unit(a, a.units_done, epoch, (uint32_t)a.num_tiles);
         tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 4);
         tl_value(a.tl, a.tl_ctas, blockIdx.x, 8, s_last ? 1ull : 0ull);
         if (!s_last) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 7);

@@ -12,6 +12,7 @@
 // fused GEMV + AllReduce writes its partials into).  The signal pad holds the
 // per-tile flags, the tile arrival counters and the status words.  Guard bands
 // are filled with 0xA5 and checked by symm_check_guards.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -75,6 +76,12 @@ struct symm_handle {
         size_t bytes = 0;
     };
     std::vector<PackedW> packed;
+    // Multi-process handle (symm_mp_alloc): this process holds rank mp_rank;
+    // every rank's slot is a CUDA VMM allocation of its own process, mapped
+    // into one reserved range at base + r * stride in every process.
+    int mp_rank = -1;
+    unsigned long long va = 0;                       // reserved range (CUdeviceptr)
+    unsigned long long mem[kMaxRanks] = {};          // mapped allocation of slot r (0: not mapped)
 };
 
 namespace {
@@ -130,13 +137,29 @@ uint32_t *pad_word(const symm_handle *h, int r, size_t off) {
     return reinterpret_cast<uint32_t *>(slot(h, r) + h->pad_off + off);
 }
 
-int check_device(const symm_handle *h) {
+// Every slot of a multi-process handle is mapped (all peers imported).
+bool mp_ready(const symm_handle *h) {
+    if (h->mp_rank < 0) return true;
+    for (int r = 0; r < h->R; ++r)
+        if (!h->mem[r]) return false;
+    return true;
+}
+
+// The handle's device is the current one.
+int check_current_device(const symm_handle *h) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev != h->device)
         return fail(SYMM_EINVAL, "current device %d differs from the handle's device %d", dev, h->device);
     return SYMM_OK;
+}
+
+// The checks before any launch: the handle's device is current and, for a
+// multi-process handle, every rank's slot is mapped.
+int check_device(const symm_handle *h) {
+    if (!mp_ready(h)) return fail(SYMM_EINVAL, "not every rank's slot is mapped yet (symm_mp_import)");
+    return check_current_device(h);
 }
 
 // [p, p + bytes) inside slot 0's user region?
@@ -168,10 +191,14 @@ const symm_handle::PackedW *find_packed(const symm_handle *h, const void *p) {
 
 // Zero flags, counters, the work counters and the launch epoch
 // (stream-ordered): the pad as symm_alloc leaves it.
+// A multi-process handle resets its own slot's pad only (rank 0's holds the
+// tile counters every rank shares).
 int reset_protocol(symm_handle *h, cudaStream_t s) {
-    cudaError_t e0 = cudaMemsetAsync(slot(h, 0) + h->pad_off + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
+    const int own = h->mp_rank >= 0 ? h->mp_rank : 0;
+    cudaError_t e0 = cudaMemsetAsync(slot(h, own) + h->pad_off + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
     if (e0 != cudaSuccess) return cuda_fail(e0, "cudaMemsetAsync(work counter)");
     for (int r = 0; r < h->R; ++r) {
+        if (h->mp_rank >= 0 && r != h->mp_rank) continue;
         cudaError_t e = cudaMemsetAsync(slot(h, r) + h->pad_off + h->flags_off, 0,
                                         h->pad_bytes - h->flags_off, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(signal pad)");
@@ -220,8 +247,9 @@ constexpr int kDynFfmaMaxBatch = 2;
 constexpr size_t kSmallWBytes = 24u << 20;
 constexpr int kSmallMaxBatch = 4;
 
+// (Not on a multi-process handle: a cluster's CTAs belong to one process.)
 bool cluster_ok(const symm_handle *h, int N, int B) {
-    return h->R <= kMaxClusterRanks && B <= kClusterMaxBatch && (N + kClusterRows - 1) / kClusterRows <= 65535;
+    return h->mp_rank < 0 && h->R <= kMaxClusterRanks && B <= kClusterMaxBatch && (N + kClusterRows - 1) / kClusterRows <= 65535;
 }
 
 int gemv_path(const symm_handle *h, int N, int B, int Kr) {
@@ -292,15 +320,16 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         pl->path = kPathDyn;
     }
     if (pl->path == kPathCluster && !cluster_ok(h, N, B))
-        return fail(SYMM_EINVAL, "the cluster kernel (path 5) needs R <= %d, B <= %d and at most 65535 row tiles",
-                    kMaxClusterRanks, kClusterMaxBatch);
+        return fail(SYMM_EINVAL,
+                    "the cluster kernel (path 5) needs R <= %d, B <= %d, at most 65535 row tiles and a "
+                    "single-process handle", kMaxClusterRanks, kClusterMaxBatch);
     pl->rows = rows_per_tile_for_path(pl->path, B);
     if (pl->rows <= 0) return fail(SYMM_EINVAL, "no GEMV kernel for B=%d", B);
     pl->tiles = (N + pl->rows - 1) / pl->rows;
     if (pl->tiles > h->max_tiles)
         return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", pl->tiles, h->max_tiles);
     pl->splits = 1;
-    pl->grid = pl->tiles * h->R;
+    pl->grid = pl->tiles * (h->mp_rank >= 0 ? 1 : h->R);
     if (pl->path == kPathDyn) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the persistent kernel needs K > 0");
         pl->engine = dyn_engine(h, B);
@@ -308,7 +337,9 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         pl->cps = dyn_cps(h);
         if (!dyn_config_supported(pl->slabs, pl->cps))
             return fail(SYMM_EINVAL, "no pipeline for %d slabs at %d CTAs per SM", pl->slabs, pl->cps);
-        const long long pairs = (long long)pl->tiles * h->R;
+        // (tile, rank) pairs this launch computes: every rank's, or on a
+        // multi-process handle the own rank's only.
+        const long long pairs = (long long)pl->tiles * (h->mp_rank >= 0 ? 1 : h->R);
         const long long KB = (Kr + dyn_block_k(pl->slabs) - 1) / dyn_block_k(pl->slabs);
         if (pairs > (1LL << 26)) return fail(SYMM_ERANGE, "too many row tiles");
         long long G = h->opt_sk_grid > 0 ? h->opt_sk_grid : (long long)num_sms(h->device) * pl->cps;
@@ -346,6 +377,93 @@ int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace symm
 
 namespace {
+
+// CUDA VMM through the runtime's driver entry points (the library links the
+// runtime only).
+struct Vmm {
+    CUresult (*granularity)(size_t *, const CUmemAllocationProp *, CUmemAllocationGranularity_flags) = nullptr;
+    CUresult (*reserve)(CUdeviceptr *, size_t, size_t, CUdeviceptr, unsigned long long) = nullptr;
+    CUresult (*addr_free)(CUdeviceptr, size_t) = nullptr;
+    CUresult (*create)(CUmemGenericAllocationHandle *, size_t, const CUmemAllocationProp *,
+                       unsigned long long) = nullptr;
+    CUresult (*release)(CUmemGenericAllocationHandle) = nullptr;
+    CUresult (*map)(CUdeviceptr, size_t, size_t, CUmemGenericAllocationHandle, unsigned long long) = nullptr;
+    CUresult (*unmap)(CUdeviceptr, size_t) = nullptr;
+    CUresult (*set_access)(CUdeviceptr, size_t, const CUmemAccessDesc *, size_t) = nullptr;
+    CUresult (*export_handle)(void *, CUmemGenericAllocationHandle, CUmemAllocationHandleType,
+                              unsigned long long) = nullptr;
+    CUresult (*import_handle)(CUmemGenericAllocationHandle *, void *, CUmemAllocationHandleType) = nullptr;
+    bool ok = false;
+};
+
+template <class F>
+bool entry(const char *name, F *fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+        return false;
+    *fn = reinterpret_cast<F>(p);
+    return true;
+}
+
+const Vmm &vmm() {
+    static const Vmm v = []() {
+        Vmm t;
+        t.ok = entry("cuMemGetAllocationGranularity", &t.granularity) && entry("cuMemAddressReserve", &t.reserve) &&
+               entry("cuMemAddressFree", &t.addr_free) && entry("cuMemCreate", &t.create) &&
+               entry("cuMemRelease", &t.release) && entry("cuMemMap", &t.map) && entry("cuMemUnmap", &t.unmap) &&
+               entry("cuMemSetAccess", &t.set_access) &&
+               entry("cuMemExportToShareableHandle", &t.export_handle) &&
+               entry("cuMemImportFromShareableHandle", &t.import_handle);
+        return t;
+    }();
+    return v;
+}
+
+int cu_fail(CUresult r, const char *what) { return fail(SYMM_ECUDA, "%s failed (CUresult %d)", what, (int)r); }
+
+CUmemAllocationProp slot_prop(int device) {
+    CUmemAllocationProp prop = {};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = device;
+    prop.requestedHandleTypes = CU_MEM_HANDLE_TYPE_POSIX_FILE_DESCRIPTOR;
+    return prop;
+}
+
+// Maps allocation `mem` as slot r of h's reserved range, read-write for the
+// handle's device.
+int map_slot(symm_handle *h, int r, CUmemGenericAllocationHandle mem) {
+    const Vmm &v = vmm();
+    const CUdeviceptr at = (CUdeviceptr)(h->va + (unsigned long long)r * h->stride);
+    CUresult c = v.map(at, h->stride, 0, mem, 0);
+    if (c != CUDA_SUCCESS) return cu_fail(c, "cuMemMap");
+    CUmemAccessDesc acc = {};
+    acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    acc.location.id = h->device;
+    acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+    c = v.set_access(at, h->stride, &acc, 1);
+    if (c != CUDA_SUCCESS) {
+        v.unmap(at, h->stride);
+        return cu_fail(c, "cuMemSetAccess");
+    }
+    h->mem[r] = (unsigned long long)mem;
+    return SYMM_OK;
+}
+
+// Unmaps and releases every slot of a multi-process handle, frees its range.
+void mp_release(symm_handle *h) {
+    const Vmm &v = vmm();
+    for (int r = 0; r < h->R; ++r) {
+        if (!h->mem[r]) continue;
+        v.unmap((CUdeviceptr)(h->va + (unsigned long long)r * h->stride), h->stride);
+        v.release((CUmemGenericAllocationHandle)h->mem[r]);
+        h->mem[r] = 0;
+    }
+    if (h->va) v.addr_free((CUdeviceptr)h->va, h->total);
+    h->va = 0;
+}
 
 // What the fused call does after the tile sums (GemvArgs::out_mode) and the
 // extra arguments of each form.
@@ -410,6 +528,8 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     }
     if (h->opt_unfused && ep.mode != kOutAllReduce)
         return fail(SYMM_EINVAL, "the unfused form (SYMM_OPT_UNFUSED) is a form of gemv_all_reduce only");
+    if (h->mp_rank >= 0 && (h->opt_unfused || ep.mode == kOutBiasZ))
+        return fail(SYMM_EINVAL, "a multi-process handle runs the all-reduce and reduce-scatter forms, fused");
     Plan pl;
     int rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
     if (rc != SYMM_OK) return rc;
@@ -428,10 +548,15 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.W = static_cast<const uint8_t *>(W_r);
     a.x = static_cast<const uint8_t *>(x_r);
     a.y = static_cast<uint8_t *>(y);
+    // Multi-process handle: this process launches its own rank's units only;
+    // its launch epoch, work counters, unit count and status words are in
+    // its own slot's pad, while the tile counters (rank 0's pad) and the
+    // flags (each rank's pad) are shared by every rank's launch.
+    const int own = h->mp_rank >= 0 ? h->mp_rank : 0;
     a.scratch = h->base + h->scratch_off;
     a.flags = pad_word(h, 0, h->flags_off);
     a.counters = pad_word(h, 0, h->counters_off);
-    a.status = pad_word(h, 0, 0);
+    a.status = pad_word(h, own, 0);
     a.stride = (long long)h->stride;
     a.R = h->R;
     a.N = N;
@@ -439,9 +564,11 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     a.B = B;
     a.rows_per_tile = rows;
     a.num_tiles = tiles;
-    a.epoch_word = pad_word(h, 0, kPadEpochOffset);
-    a.tiles_done = pad_word(h, 0, kPadTilesDoneOffset);
-    a.work = pad_word(h, 0, kPadWorkOffset);
+    a.epoch_word = pad_word(h, own, kPadEpochOffset);
+    a.tiles_done = h->mp_rank >= 0 ? nullptr : pad_word(h, 0, kPadTilesDoneOffset);
+    a.units_done = h->mp_rank >= 0 ? pad_word(h, own, kPadTilesDoneOffset) : nullptr;
+    a.my_rank = h->mp_rank;
+    a.work = pad_word(h, own, kPadWorkOffset);
     a.reverse_order = h->opt_tile_order;
     a.splits = splits;
     a.partial_stride = (long long)B * N * 4;
@@ -597,8 +724,118 @@ int symm_alloc(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad
     return SYMM_OK;
 }
 
+int symm_mp_alloc(int R, int rank, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+                  symm_handle_t **out, int *fd_out) {
+    if (!out || !fd_out) return fail(SYMM_EINVAL, "out or fd_out is NULL");
+    *out = nullptr;
+    *fd_out = -1;
+    int rc = symm_layout(R, slot_bytes, scratch_bytes, signal_pad_bytes, nullptr, nullptr);
+    if (rc != SYMM_OK) return rc;
+    if (rank < 0 || rank >= R) return fail(SYMM_EINVAL, "rank=%d outside 0..%d", rank, R - 1);
+    const Vmm &v = vmm();
+    if (!v.ok) return fail(SYMM_ECUDA, "the CUDA virtual memory entry points are not available");
+    symm_handle *h = new (std::nothrow) symm_handle;
+    if (!h) return fail(SYMM_ENOMEM, "host allocation of the handle failed");
+    h->R = R;
+    h->slot_bytes = slot_bytes;
+    h->scratch_bytes = scratch_bytes;
+    h->pad_bytes = signal_pad_bytes;
+    compute_layout(*h);
+    h->mp_rank = rank;
+    h->owned = true;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    const CUmemAllocationProp prop = slot_prop(h->device);
+    size_t gran = 0;
+    CUresult c = v.granularity(&gran, &prop, CU_MEM_ALLOC_GRANULARITY_MINIMUM);
+    if (c != CUDA_SUCCESS || gran == 0) {
+        delete h;
+        return cu_fail(c, "cuMemGetAllocationGranularity");
+    }
+    // Every rank's slot is one allocation of `stride` bytes.
+    h->stride = round_up(h->stride, gran);
+    h->total = h->stride * (size_t)R;
+    CUdeviceptr va = 0;
+    c = v.reserve(&va, h->total, gran, 0, 0);
+    if (c != CUDA_SUCCESS) {
+        delete h;
+        return cu_fail(c, "cuMemAddressReserve");
+    }
+    h->va = (unsigned long long)va;
+    h->base = reinterpret_cast<uint8_t *>(va);
+    CUmemGenericAllocationHandle mem = 0;
+    c = v.create(&mem, h->stride, &prop, 0);
+    if (c != CUDA_SUCCESS) {
+        const size_t bytes = h->stride;
+        mp_release(h);
+        delete h;
+        return c == CUDA_ERROR_OUT_OF_MEMORY ? fail(SYMM_ENOMEM, "cuMemCreate(%zu) failed", bytes)
+                                             : cu_fail(c, "cuMemCreate");
+    }
+    rc = map_slot(h, rank, mem);
+    if (rc != SYMM_OK) {
+        v.release(mem);
+        mp_release(h);
+        delete h;
+        return rc;
+    }
+    int fd = -1;
+    c = v.export_handle(&fd, mem, CU_MEM_HANDLE_TYPE_POSIX_FILE_DESCRIPTOR, 0);
+    if (c != CUDA_SUCCESS) {
+        mp_release(h);
+        delete h;
+        return cu_fail(c, "cuMemExportToShareableHandle");
+    }
+    // The own slot as symm_alloc leaves every slot: guard bands, zero scratch
+    // and pad.
+    uint8_t *sl = slot(h, rank);
+    e = cudaMemset(sl + h->guard0, kGuardByte, kGuard);
+    if (e == cudaSuccess) e = cudaMemset(sl + h->scratch_off, 0, h->guard1 - h->scratch_off);
+    if (e == cudaSuccess) e = cudaMemset(sl + h->guard1, kGuardByte, kGuard);
+    if (e == cudaSuccess) e = cudaMemset(sl + h->pad_off, 0, h->guard2 - h->pad_off);
+    if (e == cudaSuccess) e = cudaMemset(sl + h->guard2, kGuardByte, kGuard);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        mp_release(h);
+        delete h;
+        return cuda_fail(e, "initialising the slot");
+    }
+    *fd_out = fd;
+    *out = h;
+    g_err[0] = 0;
+    return SYMM_OK;
+}
+
+int symm_mp_import(symm_handle_t *h, int peer, int fd) {
+    if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank < 0) return fail(SYMM_EINVAL, "not a multi-process handle (symm_mp_alloc)");
+    if (peer < 0 || peer >= h->R || peer == h->mp_rank)
+        return fail(SYMM_EINVAL, "peer=%d must be another rank in 0..%d", peer, h->R - 1);
+    if (h->mem[peer]) return fail(SYMM_EINVAL, "rank %d's slot is already mapped", peer);
+    if (fd < 0) return fail(SYMM_EINVAL, "fd=%d is not a descriptor", fd);
+    int rc = check_current_device(h);
+    if (rc != SYMM_OK) return rc;
+    const Vmm &v = vmm();
+    CUmemGenericAllocationHandle mem = 0;
+    CUresult c = v.import_handle(&mem, reinterpret_cast<void *>((uintptr_t)fd), CU_MEM_HANDLE_TYPE_POSIX_FILE_DESCRIPTOR);
+    if (c != CUDA_SUCCESS) return cu_fail(c, "cuMemImportFromShareableHandle");
+    rc = map_slot(h, peer, mem);
+    if (rc != SYMM_OK) {
+        v.release(mem);
+        return rc;
+    }
+    g_err[0] = 0;
+    return SYMM_OK;
+}
+
 int symm_rendezvous(symm_handle_t *h, void **slot_ptrs, void **signal_pad_ptrs, size_t *stride_out) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank >= 0)
+        for (int r = 0; r < h->R; ++r)
+            if (!h->mem[r]) return fail(SYMM_EINVAL, "rank %d's slot is not mapped yet (symm_mp_import)", r);
     for (int r = 0; r < h->R; ++r) {
         if (slot_ptrs) slot_ptrs[r] = slot(h, r);
         if (signal_pad_ptrs) signal_pad_ptrs[r] = slot(h, r) + h->pad_off;
@@ -723,8 +960,11 @@ int one_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
     a.R = h->R;
     a.n = n;
     a.ctas_per_sm = h->opt_ar_cps;
-    a.kernel = h->opt_ar_kernel;
+    // A multi-process handle: the real one-shot -- this process reads every
+    // rank's input and writes its own rank's output (the per-thread kernel).
+    a.kernel = h->mp_rank >= 0 ? kArKernelPerThread : h->opt_ar_kernel;
     a.chained = h->opt_chain;
+    a.my_rank = h->mp_rank;
     cudaError_t e = launch_one_shot_all_reduce(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "one_shot_all_reduce launch");
     note_write(h, out, bytes);
@@ -766,7 +1006,8 @@ int symm_pack_w(symm_handle_t *h, const void *W_r, void *Wp, int R, int N, int K
     a.W = static_cast<const uint8_t *>(W_r);
     a.Wp = static_cast<uint8_t *>(Wp);
     a.stride = (long long)h->stride;
-    a.R = h->R;
+    a.R = h->mp_rank >= 0 ? 1 : h->R;   // a multi-process handle packs its own rank's weight
+    a.r0 = h->mp_rank >= 0 ? h->mp_rank : 0;
     a.N = N;
     a.Kr = Kr;
     cudaError_t e = launch_pack_w(a, reinterpret_cast<cudaStream_t>(stream));
@@ -819,6 +1060,7 @@ int gemv_all_reduce_bias_rmsnorm(symm_handle_t *h, const void *W_r, const void *
 
 int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank >= 0) return fail(SYMM_EINVAL, "not available on a multi-process handle");
     if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
     if (n % (size_t)R) return fail(SYMM_EINVAL, "n=%zu is not a multiple of R=%d", n, R);
     if (n == 0) return SYMM_OK;
@@ -848,6 +1090,7 @@ int reduce_scatter(symm_handle_t *h, const void *in, void *out, int R, size_t n,
 
 int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size_t n, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank >= 0) return fail(SYMM_EINVAL, "not available on a multi-process handle");
     if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
     if (n == 0) return SYMM_OK;
     if (n > SIZE_MAX / 2) return fail(SYMM_EINVAL, "n too large");
@@ -883,6 +1126,7 @@ int two_shot_all_reduce(symm_handle_t *h, const void *in, void *out, int R, size
 int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, const void *gamma, void *out, int R,
                             int rows, int H, float eps, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank >= 0) return fail(SYMM_EINVAL, "not available on a multi-process handle");
     if (R != h->R) return fail(SYMM_EINVAL, "R=%d but the handle has %d ranks", R, h->R);
     if (rows < 0 || rows > 65535) return fail(SYMM_EINVAL, "rows=%d outside 0..65535", rows);
     if (H < 8 || H % 8 || H > rmsnorm_max_h())
@@ -930,6 +1174,7 @@ int all_reduce_bias_rmsnorm(symm_handle_t *h, const void *in, const void *bias, 
 int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *out_tile, const int *roots,
                            int ntiles, int rows, int cols, long long ld_in, long long ld_out, symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (h->mp_rank >= 0) return fail(SYMM_EINVAL, "not available on a multi-process handle");
     if (!in_tiles || !roots || !out_tile) return fail(SYMM_EINVAL, "NULL argument");
     if (ntiles < 1 || ntiles > h->R || ntiles > kMaxTiles)
         return fail(SYMM_EINVAL, "ntiles=%d outside 1..%d (one root per rank at most)", ntiles, std::min(h->R, kMaxTiles));
@@ -1003,15 +1248,40 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     uint32_t st[4] = {0, 0, 0, 0};
-    e = cudaMemcpy(st, pad_word(h, 0, 0), sizeof st, cudaMemcpyDeviceToHost);
+    const int own = h->mp_rank >= 0 ? h->mp_rank : 0;   // a process latches into its own slot's words
+    e = cudaMemcpy(st, pad_word(h, own, 0), sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
-    if (code) *code = st[kStatusCode] ? SYMM_EPROTO : SYMM_OK;
-    if (rank) *rank = st[kStatusCode] ? (int)st[kStatusRank] : -1;
+    // A multi-process handle also compares the ranks' launch counts (each
+    // rank's epoch word, advanced by its own launches): read after a
+    // barrier that every live rank passed with its calls finished, a count
+    // that differs names a rank that skipped a call (or left).
+    int lag = -1;
+    uint32_t own_epoch = 0, lag_epoch = 0;
+    if (h->mp_rank >= 0 && !st[kStatusCode]) {
+        e = cudaMemcpy(&own_epoch, pad_word(h, own, kPadEpochOffset), 4, cudaMemcpyDeviceToHost);
+        for (int r = 0; r < h->R && e == cudaSuccess && lag < 0; ++r) {
+            if (r == own) continue;
+            uint32_t ep = 0;
+            e = cudaMemcpy(&ep, pad_word(h, r, kPadEpochOffset), 4, cudaMemcpyDeviceToHost);
+            if (e == cudaSuccess && ep != own_epoch) {
+                lag = r;
+                lag_epoch = ep;
+            }
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "reading the ranks' launch counts");
+    }
+    const bool err = st[kStatusCode] != 0 || lag >= 0;
+    if (code) *code = err ? SYMM_EPROTO : SYMM_OK;
+    if (rank) *rank = st[kStatusCode] ? (int)st[kStatusRank] : lag;
     if (tile) *tile = st[kStatusCode] ? (int)st[kStatusTile] : -1;
-    if (st[kStatusCode]) {
-        snprintf(g_err, sizeof g_err, "protocol error %u at rank %u tile %u epoch %u", st[kStatusCode],
-                 st[kStatusRank], st[kStatusTile], st[kStatusEpoch]);
-        e = cudaMemsetAsync(pad_word(h, 0, 0), 0, kPadStatusBytes, s);
+    if (err) {
+        if (st[kStatusCode])
+            snprintf(g_err, sizeof g_err, "protocol error %u at rank %u tile %u epoch %u", st[kStatusCode],
+                     st[kStatusRank], st[kStatusTile], st[kStatusEpoch]);
+        else
+            snprintf(g_err, sizeof g_err, "rank %d has made %u fused calls, this rank (%d) %u", lag, lag_epoch, own,
+                     own_epoch);
+        e = cudaMemsetAsync(pad_word(h, own, 0), 0, kPadStatusBytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
         int rc = reset_protocol(h, s);
         if (rc != SYMM_OK) return rc;
@@ -1041,6 +1311,7 @@ bool sm_addressable(const symm_handle *h, const void *p, size_t bytes) {
 int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
                        symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (!mp_ready(h)) return fail(SYMM_EINVAL, "not every rank's slot is mapped yet (symm_mp_import)");
     if (nranks < 0 || nranks > h->R) return fail(SYMM_EINVAL, "nranks=%d outside 0..%d", nranks, h->R);
     if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
     if (!src) return fail(SYMM_EINVAL, "src is NULL");
@@ -1072,6 +1343,7 @@ int symm_copy_to_slots(symm_handle_t *h, void *dst, const void *src, size_t byte
 int symm_copy_from_slots(symm_handle_t *h, void *dst, const void *src, size_t bytes_per_rank, int nranks,
                          symm_stream_t stream) {
     if (!h) return fail(SYMM_EINVAL, "handle is NULL");
+    if (!mp_ready(h)) return fail(SYMM_EINVAL, "not every rank's slot is mapped yet (symm_mp_import)");
     if (nranks < 0 || nranks > h->R) return fail(SYMM_EINVAL, "nranks=%d outside 0..%d", nranks, h->R);
     if (bytes_per_rank == 0 || nranks == 0) return SYMM_OK;
     if (!dst) return fail(SYMM_EINVAL, "dst is NULL");
@@ -1108,6 +1380,7 @@ int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band) {
     const size_t offs[3] = {h->guard0, h->guard1, h->guard2};
     for (int r = 0; r < h->R; ++r)
         for (int band = 0; band < 3; ++band) {
+            if (h->mp_rank >= 0 && r != h->mp_rank) continue;   // each process checks its own slot
             e = cudaMemcpy(buf, slot(h, r) + offs[band], kGuard, cudaMemcpyDeviceToHost);
             if (e != cudaSuccess) return cuda_fail(e, "reading a guard band");
             for (size_t i = 0; i < kGuard; ++i)
@@ -1123,7 +1396,11 @@ int symm_check_guards(symm_handle_t *h, int *bad_rank, int *bad_band) {
 int symm_free(symm_handle_t *h) {
     if (!h) return SYMM_OK;
     int rc = SYMM_OK;
-    if (h->owned && h->base) {
+    if (h->mp_rank >= 0) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) rc = cuda_fail(e, "cudaDeviceSynchronize");
+        mp_release(h);
+    } else if (h->owned && h->base) {
         cudaError_t e = cudaDeviceSynchronize();
         if (e == cudaSuccess) e = cudaFree(h->base);
         if (e != cudaSuccess) rc = cuda_fail(e, "cudaFree");

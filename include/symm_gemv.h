@@ -54,8 +54,8 @@
  *  - Device memory ownership: the library owns what symm_alloc allocates
  *    (backing == NULL) and frees it in symm_free; borrowed backing memory
  *    stays the caller's and must outlive the handle.
- *  - CUDA graphs: every call may be captured into a CUDA graph and the
- *    graph replayed any number of times ("PyTorch Symmetric Memory" docs:
+ *  - CUDA graphs: every call on a handle may be captured into a CUDA graph
+ *    and the graph replayed any number of times ("PyTorch Symmetric Memory" docs:
  *    the signal-pad synchronisation primitives are CUDA-graph compatible).
  *    The fused calls keep their whole protocol state in the signal pad: the
  *    launch epoch (advanced on the device by the last tile's reducer), the
@@ -63,8 +63,7 @@
  *    launch ends, so a launch depends on no host-side state and eager calls
  *    of any geometry may run on the handle between replays.  Make one eager
  *    call of each kind before capturing it, so that one-time set-up (kernel
- *    attributes, the no-allocation call's array address) happens outside
- *    the capture.
+ *    attributes) happens outside the capture.
  *  - After a launch in which a CTA gave up (a bounded wait ran out, latched
  *    in the status word), the epoch is not advanced and the results of later
  *    fused calls are undefined until symm_status has reported the error and
@@ -132,6 +131,59 @@ int symm_layout(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pa
  */
 int symm_alloc(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
                void *backing, size_t backing_bytes, symm_handle_t **out);
+
+/*
+ * symm_mp_alloc / symm_mp_import -- a handle whose R ranks are R processes
+ * (on one GPU or several GPUs of one node), the symmetric memory of the
+ * "PyTorch Symmetric Memory" docs ("Hello World": every rank allocates its
+ * symmetric buffer, `rendezvous` exchanges the handles, after which each rank
+ * holds its peers' buffer and signal-pad pointers).
+ *
+ * symm_mp_alloc allocates THIS process's slot (rank `rank` of R; sizes as for
+ * symm_alloc, identical on every rank) as a CUDA virtual-memory allocation
+ * on the current device, reserves one address range for all R slots and maps
+ * the own slot at base + rank * stride.  It returns the handle and, in
+ * *fd_out, a POSIX file descriptor of the allocation: the caller sends it to
+ * every other rank's process (over a Unix-domain socket, as the binding's
+ * multiproc.exchange_fds does) and closes it once they have it.  Host-
+ * synchronous.  Errors: SYMM_EINVAL, SYMM_ENOMEM, SYMM_ECUDA.
+ *
+ * symm_mp_import maps rank `peer`'s slot, from the descriptor this process
+ * received, at base + peer * stride.  The caller may close fd afterwards.
+ * Once every peer is imported, symm_rendezvous returns all R slot pointers
+ * and every symmetric pointer addresses rank r's instance at + r * stride, in
+ * every process alike.  The allocations stay mapped until symm_free, also
+ * after a peer's process has exited.
+ *
+ * On such a handle each process launches its own rank's share of a call:
+ *  - gemv_all_reduce / gemv_reduce_scatter (paths 1 and 4): this process
+ *    computes the units of its rank and publishes their partials; whichever
+ *    process's CTA arrives last at a tile sums every rank's partials (loads
+ *    from the peers' slots) and stores the result into every rank's y
+ *    (stores into the peers' slots).  No kernel waits on another process.
+ *  - one_shot_all_reduce: this process reads every rank's input and writes
+ *    its own rank's output.
+ *  - symm_pack_w packs the own rank's weight.
+ * The other collectives, the bias + RMSNorm form and SYMM_OPT_UNFUSED return
+ * SYMM_EINVAL.  Every rank must issue the same sequence of calls, and the
+ * caller must order them across processes the way one stream orders them on
+ * one handle: a call's inputs written in every process before any process
+ * launches it, and every process's launch of a call finished before any
+ * launches the next (e.g. stream synchronisation and a process-group barrier
+ * between calls).  A rank that skips a call (or leaves) leaves the others'
+ * tiles unreduced, and nothing waits for it.  Each process's symm_status,
+ * called after such a barrier, reports SYMM_EPROTO naming that rank: it
+ * compares the ranks' launch counts (every rank's epoch word) besides its own
+ * status words, where its kernels latch stale flags and tickets out of range
+ * found in later calls.  It resets its own slot's status words and pad (rank
+ * 0's holds the shared tile counters), so after an error every rank calls
+ * it, after a barrier.
+ * symm_check_guards checks the own slot.  No counterpart on the pages beyond
+ * the symmetric-memory semantics above.
+ */
+int symm_mp_alloc(int R, int rank, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad_bytes,
+                  symm_handle_t **out, int *fd_out);
+int symm_mp_import(symm_handle_t *h, int peer, int fd);
 
 /*
  * symm_rendezvous -- the per-rank pointer tables of the handle (PyTorch

@@ -245,7 +245,7 @@ def profiled_traffic(kernel: str, workload_name: str, source_sha: str):
 KERNEL_SOURCES = {
     "gemv_ar_ffma_kernel": ("gemv_ffma.cu",),
     "gemv_ar_dyn_kernel": ("gemv_dyn.cu", "sm100.cuh"),
-    "gemv_ar_cluster_kernel": ("gemv_cluster.cu",),
+    "gemv_ar_cluster_kernel": ("gemv_cluster.cu", "sm100.cuh"),
     "one_shot_ar_kernel": ("allreduce.cu",),
     "one_shot_ar_staged_kernel": ("allreduce.cu", "sm100.cuh"),
     "reduce_scatter_kernel": ("allreduce.cu",),
@@ -283,7 +283,8 @@ def kernel_name(plan):
     if plan["path"] == 5:
         return "gemv_ar_cluster_kernel"
     engine = "tcgen05" if plan["engine"] == 0 else "ffma"
-    return f"gemv_ar_dyn_kernel<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}>"
+    cl = f",cluster={plan['cluster']}" if plan.get("cluster") else ""
+    return f"gemv_ar_dyn_kernel<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}{cl}>"
 
 
 def timed_loop(step, n_steps, n_warmup, stream, dev, world, flush_buf, gpu_id, per_launch=True):
@@ -414,7 +415,8 @@ def make_case(args, w, local_rank, stream):
             for opt, val in ((csg.SYMM_OPT_GEMV_PATH, paths[args.gemv_path]), (csg.SYMM_OPT_SK_SLABS, args.sk_slabs),
                              (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
                              (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
-                             (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain))):
+                             (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain)),
+                             (csg.SYMM_OPT_DYN_CLUSTER, args.dyn_cluster)):
                 csg.symm_set_option(ws_.h, opt, val)
             return ws_
 
@@ -931,6 +933,8 @@ def parse_args(argv=None):
                         "row-major")
     p.add_argument("--dyn-splits", type=int, default=0,
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
+    p.add_argument("--dyn-cluster", type=int, default=-1, choices=(-1, 0, 1),
+                   help="persistent kernel: cluster epilogue -1 auto, 0 off, 1 on (SYMM_OPT_DYN_CLUSTER)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
                    help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
     p.add_argument("--ar-cps", type=int, default=0,

@@ -48,6 +48,7 @@ SYMM_OPT_AR_CTAS_PER_SM = 10
 SYMM_OPT_AR_KERNEL = 11
 SYMM_OPT_COPY_ENGINE = 12
 SYMM_OPT_UNFUSED = 13
+SYMM_OPT_DYN_CLUSTER = 14
 AR_KERNEL_AUTO, AR_KERNEL_PER_THREAD, AR_KERNEL_STAGED = 0, 1, 2   # auto is the per-thread kernel
 
 GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_DYN, GEMV_PATH_CLUSTER = 0, 1, 4, 5   # paths 2 and 3 were retired
@@ -78,7 +79,7 @@ class SymmInfo(ctypes.Structure):
 
 class GemvPlan(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int) for k in ("path", "engine", "slabs", "rows_per_tile", "tiles", "splits",
-                                            "grid", "parts_max", "kblocks", "ctas_per_sm")]
+                                            "grid", "parts_max", "kblocks", "ctas_per_sm", "cluster")]
 
 
 def library_variant() -> str:

@@ -37,6 +37,7 @@
 
 #include "internal.h"
 #include "protocol.cuh"
+#include "sm100.cuh"
 #include "timeline.cuh"
 
 namespace symm {
@@ -69,21 +70,6 @@ __device__ __forceinline__ float dot8(const uint4 &w, const uint4 &x, float acc)
     acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
     acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
     return acc;
-}
-
-// The same variable in CTA `cta` of the cluster (a shared::cluster address).
-__device__ __forceinline__ uint32_t cluster_addr(const void *local, uint32_t cta) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(remote)
-                 : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(cta));
-    return remote;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 template <int B>
@@ -161,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_cluster_kernel(const Gemv
 
     // Publish: every rank's partial is in its CTA's shared memory once all
     // CTAs of the cluster have passed this barrier (release / acquire).
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_arrive_release();
+    cluster_wait_acquire();
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 2);
 
     // This CTA's share of the tile's outputs: a contiguous range of the
@@ -185,14 +172,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_cluster_kernel(const Gemv
             if (q < R) sum += v[q];
     }
     // Done reading the peers' shared memory; the stores need none of it.
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    cluster_arrive_release();
     if (mine) {
         const int b = i / kRows;
         store_output(a, (size_t)b * a.N + n_base + (i - b * kRows), sum);
     }
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 3);
     // No CTA leaves while a peer may still read its shared memory.
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_wait_acquire();
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 4);
 }
 

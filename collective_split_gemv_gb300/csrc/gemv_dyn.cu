@@ -51,6 +51,20 @@
 // workgroup scheduling is communication-aware (units are drawn tile-major, so
 // a tile's R contributors run close together and its partials stay in L2).
 //
+// Cluster epilogue (kCl): when every unit has a CTA slot of its own (one
+// wave, no K splits), the launch is a grid of thread-block clusters of R CTAs,
+// cluster t holding the R units of row tile t (CTA rank r = rank r).  Nothing
+// is drawn; each CTA streams its one unit, and its epilogue puts the fp32
+// partial into the CTA's own shared memory (the drained ring) instead of the
+// scratch region.  One cluster barrier (release / acquire) then publishes the
+// R partials, and every CTA sums its share of the tile over them -- read from
+// the peers' shared memory, in rank order, in fp32, the same additions as
+// the global-memory reducer -- and stores the result; a second barrier keeps
+// each CTA's shared memory alive until its peers have read it.  This replaces
+// the global-memory protocol's round trips at the end of the launch (partial
+// store, fence, ticket, then flag and partial loads by the last arriver),
+// which in a one-wave launch are not hidden behind other units.
+//
 // Safety: all mbarrier waits are bounded (%globaltimer); decisions that
 // steer the group's named barrier are made uniform with bar.red.and; a CTA
 // that gave up latches a status code, waits (bounded) for its copies and MMAs
@@ -64,6 +78,8 @@
 //   8 last tile reduction done   9 exit
 //  10 units computed (count)    11 tile reductions (count)
 //  12 last stage issued         13 producer saw the end of the work
+//  14 cluster epilogue: partials published (first cluster barrier passed)
+//  15 cluster epilogue: share of the tile stored
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -206,9 +222,89 @@ __device__ __forceinline__ void load_w_slab(uint8_t *dst, const CUtensorMap *tmW
     }
 }
 
+// The cluster epilogue's sum (kCl): CTA `me` of the R-CTA cluster of row
+// tile t sums its share of the tile's [b][row] outputs over the R partials
+// (each CTA's `part`, [b][kM] fp32 in its own shared memory), in rank order,
+// element by element as reduce_items does, and stores them; kW = 4: four
+// consecutive rows per item (N % 4 == 0), else single outputs.  All kThreads
+// threads of the CTA take part; between the two cluster barriers only the
+// loads from the peers happen, the stores follow the second arrive.
+template <int kW>
+__device__ __forceinline__ void cluster_sum_tile(const GemvArgs &a, const float *part, const int *abort_word, int t,
+                                                 int me, int tid) {
+    using V = typename std::conditional<kW == 4, float4, float>::type;
+    constexpr int kPerRow = kM / kW;                         // items per batch row
+    constexpr int kMax = (kNmma * kPerRow + kThreads - 1) / kThreads;   // items per thread at R = 1, B = 16
+    const int R = a.R;
+    const int n0 = t * kM;
+    const int rows = min(kM, a.N - n0);
+    const int items = a.B * kPerRow;
+    const int share = (items + R - 1) / R;
+    // A tile is stored only if all R units were computed (a CTA that gave up
+    // has latched the status): the R abort words are read in the same round
+    // of loads as the partials.
+    int bad = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxClusterRanks; ++q)
+        if (q < R) bad |= ld_cluster_s32(cluster_addr(abort_word, (uint32_t)q));
+    V acc[kMax];
+    size_t off[kMax];
+    bool mine[kMax];
+#pragma unroll
+    for (int k = 0; k < kMax; ++k) {
+        const int l = tid + k * kThreads;                    // this thread's k-th item of the share
+        const int i = me * share + l;
+        const int b = i / kPerRow;
+        const int row = (i - b * kPerRow) * kW;
+        mine[k] = l < share && i < items && row < rows;
+        off[k] = (size_t)b * a.N + n0 + row;
+        if (mine[k]) {
+            const int e = b * kM + row;
+            V v[kMaxClusterRanks];
+#pragma unroll
+            for (int q = 0; q < kMaxClusterRanks; ++q) {
+                if (q < R) {
+                    if constexpr (kW == 4) {
+                        v[q] = ld_cluster_v4f32(cluster_addr(part + e, (uint32_t)q));
+                    } else {
+                        v[q] = ld_cluster_f32(cluster_addr(part + e, (uint32_t)q));
+                    }
+                }
+            }
+            acc[k] = v[0];
+#pragma unroll
+            for (int q = 1; q < kMaxClusterRanks; ++q) {
+                if (q < R) {
+                    if constexpr (kW == 4) {
+                        acc[k].x += v[q].x;
+                        acc[k].y += v[q].y;
+                        acc[k].z += v[q].z;
+                        acc[k].w += v[q].w;
+                    } else {
+                        acc[k] += v[q];
+                    }
+                }
+            }
+        }
+    }
+    // The peers' shared memory has been read (arrive orders the loads before
+    // it); every peer waits for this before it leaves.
+    cluster_arrive_release();
+#pragma unroll
+    for (int k = 0; k < kMax; ++k) {
+        if (mine[k] && bad == 0) {
+            if constexpr (kW == 4) {
+                store_output4(a, off[k], acc[k]);
+            } else {
+                store_output(a, off[k], acc[k]);
+            }
+        }
+    }
+}
+
 // At two CTAs per SM the register file must hold both (at most 168
 // registers a thread); the three-CTA rings do not fit it and run in two waves.
-template <int kEngine, int kSlabs, int kB, int kCps>
+template <int kEngine, int kSlabs, int kB, int kCps, bool kCl>
 __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemvArgs a, const DynGeom geo) {
@@ -219,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
+    static_assert(!kCl || (kEngine == 0 && RingT::kStageBytes >= kNmma * kM * 4),
+                  "cluster epilogue: tcgen05 engine, partial fits in the first stage");
     constexpr int kStages = RingT::kStages;
     constexpr int kStageBytes = RingT::kStageBytes;
     constexpr int kBK = 64 * kSlabs;
@@ -292,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         // unit's first stages go out before the dependency wait and x's after
         // it.  A row-major W may be the output of the kernel just before (any
         // kernel, not only this library's): it is loaded after the wait.
-        // The first unit is the CTA's own index (G <= U).
-        const int u = a.reverse_order ? U - 1 - (int)blockIdx.x : (int)blockIdx.x;
+        // The first unit is the CTA's own index (G <= U); in a cluster launch
+        // the only one, CTA rank r of cluster t holding unit t * R + r.
+        const int u = (a.reverse_order && !kCl) ? U - 1 - (int)blockIdx.x : (int)blockIdx.x;
         int t, r, sp;
         unit_of(a, u, S, &t, &r, &sp);
         const int kb0 = sp * KBs;
@@ -356,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                     ++issued;
                     break;
                 }
-                const int u = a.reverse_order ? U - 1 - (int)tk : (int)tk;
+                const int u = (a.reverse_order && !kCl) ? U - 1 - (int)tk : (int)tk;
                 int t, r, sp;
                 unit_of(a, u, S, &t, &r, &sp);
                 const int kb0 = sp * KBs;
@@ -371,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 const int kb_from = first ? kb0 + pre : kb0;   // the first unit's first stages are out
                 first = false;
                 uint32_t next_raw = 0u;
-                if (kb_from >= kb1) next_raw = atom_add_relaxed_gpu(work, 1u);
+                if (!kCl && kb_from >= kb1) next_raw = atom_add_relaxed_gpu(work, 1u);
                 for (int kb = kb_from; kb < kb1; ++kb) {
                     const int st = issued % kStages;
                     const uint32_t ph = (uint32_t)(issued / kStages) & 1u;
@@ -390,11 +489,15 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                     for (int s = 0; s < kSlabs; ++s)
                         tma_load_3d_hint(dst + kSlabs * kSlabA + s * kSlabX, &tmX, &full_bar[st], kb * kBK + s * 64,
                                          0, r, pol_x);
-                    if (kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(work, 1u);
+                    if (!kCl && kb == kb1 - 1) next_raw = atom_add_relaxed_gpu(work, 1u);
                     ++issued;
                     tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 12);
                 }
-                asm volatile("add.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"((uint32_t)geo.G));
+                if constexpr (kCl) {
+                    tk = (uint32_t)U;   // one unit per CTA, nothing drawn
+                } else {
+                    asm volatile("add.u32 %0, %1, %2;" : "=r"(tk) : "r"(next_raw), "r"((uint32_t)geo.G));
+                }
             }
             if (!ok) {
                 latch_status(a.status, kProtoTimeout, -1, -1, epoch);
@@ -529,6 +632,19 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[j]);
+                if constexpr (kCl) {
+                    // The partial goes to the drained ring (every MMA of the
+                    // CTA's one unit has completed, no copy is in flight);
+                    // the proxy fence orders those asynchronous accesses of
+                    // the ring before these plain stores.
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    float *part = reinterpret_cast<float *>(smem);
+#pragma unroll
+                    for (int b = 0; b < kNmma; ++b)
+                        if (b < a.B) part[b * kM + row] = v[b];
+                    ++seg;
+                    continue;
+                }
                 int t, r, sp;
                 unit_of(a, u, S, &t, &r, &sp);
                 const int n = t * kM + row;
@@ -627,6 +743,23 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kCl) {
+        // Every CTA of the cluster reaches this point (all waits above are
+        // bounded), also one that gave up: the barriers need all of them.
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 14);
+        const int me = (int)(blockIdx.x % (unsigned)a.R);
+        const int t = (int)(blockIdx.x / (unsigned)a.R);
+        const float *part = reinterpret_cast<const float *>(smem);
+        const int *abort_word = const_cast<const int *>(&abort_sh);
+        if ((a.N & 3) == 0)
+            cluster_sum_tile<4>(a, part, abort_word, t, me, (int)threadIdx.x);
+        else
+            cluster_sum_tile<1>(a, part, abort_word, t, me, (int)threadIdx.x);
+        if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 15);
+        cluster_wait_acquire();
+    }
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 9);
     if (kEngine == 0 && warp == 1) {
         tc_fence_after();
@@ -634,27 +767,58 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     }
 }
 
-template <int kEngine, int kSlabs, int kB, int kCps>
+template <int kEngine, int kSlabs, int kB, int kCps, bool kCl>
 cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, bool chained, cudaStream_t s) {
-    auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps>;
+    auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps, kCl>;
     constexpr int smem = Ring<kSlabs, kCps>::kSmem;
     static std::atomic<unsigned long long> attr_devices{0};
     cudaError_t e = set_smem_once(kern, smem, attr_devices);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3((unsigned)geo.G), dim3(kThreads), (size_t)smem, s, chained, m[0], m[1], a, geo);
+    if (!kCl) return launch_kernel(kern, dim3((unsigned)geo.G), dim3(kThreads), (size_t)smem, s, chained, m[0], m[1], a, geo);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)geo.G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)geo.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int nattr = 1;
+    if (chained) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        nattr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], a, geo);
 }
 
 template <int kEngine, int kB>
 cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, int slabs, int cps,
                           bool chained, cudaStream_t s) {
+    if (geo.cluster) {
+        // Cluster epilogue: tcgen05 engine, rings sized for two CTAs per SM.
+        if constexpr (kEngine == 0) {
+            switch (cps * 10 + slabs) {
+                case 21: return launch_cfg<kEngine, 1, kB, 2, true>(a, geo, m, chained, s);
+                case 22: return launch_cfg<kEngine, 2, kB, 2, true>(a, geo, m, chained, s);
+                case 23: return launch_cfg<kEngine, 3, kB, 2, true>(a, geo, m, chained, s);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (cps * 10 + slabs) {
-        case 11: return launch_cfg<kEngine, 1, kB, 1>(a, geo, m, chained, s);
-        case 12: return launch_cfg<kEngine, 2, kB, 1>(a, geo, m, chained, s);
-        case 14: return launch_cfg<kEngine, 4, kB, 1>(a, geo, m, chained, s);
-        case 21: return launch_cfg<kEngine, 1, kB, 2>(a, geo, m, chained, s);
-        case 22: return launch_cfg<kEngine, 2, kB, 2>(a, geo, m, chained, s);
-        case 23: return launch_cfg<kEngine, 3, kB, 2>(a, geo, m, chained, s);
-        case 31: return launch_cfg<kEngine, 1, kB, 3>(a, geo, m, chained, s);
+        case 11: return launch_cfg<kEngine, 1, kB, 1, false>(a, geo, m, chained, s);
+        case 12: return launch_cfg<kEngine, 2, kB, 1, false>(a, geo, m, chained, s);
+        case 14: return launch_cfg<kEngine, 4, kB, 1, false>(a, geo, m, chained, s);
+        case 21: return launch_cfg<kEngine, 1, kB, 2, false>(a, geo, m, chained, s);
+        case 22: return launch_cfg<kEngine, 2, kB, 2, false>(a, geo, m, chained, s);
+        case 23: return launch_cfg<kEngine, 3, kB, 2, false>(a, geo, m, chained, s);
+        case 31: return launch_cfg<kEngine, 1, kB, 3, false>(a, geo, m, chained, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -709,6 +873,10 @@ int dyn_block_k(int slabs) { return 64 * slabs; }
 bool dyn_config_supported(int slabs, int cps) {
     return (cps == 1 && (slabs == 1 || slabs == 2 || slabs == 4)) ||
            (cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3)) || (cps == 3 && slabs == 1);
+}
+
+bool dyn_cluster_supported(int engine, int slabs, int cps) {
+    return engine == 0 && cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3);
 }
 
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,

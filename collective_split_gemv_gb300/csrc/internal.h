@@ -283,6 +283,8 @@ struct DynGeom {
     int KB;         // K blocks per (tile, rank)
     int KBs;        // K blocks per split
     int G;
+    int cluster;    // 0: units drawn, global-memory protocol; R: cluster epilogue
+                    // (G = units, one per CTA, splits 1, clusters of R CTAs)
 };
 // Encodes the TMA descriptors of a launch (cached by the caller): `maps`
 // points at two CUtensorMap objects (W, x), 64-byte aligned.
@@ -290,6 +292,8 @@ int dyn_encode_maps(const GemvArgs &a, void *maps);
 // K elements per ring stage, and the (slabs, CTAs per SM) pipelines built.
 int dyn_block_k(int slabs);
 bool dyn_config_supported(int slabs, int ctas_per_sm);
+// Pipelines the cluster epilogue is built for (tcgen05 engine, two CTAs per SM).
+bool dyn_cluster_supported(int engine, int slabs, int ctas_per_sm);
 // chained: launch as a programmatic dependent of the previous kernel on the
 // stream (its CTAs may start while that one drains; see the kernel).
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,

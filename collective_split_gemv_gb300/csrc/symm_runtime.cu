@@ -51,6 +51,7 @@ struct symm_handle {
     int opt_ar_kernel = 0;      // one-shot all-reduce kernel (kArKernel*)
     int opt_copy_engine = 0;    // symm_copy_*: 1 = always the copy engine, 0 = SMs where possible
     int opt_unfused = 0;        // gemv_all_reduce as two kernels (GEMV partials, then their all-reduce)
+    int opt_dyn_cluster = -1;   // persistent kernel's cluster epilogue: -1 auto, 0 off, 1 on
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     // Slot-0 range written by the last kernel this handle launched (the same
@@ -296,8 +297,8 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 
 // The kernel and launch geometry gemv_all_reduce would use.
 struct Plan {
-    int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0;
-    DynGeom dyn = {0, 1, 0, 0, 0};
+    int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0, cluster = 0;
+    DynGeom dyn = {0, 1, 0, 0, 0, 0};
 };
 
 // `cap`: scratch bytes per slot the partials may use (the whole region, or
@@ -330,6 +331,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         return fail(SYMM_ERANGE, "%d row tiles exceed the signal pad's %d", pl->tiles, h->max_tiles);
     pl->splits = 1;
     pl->grid = pl->tiles * (h->mp_rank >= 0 ? 1 : h->R);
+    pl->cluster = pl->path == kPathCluster ? h->R : 0;
     if (pl->path == kPathDyn) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the persistent kernel needs K > 0");
         pl->engine = dyn_engine(h, B);
@@ -352,12 +354,33 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         long long S = h->opt_dyn_splits > 0
                           ? h->opt_dyn_splits
                           : (4 * pairs > G ? 1 : std::min<long long>(8, (G + 2 * pairs - 1) / (2 * pairs)));
+        // Cluster epilogue: one (tile, rank) unit per CTA, the R units of a
+        // tile one cluster, partials summed through distributed shared memory.
+        // Automatic when the units fit the grid in one wave (nothing would be
+        // drawn anyway, and the end of such a launch is the global-memory
+        // protocol's round trips) and need no K splits.
+        const bool cl_ok = dyn_cluster_supported(pl->engine, pl->slabs, pl->cps) && h->mp_rank < 0 &&
+                           !h->opt_unfused && h->R <= kMaxClusterRanks;
+        bool cl = false;
+        if (h->opt_dyn_cluster == 1) {
+            if (!cl_ok)
+                return fail(SYMM_EINVAL,
+                            "the cluster epilogue needs the tcgen05 engine at 2 CTAs per SM (1-3 slabs), R <= %d, "
+                            "the fused form and a single-process handle", kMaxClusterRanks);
+            if (h->opt_dyn_splits > 1) return fail(SYMM_EINVAL, "the cluster epilogue runs without K splits");
+            cl = true;
+        } else if (h->opt_dyn_cluster < 0) {
+            cl = cl_ok && h->R >= 2 && S == 1 && pairs <= G;
+        }
+        if (cl) S = 1;
         S = std::min<long long>(S, KB);
         while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;
         const long long KBs = (KB + S - 1) / S;
         S = (KB + KBs - 1) / KBs;   // no empty split
         const long long units = pairs * S;
-        G = std::max<long long>(1, std::min<long long>(G, units));
+        G = cl ? units : std::max<long long>(1, std::min<long long>(G, units));
+        pl->dyn.cluster = cl ? h->R : 0;
+        pl->cluster = pl->dyn.cluster;
         pl->dyn.units = (int)units;
         pl->dyn.splits = (int)S;
         pl->dyn.KB = (int)KB;
@@ -916,6 +939,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             if (value < 0 || value > 3) return fail(SYMM_EINVAL, "persistent-kernel CTAs per SM %d not in 0..3", value);
             h->opt_sk_cps = value;
             return SYMM_OK;
+        case SYMM_OPT_DYN_CLUSTER:
+            if (value < -1 || value > 1) return fail(SYMM_EINVAL, "cluster epilogue %d not in {-1 auto, 0, 1}", value);
+            h->opt_dyn_cluster = value;
+            return SYMM_OK;
         default:
             return fail(SYMM_EINVAL, "unknown option %d", option);
     }
@@ -938,6 +965,7 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
     out->parts_max = 1;
     out->kblocks = pl.dyn.KB;
     out->ctas_per_sm = pl.cps;
+    out->cluster = pl.cluster;
     return SYMM_OK;
 }
 

@@ -43,7 +43,8 @@ PHASES = {
                            5: "epilogue: first accumulator ready", 12: "producer: last stage issued",
                            13: "producer: end of work seen", 6: "epilogue: last accumulator ready",
                            7: "last unit published (not reduced here)", 8: "last tile reduction done",
-                           9: "exit"},
+                           14: "cluster epilogue: partials published (cluster barrier passed)",
+                           15: "cluster epilogue: share of the tile stored", 9: "exit"},
     "gemv_ar_cluster_kernel": {0: "entry", 1: "dot products done, partial in shared memory",
                                2: "partials published (first cluster barrier passed)",
                                3: "share of the tile summed and stored", 4: "exit"},

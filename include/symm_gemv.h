@@ -502,12 +502,22 @@ enum {
                                  contiguous side is device memory or pinned host memory mapped at the same
                                  address (a link in the chain of programmatic dependent launches, see
                                  SYMM_OPT_CHAIN), else with the copy engine; 1 always the copy engine */
-    SYMM_OPT_UNFUSED = 13     /* gemv_all_reduce only, for measuring what fusion buys: 1 runs the call
+    SYMM_OPT_UNFUSED = 13,    /* gemv_all_reduce only, for measuring what fusion buys: 1 runs the call
                                  unfused, as two kernels -- the persistent GEMV (path 4) storing every
                                  rank's fp32 partials, then a separate all-reduce kernel that sums them in
                                  the fused reducer's order and stores bf16 into every slot (the same
                                  bits as the fused call); 0 (default) fused.  The other forms, path 1
                                  and K == 0 return SYMM_EINVAL while it is set */
+    SYMM_OPT_DYN_CLUSTER = 14 /* path 4, the end of a launch: -1 auto (default), 0 off, 1 on.  On: the
+                                 launch is a grid of thread-block clusters of R CTAs, one (row tile, rank)
+                                 unit per CTA, the R units of a tile in one cluster; each CTA keeps its
+                                 fp32 partial in its own shared memory, and after a cluster barrier every
+                                 CTA sums its share of the tile over the R partials (read through
+                                 distributed shared memory, rank order, the same bits as the global-memory
+                                 protocol) and stores it.  It needs the tcgen05 engine at 2 CTAs per SM,
+                                 R <= 8, no K splits, the fused form and a single-process handle (else 1
+                                 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and the
+                                 units fit the persistent grid in one wave (nothing would be drawn) */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 
@@ -534,9 +544,11 @@ int symm_info(symm_handle_t *h, symm_info_t *info);
  *   grid           CTAs launched
  *   parts_max      1 (kept for layout compatibility)
  *   kblocks        path 4: K blocks per (tile, rank)
- *   ctas_per_sm    path 4: resident CTAs per SM the ring is sized for */
+ *   ctas_per_sm    path 4: resident CTAs per SM the ring is sized for
+ *   cluster        CTAs per thread-block cluster: R on path 5 and for path 4's
+ *                  cluster epilogue (SYMM_OPT_DYN_CLUSTER), else 0 */
 typedef struct {
-    int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks, ctas_per_sm;
+    int path, engine, slabs, rows_per_tile, tiles, splits, grid, parts_max, kblocks, ctas_per_sm, cluster;
 } symm_gemv_plan_t;
 int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out);
 

@@ -885,8 +885,8 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
         "us_per_call_equiv": round(sec_per_call * 1e6, 1),
         "cores": used,
         "kind": "oracle",
-        "sample": (f"{rows} of {full} {unit} of {name}, {reps} repetitions, {el:.1f} s of CPU time; "
-                   "time scaled to the full call"),
+        "sample": (f"{rows} of {full} {unit} of {name}, {reps} repetitions, {el:.3f} s wall time on {used} "
+                   f"thread{'s' if used != 1 else ''}; time scaled to the full call"),
     }
 
 

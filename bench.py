@@ -595,10 +595,13 @@ def run_ours(args, rank, world, local_rank):
         # What fusion buys: the same calls unfused (the GEMV storing every
         # rank's fp32 partials, then a separate all-reduce kernel of them),
         # timed like the main leg.
+        # (The unfused form has no tile reduction, so no cluster epilogue either.)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, 1)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, -1)
         uf_step, uf_launch, _ = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id,
                                            per_launch=not chained)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, 0)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, args.dyn_cluster)
         code, _, _ = csg.symm_status(ws.h, stream)
         if code != csg.SYMM_OK:
             raise SystemExit(f"protocol error in the unfused leg: {csg.symm_last_error()}")

@@ -516,8 +516,10 @@ enum {
                                  distributed shared memory, rank order, the same bits as the global-memory
                                  protocol) and stores it.  It needs the tcgen05 engine at 2 CTAs per SM,
                                  R <= 8, no K splits, the fused form and a single-process handle (else 1
-                                 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and the
-                                 units fit the persistent grid in one wave (nothing would be drawn) */
+                                 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and
+                                 either the units fit the persistent grid in one wave (nothing would be
+                                 drawn) or they are long (K/R >= 3072, 768 KB of W per unit), when the
+                                 hardware's scheduling of whole clusters beats drawing single units */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

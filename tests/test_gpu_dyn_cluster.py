@@ -116,11 +116,13 @@ def test_cluster_epilogue_bias_rmsnorm(R, N, K, B):
     assert tolerance_ratio(words_to_f64(got[0][0]), y_ref) <= 1.0
 
 
-def test_cluster_epilogue_is_automatic_for_one_wave_layers():
+def test_cluster_epilogue_automatic_choice():
     """attn_out_proj (64 tiles x 4 ranks = 256 units) fits the persistent
-    grid in one wave and takes the cluster epilogue; the decode layer (512
-    units), the FFMA engine, one CTA per SM, K splits, the unfused form and a
-    single rank keep the global-memory protocol."""
+    grid in one wave and takes the cluster epilogue, and so do layers of any
+    unit count whose units are long (K/R >= 3072: the decode, the large
+    layer); layers of many short units, the FFMA engine, one CTA per SM, K
+    splits, the unfused form and a single rank keep the global-memory
+    protocol."""
     ws = GemvWorkspace(4, 4 * 8192, 4 * 64, 8)    # scratch and pad for up to 256 row tiles at B = 8
     try:
         h = ws.h
@@ -130,7 +132,9 @@ def test_cluster_epilogue_is_automatic_for_one_wave_layers():
         csg.symm_set_option(h, csg.SYMM_OPT_DYN_CLUSTER, AUTO)
         assert csg.symm_gemv_plan(h, 8192, 8192, 8)["cluster"] == 4
         assert csg.symm_gemv_plan(h, 8192, 8192, 8)["grid"] == 256
-        assert csg.symm_gemv_plan(h, 4 * 8192, 8192, 8)["cluster"] == 0     # 1024 units
+        assert csg.symm_gemv_plan(h, 4 * 8192, 8192, 8)["cluster"] == 0     # 1024 units of K/R = 2048
+        long_units = csg.symm_gemv_plan(h, 4 * 8192, 4 * 3072, 8)            # 1024 units of K/R = 3072
+        assert long_units["cluster"] == 4 and long_units["grid"] == 1024
         csg.symm_set_option(h, csg.SYMM_OPT_SK_ENGINE, 1)
         assert csg.symm_gemv_plan(h, 8192, 8192, 2)["cluster"] == 0
         csg.symm_set_option(h, csg.SYMM_OPT_SK_ENGINE, -1)

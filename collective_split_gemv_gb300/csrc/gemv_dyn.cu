@@ -879,6 +879,53 @@ bool dyn_cluster_supported(int engine, int slabs, int cps) {
     return engine == 0 && cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3);
 }
 
+namespace {
+
+template <int kSlabs>
+int max_active_clusters(int R) {
+    auto kern = gemv_ar_dyn_kernel<0, kSlabs, 0, 2, true>;
+    constexpr int smem = Ring<kSlabs, 2>::kSmem;
+    static std::atomic<unsigned long long> attr_devices{0};
+    if (set_smem_once(kern, smem, attr_devices) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)R, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)R;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace
+
+bool dyn_cluster_fits(int slabs, int R) {
+    // Per device, slab count and R: 0 unknown, 1 fits, 2 does not.
+    static std::atomic<unsigned char> known[64][4][kMaxClusterRanks + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || slabs < 1 || slabs > 3 || R < 1 ||
+        R > kMaxClusterRanks)
+        return false;
+    std::atomic<unsigned char> &k = known[dev][slabs][R];
+    unsigned char v = k.load(std::memory_order_acquire);
+    if (v == 0) {
+        const int n = slabs == 1 ? max_active_clusters<1>(R) : slabs == 2 ? max_active_clusters<2>(R)
+                                                                           : max_active_clusters<3>(R);
+        v = n > 0 ? 1 : 2;
+        k.store(v, std::memory_order_release);
+    }
+    return v == 1;
+}
+
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,
                             bool chained, cudaStream_t s) {
     const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);

@@ -294,6 +294,10 @@ int dyn_block_k(int slabs);
 bool dyn_config_supported(int slabs, int ctas_per_sm);
 // Pipelines the cluster epilogue is built for (tcgen05 engine, two CTAs per SM).
 bool dyn_cluster_supported(int engine, int slabs, int ctas_per_sm);
+// Whether a cluster of R CTAs of that kernel can be resident on the current
+// device at all (the occupancy query, cached per device; false on a device
+// or partition whose GPCs cannot hold one).
+bool dyn_cluster_fits(int slabs, int R);
 // chained: launch as a programmatic dependent of the previous kernel on the
 // stream (its CTAs may start while that one drains; see the kernel).
 cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,

@@ -368,13 +368,15 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         // slower than drawn ones, 256-512 KB units about even, 0.9-2 MB units
         // 1-6 % faster.
         const bool cl_ok = dyn_cluster_supported(pl->engine, pl->slabs, pl->cps) && h->mp_rank < 0 &&
-                           !h->opt_unfused && h->R <= kMaxClusterRanks;
+                           !h->opt_unfused && h->R <= kMaxClusterRanks &&
+                           (h->opt_dyn_cluster == 0 || dyn_cluster_fits(pl->slabs, h->R));
         bool cl = false;
         if (h->opt_dyn_cluster == 1) {
             if (!cl_ok)
                 return fail(SYMM_EINVAL,
                             "the cluster epilogue needs the tcgen05 engine at 2 CTAs per SM (1-3 slabs), R <= %d, "
-                            "the fused form and a single-process handle", kMaxClusterRanks);
+                            "the fused form, a single-process handle and a device that can hold a cluster of R "
+                            "such CTAs", kMaxClusterRanks);
             if (h->opt_dyn_splits > 1) return fail(SYMM_EINVAL, "the cluster epilogue runs without K splits");
             cl = true;
         } else if (h->opt_dyn_cluster < 0) {

@@ -515,8 +515,8 @@ enum {
                                  CTA sums its share of the tile over the R partials (read through
                                  distributed shared memory, rank order, the same bits as the global-memory
                                  protocol) and stores it.  It needs the tcgen05 engine at 2 CTAs per SM,
-                                 R <= 8, no K splits, the fused form and a single-process handle (else 1
-                                 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and
+                                 R <= 8, no K splits, the fused form, a single-process handle and a device
+                                 that can hold a cluster of R such CTAs (else 1 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and
                                  either the units fit the persistent grid in one wave (nothing would be
                                  drawn) or they are long (K/R >= 3072, 768 KB of W per unit), when the
                                  hardware's scheduling of whole clusters beats drawing single units */

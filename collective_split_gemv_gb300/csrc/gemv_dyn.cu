@@ -52,14 +52,15 @@
 // a tile's R contributors run close together and its partials stay in L2).
 //
 // Cluster epilogue (kCl): when every unit has a CTA slot of its own (one
-// wave, no K splits), the launch is a grid of thread-block clusters of R CTAs,
-// cluster t holding the R units of row tile t (CTA rank r = rank r).  Nothing
-// is drawn; each CTA streams its one unit, and its epilogue puts the fp32
-// partial into the CTA's own shared memory (the drained ring) instead of the
-// scratch region.  One cluster barrier (release / acquire) then publishes the
-// R partials, and every CTA sums its share of the tile over them -- read from
-// the peers' shared memory, in rank order, in fp32, the same additions as
-// the global-memory reducer -- and stores the result; a second barrier keeps
+// wave), or units are long, the launch is a grid of thread-block clusters of
+// C = R * splits CTAs (at most 8), cluster t holding the C units of row tile
+// t (CTA rank j = contributor j: rank j / splits, K split j % splits).
+// Nothing is drawn; each CTA streams its one unit, and its epilogue puts the
+// fp32 partial into the CTA's own shared memory (the drained ring) instead of
+// the scratch region.  One cluster barrier (release / acquire) then
+// publishes the C partials, and every CTA sums its share of the tile over
+// them -- read from the peers' shared memory, in contributor order, in fp32,
+// the same additions as the global-memory reducer -- and stores the result; a second barrier keeps
 // each CTA's shared memory alive until its peers have read it.  This replaces
 // the global-memory protocol's round trips at the end of the launch (partial
 // store, fence, ticket, then flag and partial loads by the last arriver),
@@ -222,31 +223,32 @@ __device__ __forceinline__ void load_w_slab(uint8_t *dst, const CUtensorMap *tmW
     }
 }
 
-// The cluster epilogue's sum (kCl): CTA `me` of the R-CTA cluster of row
-// tile t sums its share of the tile's [b][row] outputs over the R partials
-// (each CTA's `part`, [b][kM] fp32 in its own shared memory), in rank order,
-// element by element as reduce_items does, and stores them; kW = 4: four
-// consecutive rows per item (N % 4 == 0), else single outputs.  All kThreads
-// threads of the CTA take part; between the two cluster barriers only the
-// loads from the peers happen, the stores follow the second arrive.
+// The cluster epilogue's sum (kCl): CTA `me` of the C-CTA cluster of row
+// tile t (C = R * splits contributors, CTA rank j = contributor j: rank
+// j / splits, K split j % splits) sums its share of the tile's [b][row]
+// outputs over the C partials (each CTA's `part`, [b][kM] fp32 in its own
+// shared memory), in contributor order, element by element as reduce_items
+// does, and stores them; kW = 4: four consecutive rows per item (N % 4 ==
+// 0), else single outputs.  All kThreads threads of the CTA take part;
+// between the two cluster barriers only the loads from the peers happen, the
+// stores follow the second arrive.
 template <int kW>
 __device__ __forceinline__ void cluster_sum_tile(const GemvArgs &a, const float *part, const int *abort_word, int t,
-                                                 int me, int tid) {
+                                                 int me, int C, int tid) {
     using V = typename std::conditional<kW == 4, float4, float>::type;
     constexpr int kPerRow = kM / kW;                         // items per batch row
     constexpr int kMax = (kNmma * kPerRow + kThreads - 1) / kThreads;   // items per thread at R = 1, B = 16
-    const int R = a.R;
     const int n0 = t * kM;
     const int rows = min(kM, a.N - n0);
     const int items = a.B * kPerRow;
-    const int share = (items + R - 1) / R;
-    // A tile is stored only if all R units were computed (a CTA that gave up
-    // has latched the status): the R abort words are read in the same round
+    const int share = (items + C - 1) / C;
+    // A tile is stored only if all C units were computed (a CTA that gave up
+    // has latched the status): the C abort words are read in the same round
     // of loads as the partials.
     int bad = 0;
 #pragma unroll
     for (int q = 0; q < kMaxClusterRanks; ++q)
-        if (q < R) bad |= ld_cluster_s32(cluster_addr(abort_word, (uint32_t)q));
+        if (q < C) bad |= ld_cluster_s32(cluster_addr(abort_word, (uint32_t)q));
     V acc[kMax];
     size_t off[kMax];
     bool mine[kMax];
@@ -263,7 +265,7 @@ __device__ __forceinline__ void cluster_sum_tile(const GemvArgs &a, const float 
             V v[kMaxClusterRanks];
 #pragma unroll
             for (int q = 0; q < kMaxClusterRanks; ++q) {
-                if (q < R) {
+                if (q < C) {
                     if constexpr (kW == 4) {
                         v[q] = ld_cluster_v4f32(cluster_addr(part + e, (uint32_t)q));
                     } else {
@@ -274,7 +276,7 @@ __device__ __forceinline__ void cluster_sum_tile(const GemvArgs &a, const float 
             acc[k] = v[0];
 #pragma unroll
             for (int q = 1; q < kMaxClusterRanks; ++q) {
-                if (q < R) {
+                if (q < C) {
                     if constexpr (kW == 4) {
                         acc[k].x += v[q].x;
                         acc[k].y += v[q].y;
@@ -749,14 +751,17 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         cluster_arrive_release();
         cluster_wait_acquire();
         if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 14);
-        const int me = (int)(blockIdx.x % (unsigned)a.R);
-        const int t = (int)(blockIdx.x / (unsigned)a.R);
+        // Unit u = blockIdx.x = t * C + j, j = r * S + s: the cluster of row
+        // tile t, CTA rank j.
+        const int C = a.R * S;
+        const int me = (int)(blockIdx.x % (unsigned)C);
+        const int t = (int)(blockIdx.x / (unsigned)C);
         const float *part = reinterpret_cast<const float *>(smem);
         const int *abort_word = const_cast<const int *>(&abort_sh);
         if ((a.N & 3) == 0)
-            cluster_sum_tile<4>(a, part, abort_word, t, me, (int)threadIdx.x);
+            cluster_sum_tile<4>(a, part, abort_word, t, me, C, (int)threadIdx.x);
         else
-            cluster_sum_tile<1>(a, part, abort_word, t, me, (int)threadIdx.x);
+            cluster_sum_tile<1>(a, part, abort_word, t, me, C, (int)threadIdx.x);
         if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 15);
         cluster_wait_acquire();
     }

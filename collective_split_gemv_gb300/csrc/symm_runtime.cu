@@ -357,39 +357,43 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         long long S = h->opt_dyn_splits > 0
                           ? h->opt_dyn_splits
                           : (4 * pairs > G ? 1 : std::min<long long>(8, (G + 2 * pairs - 1) / (2 * pairs)));
-        // Cluster epilogue: one (tile, rank) unit per CTA, the R units of a
-        // tile one cluster, partials summed through distributed shared memory;
-        // beyond one wave the hardware starts each cluster as slots free up.
-        // Automatic (no K splits) when the units fit the grid in one wave
-        // (nothing would be drawn anyway, and the end of such a launch is the
-        // global-memory protocol's round trips), or when they are long enough
-        // that a CTA's start-up is small against its stream: measured on
-        // 268-537 MB layers, chained calls with units of 64-128 KB ran 3-18 %
+        // Cluster epilogue: one unit per CTA, the R * S units of a tile one
+        // cluster (at most 8 CTAs), partials summed through distributed shared
+        // memory; beyond one wave the hardware starts each cluster as slots
+        // free up.  Automatic (no K splits) when the units fit the grid in one
+        // wave (nothing would be drawn anyway, and the end of such a launch is
+        // the global-memory protocol's round trips), or when they are long
+        // enough that a CTA's start-up is small against its stream: measured
+        // on 268-537 MB layers, chained calls with units of 64-128 KB ran 3-18 %
         // slower than drawn ones, 256-512 KB units about even, 0.9-2 MB units
-        // 1-6 % faster.
-        const bool cl_ok = dyn_cluster_supported(pl->engine, pl->slabs, pl->cps) && h->mp_rank < 0 &&
-                           !h->opt_unfused && h->R <= kMaxClusterRanks &&
-                           (h->opt_dyn_cluster == 0 || dyn_cluster_fits(pl->slabs, h->R));
+        // 1-6 % faster.  Forced on, it takes the requested K splits (none by
+        // default).
+        const bool cl_base = dyn_cluster_supported(pl->engine, pl->slabs, pl->cps) && h->mp_rank < 0 &&
+                             !h->opt_unfused;
         bool cl = false;
         if (h->opt_dyn_cluster == 1) {
-            if (!cl_ok)
-                return fail(SYMM_EINVAL,
-                            "the cluster epilogue needs the tcgen05 engine at 2 CTAs per SM (1-3 slabs), R <= %d, "
-                            "the fused form, a single-process handle and a device that can hold a cluster of R "
-                            "such CTAs", kMaxClusterRanks);
-            if (h->opt_dyn_splits > 1) return fail(SYMM_EINVAL, "the cluster epilogue runs without K splits");
             cl = true;
+            if (h->opt_dyn_splits <= 0) S = 1;
         } else if (h->opt_dyn_cluster < 0) {
-            cl = cl_ok && h->R >= 2 && S == 1 && (pairs <= G || Kr >= kClusterEpilogueMinKr);
+            cl = cl_base && h->R >= 2 && S == 1 && (pairs <= G || Kr >= kClusterEpilogueMinKr);
         }
-        if (cl) S = 1;
         S = std::min<long long>(S, KB);
         while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;
         const long long KBs = (KB + S - 1) / S;
         S = (KB + KBs - 1) / KBs;   // no empty split
+        if (cl) {
+            const long long C = (long long)h->R * S;
+            const bool fits = cl_base && C <= kMaxClusterRanks && dyn_cluster_fits(pl->slabs, (int)C);
+            if (!fits && h->opt_dyn_cluster == 1)
+                return fail(SYMM_EINVAL,
+                            "the cluster epilogue needs the tcgen05 engine at 2 CTAs per SM (1-3 slabs), R x splits "
+                            "<= %d, the fused form, a single-process handle and a device that can hold a cluster "
+                            "of that many such CTAs", kMaxClusterRanks);
+            cl = fits;
+        }
         const long long units = pairs * S;
         G = cl ? units : std::max<long long>(1, std::min<long long>(G, units));
-        pl->dyn.cluster = cl ? h->R : 0;
+        pl->dyn.cluster = cl ? (int)(h->R * S) : 0;
         pl->cluster = pl->dyn.cluster;
         pl->dyn.units = (int)units;
         pl->dyn.splits = (int)S;

@@ -514,12 +514,15 @@ enum {
                                  fp32 partial in its own shared memory, and after a cluster barrier every
                                  CTA sums its share of the tile over the R partials (read through
                                  distributed shared memory, rank order, the same bits as the global-memory
-                                 protocol) and stores it.  It needs the tcgen05 engine at 2 CTAs per SM,
-                                 R <= 8, no K splits, the fused form, a single-process handle and a device
-                                 that can hold a cluster of R such CTAs (else 1 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2, and
-                                 either the units fit the persistent grid in one wave (nothing would be
-                                 drawn) or they are long (K/R >= 3072, 768 KB of W per unit), when the
-                                 hardware's scheduling of whole clusters beats drawing single units */
+                                 protocol) and stores it.  With K splits (SYMM_OPT_DYN_SPLITS, honoured
+                                 when it is forced on) a cluster holds the R x splits units of a tile.  It
+                                 needs the tcgen05 engine at 2 CTAs per SM, R x splits <= 8, the fused
+                                 form, a single-process handle and a device that can hold such a cluster
+                                 (else 1 returns SYMM_EINVAL).  Auto turns it on, without K splits, when
+                                 those hold, R >= 2, and either the units fit the persistent grid in one
+                                 wave (nothing would be drawn) or they are long (K/R >= 3072, 768 KB of
+                                 W per unit), when the hardware's scheduling of whole clusters beats
+                                 drawing single units */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

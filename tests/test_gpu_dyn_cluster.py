@@ -81,6 +81,35 @@ def test_cluster_epilogue_gives_the_protocol_bits(packed, shape):
     check_gemv(W, x, got[0])
 
 
+# (R, N, K, B, splits) with R x splits <= 8: a cluster holds every rank's K splits of a tile
+SPLIT_SHAPES = [(2, 300, 2 * 1024, 3, 4), (4, 1024, 4 * 1024, 8, 2), (2, 257, 2 * 520, 16, 3), (3, 128, 3 * 384, 1, 2)]
+
+
+@pytest.mark.parametrize("packed", [False, True], ids=["rowmajor", "packed"])
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[f"R{a}N{b}K{c}B{d}S{e}" for a, b, c, d, e in SPLIT_SHAPES])
+def test_cluster_epilogue_with_k_splits_gives_the_protocol_bits(packed, shape):
+    R, N, K, B, S = shape
+    W, x = synth.gemv_inputs(R, N, K, B, seed=N + S, w_std=0.02, x="normal")
+    ref, p_off = _run(W, x, OFF, packed=packed, splits=S)
+    got, p_on = _run(W, x, ON, packed=packed, splits=S)
+    assert p_off["splits"] == S and p_on["splits"] == S and p_on["cluster"] == R * S
+    assert p_on["grid"] == p_on["tiles"] * R * S
+    for y in ref + got:
+        assert np.array_equal(y, ref[0])
+    check_gemv(W, x, got[0])
+
+
+def test_cluster_epilogue_with_k_splits_integers_bit_exact():
+    rng = np.random.default_rng(21)
+    R, N, Kr, B = 4, 300, 512, 5
+    W = f64_to_words_via_f32(rng.integers(-8, 9, size=(R, N, Kr)).astype(np.float64))
+    x = f64_to_words_via_f32(rng.integers(-8, 9, size=(R, B, Kr)).astype(np.float64))
+    (y, y2), plan = _run(W, x, ON, splits=2)
+    assert plan["cluster"] == 8
+    check_gemv(W, x, y, exact=True)
+    assert np.array_equal(y, y2)
+
+
 @pytest.mark.parametrize("slabs", [1, 2, 3])
 @pytest.mark.parametrize("chain", [0, 1])
 def test_cluster_epilogue_small_integers_bit_exact(slabs, chain):
@@ -159,7 +188,7 @@ def test_cluster_epilogue_rejections():
     try:
         s = torch.cuda.current_stream()
         for opt, val in ((csg.SYMM_OPT_SK_ENGINE, 1), (csg.SYMM_OPT_SK_CTAS_PER_SM, 1),
-                         (csg.SYMM_OPT_DYN_SPLITS, 2), (csg.SYMM_OPT_UNFUSED, 1)):
+                         (csg.SYMM_OPT_UNFUSED, 1)):
             csg.symm_set_option(ws.h, opt, val)
             with pytest.raises(csg.SymmError) as e:
                 ws.run(s)
@@ -171,6 +200,17 @@ def test_cluster_epilogue_rejections():
             with pytest.raises(csg.SymmError) as e:
                 csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, bad)
             assert e.value.code == csg.SYMM_EINVAL
+    finally:
+        ws.close()
+    # R x splits above a portable cluster
+    W, x = synth.gemv_inputs(4, 256, 4 * 768, 2, seed=2, w_std=0.02, x="normal")
+    ws = _ws(W, x, ON, splits=3)
+    try:
+        with pytest.raises(csg.SymmError) as e:
+            ws.run(torch.cuda.current_stream())
+        assert e.value.code == csg.SYMM_EINVAL
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, 2)
+        assert csg.symm_gemv_plan(ws.h, 256, 4 * 768, 2)["cluster"] == 8
     finally:
         ws.close()
     ws = GemvWorkspace(9, 64, 9 * 64, 1)

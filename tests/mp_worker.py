@@ -148,6 +148,9 @@ def leave(rk: Rank, out, survivors):
     step_barrier()
     out["first"] = rk.get_own(rk.y_off, B * N)
     out["first_status"] = np.array(csg.symm_status(rk.h, s))
+    # every rank has read its status before a survivor launches its next call
+    # (the status compares the ranks' launch counts)
+    step_barrier()
     if rk.rank == R - 1:
         return "left"   # between calls, nothing of this rank in flight
     # the others go on without it: their next call finishes (nothing waits

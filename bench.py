@@ -282,7 +282,7 @@ def kernel_name(plan):
         return "gemv_ar_ffma_kernel"
     if plan["path"] == 5:
         return "gemv_ar_cluster_kernel"
-    engine = "tcgen05" if plan["engine"] == 0 else "ffma"
+    engine = "tcgen05"
     cl = f",cluster={plan['cluster']}" if plan.get("cluster") else ""
     return f"gemv_ar_dyn_kernel<{engine},slabs={plan['slabs']},ctas_per_sm={plan['ctas_per_sm']}{cl}>"
 
@@ -938,8 +938,8 @@ def parse_args(argv=None):
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--dyn-cluster", type=int, default=-1, choices=(-1, 0, 1),
                    help="persistent kernel: cluster epilogue -1 auto, 0 off, 1 on (SYMM_OPT_DYN_CLUSTER)")
-    p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0, 1),
-                   help="TMA kernels: -1 auto, 0 tcgen05, 1 FFMA")
+    p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0),
+                   help="persistent kernel's engine: -1 auto, 0 tcgen05 (the only one)")
     p.add_argument("--ar-cps", type=int, default=0,
                    help="allreduce workload: grid cap in CTAs per SM (0 = library default)")
     p.add_argument("--copy-engine", type=int, default=0, choices=(0, 1),

@@ -1,8 +1,7 @@
 // Persistent, dynamically scheduled fused GEMV + one-shot all-reduce: one or
 // more CTAs per SM draw whole (row tile, rank) units from an atomic work
-// counter and stream them through a TMA ring into the tcgen05 tensor cores
-// (the automatic choice at every batch width) or into CUDA-core FFMA (an
-// option for B <= 2).
+// counter and stream them through a TMA ring into the tcgen05 tensor cores,
+// at every batch width.
 //
 // Why this shape: W is read exactly once, so the kernel is bound by HBM, and
 // what costs time besides bytes is (a) a CTA's start-up and wind-down, which
@@ -30,18 +29,14 @@
 //                   swizzle; W of a packed weight as kSlabs contiguous 16 KB
 //                   blocks already in that byte order) and tags every stage
 //                   with (unit, block);
-//   warp 1          tcgen05 engine: TMEM owner; lane 0 issues the MMAs of each
-//                   stage and, at a unit's last block, hands the accumulator
-//                   and the unit id to the epilogue;
-//   warps 2-5       tcgen05 engine: tcgen05.ld of the accumulator, then the
-//                   partial store and the publish / last-arriver protocol of
-//                   the tile (R * S contributors);
-//                   FFMA engine: one row per thread straight from the stage;
-//                   each unit's row sums go through a two-entry shared-memory
-//                   mailbox to warp 1, which stores, publishes and reduces
-//                   while these warps stream on.
-// Unit ids travel with the stages (producer -> MMA / FFMA consumers) and
-// through a two-entry mailbox (MMA -> epilogue) guarded by its own mbarrier.
+//   warp 1          TMEM owner; lane 0 issues the MMAs of each stage and, at a
+//                   unit's last block, hands the accumulator and the unit id
+//                   to the epilogue;
+//   warps 2-5       tcgen05.ld of the accumulator, then the partial store and
+//                   the publish / last-arriver protocol of the tile (R * S
+//                   contributors).
+// Unit ids travel with the stages (producer -> MMA) and through a two-entry
+// mailbox (MMA -> epilogue) guarded by its own mbarrier.
 // A stage tagged -1 ends the stream.
 //
 // Follows the fused GEMV + AllReduce of "Overlapping Collective Communication
@@ -170,39 +165,6 @@ __device__ __forceinline__ void unit_of(const GemvArgs &a, int u, int S, int *t,
     }
 }
 
-// The same protocol run by one warp (the FFMA engine's epilogue warp).
-__device__ __forceinline__ void publish_reduce_warp(const GemvArgs &a, uint32_t epoch, int S, int t, int r, int s,
-                                                    int lane) {
-    const uint32_t C = (uint32_t)a.R * (uint32_t)S;
-    uint32_t done = 0;   // lane 0, reducer: tiles counted before this one
-    if (lane == 0) st_relaxed_gpu_u32(flag_of(a, r, t, S, s), epoch);
-    __threadfence();
-    __syncwarp();
-    uint32_t last = 0;
-    if (lane == 0) last = take_ticket(a, t, C, r, epoch, &done) == C - 1u;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    reduce_tile(a, t, epoch, t * kM, min(kM, a.N - t * kM), (int)C,
-                [&](int j) { return contributor_partials(a, j); },
-                [](bool ok) { return __all_sync(0xffffffffu, ok) != 0; },
-                [&]() {
-                    if (lane == 0) finish_launch_if_last(a, done, epoch, t);
-                },
-                lane, 32);
-}
-
-__device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
-    acc = fmaf(bf16lo(w.x), bf16lo(x.x), acc);
-    acc = fmaf(bf16hi(w.x), bf16hi(x.x), acc);
-    acc = fmaf(bf16lo(w.y), bf16lo(x.y), acc);
-    acc = fmaf(bf16hi(w.y), bf16hi(x.y), acc);
-    acc = fmaf(bf16lo(w.z), bf16lo(x.z), acc);
-    acc = fmaf(bf16hi(w.z), bf16hi(x.z), acc);
-    acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
-    acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
-    return acc;
-}
-
 static_assert(kM == kPackRows && kSlabA == (int)kPackBlockBytes, "a stage slab is one block of the packed layout");
 
 // W slab j (64 columns) of row tile t, rank r, into one stage slab: a TMA box
@@ -306,7 +268,7 @@ __device__ __forceinline__ void cluster_sum_tile(const GemvArgs &a, const float 
 
 // At two CTAs per SM the register file must hold both (at most 168
 // registers a thread); the three-CTA rings do not fit it and run in two waves.
-template <int kEngine, int kSlabs, int kB, int kCps, bool kCl>
+template <int kSlabs, int kCps, bool kCl>
 __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     gemv_ar_dyn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemvArgs a, const DynGeom geo) {
@@ -317,8 +279,7 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
-    static_assert(!kCl || (kEngine == 0 && RingT::kStageBytes >= kNmma * kM * 4),
-                  "cluster epilogue: tcgen05 engine, partial fits in the first stage");
+    static_assert(!kCl || RingT::kStageBytes >= kNmma * kM * 4, "cluster epilogue: the partial fits in a stage");
     constexpr int kStages = RingT::kStages;
     constexpr int kStageBytes = RingT::kStageBytes;
     constexpr int kBK = 64 * kSlabs;
@@ -333,7 +294,6 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     __shared__ int stage_unit[kStages];
     __shared__ int stage_flags[kStages];   // bit 0: first block of the unit, bit 1: last
     __shared__ int acc_unit[2];
-    __shared__ float part_buf[2][kM * 2];   // FFMA engine: [buffer][b * 128 + row] partials, B <= 2
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     __shared__ int s_last;
@@ -354,27 +314,26 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kEngine == 0 ? 1 : 4);
+            mbar_init(&empty_bar[i], 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&acc_full[j], 1);
-            // tcgen05 engine: drained by the 4 epilogue warps, unit id from the
-            // MMA thread.  FFMA engine: drained by the epilogue warp (warp 1),
-            // partials handed over by the 4 compute warps.
-            mbar_init(&acc_empty[j], kEngine == 0 ? 4 : 1);
-            mbar_init(&unit_full[j], kEngine == 0 ? 1 : 4);
+            // Drained by the 4 epilogue warps; the unit id comes from the MMA
+            // thread.
+            mbar_init(&acc_empty[j], 4);
+            mbar_init(&unit_full[j], 1);
         }
         mbar_init(&drain_bar, 1);
         abort_sh = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (kEngine == 0 && warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
+    if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 1);
-    const uint32_t tmem = kEngine == 0 ? tmem_base_sh : 0u;
+    const uint32_t tmem = tmem_base_sh;
     // Launched as a programmatic dependent of the previous kernel (calls
     // chained on one stream), this grid may start while that one drains.
     // Everything below except, for a packed weight, the producer's first W
@@ -511,230 +470,124 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if constexpr (kEngine == 0) {
-            if (lane == 0) {
-                int i = 0, seg = 0;
-                bool ok = true;
-                while (true) {
-                    const int st = i % kStages;
-                    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-                    if (!mbar_wait(&full_bar[st], ph, &abort_sh)) {
+        if (lane == 0) {
+            int i = 0, seg = 0;
+            bool ok = true;
+            while (true) {
+                const int st = i % kStages;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                if (!mbar_wait(&full_bar[st], ph, &abort_sh)) {
+                    ok = false;
+                    break;
+                }
+                if (i == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 4);
+                const int u = stage_unit[st];
+                const int fl = stage_flags[st];
+                const int j = seg & 1;
+                const uint32_t use = (uint32_t)(seg >> 1);
+                if (u < 0 || (fl & 1)) {
+                    // Buffer j must have been drained (its previous unit read out).
+                    if (!mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh)) {
                         ok = false;
                         break;
                     }
-                    if (i == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 4);
-                    const int u = stage_unit[st];
-                    const int fl = stage_flags[st];
-                    const int j = seg & 1;
-                    const uint32_t use = (uint32_t)(seg >> 1);
-                    if (u < 0 || (fl & 1)) {
-                        // Buffer j must have been drained (its previous unit read out).
-                        if (!mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (u < 0) {
-                        acc_unit[j] = -1;
-                        mbar_arrive(&unit_full[j]);
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(j * kNmma);
-                    const uint32_t a_addr = smem_u32(smem + (size_t)st * kStageBytes);
-                    const uint32_t x_addr = a_addr + kSlabs * kSlabA;
+                }
+                if (u < 0) {
+                    acc_unit[j] = -1;
+                    mbar_arrive(&unit_full[j]);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(j * kNmma);
+                const uint32_t a_addr = smem_u32(smem + (size_t)st * kStageBytes);
+                const uint32_t x_addr = a_addr + kSlabs * kSlabA;
 #pragma unroll
-                    for (int s = 0; s < kSlabs; ++s)
+                for (int s = 0; s < kSlabs; ++s)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(d, smem_desc_sw128(a_addr + s * kSlabA + kk * 32),
-                                   smem_desc_sw128(x_addr + s * kSlabX + kk * 32), kIdesc,
-                                   ((fl & 1) && s == 0 && kk == 0) ? 0u : 1u);
-                    tc_commit(&empty_bar[st]);
-                    ++i;
-                    if (fl & 2) {
-                        acc_unit[j] = u;
-                        mbar_arrive(&unit_full[j]);
-                        tc_commit(&acc_full[j]);
-                        ++seg;
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma(d, smem_desc_sw128(a_addr + s * kSlabA + kk * 32),
+                               smem_desc_sw128(x_addr + s * kSlabX + kk * 32), kIdesc,
+                               ((fl & 1) && s == 0 && kk == 0) ? 0u : 1u);
+                tc_commit(&empty_bar[st]);
+                ++i;
+                if (fl & 2) {
+                    acc_unit[j] = u;
+                    mbar_arrive(&unit_full[j]);
+                    tc_commit(&acc_full[j]);
+                    ++seg;
                 }
-                if (!ok) {
-                    latch_status(a.status, kProtoTimeout, -1, -1, epoch);
-                    abort_sh = 1;
-                }
-                tc_commit(&drain_bar);
-                volatile int never = 0;
-                mbar_wait(&drain_bar, 0, &never);
-            }
-        } else {
-            // ------------------------------ FFMA engine: epilogue warp
-            // Takes each unit's partial from the compute warps, stores it,
-            // publishes it and, as the tile's last contributor, reduces the
-            // tile -- while the compute warps already stream the next unit.
-            int seg = 0;
-            bool ok = true;
-            while (true) {
-                const int j = seg & 1;
-                const uint32_t use = (uint32_t)(seg >> 1);
-                ok = __all_sync(0xffffffffu, mbar_wait_sleepy(&unit_full[j], use & 1u, &abort_sh)) != 0;
-                if (!ok) break;
-                const int u = acc_unit[j];
-                if (u < 0) break;
-                int t, r, sp;
-                unit_of(a, u, S, &t, &r, &sp);
-                float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
-                                                     (long long)sp * a.partial_stride);
-                for (int idx = lane; idx < kM * kB; idx += 32) {
-                    const int b = idx / kM;
-                    const int n = t * kM + (idx - b * kM);
-                    if (n < a.N) P[(size_t)b * a.N + n] = part_buf[j][idx];
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[j]);
-                if (a.out_mode == kOutPartials) {
-                    if (lane == 0) count_unit(a, a.tiles_done, epoch, (uint32_t)U);
-                } else {
-                    publish_reduce_warp(a, epoch, S, t, r, sp, lane);
-                    if (a.my_rank >= 0 && lane == 0) count_unit(a, a.units_done, epoch, (uint32_t)U);
-                }
-                ++seg;
             }
             if (!ok) {
                 latch_status(a.status, kProtoTimeout, -1, -1, epoch);
                 abort_sh = 1;
             }
+            tc_commit(&drain_bar);
+            volatile int never = 0;
+            mbar_wait(&drain_bar, 0, &never);
         }
     } else {
-        // ------------------------------- epilogue / FFMA consumers (warps 2-5)
+        // ---------------------------------------------- epilogue (warps 2-5)
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         const int gt = threadIdx.x - 64;
         bool ok = true;
-        if constexpr (kEngine == 0) {
-            int seg = 0;
-            int n_reduced = 0;   // timeline only
-            (void)n_reduced;
-            while (true) {
-                const int j = seg & 1;
-                const uint32_t use = (uint32_t)(seg >> 1);
-                ok = group_all(mbar_wait_sleepy(&unit_full[j], use & 1u, &abort_sh));
-                if (!ok) break;
-                const int u = acc_unit[j];
-                if (u < 0) break;
-                ok = group_all(mbar_wait_sleepy(&acc_full[j], use & 1u, &abort_sh));
-                if (!ok) break;
-                if (gt == 0) {
-                    if (seg == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 5);
-                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 6);
-                }
-                tc_fence_after();
-                float v[16];
-                tmem_ld_16(tmem + (uint32_t)(j * kNmma) + ((uint32_t)(q4 * 32) << 16), v);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[j]);
-                if constexpr (kCl) {
-                    // The partial goes to the drained ring (every MMA of the
-                    // CTA's one unit has completed, no copy is in flight);
-                    // the proxy fence orders those asynchronous accesses of
-                    // the ring before these plain stores.
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    float *part = reinterpret_cast<float *>(smem);
-#pragma unroll
-                    for (int b = 0; b < kNmma; ++b)
-                        if (b < a.B) part[b * kM + row] = v[b];
-                    ++seg;
-                    continue;
-                }
-                int t, r, sp;
-                unit_of(a, u, S, &t, &r, &sp);
-                const int n = t * kM + row;
-                if (n < a.N) {
-                    float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
-                                                         (long long)sp * a.partial_stride);
-#pragma unroll
-                    for (int b = 0; b < kNmma; ++b)
-                        if (b < a.B) P[(size_t)b * a.N + n] = v[b];
-                }
-                bool reduced = false;
-                if (a.out_mode == kOutPartials) {
-                    if (gt == 0) count_unit(a, a.tiles_done, epoch, (uint32_t)U);
-                } else {
-                    reduced = publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last);
-                    if (a.my_rank >= 0 && gt == 0) count_unit(a, a.units_done, epoch, (uint32_t)U);
-                }
-                ++seg;
-                if (gt == 0) {
-                    tl_stamp(a.tl, a.tl_ctas, blockIdx.x, reduced ? 8 : 7);
-                    if (reduced) tl_value(a.tl, a.tl_ctas, blockIdx.x, 11, (unsigned long long)++n_reduced);
-                    tl_value(a.tl, a.tl_ctas, blockIdx.x, 10, (unsigned long long)seg);
-                }
+        int seg = 0;
+        int n_reduced = 0;   // timeline only
+        (void)n_reduced;
+        while (true) {
+            const int j = seg & 1;
+            const uint32_t use = (uint32_t)(seg >> 1);
+            ok = group_all(mbar_wait_sleepy(&unit_full[j], use & 1u, &abort_sh));
+            if (!ok) break;
+            const int u = acc_unit[j];
+            if (u < 0) break;
+            ok = group_all(mbar_wait_sleepy(&acc_full[j], use & 1u, &abort_sh));
+            if (!ok) break;
+            if (gt == 0) {
+                if (seg == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 5);
+                tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 6);
             }
-        } else {
-            int i = 0, seg = 0;
-            float acc0[kB], acc1[kB];
+            tc_fence_after();
+            float v[16];
+            tmem_ld_16(tmem + (uint32_t)(j * kNmma) + ((uint32_t)(q4 * 32) << 16), v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[j]);
+            if constexpr (kCl) {
+                // The partial goes to the drained ring (every MMA of the
+                // CTA's one unit has completed, no copy is in flight);
+                // the proxy fence orders those asynchronous accesses of
+                // the ring before these plain stores.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                float *part = reinterpret_cast<float *>(smem);
 #pragma unroll
-            for (int b = 0; b < kB; ++b) acc0[b] = acc1[b] = 0.f;
-            while (true) {
-                const int st = i % kStages;
-                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-                ok = group_all(mbar_wait(&full_bar[st], ph, &abort_sh));
-                if (!ok) break;
-                const int u = stage_unit[st];
-                const int fl = stage_flags[st];
-                if (u < 0) {
-                    // End of the stream: tell the epilogue warp.
-                    const int j = seg & 1;
-                    const uint32_t use = (uint32_t)(seg >> 1);
-                    ok = group_all(mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh));
-                    if (!ok) break;
-                    if (gt == 0) acc_unit[j] = -1;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&unit_full[j]);
-                    break;
-                }
-                if (fl & 1) {
+                for (int b = 0; b < kNmma; ++b)
+                    if (b < a.B) part[b * kM + row] = v[b];
+                ++seg;
+                continue;
+            }
+            int t, r, sp;
+            unit_of(a, u, S, &t, &r, &sp);
+            const int n = t * kM + row;
+            if (n < a.N) {
+                float *P = reinterpret_cast<float *>(a.scratch + (long long)r * a.stride +
+                                                     (long long)sp * a.partial_stride);
 #pragma unroll
-                    for (int b = 0; b < kB; ++b) acc0[b] = acc1[b] = 0.f;
-                }
-                const uint8_t *A = smem + (size_t)st * kStageBytes;
-                const uint8_t *X = A + kSlabs * kSlabA;
-#pragma unroll
-                for (int s = 0; s < kSlabs; ++s)
-#pragma unroll
-                    for (int jj = 0; jj < 8; jj += 2) {
-                        const uint4 w0 = *reinterpret_cast<const uint4 *>(A + s * kSlabA + row * 128 +
-                                                                          ((jj ^ (row & 7)) << 4));
-                        const uint4 w1 = *reinterpret_cast<const uint4 *>(A + s * kSlabA + row * 128 +
-                                                                          (((jj + 1) ^ (row & 7)) << 4));
-#pragma unroll
-                        for (int b = 0; b < kB; ++b) {
-                            const uint4 x0 = *reinterpret_cast<const uint4 *>(X + s * kSlabX + b * 128 +
-                                                                              ((jj ^ (b & 7)) << 4));
-                            const uint4 x1 = *reinterpret_cast<const uint4 *>(X + s * kSlabX + b * 128 +
-                                                                              (((jj + 1) ^ (b & 7)) << 4));
-                            acc0[b] = dot8_bf16(w0, x0, acc0[b]);
-                            acc1[b] = dot8_bf16(w1, x1, acc1[b]);
-                        }
-                    }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_bar[st]);
-                ++i;
-                if (fl & 2) {
-                    // Hand the unit's partial to the epilogue warp (buffer j is
-                    // free once the unit two before it has been taken).
-                    const int j = seg & 1;
-                    const uint32_t use = (uint32_t)(seg >> 1);
-                    ok = group_all(mbar_wait(&acc_empty[j], (use & 1u) ^ 1u, &abort_sh));
-                    if (!ok) break;
-#pragma unroll
-                    for (int b = 0; b < kB; ++b) part_buf[j][b * kM + row] = acc0[b] + acc1[b];
-                    if (gt == 0) acc_unit[j] = u;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&unit_full[j]);
-                    ++seg;
-                }
+                for (int b = 0; b < kNmma; ++b)
+                    if (b < a.B) P[(size_t)b * a.N + n] = v[b];
+            }
+            bool reduced = false;
+            if (a.out_mode == kOutPartials) {
+                if (gt == 0) count_unit(a, a.tiles_done, epoch, (uint32_t)U);
+            } else {
+                reduced = publish_reduce_unit(a, epoch, S, t, r, sp, gt, &s_last);
+                if (a.my_rank >= 0 && gt == 0) count_unit(a, a.units_done, epoch, (uint32_t)U);
+            }
+            ++seg;
+            if (gt == 0) {
+                tl_stamp(a.tl, a.tl_ctas, blockIdx.x, reduced ? 8 : 7);
+                if (reduced) tl_value(a.tl, a.tl_ctas, blockIdx.x, 11, (unsigned long long)++n_reduced);
+                tl_value(a.tl, a.tl_ctas, blockIdx.x, 10, (unsigned long long)seg);
             }
         }
         if (!ok) {
@@ -766,15 +619,15 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         cluster_wait_acquire();
     }
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 9);
-    if (kEngine == 0 && warp == 1) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int kEngine, int kSlabs, int kB, int kCps, bool kCl>
+template <int kSlabs, int kCps, bool kCl>
 cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, bool chained, cudaStream_t s) {
-    auto kern = gemv_ar_dyn_kernel<kEngine, kSlabs, kB, kCps, kCl>;
+    auto kern = gemv_ar_dyn_kernel<kSlabs, kCps, kCl>;
     constexpr int smem = Ring<kSlabs, kCps>::kSmem;
     static std::atomic<unsigned long long> attr_devices{0};
     cudaError_t e = set_smem_once(kern, smem, attr_devices);
@@ -801,29 +654,25 @@ cudaError_t launch_cfg(const GemvArgs &a, const DynGeom &geo, const CUtensorMap 
     return cudaLaunchKernelEx(&cfg, kern, m[0], m[1], a, geo);
 }
 
-template <int kEngine, int kB>
-cudaError_t launch_engine(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, int slabs, int cps,
-                          bool chained, cudaStream_t s) {
+cudaError_t launch_pipeline(const GemvArgs &a, const DynGeom &geo, const CUtensorMap *m, int slabs, int cps,
+                            bool chained, cudaStream_t s) {
     if (geo.cluster) {
-        // Cluster epilogue: tcgen05 engine, rings sized for two CTAs per SM.
-        if constexpr (kEngine == 0) {
-            switch (cps * 10 + slabs) {
-                case 21: return launch_cfg<kEngine, 1, kB, 2, true>(a, geo, m, chained, s);
-                case 22: return launch_cfg<kEngine, 2, kB, 2, true>(a, geo, m, chained, s);
-                case 23: return launch_cfg<kEngine, 3, kB, 2, true>(a, geo, m, chained, s);
-                default: return cudaErrorInvalidValue;
-            }
+        // Cluster epilogue: rings sized for two CTAs per SM.
+        switch (cps * 10 + slabs) {
+            case 21: return launch_cfg<1, 2, true>(a, geo, m, chained, s);
+            case 22: return launch_cfg<2, 2, true>(a, geo, m, chained, s);
+            case 23: return launch_cfg<3, 2, true>(a, geo, m, chained, s);
+            default: return cudaErrorInvalidValue;
         }
-        return cudaErrorInvalidValue;
     }
     switch (cps * 10 + slabs) {
-        case 11: return launch_cfg<kEngine, 1, kB, 1, false>(a, geo, m, chained, s);
-        case 12: return launch_cfg<kEngine, 2, kB, 1, false>(a, geo, m, chained, s);
-        case 14: return launch_cfg<kEngine, 4, kB, 1, false>(a, geo, m, chained, s);
-        case 21: return launch_cfg<kEngine, 1, kB, 2, false>(a, geo, m, chained, s);
-        case 22: return launch_cfg<kEngine, 2, kB, 2, false>(a, geo, m, chained, s);
-        case 23: return launch_cfg<kEngine, 3, kB, 2, false>(a, geo, m, chained, s);
-        case 31: return launch_cfg<kEngine, 1, kB, 3, false>(a, geo, m, chained, s);
+        case 11: return launch_cfg<1, 1, false>(a, geo, m, chained, s);
+        case 12: return launch_cfg<2, 1, false>(a, geo, m, chained, s);
+        case 14: return launch_cfg<4, 1, false>(a, geo, m, chained, s);
+        case 21: return launch_cfg<1, 2, false>(a, geo, m, chained, s);
+        case 22: return launch_cfg<2, 2, false>(a, geo, m, chained, s);
+        case 23: return launch_cfg<3, 2, false>(a, geo, m, chained, s);
+        case 31: return launch_cfg<1, 3, false>(a, geo, m, chained, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -880,15 +729,15 @@ bool dyn_config_supported(int slabs, int cps) {
            (cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3)) || (cps == 3 && slabs == 1);
 }
 
-bool dyn_cluster_supported(int engine, int slabs, int cps) {
-    return engine == 0 && cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3);
+bool dyn_cluster_supported(int slabs, int cps) {
+    return cps == 2 && (slabs == 1 || slabs == 2 || slabs == 3);
 }
 
 namespace {
 
 template <int kSlabs>
 int max_active_clusters(int R) {
-    auto kern = gemv_ar_dyn_kernel<0, kSlabs, 0, 2, true>;
+    auto kern = gemv_ar_dyn_kernel<kSlabs, 2, true>;
     constexpr int smem = Ring<kSlabs, 2>::kSmem;
     static std::atomic<unsigned long long> attr_devices{0};
     if (set_smem_once(kern, smem, attr_devices) != cudaSuccess) return 0;
@@ -931,13 +780,9 @@ bool dyn_cluster_fits(int slabs, int R) {
     return v == 1;
 }
 
-cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs, int cps,
+cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int slabs, int cps,
                             bool chained, cudaStream_t s) {
-    const CUtensorMap *m = static_cast<const CUtensorMap *>(maps);
-    if (engine == 0) return launch_engine<0, 0>(a, geo, m, slabs, cps, chained, s);
-    if (a.B == 1) return launch_engine<1, 1>(a, geo, m, slabs, cps, chained, s);
-    if (a.B == 2) return launch_engine<1, 2>(a, geo, m, slabs, cps, chained, s);
-    return cudaErrorInvalidValue;
+    return launch_pipeline(a, geo, static_cast<const CUtensorMap *>(maps), slabs, cps, chained, s);
 }
 
 }  // namespace symm

@@ -272,10 +272,10 @@ size_t ffma_smem_bytes(int B, int kc_cap);
 int ffma_kc_cap(int B, int Kr);
 cudaError_t launch_gemv_ffma(const GemvArgs &a, cudaStream_t s);
 
-// Persistent dynamically scheduled kernel (TMA ring into tcgen05, or an FFMA
-// engine for B <= 2): 128-row tiles, batch padded to 16.  G CTAs draw the
-// U = T*R*splits units (KB K-blocks each) from the work counter
-// work[epoch & 1] (slot 0's pad).
+// Persistent dynamically scheduled kernel (TMA ring into tcgen05): 128-row
+// tiles, batch padded to 16.  G CTAs draw the U = T*R*splits units (KB
+// K-blocks each) from the work counter work[epoch & 1] (slot 0's pad), or,
+// with the cluster epilogue, one unit per CTA in clusters of R*splits.
 constexpr int kDynRows = 128;
 struct DynGeom {
     int units;      // T * R * splits
@@ -292,15 +292,15 @@ int dyn_encode_maps(const GemvArgs &a, void *maps);
 // K elements per ring stage, and the (slabs, CTAs per SM) pipelines built.
 int dyn_block_k(int slabs);
 bool dyn_config_supported(int slabs, int ctas_per_sm);
-// Pipelines the cluster epilogue is built for (tcgen05 engine, two CTAs per SM).
-bool dyn_cluster_supported(int engine, int slabs, int ctas_per_sm);
+// Pipelines the cluster epilogue is built for (two CTAs per SM).
+bool dyn_cluster_supported(int slabs, int ctas_per_sm);
 // Whether a cluster of R CTAs of that kernel can be resident on the current
 // device at all (the occupancy query, cached per device; false on a device
 // or partition whose GPCs cannot hold one).
 bool dyn_cluster_fits(int slabs, int R);
 // chained: launch as a programmatic dependent of the previous kernel on the
 // stream (its CTAs may start while that one drains; see the kernel).
-cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int engine, int slabs,
-                            int ctas_per_sm, bool chained, cudaStream_t s);
+cudaError_t launch_gemv_dyn(const GemvArgs &a, const DynGeom &geo, const void *maps, int slabs, int ctas_per_sm,
+                            bool chained, cudaStream_t s);
 
 }  // namespace symm

@@ -41,7 +41,6 @@ struct symm_handle {
     int opt_gemv_path = 0;
     int opt_tile_order = 0;
     int opt_sk_slabs = 0;
-    int opt_sk_engine = -1;
     int opt_sk_cps = 0;
     int opt_sk_grid = 0;
     int opt_dyn_splits = 0;
@@ -225,21 +224,18 @@ int num_sms(int device) {
 }
 
 // Kernels: 1 CUDA-core, one CTA per (tile, rank), 128-bit loads; 4
-// persistent CTAs drawing (tile, rank) units from a work counter (TMA ring,
-// double-buffered accumulator; the tcgen05 engine, or as an option the FFMA
-// engine for B <= kDynFfmaMaxBatch).  The automatic choice is 4 whenever
-// K > 0 (1 for K = 0, and for small W, below), with two CTAs per SM, two
-// 64-column slabs per stage and the tcgen05 engine at every batch width: the
+// persistent CTAs drawing (tile, rank) units from a work counter, or one CTA
+// per unit in clusters (TMA ring into tcgen05, double-buffered accumulator in
+// TMEM).  The automatic choice is 4 whenever K > 0 (1 for K = 0, and for
+// small W, below), with two CTAs per SM and two 64-column slabs per stage: the
 // fastest configuration measured on the decode (B = 1), attention-projection
-// (B = 8) and large (B = 16) shapes, and tcgen05 beat FFMA at B = 1 and 2 on
-// every shape measured (34 MB to 1.7 GB of W, packed or row-major).  Paths 2
-// (one tensor-core CTA per tile) and 3 (static stream-K partition) were
-// retired: neither won on any shape measured.  5 is the cluster kernel for
+// (B = 8) and large (B = 16) shapes.  Paths 2 (one tensor-core CTA per tile)
+// and 3 (static stream-K partition) were retired, and so was the persistent
+// kernel's CUDA-core engine: none of them won on any shape measured.  5 is the cluster kernel for
 // small layers: one thread-block cluster of R CTAs per row tile, the partials
 // exchanged through distributed shared memory instead of the global-memory
 // protocol (R <= 8, B <= 4).
 constexpr int kPathFfma = 1, kPathDyn = 4, kPathCluster = 5;
-constexpr int kDynFfmaMaxBatch = 2;
 // K/R from which the persistent kernel's units (128 rows x K/R bf16, 768 KB
 // here) take the cluster epilogue even when they do not fit in one wave.
 constexpr int kClusterEpilogueMinKr = 3072;
@@ -272,11 +268,6 @@ int rows_per_tile_for_path(int path, int B) {
         case kPathCluster: return kClusterRows;
         default: return 0;
     }
-}
-
-int dyn_engine(const symm_handle *h, int B) {
-    if (h->opt_sk_engine >= 0) return (h->opt_sk_engine == 1 && B > kDynFfmaMaxBatch) ? 0 : h->opt_sk_engine;
-    return 0;
 }
 
 int dyn_slabs(const symm_handle *h) { return h->opt_sk_slabs > 0 ? h->opt_sk_slabs : 2; }
@@ -337,7 +328,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
     pl->cluster = pl->path == kPathCluster ? h->R : 0;
     if (pl->path == kPathDyn) {
         if (Kr == 0) return fail(SYMM_EINVAL, "the persistent kernel needs K > 0");
-        pl->engine = dyn_engine(h, B);
+        pl->engine = 0;   // tcgen05 (the CUDA-core engine was retired)
         pl->slabs = dyn_slabs(h);
         pl->cps = dyn_cps(h);
         if (!dyn_config_supported(pl->slabs, pl->cps))
@@ -368,7 +359,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         // slower than drawn ones, 256-512 KB units about even, 0.9-2 MB units
         // 1-6 % faster.  Forced on, it takes the requested K splits (none by
         // default).
-        const bool cl_base = dyn_cluster_supported(pl->engine, pl->slabs, pl->cps) && h->mp_rank < 0 &&
+        const bool cl_base = dyn_cluster_supported(pl->slabs, pl->cps) && h->mp_rank < 0 &&
                              !h->opt_unfused;
         bool cl = false;
         if (h->opt_dyn_cluster == 1) {
@@ -386,7 +377,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
             const bool fits = cl_base && C <= kMaxClusterRanks && dyn_cluster_fits(pl->slabs, (int)C);
             if (!fits && h->opt_dyn_cluster == 1)
                 return fail(SYMM_EINVAL,
-                            "the cluster epilogue needs the tcgen05 engine at 2 CTAs per SM (1-3 slabs), R x splits "
+                            "the cluster epilogue needs 2 CTAs per SM (1-3 slabs), R x splits "
                             "<= %d, the fused form, a single-process handle and a device that can hold a cluster "
                             "of that many such CTAs", kMaxClusterRanks);
             cl = fits;
@@ -570,7 +561,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
     Plan pl;
     int rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
     if (rc != SYMM_OK) return rc;
-    const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits, engine = pl.engine,
+    const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits,
               slabs = pl.slabs, cps = pl.cps;
     const DynGeom dyn = pl.dyn;
     rc = check_device(h);
@@ -637,7 +628,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             const void *maps = tc_maps_for(h, a, &err);
             if (!maps) return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
             const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_write, h->last_write_bytes);
-            e = launch_gemv_dyn(a, dyn, maps, engine, slabs, cps, chained, s);
+            e = launch_gemv_dyn(a, dyn, maps, slabs, cps, chained, s);
             break;
         }
         default:
@@ -914,9 +905,10 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
             h->opt_sk_slabs = value;
             return SYMM_OK;
         case SYMM_OPT_SK_ENGINE:
-            if (value < -1 || value > 1) return fail(SYMM_EINVAL, "persistent-kernel engine %d not in {-1 auto, 0, 1}", value);
-            h->opt_sk_engine = value;
-            return SYMM_OK;
+            if (value == 1)
+                return fail(SYMM_EINVAL, "the persistent kernel's CUDA-core engine (1) was retired; -1 auto or 0 tcgen05");
+            if (value < -1 || value > 0) return fail(SYMM_EINVAL, "persistent-kernel engine %d not in {-1 auto, 0}", value);
+            return SYMM_OK;   // tcgen05, the only engine
         case SYMM_OPT_SK_GRID:
             if (value < 0) return fail(SYMM_EINVAL, "persistent grid %d: 0 auto or a CTA count > 0", value);
             h->opt_sk_grid = value;

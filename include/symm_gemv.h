@@ -468,8 +468,8 @@ enum {
     SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
     SYMM_OPT_SK_SLABS = 3,    /* path 4: 64-column slabs per pipeline stage, 0 auto (2), 1..4 (the
                                  instantiated pipelines: 1, 2, 4 slabs at 1 CTA per SM; 1, 2, 3 at 2; 1 at 3) */
-    SYMM_OPT_SK_ENGINE = 4,   /* path 4: -1 auto (tcgen05), 0 tcgen05, 1 FFMA (B <= 2; wider batches run
-                                 tcgen05) */
+    SYMM_OPT_SK_ENGINE = 4,   /* path 4: -1 auto or 0, both the tcgen05 engine; 1 (a CUDA-core engine) was
+                                 retired, having won on no shape measured, and returns SYMM_EINVAL */
     SYMM_OPT_SK_CTAS_PER_SM = 5, /* path 4: CTAs per SM the ring is sized for, 0 auto (2), 1..3 (the ring
                                  shrinks).  By its registers the kernel holds fewer CTAs per SM than 3:
                                  at 3 the grid runs in two waves, correctly but slower */
@@ -516,7 +516,7 @@ enum {
                                  distributed shared memory, rank order, the same bits as the global-memory
                                  protocol) and stores it.  With K splits (SYMM_OPT_DYN_SPLITS, honoured
                                  when it is forced on) a cluster holds the R x splits units of a tile.  It
-                                 needs the tcgen05 engine at 2 CTAs per SM, R x splits <= 8, the fused
+                                 needs 2 CTAs per SM, R x splits <= 8, the fused
                                  form, a single-process handle and a device that can hold such a cluster
                                  (else 1 returns SYMM_EINVAL).  Auto turns it on, without K splits, when
                                  those hold, R >= 2, and either the units fit the persistent grid in one
@@ -542,7 +542,7 @@ int symm_info(symm_handle_t *h, symm_info_t *info);
  * weight (symm_pack_w) runs path 4 with the plan reported while
  * SYMM_OPT_GEMV_PATH is 4.
  *   path           1 CUDA-core per tile, 4 persistent dynamic, 5 cluster per tile
- *   engine         path 4 compute engine: 0 tcgen05, 1 FFMA
+ *   engine         path 4 compute engine: 0 (tcgen05)
  *   slabs          path 4: 64-column slabs per pipeline stage
  *   rows_per_tile  output rows per tile; tiles = ceil(N / rows_per_tile)
  *   splits         K-splits per rank (path 4)

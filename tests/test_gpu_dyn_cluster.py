@@ -149,9 +149,8 @@ def test_cluster_epilogue_automatic_choice():
     """attn_out_proj (64 tiles x 4 ranks = 256 units) fits the persistent
     grid in one wave and takes the cluster epilogue, and so do layers of any
     unit count whose units are long (K/R >= 3072: the decode, the large
-    layer); layers of many short units, the FFMA engine, one CTA per SM, K
-    splits, the unfused form and a single rank keep the global-memory
-    protocol."""
+    layer); layers of many short units, one CTA per SM, K splits, the
+    unfused form and a single rank keep the global-memory protocol."""
     ws = GemvWorkspace(4, 4 * 8192, 4 * 64, 8)    # scratch and pad for up to 256 row tiles at B = 8
     try:
         h = ws.h
@@ -164,9 +163,6 @@ def test_cluster_epilogue_automatic_choice():
         assert csg.symm_gemv_plan(h, 4 * 8192, 8192, 8)["cluster"] == 0     # 1024 units of K/R = 2048
         long_units = csg.symm_gemv_plan(h, 4 * 8192, 4 * 3072, 8)            # 1024 units of K/R = 3072
         assert long_units["cluster"] == 4 and long_units["grid"] == 1024
-        csg.symm_set_option(h, csg.SYMM_OPT_SK_ENGINE, 1)
-        assert csg.symm_gemv_plan(h, 8192, 8192, 2)["cluster"] == 0
-        csg.symm_set_option(h, csg.SYMM_OPT_SK_ENGINE, -1)
         csg.symm_set_option(h, csg.SYMM_OPT_SK_CTAS_PER_SM, 1)
         assert csg.symm_gemv_plan(h, 8192, 8192, 8)["cluster"] == 0
         csg.symm_set_option(h, csg.SYMM_OPT_SK_CTAS_PER_SM, 0)
@@ -187,13 +183,12 @@ def test_cluster_epilogue_rejections():
     ws = _ws(W, x, ON)
     try:
         s = torch.cuda.current_stream()
-        for opt, val in ((csg.SYMM_OPT_SK_ENGINE, 1), (csg.SYMM_OPT_SK_CTAS_PER_SM, 1),
-                         (csg.SYMM_OPT_UNFUSED, 1)):
+        for opt, val in ((csg.SYMM_OPT_SK_CTAS_PER_SM, 1), (csg.SYMM_OPT_UNFUSED, 1)):
             csg.symm_set_option(ws.h, opt, val)
             with pytest.raises(csg.SymmError) as e:
                 ws.run(s)
             assert e.value.code == csg.SYMM_EINVAL
-            csg.symm_set_option(ws.h, opt, {csg.SYMM_OPT_SK_ENGINE: -1}.get(opt, 0))
+            csg.symm_set_option(ws.h, opt, 0)
         ws.run(s)
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
         for bad in (-2, 2):

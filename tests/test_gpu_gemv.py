@@ -207,6 +207,22 @@ def test_bad_arguments_are_rejected_without_launch():
         ws.close()
 
 
+def test_retired_kernels_and_engine_are_refused():
+    """Paths 2 and 3 and the persistent kernel's CUDA-core engine were
+    retired (none won on any shape measured): asking for them is an error,
+    not a silent substitute."""
+    ws = GemvWorkspace(2, 64, 128, 1)
+    try:
+        for opt, val in ((csg.SYMM_OPT_GEMV_PATH, 2), (csg.SYMM_OPT_GEMV_PATH, 3), (csg.SYMM_OPT_SK_ENGINE, 1)):
+            with pytest.raises(csg.SymmError) as e:
+                csg.symm_set_option(ws.h, opt, val)
+            assert e.value.code == csg.SYMM_EINVAL and "retired" in str(e.value)
+        for val in (-1, 0):
+            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, val)
+    finally:
+        ws.close()
+
+
 def test_capacity_errors():
     # scratch too small for B*N fp32 partials
     h = csg.symm_alloc(2, 1 << 20, 256, 4096)
@@ -335,17 +351,16 @@ def test_many_launches_leave_the_pad_consistent(path):
 # ------------------------------------------- persistent-kernel variants
 
 SK_PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (3, 2), (1, 3)]   # (slabs, CTAs per SM)
-SK_VARIANTS = [(engine, slabs, cps) for engine in (0, 1) for slabs, cps in SK_PIPES]
+SK_VARIANTS = [(slabs, cps) for slabs, cps in SK_PIPES]
 SK_SHAPES = [(8, 300, 8 * 264, 2), (4, 1000, 4 * 2056, 2), (2, 17, 2 * 8, 1), (3, 513, 3 * 4096, 2),
              (8, 2048, 8 * 512, 1)]
 
 
 @pytest.mark.parametrize("path", [csg.GEMV_PATH_DYN], ids=["persistent"])
-@pytest.mark.parametrize("engine,slabs,cps", SK_VARIANTS,
-                         ids=[f"eng{e}-slabs{s}-cps{c}" for e, s, c in SK_VARIANTS])
+@pytest.mark.parametrize("slabs,cps", SK_VARIANTS, ids=[f"slabs{s}-cps{c}" for s, c in SK_VARIANTS])
 @pytest.mark.parametrize("shape", SK_SHAPES, ids=[f"R{a}N{b}K{c}B{d}" for a, b, c, d in SK_SHAPES])
-def test_tma_kernels_engines_and_pipelines(path, engine, slabs, cps, shape):
-    """The persistent TMA kernel, both engines, every pipeline shape: integer inputs bit-exact, normal inputs within tolerance,
+def test_tma_kernels_pipelines(path, slabs, cps, shape):
+    """The persistent TMA kernel, every pipeline shape: integer inputs bit-exact, normal inputs within tolerance,
     replicas identical, reversed CTA / unit order identical."""
     R, N, K, B = shape
     for kind in ("int", "normal"):
@@ -356,11 +371,10 @@ def test_tma_kernels_engines_and_pipelines(path, engine, slabs, cps, shape):
         ws = GemvWorkspace(R, N, K, B)
         try:
             csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
-            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
             csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_SLABS, slabs)
             csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_CTAS_PER_SM, cps)
             plan = csg.symm_gemv_plan(ws.h, N, K, B)
-            assert plan["path"] == path and plan["engine"] == engine and plan["slabs"] == slabs
+            assert plan["path"] == path and plan["engine"] == 0 and plan["slabs"] == slabs
             assert plan["ctas_per_sm"] == cps
             ws.load_W(W)
             ws.load_x(x)
@@ -380,11 +394,10 @@ def test_tma_kernels_engines_and_pipelines(path, engine, slabs, cps, shape):
         check_gemv(W, x, y0, exact=(kind == "int"))
 
 
-@pytest.mark.parametrize("engine", [0, 1])
 @pytest.mark.parametrize("splits", [2, 3, 5])
 @pytest.mark.parametrize("shape", [(8, 300, 8 * 1032, 2), (4, 513, 4 * 4096, 1), (2, 130, 2 * 520, 2)],
                          ids=["R8N300", "R4N513", "R2N130"])
-def test_persistent_kernel_k_splits(engine, splits, shape):
+def test_persistent_kernel_k_splits(splits, shape):
     """The persistent kernel with every (tile, rank) cut into K splits: more,
     smaller units for the work counter; integer inputs stay bit-exact."""
     R, N, K, B = shape
@@ -394,7 +407,6 @@ def test_persistent_kernel_k_splits(engine, splits, shape):
         ws = GemvWorkspace(R, N, K, B)
         try:
             csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
-            csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
             csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, splits)
             plan = csg.symm_gemv_plan(ws.h, N, K, B)
             assert plan["splits"] > 1

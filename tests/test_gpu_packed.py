@@ -98,19 +98,18 @@ PIPES = [(1, 1), (2, 1), (4, 1), (1, 2), (2, 2), (3, 2), (1, 3)]   # (slabs, CTA
 SHAPES = [(8, 300, 264, 2), (4, 1000, 2056, 3), (2, 17, 8, 1), (3, 513, 4096, 16), (2, 129, 72, 8)]
 
 
-# the FFMA engine serves B <= 2 only
-VARIANTS = [(e, s, c, sh) for e in (0, 1) for s, c in PIPES for sh in SHAPES if e == 0 or sh[3] <= 2]
+VARIANTS = [(s, c, sh) for s, c in PIPES for sh in SHAPES]
 
 
-@pytest.mark.parametrize("engine,slabs,cps,shape", VARIANTS,
-                         ids=[f"eng{e}-slabs{s}-cps{c}-R{a}N{b}Kr{k}B{d}" for e, s, c, (a, b, k, d) in VARIANTS])
-def test_packed_equals_row_major_on_every_pipeline(engine, slabs, cps, shape):
-    """Both engines, every ring shape, ragged rows and columns (K/R not a
+@pytest.mark.parametrize("slabs,cps,shape", VARIANTS,
+                         ids=[f"slabs{s}-cps{c}-R{a}N{b}Kr{k}B{d}" for s, c, (a, b, k, d) in VARIANTS])
+def test_packed_equals_row_major_on_every_pipeline(slabs, cps, shape):
+    """Every ring shape, ragged rows and columns (K/R not a
     multiple of a stage): packed == row-major bitwise; the integer case
     equals the oracle."""
     R, N, Kr, B = shape
-    opts = ((csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN), (csg.SYMM_OPT_SK_ENGINE, engine),
-            (csg.SYMM_OPT_SK_SLABS, slabs), (csg.SYMM_OPT_SK_CTAS_PER_SM, cps))
+    opts = ((csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN), (csg.SYMM_OPT_SK_SLABS, slabs),
+            (csg.SYMM_OPT_SK_CTAS_PER_SM, cps))
     for kind in ("int", "normal"):
         if kind == "int":
             W, x = _int_case(R, N, Kr, B, seed=N + slabs)
@@ -123,14 +122,12 @@ def test_packed_equals_row_major_on_every_pipeline(engine, slabs, cps, shape):
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5])
-@pytest.mark.parametrize("engine", [0, 1])
-def test_packed_with_k_splits_and_reversed_order(splits, engine):
+def test_packed_with_k_splits_and_reversed_order(splits):
     """K splits (more, smaller units) and reversed unit order on packed
     weights; the row-major call runs the same kernel and plan."""
     R, N, Kr, B = 4, 513, 1032, 2
     W, x = synth.gemv_inputs(R, N, R * Kr, B, 40 + splits, 0.02, "normal")
-    opts = ((csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN), (csg.SYMM_OPT_SK_ENGINE, engine),
-            (csg.SYMM_OPT_DYN_SPLITS, splits))
+    opts = ((csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN), (csg.SYMM_OPT_DYN_SPLITS, splits))
     y_pk = _run(W, x, True, opts)
     assert np.array_equal(y_pk, _run(W, x, True, opts, order=1))
     assert np.array_equal(y_pk, _run(W, x, False, opts))

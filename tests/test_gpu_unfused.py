@@ -1,8 +1,8 @@
 """The unfused form of the fused layer (SYMM_OPT_UNFUSED): the persistent
 GEMV storing every rank's fp32 partials, then a separate all-reduce kernel
 over them.  It exists to measure what fusion buys, so it must compute exactly
-what the fused call computes: the same bits, on every shape, engine, split
-count and weight layout, and the oracle's words on small-integer inputs."""
+what the fused call computes: the same bits, on every shape, split count and
+weight layout, and the oracle's words on small-integer inputs."""
 from __future__ import annotations
 
 import numpy as np
@@ -23,13 +23,12 @@ def _gpu():
     require_gpu()
 
 
-def _run(W, x, unfused, engine=-1, splits=0, packed=False, chain=1, repeat=2):
+def _run(W, x, unfused, splits=0, packed=False, chain=1, repeat=2):
     R, N, Kr = W.shape
     B = x.shape[1]
     ws = GemvWorkspace(R, N, R * Kr, B, packed=packed)
     try:
         csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
-        csg.symm_set_option(ws.h, csg.SYMM_OPT_SK_ENGINE, engine)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, splits)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, chain)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, int(unfused))
@@ -52,15 +51,14 @@ SHAPES = [(8, 1000, 8 * 512, 1), (4, 8192 // 8, 4 * 1024, 8), (2, 130, 2 * 520, 
           (3, 257, 3 * 136, 2)]
 
 
-@pytest.mark.parametrize("engine", [0, 1])
 @pytest.mark.parametrize("splits", [0, 3])
 @pytest.mark.parametrize("packed", [False, True], ids=["rowmajor", "packed"])
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"R{a}N{b}K{c}B{d}" for a, b, c, d in SHAPES])
-def test_unfused_gives_the_fused_bits(engine, splits, packed, shape):
+def test_unfused_gives_the_fused_bits(splits, packed, shape):
     R, N, K, B = shape
     W, x = synth.gemv_inputs(R, N, K, B, seed=N + B + splits, w_std=0.02, x="normal")
-    fused = _run(W, x, False, engine, splits, packed)
-    unfused = _run(W, x, True, engine, splits, packed)
+    fused = _run(W, x, False, splits, packed)
+    unfused = _run(W, x, True, splits, packed)
     for y in fused + unfused:
         assert np.array_equal(y, fused[0])
     check_gemv(W, x, unfused[0])

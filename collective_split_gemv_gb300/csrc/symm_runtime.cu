@@ -195,7 +195,17 @@ const symm_handle::PackedW *find_packed(const symm_handle *h, const void *p) {
 // tile counters every rank shares).
 int reset_protocol(symm_handle *h, cudaStream_t s) {
     const int own = h->mp_rank >= 0 ? h->mp_rank : 0;
-    cudaError_t e0 = cudaMemsetAsync(slot(h, own) + h->pad_off + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
+    uint8_t *pad = slot(h, own) + h->pad_off;
+    cudaError_t e0;
+    if (h->mp_rank >= 0) {
+        // A process keeps its launch count (the epoch word): the other ranks
+        // compare theirs with it, and each process resets on its own.
+        e0 = cudaMemsetAsync(pad + kPadWorkOffset, 0, kPadEpochOffset - kPadWorkOffset, s);
+        if (e0 == cudaSuccess)
+            e0 = cudaMemsetAsync(pad + kPadEpochOffset + 4, 0, kPadStatusBytes - kPadEpochOffset - 4, s);
+    } else {
+        e0 = cudaMemsetAsync(pad + kPadWorkOffset, 0, kPadStatusBytes - kPadWorkOffset, s);
+    }
     if (e0 != cudaSuccess) return cuda_fail(e0, "cudaMemsetAsync(work counter)");
     for (int r = 0; r < h->R; ++r) {
         if (h->mp_rank >= 0 && r != h->mp_rank) continue;

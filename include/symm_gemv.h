@@ -176,8 +176,9 @@ int symm_alloc(int R, size_t slot_bytes, size_t scratch_bytes, size_t signal_pad
  * compares the ranks' launch counts (every rank's epoch word) besides its own
  * status words, where its kernels latch stale flags and tickets out of range
  * found in later calls.  It resets its own slot's status words and pad (rank
- * 0's holds the shared tile counters), so after an error every rank calls
- * it, after a barrier.
+ * 0's holds the shared tile counters) but keeps the process's launch count,
+ * so the ranks' counts stay comparable whatever order they reset in; after an
+ * error every rank calls it, after a barrier.
  * symm_check_guards checks the own slot.  No counterpart on the pages beyond
  * the symmetric-memory semantics above.
  */
@@ -257,7 +258,8 @@ int gemv_all_reduce(symm_handle_t *h, const void *W_r, const void *x_r, void *y,
  *         the handle overlapped on different streams).
  *   rank, tile  out: where it was detected (-1 if none).
  * After an error the signal pad's flags, counters and launch epoch are reset
- * so the handle is usable again.  Returns SYMM_OK if the status could be read (whatever
+ * so the handle is usable again (a multi-process handle keeps the epoch, its
+ * launch count).  Returns SYMM_OK if the status could be read (whatever
  * `code` says), SYMM_ECUDA otherwise.
  */
 int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, int *tile);

@@ -80,7 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_cluster_kernel(const Gemv
     const int t = blockIdx.y;
     const int R = a.R;
     const int tl_cta = t * R + r;
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 0);
+    if (threadIdx.x == 0) {
+        tl_begin();
+        tl_stamp(a.tl, a.tl_ctas, tl_cta, 0);
+    }
     // Chained calls: let the next kernel be scheduled early; wait for the one
     // before (which may have written W, x or y) before touching memory.
     chain_entry();
@@ -180,7 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_cluster_kernel(const Gemv
     if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 3);
     // No CTA leaves while a peer may still read its shared memory.
     cluster_wait_acquire();
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 4);
+    if (threadIdx.x == 0) {
+        tl_stamp(a.tl, a.tl_ctas, tl_cta, 4);
+        tl_end(a.tl, a.tl_ctas, tl_cta);
+    }
 }
 
 template <int B>

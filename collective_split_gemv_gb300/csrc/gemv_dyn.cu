@@ -276,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
     // when calls are chained) may be scheduled as CTAs of this one retire;
     // they wait for this grid before touching anything it writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
+    if (threadIdx.x == 0) {
+        tl_begin();
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
+    }
     using RingT = Ring<kSlabs, kCps>;
     static_assert(RingT::kStages >= 2, "the ring needs at least two stages");
     static_assert(!kCl || RingT::kStageBytes >= kNmma * kM * 4, "cluster epilogue: the partial fits in a stage");
@@ -618,7 +621,11 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
         if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 15);
         cluster_wait_acquire();
     }
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 9);
+    if (threadIdx.x == 0) {
+        // (every other thread's stamps came before the barrier above)
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 9);
+        tl_end(a.tl, a.tl_ctas, blockIdx.x);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -57,7 +57,10 @@ __device__ __forceinline__ float dot8(const uint4 &w, const float4 &lo, const fl
 
 template <int B>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ar_ffma_kernel(const GemvArgs a) {
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
+    if (threadIdx.x == 0) {
+        tl_begin();
+        tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 0);
+    }
     chain_entry();
     // Thread 0 publishes; its read of the launch epoch overlaps the streaming.
     const uint32_t epoch = threadIdx.x == 0 ? read_launch_epoch(a) : 0u;
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ar_ffma_kernel(const GemvArg
             if (rowok[g] && lane == ((g * B + b) & 31)) P[(size_t)b * a.N + row0 + g] = acc[g][b];
 
     publish_and_reduce(a, epoch, t, r, 0);
+    if (threadIdx.x == 0) tl_end(a.tl, a.tl_ctas, blockIdx.x);
 }
 
 template <int B>

@@ -83,7 +83,10 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(csize));
     const int row = blockIdx.y;
     const int tl_cta = (int)(blockIdx.y * gridDim.x + blockIdx.x);
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 0);
+    if (threadIdx.x == 0) {
+        tl_begin();
+        tl_stamp(a.tl, a.tl_ctas, tl_cta, 0);
+    }
     const int H8 = a.H / 8;
     const int v0 = (int)crank * chunk;
     const int v1 = min(H8, v0 + chunk);
@@ -195,7 +198,10 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_rows_kernel(const RmsNormArg
             for (int q = 0; q < a.R; ++q) st_v4(dst + (long long)q * a.stride, o);
         }
     }
-    if (threadIdx.x == 0) tl_stamp(a.tl, a.tl_ctas, tl_cta, 6);
+    if (threadIdx.x == 0) {
+        tl_stamp(a.tl, a.tl_ctas, tl_cta, 6);
+        tl_end(a.tl, a.tl_ctas, tl_cta);
+    }
 }
 
 template <int kSrc, int kV>

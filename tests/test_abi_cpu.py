@@ -130,3 +130,13 @@ def test_alloc_without_gpu_reports_cuda_error(lib):
 def test_library_is_sm103a_only():
     assert any("compute_103a,code=sm_103a" in f for f in _build.NVCC_FLAGS)
     assert not any("sm_90" in f or "sm_100" in f for f in _build.NVCC_FLAGS)
+
+
+def test_timeline_variant_builds_with_the_same_boundary():
+    """The timeline build (per-CTA phase stamps, -DSYMM_TIMELINE) compiles and
+    exports every entry point the product library does."""
+    import ctypes
+
+    tl = ctypes.CDLL(_build.build(variant="timeline"))
+    for name in _declared_functions():
+        assert hasattr(tl, name), name

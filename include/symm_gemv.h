@@ -467,7 +467,8 @@ enum {
                                  signal pad).  2 and 3 (a tensor-core kernel per tile and a static
                                  stream-K partition) were retired: neither won on any shape measured;
                                  they return SYMM_EINVAL */
-    SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence) */
+    SYMM_OPT_TILE_ORDER = 2,  /* 0 natural CTA order, 1 reversed (tests arrival-order independence; the
+                                 cluster epilogue, which has no arrival order, ignores it) */
     SYMM_OPT_SK_SLABS = 3,    /* path 4: 64-column slabs per pipeline stage, 0 auto (2), 1..4 (the
                                  instantiated pipelines: 1, 2, 4 slabs at 1 CTA per SM; 1, 2, 3 at 2; 1 at 3) */
     SYMM_OPT_SK_ENGINE = 4,   /* path 4: -1 auto or 0, both the tcgen05 engine; 1 (a CUDA-core engine) was

@@ -20,15 +20,18 @@ def require_gpu():
     csg.lib()
 
 
-def run_gemv(W, x, path=csg.GEMV_PATH_AUTO, order=0, repeat=1, y_fill=0xFF):
+def run_gemv(W, x, path=csg.GEMV_PATH_AUTO, order=0, repeat=1, y_fill=0xFF, options=()):
     """Run the fused kernel `repeat` times; returns (list of y (R, B, N) words,
-    workspace status triple of the last run)."""
+    workspace status triple of the last run).  `options`: further
+    (option, value) pairs set on the handle."""
     R, N, Kr = W.shape
     B = x.shape[1]
     ws = GemvWorkspace(R, N, R * Kr, B)
     try:
         csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, path)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_TILE_ORDER, order)
+        for opt, val in options:
+            csg.symm_set_option(ws.h, opt, val)
         ws.load_W(W)
         ws.load_x(x)
         stream = torch.cuda.current_stream()

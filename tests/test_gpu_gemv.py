@@ -148,7 +148,9 @@ def test_rank_counts_and_shapes(R, N, Kr, B):
 @pytest.mark.parametrize("name", ["tiny", "attn_out_proj", "mlp_down_decode", "mlp_down_large"])
 def test_full_size_workload(name):
     """The benchmark's workloads at full size, every output against the fp64
-    oracle; second run and reversed CTA order bit-identical."""
+    oracle; second run and reversed CTA order bit-identical, and so is the
+    persistent kernel's other ending (drawn units with the global-memory
+    protocol where the plan takes the cluster epilogue), in reversed order."""
     W, x = synth.workload_inputs(name)
     y_ref, y_or = oracle.gemv_all_reduce(W, x)
     outs, status = run_gemv(W, x, repeat=2)
@@ -171,6 +173,9 @@ def test_full_size_workload(name):
     assert eq >= 0.99 and ulp_big <= 1
     (y_rev,), _ = run_gemv(W, x, order=1)
     assert np.array_equal(y_rev, outs[0])
+    (y_drawn,), st = run_gemv(W, x, order=1, options=((csg.SYMM_OPT_DYN_CLUSTER, 0),))
+    assert st[0] == csg.SYMM_OK
+    assert np.array_equal(y_drawn, outs[0])
 
 
 # --------------------------------------------------------------- arguments

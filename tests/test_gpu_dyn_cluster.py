@@ -295,3 +295,27 @@ def test_cluster_epilogue_attn_out_proj_full_size():
     ref, _ = _run(W, x, OFF, packed=True, repeat=1, splits=1)
     assert np.array_equal(got[0], ref[0])
     check_gemv(W, x, got[0])
+
+
+def test_long_chain_of_cluster_launches():
+    """Hundreds of chained cluster-epilogue calls (each a programmatic
+    dependent of the one before, every CTA a cluster member), alternating two
+    activations: the last result is the oracle's for the last inputs and the
+    status stays clean."""
+    R, N, K, B = 8, 2048, 8 * 3072, 1          # long units: the automatic plan takes clusters
+    W, x0 = synth.gemv_inputs(R, N, K, B, seed=31, w_std=0.02, x="normal")
+    _, x1 = synth.gemv_inputs(R, N, K, B, seed=32, w_std=0.02, x="normal")
+    ws = GemvWorkspace(R, N, K, B, copies=1, packed=True)
+    try:
+        plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        assert plan["path"] == csg.GEMV_PATH_DYN and plan["cluster"] == R
+        ws.load_W(W)
+        s = torch.cuda.current_stream()
+        for i in range(400):
+            if i % 100 == 0:
+                ws.load_x(x0 if (i // 100) % 2 == 0 else x1)   # stream-ordered rewrite of x between runs of calls
+            ws.run(s)
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        check_gemv(W, x1, ws.read_y())
+    finally:
+        ws.close()

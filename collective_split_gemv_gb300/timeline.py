@@ -52,6 +52,9 @@ PHASES = {
                             3: "row loaded, squares summed", 4: "first cluster barrier passed",
                             5: "second cluster barrier passed", 6: "stores issued"},
 }
+# The slot that marks a CTA's first data (for the chained view).
+FIRST_DATA = {"gemv_ar_dyn_kernel": 4, "gemv_ar_ffma_kernel": 1, "gemv_ar_cluster_kernel": 1,
+              "rmsnorm_rows_kernel": 3}
 COUNTS = {"gemv_ar_ffma_kernel": {8: "tiles reduced"},
           "gemv_ar_dyn_kernel": {10: "units computed", 11: "tile reductions"}}
 
@@ -67,6 +70,9 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--w-layout", choices=("packed", "row_major"), default="packed")
+    p.add_argument("--chain", type=int, default=0,
+                   help="also time this many calls chained back to back (SYMM_OPT_CHAIN 1), one timeline "
+                        "buffer each, and report how consecutive launches overlap")
     p.add_argument("--opt", action="append", default=[],
                    help="handle option NAME=VALUE (e.g. SYMM_OPT_GEMV_PATH=1), repeatable")
     args = p.parse_args(argv)
@@ -186,6 +192,31 @@ def main(argv=None):
             for s in counts:
                 col = t[:, s]
                 counts[s].append((int(col.min()), float(np.mean(col)), int(col.max()), int(col.sum())))
+    chain_rows = []
+    if args.chain > 1:
+        # Calls chained back to back (each a programmatic dependent of the
+        # one before), one buffer per call; the stamps share one clock.
+        bufs = [torch.zeros(ctas * slots, dtype=torch.int64, device=dev) for _ in range(args.chain)]
+        first_data = FIRST_DATA.get(kernel, 1)
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 1)
+        with torch.cuda.stream(stream):
+            for rep_i in range(3):
+                for b in bufs:
+                    b.zero_()
+                prelude(rep_i)
+                for k, b in enumerate(bufs):
+                    csg.symm_set_timeline(ws.h, b.data_ptr(), b.numel() * 8)
+                    run(k)
+                stream.synchronize()
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 0)
+        ts = [b.view(ctas, slots).cpu().numpy().astype(np.int64) for b in bufs]
+        t0 = int(ts[0][:, 0][ts[0][:, 0] > 0].min())
+        for k, t in enumerate(ts):
+            entry = t[:, 0][t[:, 0] > 0]
+            data = t[:, first_data][t[:, first_data] > 10**12]
+            last = int(t[t > 10**12].max())
+            chain_rows.append(((int(entry.min()) - t0) / 1e3, (float(np.median(data)) - t0) / 1e3 if data.size else
+                               float("nan"), (int(entry.max()) - t0) / 1e3, (last - t0) / 1e3))
     code, _, _ = csg.symm_status(ws.h, stream)
     if code != csg.SYMM_OK:
         raise SystemExit(f"protocol error: {csg.symm_last_error()}")
@@ -218,6 +249,18 @@ def main(argv=None):
         if v:
             print(f"\n- {name} per CTA: min {v[-1][0]}, mean {v[-1][1]:.2f}, max {v[-1][2]}, total {v[-1][3]}")
     print("\n(times: after the first CTA's entry, median over the launches of each CTA statistic)")
+    if chain_rows:
+        print(f"\n## {len(chain_rows)} calls chained back to back (the last of 3 repetitions)\n")
+        print("Times after the first call's first CTA entry, µs; 'first data' is the median CTA's "
+              f"'{phases.get(FIRST_DATA.get(kernel, 1), 'phase 1')}'.\n")
+        print("| call | first CTA entry | first data (median CTA) | last CTA entry | last stamp | "
+              "entry after the previous call's last stamp |")
+        print("|---|---|---|---|---|---|")
+        for k, (e0, fd, e1, end) in enumerate(chain_rows):
+            gap = "" if k == 0 else f"{e0 - chain_rows[k - 1][3]:.2f}"
+            print(f"| {k} | {e0:.2f} | {fd:.2f} | {e1:.2f} | {end:.2f} | {gap} |")
+        per_call = (chain_rows[-1][3] - chain_rows[0][3]) / (len(chain_rows) - 1)
+        print(f"\nLast stamp to last stamp: {per_call:.2f} µs per call.")
 
 
 if __name__ == "__main__":

@@ -1325,7 +1325,9 @@ int symm_status(symm_handle_t *h, symm_stream_t stream, int *code, int *rank, in
         else
             snprintf(g_err, sizeof g_err, "rank %d has made %u fused calls, this rank (%d) %u", lag, lag_epoch, own,
                      own_epoch);
-        e = cudaMemsetAsync(pad_word(h, own, 0), 0, kPadStatusBytes, s);
+        // the four status words only: reset_protocol clears the counters and
+        // keeps a multi-process rank's launch count, which the others compare
+        e = cudaMemsetAsync(pad_word(h, own, 0), 0, 4 * sizeof(uint32_t), s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
         int rc = reset_protocol(h, s);
         if (rc != SYMM_OK) return rc;

@@ -50,7 +50,7 @@ def _run(scenario, world, tmp_path, timeout=300):
     return [dict(np.load(os.path.join(tmp_path, f"out{r}.npz"))) for r in range(world)]
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 4, 8])
 def test_multiprocess_gemv_all_reduce(world, tmp_path):
     outs = _run("gemv", world, tmp_path)
     R = world
@@ -87,7 +87,7 @@ def test_multiprocess_gemv_all_reduce(world, tmp_path):
         assert int(outs[r]["guards"][0]) == csg.SYMM_OK
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 4, 8])
 def test_multiprocess_one_shot_all_reduce(world, tmp_path):
     outs = _run("oneshot", world, tmp_path)
     for i in range(2):

@@ -816,26 +816,31 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
     used = threads
     nbytes = workload_bytes(w, ar_op)
     kind, R = w["kind"], w["R"]
+    # make(rows) prepares a sample of the call's inputs (the first `rows`
+    # rows, made contiguous: input preparation, outside the timed loop) and
+    # returns the oracle call on it.
     if kind == "allreduce":
         inp = synth.allreduce_inputs(R, w["n"], w["seed"])
         full = inp.shape[1]
         if ar_op == "reduce_scatter":
             used = 1    # single-threaded oracle function
 
-            def call(rows):
-                m = max(R, rows // R * R)
-                oracle.reduce_scatter(np.ascontiguousarray(inp[:, :m]))
+            def make(rows):   # rows: a multiple of R (rounded below)
+                part = np.ascontiguousarray(inp[:, :rows])
+                return lambda: oracle.reduce_scatter(part)
         else:   # the two-shot all-reduce reaches the all-reduce definition
-            def call(rows):
-                oracle.one_shot_all_reduce(np.ascontiguousarray(inp[:, :rows]), threads=threads)
+            def make(rows):
+                part = np.ascontiguousarray(inp[:, :rows])
+                return lambda: oracle.one_shot_all_reduce(part, threads=threads)
         unit = "elements per slot"
     elif kind == "ar_rmsnorm":
         inp, bias, gamma = synth.rmsnorm_inputs(R, w["rows"], w["H"], w["seed"])
         full = w["rows"]
         used = 1
 
-        def call(rows):
-            oracle.all_reduce_bias_rmsnorm(np.ascontiguousarray(inp[:, :rows]), bias, gamma, w["eps"])
+        def make(rows):
+            part = np.ascontiguousarray(inp[:, :rows])
+            return lambda: oracle.all_reduce_bias_rmsnorm(part, bias, gamma, w["eps"])
         unit = "rows"
     elif kind == "tile":
         used = 1
@@ -846,27 +851,32 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
         offs = [0, h, h * w["cols"], h * w["cols"] + h]
         full = h
 
-        def call(rows):
-            oracle.tile_reduce(flat, out, offs, 0, [0, 1, 2, 3], rows, w["cols"] // 2, w["cols"], w["cols"] // 2)
+        def make(rows):
+            return lambda: oracle.tile_reduce(flat, out, offs, 0, [0, 1, 2, 3], rows, w["cols"] // 2, w["cols"],
+                                              w["cols"] // 2)
         unit = "tile rows"
     else:
         W, x = synth.gemv_inputs(R, w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
         full = w["N"]
         if kind == "gemv_rs":
-            def call(rows):
-                oracle.gemv_reduce_scatter(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
+            def make(rows):
+                part = np.ascontiguousarray(W[:, :rows])
+                return lambda: oracle.gemv_reduce_scatter(part, x, threads=threads)
         elif kind == "gemv_rmsnorm":
             bias, gamma = synth.norm_vectors(w["N"], w["seed"])
 
-            def call(rows):
-                oracle.gemv_bias_rmsnorm(np.ascontiguousarray(W[:, :rows]), x, bias[:rows], gamma[:rows],
-                                         w["eps"], threads=threads)
+            def make(rows):
+                part = np.ascontiguousarray(W[:, :rows])
+                return lambda: oracle.gemv_bias_rmsnorm(part, x, bias[:rows], gamma[:rows], w["eps"],
+                                                        threads=threads)
         else:
-            def call(rows):
-                oracle.gemv_all_reduce(np.ascontiguousarray(W[:, :rows]), x, threads=threads)
+            def make(rows):
+                part = np.ascontiguousarray(W[:, :rows])
+                return lambda: oracle.gemv_all_reduce(part, x, threads=threads)
         unit = "rows"
+    call = make(full)
     t = time.perf_counter()
-    call(full)                                  # calibration: one full call
+    call()                                      # calibration: one full call
     t_full = max(time.perf_counter() - t, 1e-6)
     if steps is None:
         rows = full if t_full <= budget_s else max(1, int(full * budget_s / t_full))
@@ -875,11 +885,16 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
         per_step = budget_s / max(1, steps + warmup)
         rows = max(1, min(full, int(full * per_step / t_full)))
         reps = steps
+    if kind == "allreduce" and ar_op == "reduce_scatter":
+        rows = min(full, max(R, rows // R * R))   # whole owner blocks
+    if rows != full:
+        call = make(rows)
+    if steps is not None:
         for _ in range(warmup):
-            call(rows)
+            call()
     t = time.perf_counter()
     for _ in range(reps):
-        call(rows)
+        call()
     el = time.perf_counter() - t
     sec_per_call = el / reps * full / rows
     return {

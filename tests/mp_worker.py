@@ -14,7 +14,8 @@ with the oracle.  Scenarios:
            packed weights; gemv_reduce_scatter;
   oneshot  one_shot_all_reduce, two calls;
   leave    rank world-1 leaves after the first call (its kernels finished);
-           the others make two more calls and report symm_status.
+           the others make one more call and report symm_status one after
+           another.
 """
 from __future__ import annotations
 
@@ -158,7 +159,13 @@ def leave(rk: Rank, out, survivors):
     csg.gemv_all_reduce(rk.h, rk.ptr(rk.w_off), rk.ptr(rk.x_off), rk.ptr(rk.y_off), R, N, R * KR, B, s)
     torch.cuda.synchronize()
     dist.barrier(group=survivors)
-    out["status"] = np.array(csg.symm_status(rk.h, s))
+    # the survivors report one after another, in rank order: each report
+    # resets that rank's pad (its launch count kept), and the later reports
+    # read the pads of the ranks that have already reset
+    for turn in range(R - 1):
+        if turn == rk.rank:
+            out["status"] = np.array(csg.symm_status(rk.h, s))
+        dist.barrier(group=survivors)
     return "stayed"
 
 

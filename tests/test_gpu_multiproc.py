@@ -101,12 +101,14 @@ def test_multiprocess_one_shot_all_reduce(world, tmp_path):
         assert int(outs[r]["status"][0]) == csg.SYMM_OK
 
 
-def test_rank_leaving_between_calls_is_reported(tmp_path):
-    """Rank 2 of 3 leaves after the first call; ranks 0 and 1 make one more
+@pytest.mark.parametrize("world", [3, 5])
+def test_rank_leaving_between_calls_is_reported(world, tmp_path):
+    """The last rank leaves after the first call; the others make one more
     call, which finishes (no kernel waits for the missing contributions), and
-    after their barrier both report SYMM_EPROTO naming rank 2, whose launch
-    count fell behind theirs."""
-    world = 3
+    after their barrier each reports SYMM_EPROTO naming the rank that left,
+    whose launch count fell behind theirs.  They report one after another,
+    so every report after the first reads the pads of survivors that have
+    already reset theirs: a reset must keep a rank's launch count."""
     outs = _run("leave", world, tmp_path, timeout=180)
     W, x = synth.gemv_inputs(world, N, world * KR, B, seed=12, w_std=0.02, x="normal")
     y_ref, _ = oracle.gemv_all_reduce(W, x)

@@ -568,14 +568,15 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
         return fail(SYMM_EINVAL, "the unfused form (SYMM_OPT_UNFUSED) is a form of gemv_all_reduce only");
     if (h->mp_rank >= 0 && (h->opt_unfused || ep.mode == kOutBiasZ))
         return fail(SYMM_EINVAL, "a multi-process handle runs the all-reduce and reduce-scatter forms, fused");
+    // (the plan asks the handle's device whether a cluster launch fits)
+    int rc = check_device(h);
+    if (rc != SYMM_OK) return rc;
     Plan pl;
-    int rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
+    rc = make_plan(h, N, Kr, B, &pl, cap, pw != nullptr);
     if (rc != SYMM_OK) return rc;
     const int path = pl.path, rows = pl.rows, tiles = pl.tiles, splits = pl.splits,
               slabs = pl.slabs, cps = pl.cps;
     const DynGeom dyn = pl.dyn;
-    rc = check_device(h);
-    if (rc != SYMM_OK) return rc;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The launch epoch, the tickets and the work counter live in the signal
@@ -968,8 +969,10 @@ int symm_gemv_plan(symm_handle_t *h, int N, int K, int B, symm_gemv_plan_t *out)
     if (!h || !out) return fail(SYMM_EINVAL, "NULL argument");
     if (N < 1 || K < 0 || B < 1 || B > SYMM_MAX_BATCH || K % h->R || (K / h->R) % 8)
         return fail(SYMM_EINVAL, "no plan for N=%d K=%d B=%d on %d ranks", N, K, B, h->R);
+    int rc = check_current_device(h);   // the plan depends on the device's occupancy
+    if (rc != SYMM_OK) return rc;
     Plan pl;
-    int rc = make_plan(h, N, K / h->R, B, &pl, h->scratch_bytes);
+    rc = make_plan(h, N, K / h->R, B, &pl, h->scratch_bytes);
     if (rc != SYMM_OK) return rc;
     out->path = pl.path;
     out->engine = pl.engine;

@@ -416,8 +416,7 @@ def make_case(args, w, local_rank, stream):
                              (csg.SYMM_OPT_SK_ENGINE, args.sk_engine), (csg.SYMM_OPT_SK_CTAS_PER_SM, args.sk_cps),
                              (csg.SYMM_OPT_SK_GRID, args.sk_grid), (csg.SYMM_OPT_DYN_SPLITS, args.dyn_splits),
                              (csg.SYMM_OPT_NORM_PDL, args.norm_pdl), (csg.SYMM_OPT_CHAIN, int(args.chain)),
-                             (csg.SYMM_OPT_DYN_CLUSTER, args.dyn_cluster),
-                             (csg.SYMM_OPT_DYN_PREFETCH, args.dyn_prefetch)):
+                             (csg.SYMM_OPT_DYN_CLUSTER, args.dyn_cluster)):
                 csg.symm_set_option(ws_.h, opt, val)
             return ws_
 
@@ -954,9 +953,6 @@ def parse_args(argv=None):
                    help="persistent kernel: K splits per (tile, rank) (0 = library default)")
     p.add_argument("--dyn-cluster", type=int, default=-1, choices=(-1, 0, 1),
                    help="persistent kernel: cluster epilogue -1 auto, 0 off, 1 on (SYMM_OPT_DYN_CLUSTER)")
-    p.add_argument("--dyn-prefetch", type=int, default=-1,
-                   help="cluster epilogue, chained calls: MB of W the early CTAs prefetch into L2 "
-                        "(-1 default, 0 off; SYMM_OPT_DYN_PREFETCH)")
     p.add_argument("--sk-engine", type=int, default=-1, choices=(-1, 0),
                    help="persistent kernel's engine: -1 auto, 0 tcgen05 (the only one)")
     p.add_argument("--ar-cps", type=int, default=0,

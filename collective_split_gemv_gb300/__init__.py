@@ -49,7 +49,6 @@ SYMM_OPT_AR_KERNEL = 11
 SYMM_OPT_COPY_ENGINE = 12
 SYMM_OPT_UNFUSED = 13
 SYMM_OPT_DYN_CLUSTER = 14
-SYMM_OPT_DYN_PREFETCH = 15
 AR_KERNEL_AUTO, AR_KERNEL_PER_THREAD, AR_KERNEL_STAGED = 0, 1, 2   # auto is the per-thread kernel
 
 GEMV_PATH_AUTO, GEMV_PATH_FFMA, GEMV_PATH_DYN, GEMV_PATH_CLUSTER = 0, 1, 4, 5   # paths 2 and 3 were retired

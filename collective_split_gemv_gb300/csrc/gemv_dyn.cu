@@ -59,10 +59,7 @@
 // each CTA's shared memory alive until its peers have read it.  This replaces
 // the global-memory protocol's round trips at the end of the launch (partial
 // store, fence, ticket, then flag and partial loads by the last arriver),
-// which in a one-wave launch are not hidden behind other units.  A one-wave
-// launch also leaves CTA slots free, where the next chained call's first
-// clusters start and wait for it: with a packed weight they prefetch their
-// units' blocks into L2 meanwhile (the host decides which, DynGeom).
+// which in a one-wave launch are not hidden behind other units.
 //
 // Safety: all mbarrier waits are bounded (%globaltimer); decisions that
 // steer the group's named barrier are made uniform with bar.red.and; a CTA
@@ -169,13 +166,6 @@ __device__ __forceinline__ void unit_of(const GemvArgs &a, int u, int S, int *t,
 }
 
 static_assert(kM == kPackRows && kSlabA == (int)kPackBlockBytes, "a stage slab is one block of the packed layout");
-
-// Moves [p, p + bytes) from HBM into L2 with the given eviction policy (no
-// shared memory, no completion to wait for); p and bytes multiples of 16.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes, uint64_t policy) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(policy)
-                 : "memory");
-}
 
 // W slab j (64 columns) of row tile t, rank r, into one stage slab: a TMA box
 // of the row-major W_r, or the same bytes as one contiguous block of the
@@ -383,20 +373,6 @@ __global__ void __launch_bounds__(kThreads, kCps == 2 ? 2 : 1)
 #pragma unroll
             for (int s = 0; s < kSlabs; ++s)
                 load_w_slab(dst + s * kSlabA, &tmW, a, &full_bar[i], kb * kSlabs + s, t, r, pol_w);
-        }
-        // A CTA that starts while the previous call still streams (the host
-        // names them: the first prefetch_ctas of a chained launch whose
-        // predecessor leaves resident slots free) would hold one ring of W at
-        // the wait below; it moves the rest of its unit's packed blocks into
-        // L2 meanwhile, with HBM bandwidth the previous call leaves unused.
-        // Evict-first, like the stream's own W loads (normal priority measured
-        // the same, and would keep the lines after their one use).
-        if (kCl && a.w_packed && (int)blockIdx.x < geo.prefetch_ctas) {
-            const int J = (a.Kr + kPackCols - 1) / kPackCols;
-            const int j1 = min(J, kb1 * kSlabs);
-            const uint8_t *unit_w = a.W + (long long)r * a.stride + (size_t)t * J * kPackBlockBytes;
-            for (int j = (kb0 + pre) * kSlabs; j < j1; ++j)
-                prefetch_l2_bulk(unit_w + (size_t)j * kPackBlockBytes, (uint32_t)kPackBlockBytes, pol_w);
         }
         if (a.w_early) griddep_wait();
         tl_stamp(a.tl, a.tl_ctas, blockIdx.x, 3);

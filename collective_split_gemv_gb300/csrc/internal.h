@@ -285,9 +285,6 @@ struct DynGeom {
     int G;
     int cluster;    // 0: units drawn, global-memory protocol; R: cluster epilogue
                     // (G = units, one per CTA, splits 1, clusters of R CTAs)
-    int prefetch_ctas;   // cluster epilogue, packed W, chained launch: CTAs
-                         // [0, prefetch_ctas) move the rest of their unit's W
-                         // into L2 before the dependency wait
 };
 // Encodes the TMA descriptors of a launch (cached by the caller): `maps`
 // points at two CUtensorMap objects (W, x), 64-byte aligned.

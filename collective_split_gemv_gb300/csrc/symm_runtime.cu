@@ -51,7 +51,6 @@ struct symm_handle {
     int opt_copy_engine = 0;    // symm_copy_*: 1 = always the copy engine, 0 = SMs where possible
     int opt_unfused = 0;        // gemv_all_reduce as two kernels (GEMV partials, then their all-reduce)
     int opt_dyn_cluster = -1;   // persistent kernel's cluster epilogue: -1 auto, 0 off, 1 on
-    int opt_dyn_prefetch = -1;  // cluster epilogue's L2 prefetch budget: -1 default, 0 off, else MB
     // y of the last persistent-kernel launch on the handle: a chained launch
     // reads W before its predecessor has finished, so W must not overlap it.
     // Slot-0 range written by the last kernel this handle launched (the same
@@ -250,10 +249,6 @@ constexpr int kPathFfma = 1, kPathDyn = 4, kPathCluster = 5;
 // K/R from which the persistent kernel's units (128 rows x K/R bf16, 768 KB
 // here) take the cluster epilogue even when they do not fit in one wave.
 constexpr int kClusterEpilogueMinKr = 3072;
-// L2 the early CTAs of a chained cluster-epilogue launch may fill with their
-// units' W ahead of the dependency wait (of 129 MB; the streamed W around it
-// is marked evict-first).
-constexpr long long kDynPrefetchDefaultMB = 64;
 
 // Below this many bytes of W a call is latency-bound: the persistent
 // kernel's start-up costs more than it saves, and for narrow batches a
@@ -307,7 +302,7 @@ const void *tc_maps_for(symm_handle *h, const GemvArgs &a, int *err) {
 // The kernel and launch geometry gemv_all_reduce would use.
 struct Plan {
     int path = 0, engine = 0, slabs = 0, cps = 0, rows = 0, tiles = 0, splits = 1, grid = 0, cluster = 0;
-    DynGeom dyn = {0, 1, 0, 0, 0, 0, 0};
+    DynGeom dyn = {0, 1, 0, 0, 0, 0};
 };
 
 // `cap`: scratch bytes per slot the partials may use (the whole region, or
@@ -400,26 +395,6 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         const long long units = pairs * S;
         G = cl ? units : std::max<long long>(1, std::min<long long>(G, units));
         pl->dyn.cluster = cl ? (int)(h->R * S) : 0;
-        // A launch of one wave leaves resident slots free: the next chained
-        // call's first clusters start there and wait through the whole call.
-        // With a packed weight they prefetch their units' W into L2 meanwhile
-        // (within the budget).  Measured: 5 % faster chained calls on the
-        // one-wave attention projection (21.2 -> 20.1 us); in a launch of
-        // several waves the free slots come with the last wave only, and the
-        // prefetch requests (tens of MB at once) delayed the other CTAs'
-        // first loads: 1-2 % slower on the decode and large layers.
-        // Resident clusters: the SMs' CTA slots over the cluster size (the
-        // occupancy query answers for one CTA per SM, while the hardware
-        // places two: a decode launch's first wave holds 38 clusters of 8).
-        pl->dyn.prefetch_ctas = 0;
-        if (cl && packed && h->opt_dyn_prefetch != 0) {
-            const long long C = (long long)h->R * S;
-            const long long n = (long long)num_sms(h->device) * pl->cps / C;
-            const long long early = pl->tiles < n ? (n - pl->tiles) * C : 0;
-            const long long unit_bytes = KBs * pl->slabs * (long long)kPackBlockBytes;
-            const long long budget = (h->opt_dyn_prefetch < 0 ? kDynPrefetchDefaultMB : h->opt_dyn_prefetch) << 20;
-            pl->dyn.prefetch_ctas = (int)std::min(early, budget / unit_bytes);
-        }
         pl->cluster = pl->dyn.cluster;
         pl->dyn.units = (int)units;
         pl->dyn.splits = (int)S;
@@ -664,9 +639,7 @@ int gemv_common(symm_handle *h, const void *W_r, const void *x_r, void *y, int R
             const void *maps = tc_maps_for(h, a, &err);
             if (!maps) return fail(SYMM_ECUDA, "cuTensorMapEncodeTiled failed (%d)", err);
             const bool chained = h->opt_chain != 0 && !overlaps(W_r, wbytes, h->last_write, h->last_write_bytes);
-            DynGeom g = dyn;
-            if (!chained) g.prefetch_ctas = 0;   // nothing to wait for: no early CTAs
-            e = launch_gemv_dyn(a, g, maps, slabs, cps, chained, s);
+            e = launch_gemv_dyn(a, dyn, maps, slabs, cps, chained, s);
             break;
         }
         default:
@@ -986,11 +959,6 @@ int symm_set_option(symm_handle_t *h, int option, int value) {
         case SYMM_OPT_DYN_CLUSTER:
             if (value < -1 || value > 1) return fail(SYMM_EINVAL, "cluster epilogue %d not in {-1 auto, 0, 1}", value);
             h->opt_dyn_cluster = value;
-            return SYMM_OK;
-        case SYMM_OPT_DYN_PREFETCH:
-            if (value < -1 || value > 1024)
-                return fail(SYMM_EINVAL, "L2 prefetch budget %d not in -1 (default), 0 (off), 1..1024 MB", value);
-            h->opt_dyn_prefetch = value;
             return SYMM_OK;
         default:
             return fail(SYMM_EINVAL, "unknown option %d", option);

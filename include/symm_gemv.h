@@ -525,13 +525,7 @@ enum {
                                  those hold, R >= 2, and either the units fit the persistent grid in one
                                  wave (nothing would be drawn) or they are long (K/R >= 3072, 768 KB of
                                  W per unit), when the hardware's scheduling of whole clusters beats
-                                 drawing single units */,
-    SYMM_OPT_DYN_PREFETCH = 15 /* path 4 with the cluster epilogue, a packed weight and a chained launch
-                                 of one wave (the tiles' clusters all resident at once): the next call's
-                                 first clusters start in the slots the launch leaves free and wait there
-                                 for it to end; they move the rest of their units' weight blocks into L2
-                                 meanwhile (cp.async.bulk.prefetch), at most this many MB in all: -1 the
-                                 default (64), 0 off, 1..1024.  The results do not depend on it */
+                                 drawing single units */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

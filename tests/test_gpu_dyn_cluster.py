@@ -195,10 +195,6 @@ def test_cluster_epilogue_rejections():
             with pytest.raises(csg.SymmError) as e:
                 csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, bad)
             assert e.value.code == csg.SYMM_EINVAL
-        for bad in (-2, 1025):
-            with pytest.raises(csg.SymmError) as e:
-                csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_PREFETCH, bad)
-            assert e.value.code == csg.SYMM_EINVAL
     finally:
         ws.close()
     # R x splits above a portable cluster
@@ -221,36 +217,6 @@ def test_cluster_epilogue_rejections():
         assert e.value.code == csg.SYMM_EINVAL
     finally:
         ws.close()
-
-
-# (R, N, K, B): one wave of 8-CTA clusters (30 tiles) and of 4-CTA clusters
-# (8 tiles), where the next call's first CTAs start early and prefetch; and
-# two waves (50 tiles of 8-CTA clusters), where they do not
-PREFETCH_SHAPES = [(8, 30 * 128, 8 * 1024, 1), (4, 1024, 4 * 1024, 8), (8, 50 * 128, 8 * 1024, 1)]
-
-
-@pytest.mark.parametrize("shape", PREFETCH_SHAPES, ids=["one_wave_R8", "one_wave_R4", "two_waves"])
-def test_l2_prefetch_leaves_the_bits(shape):
-    """The early CTAs of chained calls prefetch their units' packed W into
-    L2 before the dependency wait (SYMM_OPT_DYN_PREFETCH): it moves bytes
-    only, so the default budget, none, 1 MB and 1024 MB give the drawn
-    protocol's bits over a chain of calls."""
-    R, N, K, B = shape
-    W, x = synth.gemv_inputs(R, N, K, B, seed=41, w_std=0.02, x="normal")
-    ref, _ = _run(W, x, OFF, packed=True, repeat=1, splits=1)
-    for budget in (-1, 0, 1, 1024):
-        ws = _ws(W, x, ON, packed=True)
-        try:
-            csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_PREFETCH, budget)
-            s = torch.cuda.current_stream()
-            for _ in range(6):      # chained: every call after the first may prefetch
-                ws.run(s)
-            assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
-            assert np.array_equal(ws.read_y(), ref[0]), budget
-            assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
-        finally:
-            ws.close()
-    check_gemv(W, x, ref[0])
 
 
 def test_cluster_and_drawn_launches_alternate_on_one_handle():

@@ -15,7 +15,9 @@ with the oracle.  Scenarios:
   oneshot  one_shot_all_reduce, two calls;
   leave    rank world-1 leaves after the first call (its kernels finished);
            the others make one more call and report symm_status one after
-           another.
+           another;
+  leave0   the same with rank 0 leaving, whose pad holds the tile counters
+           every rank shares.
 """
 from __future__ import annotations
 
@@ -137,7 +139,7 @@ def oneshot(rk: Rank, out):
     out["status"] = np.array(csg.symm_status(rk.h, s))
 
 
-def leave(rk: Rank, out, survivors):
+def leave(rk: Rank, out, survivors, leaver):
     R = rk.world
     s = torch.cuda.current_stream()
     W, x = synth.gemv_inputs(R, N, R * KR, B, seed=12, w_std=0.02, x="normal")
@@ -152,7 +154,7 @@ def leave(rk: Rank, out, survivors):
     # every rank has read its status before a survivor launches its next call
     # (the status compares the ranks' launch counts)
     step_barrier()
-    if rk.rank == R - 1:
+    if rk.rank == leaver:
         return "left"   # between calls, nothing of this rank in flight
     # the others go on without it: their next call finishes (nothing waits
     # for the missing rank) and symm_status, after their barrier, reports it
@@ -162,7 +164,7 @@ def leave(rk: Rank, out, survivors):
     # the survivors report one after another, in rank order: each report
     # resets that rank's pad (its launch count kept), and the later reports
     # read the pads of the ranks that have already reset
-    for turn in range(R - 1):
+    for turn in [r for r in range(R) if r != leaver]:
         if turn == rk.rank:
             out["status"] = np.array(csg.symm_status(rk.h, s))
         dist.barrier(group=survivors)
@@ -176,7 +178,8 @@ def main():
     # (after their kernels have finished) instead of blocking
     dist.init_process_group("gloo", init_method=f"file://{tmpdir}/pg", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=60))
-    survivors = dist.new_group(list(range(world - 1))) if world > 1 else None
+    leaver = 0 if scenario == "leave0" else world - 1
+    survivors = dist.new_group([r for r in range(world) if r != leaver]) if world > 1 else None
     rk = Rank(rank, world, tmpdir)
     out = {}
     try:
@@ -184,14 +187,14 @@ def main():
             gemv(rk, out)
         elif scenario == "oneshot":
             oneshot(rk, out)
-        elif scenario == "leave":
-            out["role"] = np.array([1 if leave(rk, out, survivors) == "left" else 0])
+        elif scenario in ("leave", "leave0"):
+            out["role"] = np.array([1 if leave(rk, out, survivors, leaver) == "left" else 0])
         else:
             raise SystemExit(f"unknown scenario {scenario}")
         np.savez(os.path.join(tmpdir, f"out{rank}.npz"), **out)
     finally:
         torch.cuda.synchronize()
-        if scenario != "leave":
+        if scenario not in ("leave", "leave0"):
             dist.barrier()
         csg.symm_free(rk.h)
     os._exit(0)   # no process-group teardown: a rank may have left

@@ -101,22 +101,26 @@ def test_multiprocess_one_shot_all_reduce(world, tmp_path):
         assert int(outs[r]["status"][0]) == csg.SYMM_OK
 
 
-@pytest.mark.parametrize("world", [3, 5])
-def test_rank_leaving_between_calls_is_reported(world, tmp_path):
-    """The last rank leaves after the first call; the others make one more
+@pytest.mark.parametrize("world,leaver", [(3, 2), (5, 4), (3, 0)])
+def test_rank_leaving_between_calls_is_reported(world, leaver, tmp_path):
+    """A rank leaves after the first call (the last one, or rank 0, whose pad
+    holds the tile counters every rank shares); the others make one more
     call, which finishes (no kernel waits for the missing contributions), and
     after their barrier each reports SYMM_EPROTO naming the rank that left,
     whose launch count fell behind theirs.  They report one after another,
     so every report after the first reads the pads of survivors that have
     already reset theirs: a reset must keep a rank's launch count."""
-    outs = _run("leave", world, tmp_path, timeout=180)
+    assert leaver in (0, world - 1)
+    outs = _run("leave0" if leaver == 0 else "leave", world, tmp_path, timeout=180)
     W, x = synth.gemv_inputs(world, N, world * KR, B, seed=12, w_std=0.02, x="normal")
     y_ref, _ = oracle.gemv_all_reduce(W, x)
     for r in range(world):
         assert int(outs[r]["first_status"][0]) == csg.SYMM_OK
         assert tolerance_ratio(words_to_f64(outs[r]["first"].reshape(B, N)), y_ref) <= 1.0
-    assert int(outs[world - 1]["role"][0]) == 1
-    for r in range(world - 1):
+    assert int(outs[leaver]["role"][0]) == 1
+    for r in range(world):
+        if r == leaver:
+            continue
         assert int(outs[r]["role"][0]) == 0
         assert int(outs[r]["status"][0]) == csg.SYMM_EPROTO, outs[r]["status"]
-        assert int(outs[r]["status"][1]) == world - 1, outs[r]["status"]
+        assert int(outs[r]["status"][1]) == leaver, outs[r]["status"]

@@ -22,6 +22,8 @@
 #include <new>
 #include <vector>
 
+#include <unistd.h>
+
 #include "../../include/symm_gemv.h"
 #include "internal.h"
 #include "timeline.cuh"
@@ -838,6 +840,7 @@ int symm_mp_alloc(int R, int rank, size_t slot_bytes, size_t scratch_bytes, size
     if (e == cudaSuccess) e = cudaMemset(sl + h->guard2, kGuardByte, kGuard);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
+        close(fd);   // never handed out
         mp_release(h);
         delete h;
         return cuda_fail(e, "initialising the slot");

@@ -42,14 +42,25 @@ def exchange_fds(rank: int, world: int, my_fd: int, sock_dir: str, barrier) -> d
                 c.connect(os.path.join(sock_dir, f"slot{q}.sock"))
                 socket.send_fds(c, [struct.pack("<i", rank)], [my_fd])
         got = {}
-        for _ in range(world - 1):
-            conn, _ = srv.accept()
-            with conn:
-                msg, fds, _, _ = socket.recv_fds(conn, 4, 1)
-                if len(msg) != 4 or len(fds) != 1:
-                    raise RuntimeError("malformed descriptor message")
-                got[struct.unpack("<i", msg)[0]] = fds[0]
-        barrier()                                   # every rank has every descriptor
+        try:
+            for _ in range(world - 1):
+                conn, _ = srv.accept()
+                with conn:
+                    msg, fds, _, _ = socket.recv_fds(conn, 4, 1)
+                    if len(msg) != 4 or len(fds) != 1:
+                        for f in fds:
+                            os.close(f)
+                        raise RuntimeError("malformed descriptor message")
+                    peer = struct.unpack("<i", msg)[0]
+                    if peer in got or not 0 <= peer < world or peer == rank:
+                        os.close(fds[0])
+                        raise RuntimeError(f"unexpected descriptor from rank {peer}")
+                    got[peer] = fds[0]
+            barrier()                               # every rank has every descriptor
+        except BaseException:
+            for f in got.values():                  # none of them reaches the caller
+                os.close(f)
+            raise
         return got
     finally:
         srv.close()

@@ -54,3 +54,47 @@ def test_descriptors_travel_between_processes(world, tmp_path):
         outs.append((p.returncode, out, err))
     for r, (rc, out, err) in enumerate(outs):
         assert rc == 0 and f"ok {r}" in out, (r, rc, out, err[-2000:])
+
+
+def test_a_descriptor_from_an_unexpected_rank_is_refused(tmp_path):
+    """Rank 0 of 2 exchanges with a fake peer that claims to be rank 0 too:
+    exchange_fds raises, and neither the descriptor it received nor any other
+    stays open in this process."""
+    import socket
+    import struct
+    import threading
+
+    from collective_split_gemv_gb300.multiproc import exchange_fds
+
+    peer_sock = socket.socket(socket.AF_UNIX, socket.SOCK_STREAM)
+    peer_sock.bind(str(tmp_path / "slot1.sock"))
+    peer_sock.listen(1)
+    rd, wr = os.pipe()
+    fake_rd, fake_wr = os.pipe()
+
+    def fake_peer():
+        conn, _ = peer_sock.accept()                # rank 0 sends its descriptor
+        with conn:
+            _, fds, _, _ = socket.recv_fds(conn, 4, 1)
+            for f in fds:
+                os.close(f)
+        with socket.socket(socket.AF_UNIX, socket.SOCK_STREAM) as c:
+            c.connect(str(tmp_path / "slot0.sock"))
+            socket.send_fds(c, [struct.pack("<i", 0)], [fake_wr])   # the wrong rank
+
+    t = threading.Thread(target=fake_peer)
+    before = set(os.listdir("/proc/self/fd"))
+    started = []
+
+    def barrier():
+        if not started:
+            started.append(1)
+            t.start()
+
+    with pytest.raises(RuntimeError, match="unexpected descriptor"):
+        exchange_fds(0, 2, wr, str(tmp_path), barrier)
+    t.join(timeout=30)
+    peer_sock.close()
+    assert set(os.listdir("/proc/self/fd")) <= before | {str(fake_rd), str(fake_wr), str(rd), str(wr)}
+    for f in (rd, wr, fake_rd, fake_wr):
+        os.close(f)

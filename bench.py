@@ -454,6 +454,7 @@ def make_case(args, w, local_rank, stream):
             # e2e: per-step inputs are x_r (W_r are resident model weights); result y
             "in_host": _pinned(x), "in_dst": ws.x_ptr(), "in_bytes": ws.x_bytes,
             "out_src": ws.y_ptr(), "out_bytes": out_rows * N * 2,
+            "read_out": ws.read_y_rs if kind == "gemv_rs" else ws.read_y,
             "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
             "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
                        "w_layout": ("packed (symm_pack_w once at load, untimed; the same bytes per call)"
@@ -482,6 +483,7 @@ def make_case(args, w, local_rank, stream):
             "run0": lambda: ws.run(stream, copy=0, op=op),
             "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
             "out_src": ws.base + ws.out_offs[0], "out_bytes": out_n * 2,
+            "read_out": lambda: ws.read_out(copy=0, count=out_n),
             "launches_per_step": 2 if op == "two_shot" else 1,
             "chainable": True,
             "config": {"R": R, "n": n, "op": op, **({"ar_kernel": "staged" if staged else "per_thread"}
@@ -501,6 +503,7 @@ def make_case(args, w, local_rank, stream):
             "run0": lambda: ws.run(stream, copy=0, eps=eps),
             "in_host": _pinned(inp), "in_dst": ws.base + ws.in_offs[0], "in_bytes": ws.bytes,
             "out_src": ws.base + ws.out_offs[0], "out_bytes": ws.bytes,
+            "read_out": lambda: ws.read_out(copy=0),
             "launches_per_step": 1,
             "config": {"R": R, "rows": rows, "H": H, "eps": eps},
         }
@@ -685,6 +688,11 @@ def run_ours(args, rank, world, local_rank):
         [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms),
          unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0, e2e_graph_ms,
          row_major if row_major is not None else 0.0, unfused if unfused is not None else 0.0], world, dev)
+    # the last call's result (every slot; all legs computed it from the same
+    # inputs), for the oracle leg's check -- read before the handle is freed
+    gpu_out = None
+    if rank == 0 and not args.no_cpu_baseline and c.get("read_out") is not None:
+        gpu_out = c["read_out"]()
     ws.close()
     if rank != 0:
         return None
@@ -787,25 +795,31 @@ def run_ours(args, rank, world, local_rank):
                      + (", then packed (symm_pack_w)" if ws.packed else "")),
         }
     if not args.no_cpu_baseline:
-        cb = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op)
+        cb = cpu_baseline(args.workload, budget_s=args.cpu_seconds, ar_op=args.ar_op, gpu_out=gpu_out)
+        parity = cb.pop("parity", None)
         if cb["cores"] > 1:   # the same oracle on one core, a shorter sample
             one = cpu_baseline(args.workload, budget_s=min(args.cpu_seconds, 4.0), ar_op=args.ar_op, threads=1)
             cb["one_thread"] = {k: one[k] for k in ("value", "unit", "us_per_call_equiv", "cores", "sample")}
         line["cpu_baseline"] = cb
+        if parity is not None:
+            line["parity"] = parity
     return line
 
 
 # ------------------------------------------------------------ CPU oracle
 
 
-def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", threads=None):
+def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", threads=None, gpu_out=None):
     """Time the oracle (as it is) on this host's cores on the workload: with
     `steps` None, repeat the full call for about `budget_s` seconds; else run
     exactly `steps` calls, each on a row sample sized so that all of them fit
     in about `budget_s`.  Returns the cpu_baseline object (GB/s of algorithmic
     bytes, the time scaled to a full call).  `threads`: the oracle's threads
     where it is multithreaded (None: every host core); `cores` in the result
-    is what the call actually used."""
+    is what the call actually used.  `gpu_out`: the GPU path's last result on
+    the same inputs, every slot's words; the object then carries `parity`,
+    that result checked against the oracle's on the sample (after the
+    timing)."""
     import numpy as np
 
     import oracle
@@ -896,6 +910,9 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
     for _ in range(reps):
         call()
     el = time.perf_counter() - t
+    parity = None
+    if gpu_out is not None:
+        parity = parity_check(kind, ar_op, call(), np.asarray(gpu_out), rows, full, R, unit)
     sec_per_call = el / reps * full / rows
     return {
         "value": round(nbytes / sec_per_call / 1e9, 4),
@@ -905,6 +922,75 @@ def cpu_baseline(name, budget_s=10.0, steps=None, warmup=0, ar_op="one_shot", th
         "kind": "oracle",
         "sample": (f"{rows} of {full} {unit} of {name}, {reps} repetitions, {el:.3f} s wall time on {used} "
                    f"thread{'s' if used != 1 else ''}; time scaled to the full call"),
+        **({"parity": parity} if parity is not None else {}),
+    }
+
+
+# The accuracy bar of the fused call: |y - y_ref| <= REL |y_ref| + ABS rms(y_ref),
+# y_ref the oracle's fp64 value before rounding.
+TOL_REL, TOL_ABS = 4e-3, 1e-3
+
+
+def _bf16_f64(words):
+    import numpy as np
+
+    return (np.asarray(words, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def tolerance_ratio(y, y_ref):
+    """max over outputs of |y - y_ref| / (REL |y_ref| + ABS rms(y_ref))."""
+    import numpy as np
+
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    if y_ref.size == 0:
+        return 0.0
+    bound = TOL_REL * np.abs(y_ref) + TOL_ABS * float(np.sqrt(np.mean(y_ref * y_ref)))
+    err = np.abs(np.asarray(y, dtype=np.float64) - y_ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0), np.where(err > 0, np.inf, 0.0))
+    return float(np.max(r))
+
+
+def parity_check(kind, ar_op, ref, gpu_out, rows, full, R, unit):
+    """The GPU result (every slot's words) against the oracle's (y_ref fp64,
+    words) on the first `rows` rows: the worst error over the tolerance, the
+    fraction of outputs equal to the oracle's correctly rounded words, and
+    whether the R replicas are bitwise identical.  None where a row sample of
+    the form is not a sample of the full result (a normalisation over the
+    whole row, a reduce-scatter's owner blocks)."""
+    import numpy as np
+
+    y_ref, words = ref
+    replicas = None
+    if kind in ("gemv", "gemv_rmsnorm"):
+        if kind == "gemv_rmsnorm" and rows != full:
+            return None
+        got = gpu_out[:, :, :rows]
+        replicas = bool(all(np.array_equal(got[r], got[0]) for r in range(R)))
+        y, want = got[0], words[0]
+    elif kind == "gemv_rs":
+        got = gpu_out[:, :, :rows]                      # slot s: batch rows s*B/R ... of the sum
+        y, want = got.reshape(-1, rows), np.asarray(words).reshape(-1, rows)
+    elif kind == "allreduce" and ar_op != "reduce_scatter":
+        got = gpu_out[:, :rows]
+        replicas = bool(all(np.array_equal(got[r], got[0]) for r in range(R)))
+        y, want = got[0], words[0]
+    elif kind == "allreduce" and rows == full:
+        y, want = gpu_out.reshape(-1), np.asarray(words).reshape(-1)
+    elif kind == "ar_rmsnorm":
+        got = gpu_out[:, :rows]
+        replicas = bool(all(np.array_equal(got[r], got[0]) for r in range(R)))
+        y, want = got[0], words[0]
+    else:
+        return None
+    ratio = tolerance_ratio(_bf16_f64(y), np.asarray(y_ref).reshape(np.shape(y)))
+    return {
+        "checked": f"{rows} of {full} {unit}, every output of those, against the oracle (fp64)",
+        "tolerance": "|y - y_ref| <= 4e-3 |y_ref| + 1e-3 rms(y_ref), y_ref before rounding",
+        "max_tol_ratio": round(ratio, 4),
+        "bit_equal_frac": round(float(np.mean(np.asarray(y) == np.asarray(want))), 6),
+        "replicas_identical": replicas,
+        "passed": bool(ratio <= 1.0 and replicas is not False),
     }
 
 

@@ -112,3 +112,37 @@ def test_reference_arm_line_follows_the_contract(workload, threads):
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["sample"]
     assert cb["cores"] == (threads if threads is not None else bench.host_cores())
     assert bench.run_reference(args, 1, 2) is None   # other ranks print nothing
+
+
+@pytest.mark.parametrize("workload", ["tiny", "allreduce"])
+def test_parity_object_of_the_oracle_leg(workload):
+    """The bench's parity check: the oracle's own words pass (their ratio is
+    their rounding, at most half a bf16 ulp, so below 1) with every output
+    bit-equal; a large change in one output (every replica) fails the
+    tolerance; one replica that differs is reported."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    w = bench.workload(workload)
+    if workload == "tiny":
+        W, x = synth.gemv_inputs(w["R"], w["N"], w["K"], w["B"], w["seed"], w["w_std"], w["x"])
+        y_ref, words = oracle.gemv_all_reduce(W, x)
+        at = (slice(None), *np.unravel_index(np.argmax(np.abs(y_ref)), y_ref.shape))
+        first = (1, 0, 0)
+    else:
+        inp = synth.allreduce_inputs(w["R"], w["n"], w["seed"])
+        y_ref, words = oracle.one_shot_all_reduce(inp)
+        at = (slice(None), int(np.argmax(np.abs(y_ref))))
+        first = (1, 0)
+    p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=words)["parity"]
+    assert p["passed"] and p["max_tol_ratio"] <= 1.0 and p["bit_equal_frac"] == 1.0 and p["replicas_identical"]
+    bad = words.copy()
+    bad[at] ^= 0x0040                       # the largest output changed by a quarter or more
+    p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=bad)["parity"]
+    assert not p["passed"] and p["max_tol_ratio"] > 1
+    odd = words.copy()
+    odd[first] ^= 1                         # one ulp in one replica
+    p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=odd)["parity"]
+    assert p["replicas_identical"] is False and not p["passed"]

@@ -937,6 +937,18 @@ def _bf16_f64(words):
     return (np.asarray(words, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def ulp_distance(a, b):
+    """Units in the last place between bf16 words, through their ordering
+    as sign-magnitude integers (+0 and -0 are 0 apart)."""
+    import numpy as np
+
+    def key(w):
+        w = np.asarray(w, dtype=np.uint16).astype(np.int64)
+        return np.where(w & 0x8000, -(w & 0x7FFF), w)
+
+    return np.abs(key(a) - key(b))
+
+
 def tolerance_ratio(y, y_ref):
     """max over outputs of |y - y_ref| / (REL |y_ref| + ABS rms(y_ref))."""
     import numpy as np
@@ -989,6 +1001,7 @@ def parity_check(kind, ar_op, ref, gpu_out, rows, full, R, unit):
         "tolerance": "|y - y_ref| <= 4e-3 |y_ref| + 1e-3 rms(y_ref), y_ref before rounding",
         "max_tol_ratio": round(ratio, 4),
         "bit_equal_frac": round(float(np.mean(np.asarray(y) == np.asarray(want))), 6),
+        "max_ulp": int(ulp_distance(y, want).max(initial=0)),
         "replicas_identical": replicas,
         "passed": bool(ratio <= 1.0 and replicas is not False),
     }

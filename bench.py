@@ -354,6 +354,30 @@ def empty_launch_floor(stream, dev, flush_buf, n=50):
     return statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends))
 
 
+def gpu_bound_region(fn, n_steps, stream, dev, world, sleep_ms=20.0):
+    """Per-step time of fn(0..n-1) as the GPU runs them back to back: the
+    steps are enqueued behind a sleep kernel, so the host's launch rate does
+    not set the pace, and timed from an event after the sleep.  Returns
+    (ms per step, whether the host fell behind the sleep)."""
+    import torch
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(sleep_ms * 1e-3 * 2.2e9))    # at most this many SM cycles
+        t = time.perf_counter()
+        a.record(stream)
+        for i in range(n_steps):
+            fn(i)
+        b.record(stream)
+        host_ms = (time.perf_counter() - t) * 1e3
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / n_steps, host_ms > 0.5 * sleep_ms
+
+
 def chunked_spread(step, n_steps, stream, dev, world, chunk=None):
     """The same n_steps chained calls once more, with an event after every
     `chunk` calls (each event ends one chain: the call after it starts in
@@ -396,7 +420,8 @@ def make_case(args, w, local_rank, stream):
     in_host / in_dst / in_bytes (per-step inputs for the end-to-end leg: one
     pinned buffer of R blocks, their symmetric destination and the bytes per
     rank), out_src / out_bytes (the result in slot 0, read back), kernel, config, per_copy, copies,
-    launches_per_step, W (GEMV weights, for the weights-from-host leg)."""
+    launches_per_step, W (GEMV weights, for the weights-from-host leg), read_out() (every slot's
+    result), producer() (GEMV: one kernel rewriting every rank's x in place, for the in-step leg)."""
     import collective_split_gemv_gb300 as csg
     import synth
     from collective_split_gemv_gb300.workspace import (AllReduceWorkspace, GemvWorkspace, RmsNormWorkspace,
@@ -445,6 +470,17 @@ def make_case(args, w, local_rank, stream):
             # shown is that of the all-reduce form of the same shape
         kernel = kernel_name(plan) + ("+rmsnorm_rows_kernel<z>" if kind == "gemv_rmsnorm" else "")
         out_rows = B // R if kind == "gemv_rs" else B
+        # The layer's input written by a kernel of another library just before
+        # the call (as the previous layer's kernel would): one strided copy of
+        # the same bytes into every rank's x.
+        import numpy as np
+        import torch
+
+        dev = torch.device("cuda", local_rank)
+        span = (R - 1) * ws.stride + ws.x_off + ws.x_bytes
+        slots_u8 = torch.as_tensor(csg.DeviceView(ws.base, (span,)), device=dev)
+        x_slots = torch.as_strided(slots_u8, (R, ws.x_bytes), (ws.stride, 1), ws.x_off)
+        x_src = torch.from_numpy(np.ascontiguousarray(x).view(np.uint8).reshape(R, -1)).to(dev)
         return {
             "ws": ws, "W": W, "copies": copies, "per_copy": W.nbytes, "kernel": kernel,
             "step": lambda i: ws.run(stream, copy=i % copies, mode=mode, eps=eps),
@@ -455,6 +491,7 @@ def make_case(args, w, local_rank, stream):
             "in_host": _pinned(x), "in_dst": ws.x_ptr(), "in_bytes": ws.x_bytes,
             "out_src": ws.y_ptr(), "out_bytes": out_rows * N * 2,
             "read_out": ws.read_y_rs if kind == "gemv_rs" else ws.read_y,
+            "producer": lambda: x_slots.copy_(x_src),
             "launches_per_step": 2 if kind == "gemv_rmsnorm" else 1,
             "config": {"R": R, "N": N, "K": K, "K_per_rank": K // R, "B": B, "plan": plan,
                        "w_layout": ("packed (symm_pack_w once at load, untimed; the same bytes per call)"
@@ -579,6 +616,23 @@ def run_ours(args, rank, world, local_rank):
         u_step, u_launch, _ = timed_loop(step, args.steps, args.warmup, stream, dev, world, flush_buf, gpu_id)
         csg.symm_set_option(ws.h, csg.SYMM_OPT_CHAIN, 1)
         unchained = (u_step, statistics.mean(u_launch), statistics.median(u_launch), _p10_p90(u_launch))
+    in_step = None
+    if chained and c.get("producer") is not None:
+        # The call inside a step: another library's kernel writes the layer's
+        # input x into the R slots, then the call (chained, the library
+        # default; the producer does not release it early, so the call pays
+        # its own start-up).  Its cost is the step's time minus the
+        # producer's alone, both as the GPU runs the steps back to back (no
+        # event between launches, and not paced by the host's launches).
+        prod = c["producer"]
+        n_in = min(args.steps, 200)
+        with torch.cuda.stream(stream):
+            for i in range(min(args.warmup, 10)):
+                prod()
+                step(i)
+        ps_ms, host_a = gpu_bound_region(lambda i: (prod(), step(i)), n_in, stream, dev, world)
+        p_ms, host_b = gpu_bound_region(lambda i: prod(), n_in, stream, dev, world)
+        in_step = (ps_ms, p_ms, n_in, host_a or host_b)
     code, _, _ = csg.symm_status(ws.h, stream)
     if code != csg.SYMM_OK:
         raise SystemExit(f"protocol error in the timed region: {csg.symm_last_error()}")
@@ -684,10 +738,12 @@ def run_ours(args, rank, world, local_rank):
     code, _, _ = csg.symm_status(ws.h, stream)
     assert code == csg.SYMM_OK
 
-    step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms, rm_ms, uf_ms = max_over_ranks(
+    (step_ms, e2e_ms, ew_ms, mean_launch_ms, u_step_ms, u_launch_ms, e2e_graph_ms, rm_ms, uf_ms, ps_ms,
+     p_ms) = max_over_ranks(
         [step_ms, e2e_ms, ew if ew is not None else 0.0, statistics.mean(launch_ms),
          unchained[0] if unchained else 0.0, unchained[1] if unchained else 0.0, e2e_graph_ms,
-         row_major if row_major is not None else 0.0, unfused if unfused is not None else 0.0], world, dev)
+         row_major if row_major is not None else 0.0, unfused if unfused is not None else 0.0,
+         in_step[0] if in_step else 0.0, in_step[1] if in_step else 0.0], world, dev)
     # the last call's result (every slot; all legs computed it from the same
     # inputs), for the oracle leg's check -- read before the handle is freed
     gpu_out = None
@@ -770,6 +826,18 @@ def run_ours(args, rank, world, local_rank):
             "p10_p90_launch_us": [round(q * 1e3, 3) for q in unchained[3]],
             "achieved": round(nbytes / (u_launch_ms * 1e-3) / 1e9, 1),
             "frac": round(nbytes / (u_launch_ms * 1e-3) / 1e9 / peak, 4),
+        }
+    if in_step is not None:
+        call_ms = ps_ms - p_ms
+        line["in_step"] = {
+            "what": ("each step: one kernel of another library writes the layer's input x into the R slots "
+                     "(as the previous layer's kernel would), then the call; per call = the step's time minus "
+                     "the producer's alone, each over a region of steps the GPU runs back to back (enqueued "
+                     "behind a sleep kernel; no event between launches)"),
+            "steps": in_step[2], "host_fell_behind": in_step[3],
+            "us_per_call": round(call_ms * 1e3, 3), "producer_us": round(p_ms * 1e3, 3),
+            "achieved": round(nbytes / (call_ms * 1e-3) / 1e9, 1),
+            "frac": round(nbytes / (call_ms * 1e-3) / 1e9 / peak, 4),
         }
     if row_major is not None:
         line["row_major_w"] = {

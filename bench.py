@@ -1063,13 +1063,17 @@ def parity_check(kind, ar_op, ref, gpu_out, rows, full, R, unit):
         y, want = got[0], words[0]
     else:
         return None
-    ratio = tolerance_ratio(_bf16_f64(y), np.asarray(y_ref).reshape(np.shape(y)))
+    ref_v = np.asarray(y_ref).reshape(np.shape(y))
+    ratio = tolerance_ratio(_bf16_f64(y), ref_v)
+    ulps = ulp_distance(y, want)
+    big = np.abs(ref_v) >= 0.1 * float(np.sqrt(np.mean(ref_v * ref_v)))   # outside the cancellation zone
     return {
         "checked": f"{rows} of {full} {unit}, every output of those, against the oracle (fp64)",
         "tolerance": "|y - y_ref| <= 4e-3 |y_ref| + 1e-3 rms(y_ref), y_ref before rounding",
         "max_tol_ratio": round(ratio, 4),
         "bit_equal_frac": round(float(np.mean(np.asarray(y) == np.asarray(want))), 6),
-        "max_ulp": int(ulp_distance(y, want).max(initial=0)),
+        "max_ulp": int(ulps.max(initial=0)),
+        "max_ulp_where_abs_ge_0.1_rms": int(ulps[big].max(initial=0)),
         "replicas_identical": replicas,
         "passed": bool(ratio <= 1.0 and replicas is not False),
     }

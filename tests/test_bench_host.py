@@ -138,7 +138,7 @@ def test_parity_object_of_the_oracle_leg(workload):
         first = (1, 0)
     p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=words)["parity"]
     assert p["passed"] and p["max_tol_ratio"] <= 1.0 and p["bit_equal_frac"] == 1.0 and p["replicas_identical"]
-    assert p["max_ulp"] == 0
+    assert p["max_ulp"] == 0 and p["max_ulp_where_abs_ge_0.1_rms"] == 0
     bad = words.copy()
     bad[at] ^= 0x0040                       # the largest output changed by a quarter or more
     p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=bad)["parity"]

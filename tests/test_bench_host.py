@@ -147,3 +147,47 @@ def test_parity_object_of_the_oracle_leg(workload):
     odd[first] ^= 1                         # one ulp in one replica
     p = bench.cpu_baseline(workload, budget_s=0.5, gpu_out=odd)["parity"]
     assert p["replicas_identical"] is False and not p["passed"]
+
+
+def test_parity_check_of_every_form():
+    """parity_check on small oracle results of each form: the oracle's own
+    words pass; the largest output changed by a quarter or more (alike in
+    every replica) fails; the forms whose row sample is no sample of the
+    call (a normalisation over the whole row on a partial sample, a
+    reduce-scatter's blocks on a prefix) are skipped."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    R, N, Kr, B = 4, 64, 32, 8
+    W, x = synth.gemv_inputs(R, N, R * Kr, B, seed=5, w_std=0.05, x="normal")
+    bias, gamma = synth.norm_vectors(N, 5)
+    inp = synth.allreduce_inputs(R, 256, 6)
+    rin, rbias, rgamma = synth.rmsnorm_inputs(R, 3, 64, 7)
+    # (kind, op, oracle result, rows = full, does every slot hold a replica)
+    cases = [
+        ("gemv", "one_shot", oracle.gemv_all_reduce(W, x), N, True),
+        ("gemv_rs", "one_shot", oracle.gemv_reduce_scatter(W, x), N, False),
+        ("gemv_rmsnorm", "one_shot", oracle.gemv_bias_rmsnorm(W, x, bias, gamma, 1e-6), N, True),
+        ("allreduce", "reduce_scatter", oracle.reduce_scatter(inp), 256, False),
+        ("ar_rmsnorm", "one_shot", oracle.all_reduce_bias_rmsnorm(rin, rbias, rgamma, 1e-6), 3, True),
+    ]
+    for kind, op, ref, rows, replicated in cases:
+        y_ref, words = ref
+        p = bench.parity_check(kind, op, ref, np.asarray(words), rows, rows, R, "rows")
+        assert p is not None and p["passed"] and p["max_ulp"] == 0, (kind, p)
+        at = int(np.argmax(np.abs(np.asarray(y_ref)).reshape(-1)))
+        bad = np.array(words, copy=True)
+        if replicated:          # the same output of every replica
+            per = bad.reshape(R, -1)
+            per[:, at] ^= 0x0040
+        else:                   # the slots' blocks, in order, are the whole result
+            bad.reshape(-1)[at] ^= 0x0040
+        p = bench.parity_check(kind, op, ref, bad, rows, rows, R, "rows")
+        assert not p["passed"] and p["max_tol_ratio"] > 1, (kind, p)
+    # a row sample that is no sample of the form
+    assert bench.parity_check("gemv_rmsnorm", "one_shot", cases[2][2], cases[2][2][1], N // 2, N, R, "rows") is None
+    assert bench.parity_check("allreduce", "reduce_scatter", cases[3][2], cases[3][2][1], 128, 256, R, "rows") \
+        is None
+    assert bench.parity_check("tile", "one_shot", cases[0][2], cases[0][2][1], N, N, R, "rows") is None

@@ -319,3 +319,34 @@ def test_long_chain_of_cluster_launches():
         check_gemv(W, x1, ws.read_y())
     finally:
         ws.close()
+
+
+def test_twenty_thousand_chained_calls_across_endings():
+    """20,000 chained calls on one handle, switching every 500 calls between
+    drawn units (the launch epoch, flags, tickets and work counters advance
+    every launch), the cluster epilogue, K splits and the unfused form: the
+    protocol state the pad carries stays consistent (clean status) and the
+    last result is the oracle's."""
+    R, N, K, B = 8, 2048, 8 * 512, 2
+    W, x = synth.gemv_inputs(R, N, K, B, seed=44, w_std=0.02, x="normal")
+    ws = GemvWorkspace(R, N, K, B, packed=True)
+    try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+        ws.load_W(W)
+        ws.load_x(x)
+        s = torch.cuda.current_stream()
+        modes = [(OFF, 0, 0), (ON, 0, 0), (OFF, 2, 0), (OFF, 0, 1)]   # (cluster, splits, unfused)
+        for i in range(20000):
+            if i % 500 == 0:
+                cl, sp, uf = modes[(i // 500) % len(modes)]
+                csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, cl)
+                csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_SPLITS, sp)
+                csg.symm_set_option(ws.h, csg.SYMM_OPT_UNFUSED, uf)
+            ws.run(s)
+            if i % 5000 == 4999:
+                assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK, i
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        check_gemv(W, x, ws.read_y())
+        assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
+    finally:
+        ws.close()

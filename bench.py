@@ -97,8 +97,21 @@ def tile_bytes(R, rows, cols, ntiles):
 
 
 def workload(name):
+    """A named workload (synth.WORKLOADS), or "gemv:R,N,K,B": the fused GEMV +
+    all-reduce of that shape on seeded inputs (W ~ N(0, 0.01), x ~ N(0, 1))."""
     import synth
 
+    if name.startswith("gemv:"):
+        try:
+            R, N, K, B = (int(v) for v in name[len("gemv:"):].split(","))
+        except ValueError:
+            raise SystemExit(f"workload {name!r}: expected gemv:R,N,K,B") from None
+        if not (1 <= R <= 64 and N >= 1 and K >= R and K % R == 0 and (K // R) % 8 == 0 and 1 <= B <= 16):
+            raise SystemExit(f"workload {name!r}: needs 1 <= R <= 64, K a multiple of R with K/R a multiple "
+                             "of 8, N >= 1 and 1 <= B <= 16")
+        return dict(kind="gemv", R=R, N=N, K=K, B=B, seed=5, w_std=0.01, x="normal")
+    if name not in synth.WORKLOADS:
+        raise SystemExit(f"unknown workload {name!r}: one of {sorted(synth.WORKLOADS)} or gemv:R,N,K,B")
     return dict(synth.WORKLOADS[name])
 
 
@@ -1106,7 +1119,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=100)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="mlp_down_decode")
+    p.add_argument("--workload", default="mlp_down_decode",
+                   help="a named workload (synth.WORKLOADS) or gemv:R,N,K,B for the fused GEMV of any shape")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--gemv-path", choices=("auto", "ffma", "dyn", "cluster"), default="auto",

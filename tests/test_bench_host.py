@@ -191,3 +191,16 @@ def test_parity_check_of_every_form():
     assert bench.parity_check("allreduce", "reduce_scatter", cases[3][2], cases[3][2][1], 128, 256, R, "rows") \
         is None
     assert bench.parity_check("tile", "one_shot", cases[0][2], cases[0][2][1], N, N, R, "rows") is None
+
+
+def test_workload_of_any_gemv_shape():
+    """--workload gemv:R,N,K,B names the fused GEMV of that shape; shapes
+    the call refuses, malformed names and unknown names are refused."""
+    w = bench.workload("gemv:8,8192,28672,4")
+    assert (w["kind"], w["R"], w["N"], w["K"], w["B"]) == ("gemv", 8, 8192, 28672, 4)
+    assert bench.workload_bytes(w) == bench.algorithmic_bytes(8, 8192, 28672, 4)
+    # K not a multiple of R, B above 16, not integers, too few numbers, unknown, K/R not a multiple of 8
+    for bad in ("gemv:8,8192,28671,4", "gemv:8,8192,28672,17", "gemv:8,8192,8*4,1", "gemv:8,8192", "nonesuch",
+                "gemv:8,8192,96,1"):
+        with pytest.raises(SystemExit):
+            bench.workload(bad)

@@ -379,6 +379,15 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
             if (h->opt_dyn_splits <= 0) S = 1;
         } else if (h->opt_dyn_cluster < 0) {
             cl = cl_base && h->R >= 2 && S == 1 && (pairs <= G || Kr >= kClusterEpilogueMinKr);
+            // Units that fill at most half of the CTA slots leave SMs idle:
+            // split K inside the clusters (R x S CTAs each, at most 8) while
+            // the launch stays one wave.  Measured (chained us per call, two
+            // runs): R = 2, N = 8192, K/R = 14336: 2 splits, 256 CTAs, 72.5 ->
+            // 66.5-66.9; R = 4, N = 4096, K/R = 2048, B = 8: 14.6 -> 13.2-13.4;
+            // R = 3, N = 4096, K/R = 4096: 22.0 -> 17.6.  3 splits on the first
+            // (two uneven waves) lost.
+            if (cl && h->opt_dyn_splits <= 0 && 2 * pairs <= G)
+                while (h->R * (S + 1) <= kMaxClusterRanks && pairs * (S + 1) <= G) ++S;
         }
         S = std::min<long long>(S, KB);
         while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;

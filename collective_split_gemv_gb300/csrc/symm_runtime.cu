@@ -371,23 +371,36 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         // slower than drawn ones, 256-512 KB units about even, 0.9-2 MB units
         // 1-6 % faster.  Forced on, it takes the requested K splits (none by
         // default).
-        const bool cl_base = dyn_cluster_supported(pl->slabs, pl->cps) && h->mp_rank < 0 &&
-                             !h->opt_unfused;
+        // (cl_ok: the cluster epilogue could run this shape; the unfused form
+        // takes the splits it would have, without the clusters, so that its
+        // partials are summed in the fused call's order)
+        const bool cl_ok = dyn_cluster_supported(pl->slabs, pl->cps) && h->mp_rank < 0;
+        const bool cl_base = cl_ok && !h->opt_unfused;
         bool cl = false;
         if (h->opt_dyn_cluster == 1) {
             cl = true;
             if (h->opt_dyn_splits <= 0) S = 1;
         } else if (h->opt_dyn_cluster < 0) {
-            cl = cl_base && h->R >= 2 && S == 1 && (pairs <= G || Kr >= kClusterEpilogueMinKr);
-            // Units that fill at most half of the CTA slots leave SMs idle:
-            // split K inside the clusters (R x S CTAs each, at most 8) while
-            // the launch stays one wave.  Measured (chained us per call, two
-            // runs): R = 2, N = 8192, K/R = 14336: 2 splits, 256 CTAs, 72.5 ->
-            // 66.5-66.9; R = 4, N = 4096, K/R = 2048, B = 8: 14.6 -> 13.2-13.4;
-            // R = 3, N = 4096, K/R = 4096: 22.0 -> 17.6.  3 splits on the first
-            // (two uneven waves) lost.
-            if (cl && h->opt_dyn_splits <= 0 && 2 * pairs <= G)
+            if (cl_ok && h->R >= 2 && 2 * h->R <= kMaxClusterRanks && h->opt_dyn_splits <= 0 && 2 * pairs <= G) {
+                // Units that fill at most half of the CTA slots leave SMs
+                // idle: split K inside the clusters (R x S CTAs each, at most
+                // 8) as far as the launch stays one wave.  Measured (chained
+                // us per call, two runs each), against the plan without it
+                // (clusters of R, or drawn K-split units for the smallest):
+                // R = 2, N = 8192, K/R = 14336: 2 splits, 72.5 -> 66.5-66.9;
+                // R = 4, N = 4096, K/R = 2048, B = 8: 14.6 -> 13.2-13.4;
+                // R = 3, N = 4096, K/R = 4096: 22.0 -> 17.6; R = 2, N = 4096,
+                // K/R = 4096, B = 4: 16.7 -> 13.1; R = 4, N = 2048, K/R = 4096:
+                // 20.6-21.0 -> 14.2-14.4; R = 2, N = 2048, K/R = 8192: 19.0-19.7
+                // -> 14.3-14.4.  3 splits on the first (two uneven waves) lost;
+                // at R = 8 no split fits a cluster, and clusters of 8 without
+                // splits measured 2 % behind drawn K-split units there.
+                cl = cl_base;
+                S = 1;
                 while (h->R * (S + 1) <= kMaxClusterRanks && pairs * (S + 1) <= G) ++S;
+            } else {
+                cl = cl_base && h->R >= 2 && S == 1 && (pairs <= G || Kr >= kClusterEpilogueMinKr);
+            }
         }
         S = std::min<long long>(S, KB);
         while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;

@@ -53,14 +53,16 @@ def _case(R=4, N=576, K=2048, B=2, seed=41):
 @pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("B", [2, 8])
 def test_pad_is_clean_after_every_launch(path, B):
-    """After launch e: the epoch word holds e, tiles_done and every tile
-    counter are zero, and the work counter the next launch draws from
-    (work[(e + 1) & 1]) is zero."""
+    """The global-memory protocol (per-tile kernel, and the persistent
+    kernel drawing units): after launch e the epoch word holds e, tiles_done
+    and every tile counter are zero, and the work counter the next launch
+    draws from (work[(e + 1) & 1]) is zero."""
     R, N, K = 4, 576, 2048
     W, x = _case(R, N, K, B)
     ws = GemvWorkspace(R, N, K, B)
     try:
         csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, PATHS[path])
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_DYN_CLUSTER, 0)
         ws.load_W(W)
         ws.load_x(x)
         plan = csg.symm_gemv_plan(ws.h, N, K, B)
@@ -75,6 +77,34 @@ def test_pad_is_clean_after_every_launch(path, B):
             if path == "dyn":
                 units = plan["tiles"] * R * plan["splits"]
                 assert words[WORK_OFF // 4 + (e & 1)] == units   # every unit drawn, plus one stop per CTA
+        assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
+        check_gemv(W, x, ws.read_y())
+    finally:
+        ws.close()
+
+
+@pytest.mark.parametrize("B", [2, 8])
+def test_cluster_epilogue_leaves_the_pad_untouched(B):
+    """The persistent kernel's cluster epilogue (the automatic plan of this
+    small layer: K split inside the clusters) draws nothing and publishes
+    nothing: the epoch, work counters, tiles_done and tile counters stay
+    zero launch after launch."""
+    R, N, K = 4, 576, 2048
+    W, x = _case(R, N, K, B)
+    ws = GemvWorkspace(R, N, K, B)
+    try:
+        csg.symm_set_option(ws.h, csg.SYMM_OPT_GEMV_PATH, csg.GEMV_PATH_DYN)
+        ws.load_W(W)
+        ws.load_x(x)
+        plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        assert plan["cluster"] == R * plan["splits"] and plan["splits"] > 1
+        s = torch.cuda.current_stream()
+        for _ in range(4):
+            ws.run(s)
+            words = _pad_words(ws, 128)
+            assert not words[WORK_OFF // 4:WORK_OFF // 4 + 2].any()
+            assert words[EPOCH_OFF // 4] == 0 and words[DONE_OFF // 4] == 0
+            assert not _counters(ws, plan["tiles"]).any()
         assert csg.symm_status(ws.h, s)[0] == csg.SYMM_OK
         check_gemv(W, x, ws.read_y())
     finally:

@@ -381,7 +381,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
             cl = true;
             if (h->opt_dyn_splits <= 0) S = 1;
         } else if (h->opt_dyn_cluster < 0) {
-            if (cl_ok && h->R >= 2 && 2 * h->R <= kMaxClusterRanks && h->opt_dyn_splits <= 0 && 2 * pairs <= G) {
+            if (cl_ok && 2 * h->R <= kMaxClusterRanks && h->opt_dyn_splits <= 0 && 2 * pairs <= G) {
                 // Units that fill at most half of the CTA slots leave SMs
                 // idle: split K inside the clusters (R x S CTAs each, at most
                 // 8) as far as the launch stays one wave.  Measured (chained
@@ -392,9 +392,12 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
                 // R = 3, N = 4096, K/R = 4096: 22.0 -> 17.6; R = 2, N = 4096,
                 // K/R = 4096, B = 4: 16.7 -> 13.1; R = 4, N = 2048, K/R = 4096:
                 // 20.6-21.0 -> 14.2-14.4; R = 2, N = 2048, K/R = 8192: 19.0-19.7
-                // -> 14.3-14.4.  3 splits on the first (two uneven waves) lost;
-                // at R = 8 no split fits a cluster, and clusters of 8 without
-                // splits measured 2 % behind drawn K-split units there.
+                // -> 14.3-14.4; one rank (the K splits are then the cluster),
+                // N = 8192, K = 28672: 73.9-75.4 -> 65.8 (4 splits); N = 4096,
+                // K = 16384, B = 4: 29.6-30.0 -> 23.9.  3 splits on the first
+                // (two uneven waves) lost; at R = 8 no split fits a cluster, and
+                // clusters of 8 without splits measured 2 % behind drawn K-split
+                // units there.
                 cl = cl_base;
                 S = 1;
                 while (h->R * (S + 1) <= kMaxClusterRanks && pairs * (S + 1) <= G) ++S;
@@ -406,6 +409,7 @@ int make_plan(const symm_handle *h, int N, int Kr, int B, Plan *pl, size_t cap, 
         while (S > 1 && ((size_t)S * B * N * 4 > cap || (long long)pl->tiles * S > h->max_tiles)) --S;
         const long long KBs = (KB + S - 1) / S;
         S = (KB + KBs - 1) / KBs;   // no empty split
+        if (cl && h->opt_dyn_cluster < 0 && h->R * S < 2) cl = false;   // automatic: a cluster of one CTA gains nothing
         if (cl) {
             const long long C = (long long)h->R * S;
             const bool fits = cl_base && C <= kMaxClusterRanks && dyn_cluster_fits(pl->slabs, (int)C);

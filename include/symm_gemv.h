@@ -521,12 +521,14 @@ enum {
                                  when it is forced on) a cluster holds the R x splits units of a tile.  It
                                  needs 2 CTAs per SM, R x splits <= 8, the fused
                                  form, a single-process handle and a device that can hold such a cluster
-                                 (else 1 returns SYMM_EINVAL).  Auto turns it on when those hold, R >= 2,
-                                 and either the units fit the persistent grid in one wave (nothing would
-                                 be drawn) or they are long (K/R >= 3072, 768 KB of W per unit), when the
-                                 hardware's scheduling of whole clusters beats drawing single units; if
-                                 the units then fill at most half of the grid, it splits K inside the
-                                 clusters (R x splits <= 8) as far as one wave holds */
+                                 (else 1 returns SYMM_EINVAL).  Auto, where those hold: for R <= 4 whose
+                                 (tile, rank) units fill at most half of the persistent grid, it splits
+                                 K inside the clusters (R x splits <= 8) as far as one wave holds (with
+                                 SYMM_OPT_DYN_SPLITS unset; R = 1 too, the splits then being the
+                                 cluster); otherwise, for R >= 2 without K splits, it turns it on when
+                                 the units fit the grid in one wave (nothing would be drawn) or are long
+                                 (K/R >= 3072, 768 KB of W per unit), when the hardware's scheduling of
+                                 whole clusters beats drawing single units */
 };
 int symm_set_option(symm_handle_t *h, int option, int value);
 

@@ -258,6 +258,17 @@ constexpr int kClusterEpilogueMinKr = 3072;
 // where R and B allow it, else the CUDA-core one.
 constexpr size_t kSmallWBytes = 24u << 20;
 constexpr int kSmallMaxBatch = 4;
+// The cluster kernel does every product on the CUDA cores, one cluster of R
+// CTAs per 16 rows: it returns first while its CTAs times the batch width
+// stay at most this, beyond that the persistent kernel's tensor cores do.
+// Measured per launch, L2 flushed, cluster kernel / persistent kernel, us
+// (R, N, K, B; CTAs x B): 2, 256, 512, 1 (32): 7.0 / 12.4; 2, 2048, 4096,
+// 1 (256): 10.4 / 13.5; 2, 1024, 4096, 4 (512): 11.0 / 12.4; 4, 2048, 4096,
+// 1 (512): 12.3 / 13.5; 8, 1024, 4096, 1 (512): 11.3 / 16.8; 2, 4096, 2048,
+// 2 (1024): 13.1 / 13.1; 4, 1024, 4096, 4 (1024): 13.8 / 12.4; 8, 2048,
+// 4096, 1 (1024): 14.5 / 13.7; 4, 4096, 2048, 2 (2048): 17.5 / 13.2; 8,
+// 1024, 2048, 4 (2048): 20.5 / 15.9; 8, 4096, 2048, 4 (8192): 56.3 / 13.4.
+constexpr long long kClusterMaxWork = 512;
 
 // (Not on a multi-process handle: a cluster's CTAs belong to one process.)
 bool cluster_ok(const symm_handle *h, int N, int B) {
@@ -268,7 +279,11 @@ int gemv_path(const symm_handle *h, int N, int B, int Kr) {
     if (h->opt_gemv_path != 0) return h->opt_gemv_path;
     if (Kr == 0) return kPathFfma;
     const size_t wbytes = (size_t)N * (size_t)Kr * 2 * (size_t)h->R;
-    if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) return cluster_ok(h, N, B) ? kPathCluster : kPathFfma;
+    if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) {
+        if (!cluster_ok(h, N, B)) return kPathFfma;
+        const long long ctas = (long long)h->R * ((N + kClusterRows - 1) / kClusterRows);
+        return ctas * B <= kClusterMaxWork ? kPathCluster : kPathDyn;
+    }
     return kPathDyn;
 }
 

@@ -459,7 +459,9 @@ int multi_root_tile_reduce(symm_handle_t *h, const void *const *in_tiles, void *
  * others exist for tests and measurements. */
 enum {
     SYMM_OPT_GEMV_PATH = 1,   /* 0 auto: 4 when K > 0 and W_r of all ranks is over 24 MB or B > 4; else 5
-                                 when R <= 8 and B <= 4; else 1.  1 CUDA-core kernel, one CTA per (row
+                                 when R <= 8, B <= 4 and its CTAs (R x ceil(N / 16)) times B are at most
+                                 512, else 4; 1 where 5 cannot run (R > 8, a multi-process handle) and
+                                 for K = 0.  1 CUDA-core kernel, one CTA per (row
                                  tile, rank); 4 persistent kernel drawing (tile, rank) units from a work
                                  counter; 5 cluster kernel for small layers, one thread-block cluster of R
                                  CTAs per 16-row tile, the partials exchanged through distributed shared

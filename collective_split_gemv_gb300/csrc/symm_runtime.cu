@@ -280,9 +280,18 @@ int gemv_path(const symm_handle *h, int N, int B, int Kr) {
     if (Kr == 0) return kPathFfma;
     const size_t wbytes = (size_t)N * (size_t)Kr * 2 * (size_t)h->R;
     if (wbytes <= kSmallWBytes && B <= kSmallMaxBatch) {
-        if (!cluster_ok(h, N, B)) return kPathFfma;
-        const long long ctas = (long long)h->R * ((N + kClusterRows - 1) / kClusterRows);
-        return ctas * B <= kClusterMaxWork ? kPathCluster : kPathDyn;
+        // The per-tile kernels do every product on the CUDA cores: the
+        // cluster kernel where it can run, else the per-tile one (R > 8, a
+        // multi-process handle), each under the same bound.  Per-tile kernel
+        // / persistent kernel, per launch, L2 flushed, us (R, N, K, B; CTAs x
+        // B): 16, 256, 4096, 1 (256): 12.9 / 16.9; 16, 1024, 8192, 1 (1024):
+        // 22.7 / 18.4; 32, 512, 8192, 1 (1024): 24.4 / 19.0; 16, 2048, 4096,
+        // 2 (4096): 32.5 / 18.8; 64, 1024, 8192, 1 (4096): 58.4 / 41.1.
+        const bool clu = cluster_ok(h, N, B);
+        const int rows = clu ? kClusterRows : ffma_rows_per_tile(B);
+        const long long ctas = (long long)h->R * ((N + rows - 1) / rows);
+        if (ctas * B > kClusterMaxWork) return kPathDyn;
+        return clu ? kPathCluster : kPathFfma;
     }
     return kPathDyn;
 }

@@ -350,3 +350,30 @@ def test_twenty_thousand_chained_calls_across_endings():
         assert csg.symm_check_guards(ws.h)[0] == csg.SYMM_OK
     finally:
         ws.close()
+
+
+@pytest.mark.parametrize("shape,want", [
+    # (R, N, K, B): (path, CTAs per cluster, K splits) of the automatic plan
+    ((2, 256, 512, 1), (csg.GEMV_PATH_CLUSTER, 2, 1)),            # the tiny layer: cluster kernel
+    ((8, 1024, 8 * 512, 1), (csg.GEMV_PATH_CLUSTER, 8, 1)),       # 512 CTAs x B = 1: still the cluster kernel
+    ((8, 4096, 2048, 4), (csg.GEMV_PATH_DYN, 8, 1)),              # small W, 8192 CTAs x B: persistent kernel
+    ((16, 256, 16 * 256, 1), (csg.GEMV_PATH_FFMA, 0, 1)),         # R > 8, 256 CTAs: per-tile kernel
+    ((16, 1024, 16 * 512, 1), (csg.GEMV_PATH_DYN, 0, 1)),         # R > 8, 1024 CTAs: persistent, drawn units
+    ((2, 8192, 28672, 1), (csg.GEMV_PATH_DYN, 4, 2)),             # half-empty wave: K split inside clusters
+    ((1, 8192, 28672, 1), (csg.GEMV_PATH_DYN, 4, 4)),             # one rank: the splits are the cluster
+    ((4, 8192, 8192, 8), (csg.GEMV_PATH_DYN, 4, 1)),              # attn_out_proj: one wave, no split
+    ((8, 8192, 28672, 1), (csg.GEMV_PATH_DYN, 8, 1)),             # the decode layer
+], ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) and len(v) == 4 else None)
+def test_automatic_plans(shape, want):
+    """The automatic plan of representative layers on a GPU of 152 SMs (two
+    persistent CTAs per SM): which kernel, the cluster size and the K splits
+    that measured fastest."""
+    if torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count != 152:
+        pytest.skip("the plans were measured on 152 SMs")
+    R, N, K, B = shape
+    ws = GemvWorkspace(R, N, K, B)
+    try:
+        plan = csg.symm_gemv_plan(ws.h, N, K, B)
+        assert (plan["path"], plan["cluster"], plan["splits"]) == want, plan
+    finally:
+        ws.close()
